@@ -1,0 +1,213 @@
+/*
+ * pfkv.h -- C ABI of libpfkv: decode attention over a paged KV cache stored as
+ * 8-bit e4m3 floating point and converted back when it is read, for NVIDIA
+ * GB300 (sm_103a).
+ *
+ * Sources of the operations (web pages; section named in each entry below):
+ *  - "Inference-engine scheduling explainer": 推論エンジンの実践：Continuous
+ *    Batching・Prefix Cache・Speculative Decoding (deepseekmodel.com).
+ *  - "Workers AI post": より小さく、高速で、安全に：Kimi と GLM を大規模に展開
+ *    するための実行方法 (Cloudflare Workers AI, HN mirror).
+ *  - "kLLM article": 快手万擎大模型推理成本和性能优化实践 (6aiq.com).
+ *
+ * Conventions for every call
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    never allocates, frees or retains them.  Work is enqueued on `stream`
+ *    (asynchronous; no call synchronises unless its comment says so).
+ *  - bf16 = IEEE bfloat16 bit patterns (uint16); e4m3 = OCP 8-bit E4M3 codes
+ *    (uint8: bias 7, subnormals, 0x7F/0xFF NaN, no infinity, max 448).
+ *  - Layouts are row-major (C order) with the shapes written in brackets.
+ *  - Paged caches: K and V are separate tensors [num_pages][Hkv][P][D]; the
+ *    token at logical position t of request b lives in page
+ *    block_tables[b][t / P], row t % P ("slot" = page * P + t % P).  The MLA
+ *    latent cache is [num_pages][P][Dqk] (the same layout with Hkv = 1).
+ *  - context_lens[b] counts every token attended, including tokens appended
+ *    in the same step.
+ *  - Return value: PFKV_OK, or a negative pfkv_status for argument, support or
+ *    launch errors, detected synchronously before anything is enqueued (a
+ *    launch error after enqueueing is reported as PFKV_ERR_CUDA).
+ *    pfkv_last_error() gives a message for the calling thread.
+ *  - Data errors that only the GPU can see (a block-table entry outside the
+ *    pool, a top-k index beyond the context) never cause an out-of-bounds
+ *    access: the kernels clamp or skip, and set a bit in the status word at the
+ *    start of the workspace (read it with pfkv_workspace_status) or, for
+ *    pfkv_validate_tables, in the caller's error word.
+ *  - No kernel spins on memory written by another kernel.  Intra-kernel
+ *    barrier waits are bounded (about one second); on expiry the kernel sets
+ *    PFKV_DEVERR_WAIT_TIMEOUT and returns.
+ */
+#ifndef PFKV_H
+#define PFKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define PFKV_API __attribute__((visibility("default")))
+#else
+#define PFKV_API
+#endif
+
+/* CUDA stream handle (cudaStream_t); declared opaquely so that this header
+ * does not require the CUDA headers.  NULL is the legacy default stream. */
+typedef struct CUstream_st *pfkv_stream_t;
+
+typedef enum {
+  PFKV_OK = 0,
+  PFKV_ERR_INVALID_ARG = -1, /* null pointer, negative size, bad shape */
+  PFKV_ERR_UNSUPPORTED = -2, /* valid but not implemented (head_dim, page size, ...) */
+  PFKV_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed */
+  PFKV_ERR_INDEX = -4,       /* an index error was found (status word set) */
+  PFKV_ERR_WORKSPACE = -5    /* workspace too small for this call */
+} pfkv_status;
+
+typedef enum { PFKV_CACHE_FP8_E4M3 = 0, PFKV_CACHE_BF16 = 1 } pfkv_cache_dtype;
+
+/* Bits of the device status word (workspace header / validation word). */
+#define PFKV_DEVERR_WAIT_TIMEOUT 0x01 /* a bounded barrier wait expired */
+#define PFKV_DEVERR_BAD_PAGE 0x02     /* block-table entry outside [0, num_pages) */
+#define PFKV_DEVERR_BAD_CONTEXT 0x04  /* context_lens[b] < 0 or > max_pages_per_seq * P */
+#define PFKV_DEVERR_WORKSPACE 0x08    /* partial-state slots exceeded the workspace */
+#define PFKV_DEVERR_BAD_TOPK 0x10     /* top-k index >= context length */
+#define PFKV_DEVERR_BAD_SLOT 0x20     /* slot_mapping entry >= num_pages * P */
+
+/* ------------------------------------------------------------------------ */
+/* kv_append_fp8 -- quantise new K/V rows to e4m3 and scatter them into pages.
+ *
+ * Workers AI post, §1 "KV キャッシュの量子化": the cache holds 8-bit e4m3
+ * instead of BF16, halving its size.  Inference-engine scheduling explainer,
+ * section "FP8 KV のエンジニアリング上の制約": the scale is per tensor, per head
+ * or per token; this call takes one fp32 scale per tensor (one for K, one for
+ * V).  Section "PagedAttention の 2 つの原語": KV goes to fixed-size pages
+ * through a slot mapping.
+ *
+ * For token i < num_tokens, head h, element d:
+ *     code = e4m3_rne_satfinite( fp32(x[i][h][d]) / scale )   (IEEE fp32 divide)
+ * stored at cache[slot / P][h][slot % P][d] with slot = slot_mapping[i].
+ *   k_new, v_new   bf16 [num_tokens][num_kv_heads][head_dim]
+ *   k_cache, v_cache  e4m3 [num_pages][num_kv_heads][page_size][head_dim]
+ *   slot_mapping   int64 [num_tokens]; slot < 0 skips the token; a slot
+ *                  >= num_pages * page_size is skipped (nothing is written).
+ * One latent tensor (MLA cKV): pass v_new = v_cache = NULL, num_kv_heads = 1,
+ * head_dim = Dqk; v_scale is then ignored.
+ * Supported: head_dim a multiple of 16, page_size >= 1, scales > 0 and finite.
+ * Errors: PFKV_ERR_INVALID_ARG for null k pointers, num_tokens < 0, bad dims
+ * or scales.  num_tokens == 0 enqueues nothing. */
+PFKV_API int pfkv_kv_append_fp8(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                       const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                       int head_dim, int page_size, int64_t num_pages, float k_scale,
+                       float v_scale, pfkv_stream_t stream);
+
+/* Same scatter into a bf16 cache (no quantisation), for the BF16-cache
+ * comparison the Workers AI post makes (§1: FP8 halves the cache bytes). */
+PFKV_API int pfkv_kv_append_bf16(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                        const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                        int head_dim, int page_size, int64_t num_pages, pfkv_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* paged_decode_attn -- one decode step of GQA/MHA attention over the paged
+ * cache, dequantising on read, with split-KV and a log-sum-exp merge.
+ *
+ * Explainer, "PagedAttention の 2 つの原語": the kernel resolves KV addresses
+ * through block_table.  Workers AI post, §1: the FP8 attention kernel converts
+ * values as it reads them.  kLLM article, §5.2.2: blockwise attention keeps
+ * (m, ℓ, O) per block so that the merged result equals full attention.
+ *
+ * For request b, query head h (KV head kvh = h / (Hq / Hkv)), t < L_b:
+ *   s_t  = softmax_scale * sum_d q[b][h][d] * K(t)[d] * k_scale
+ *   out  = sum_t e^{s_t - m} V(t) * v_scale / sum_t e^{s_t - m}
+ *   lse  = m + ln sum_t e^{s_t - m}          (m = max_t s_t; natural log)
+ * where K(t)/V(t) are the e4m3 (or bf16) rows at block_tables[b][t / P].
+ * The work is split into contiguous runs of 16-token tiles balanced over all
+ * warps of a persistent grid; runs that do not cover a whole request write
+ * fp32 partial states to the workspace and a merge kernel combines them.
+ *   out            bf16 [batch][num_q_heads][head_dim]
+ *   q              bf16 [batch][num_q_heads][head_dim]
+ *   k_cache/v_cache  e4m3 or bf16 [num_pages][num_kv_heads][page_size][head_dim]
+ *   block_tables   int32 [batch][max_pages_per_seq]
+ *   context_lens   int32 [batch] (device)
+ *   kv_split_tokens  0: split only for balance; > 0: additionally cut every
+ *                  request into chunks of this many tokens, each merged by
+ *                  log-sum-exp (must be a multiple of 16)
+ *   lse_out        optional fp32 [batch][num_q_heads] (NULL: not written)
+ *   workspace      device scratch of at least pfkv_paged_decode_workspace_size()
+ *                  bytes, 256-byte aligned; contents on entry are ignored.
+ * L_b == 0 gives out = 0 and lse = -inf.  For a bf16 cache the scales still
+ * multiply (pass 1.0).
+ * Supported: head_dim 128; page_size a multiple of 16; num_q_heads /
+ * num_kv_heads in 1..16; num_pages * num_kv_heads * page_size < 2^31.
+ * Device errors (status word): PFKV_DEVERR_BAD_PAGE (rows outside the pool
+ * read as zeros), PFKV_DEVERR_BAD_CONTEXT (length clamped to the table),
+ * PFKV_DEVERR_WORKSPACE, PFKV_DEVERR_WAIT_TIMEOUT. */
+PFKV_API size_t pfkv_paged_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads,
+                                        int head_dim, int kv_split_tokens,
+                                        int64_t max_total_chunks);
+PFKV_API int pfkv_paged_decode_attn(void *out, const void *q, const void *k_cache, const void *v_cache,
+                           pfkv_cache_dtype cache_dtype, const int32_t *block_tables,
+                           int max_pages_per_seq, const int32_t *context_lens, int batch,
+                           int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+                           int64_t num_pages, float k_scale, float v_scale, float softmax_scale,
+                           int kv_split_tokens, void *workspace, size_t workspace_bytes,
+                           float *lse_out, pfkv_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* mla_decode_attn -- MLA absorbed-latent decode over one shared e4m3 latent
+ * row per token, optionally restricted to a top-k token list.
+ *
+ * kLLM article, §5.1.1: DSA selects the top-k historical tokens that take part
+ * in attention and MLA keeps a compressed per-token cKV; §5.1.2: that cKV is
+ * shared by all heads.  Absorbed reading: the whole Dqk-wide row is the key,
+ * its first d_latent entries are the value.
+ *   s_t = softmax_scale * sum_{d<Dqk} q[b][h][d] * c_t[d] * ckv_scale
+ *   out = sum_t e^{s_t - m} c_t[0:d_latent] * ckv_scale / sum_t e^{s_t - m}
+ * over t in topk_idx[b][0:topk] (entries < 0 are padding and skipped), or over
+ * every t < L_b when topk_idx is NULL.  Dqk = d_latent + d_rope.
+ *   out        bf16 [batch][num_heads][d_latent]
+ *   q          bf16 [batch][num_heads][Dqk]
+ *   ckv_cache  e4m3 [num_pages][page_size][Dqk]
+ *   topk_idx   int32 [batch][topk] or NULL
+ *   lse_out    optional fp32 [batch][num_heads]
+ * Supported: d_latent 512, d_rope 64, num_heads 128 or fewer and a multiple of
+ * 16, page_size a multiple of 16.  Listed indices >= L_b are skipped and set
+ * PFKV_DEVERR_BAD_TOPK. */
+PFKV_API size_t pfkv_mla_decode_workspace_size(int batch, int num_heads, int d_latent, int topk);
+PFKV_API int pfkv_mla_decode_attn(void *out, const void *q, const void *ckv_cache,
+                         const int32_t *block_tables, int max_pages_per_seq,
+                         const int32_t *context_lens, const int32_t *topk_idx, int topk,
+                         int batch, int num_heads, int d_latent, int d_rope, int page_size,
+                         int64_t num_pages, float ckv_scale, float softmax_scale,
+                         void *workspace, size_t workspace_bytes, float *lse_out,
+                         pfkv_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* validate_tables -- opt-in index check before decode (Workers AI post, §3
+ * "共用 KV キャッシュの保護": verify the request-to-page mapping before reading,
+ * as a separate batched check rather than inside the attention kernel).
+ * Zeroes *d_err_word, then ORs PFKV_DEVERR_* bits for: context_lens out of
+ * range, a block-table entry used by some request outside [0, num_pages), a
+ * top-k index >= its context length (topk_idx may be NULL), a slot_mapping
+ * entry >= num_pages * page_size (slot_mapping may be NULL).  d_err_word is a
+ * device int32; read it after the stream reaches this point. */
+PFKV_API int pfkv_validate_tables(const int32_t *block_tables, int max_pages_per_seq,
+                         const int32_t *context_lens, int batch, int page_size, int64_t num_pages,
+                         const int32_t *topk_idx, int topk, const int64_t *slot_mapping,
+                         int num_slots, int32_t *d_err_word, pfkv_stream_t stream);
+
+/* Copy the workspace status word (bits PFKV_DEVERR_*) to *status after
+ * synchronising `stream`.  Returns PFKV_OK, or PFKV_ERR_CUDA. */
+PFKV_API int pfkv_workspace_status(const void *workspace, int32_t *status, pfkv_stream_t stream);
+
+/* Message describing the last error on the calling thread ("" if none). */
+PFKV_API const char *pfkv_last_error(void);
+
+/* Library version string. */
+PFKV_API const char *pfkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PFKV_H */

@@ -75,10 +75,16 @@ uint8_t orc_e4m3_encode(float x)
     double a = fabs((double)x);
     if (a >= 448.0)
         return (uint8_t)(sign | 0x7E);
-    /* magnitudes of codes 0x00..0x7E increase strictly with the code */
-    int lo = 0;
-    while (lo < 0x7E && orc_e4m3_value((uint8_t)(lo + 1)) <= a)
-        lo++;
+    /* magnitudes of codes 0x00..0x7E increase strictly with the code: find the
+     * largest code lo with value(lo) <= a by bisection over the grid */
+    int lo = 0, hi = 0x7E; /* value(lo) <= a < value(hi) (a < 448 here) */
+    while (hi - lo > 1) {
+        int mid = (lo + hi) / 2;
+        if (orc_e4m3_value((uint8_t)mid) <= a)
+            lo = mid;
+        else
+            hi = mid;
+    }
     /* value(lo) <= a < value(lo+1) */
     double vlo = orc_e4m3_value((uint8_t)lo);
     double vhi = orc_e4m3_value((uint8_t)(lo + 1));

@@ -137,6 +137,14 @@ class PagedWorkload:
         return gen.normal_bf16(key, self.kv_index(b, t0, t1).reshape(-1).astype(np.uint64)).reshape(
             t1 - t0, self.Hkv, self.D)
 
+    def kv_head_bits(self, which: str, b: int, kvh: int, t0: int, t1: int) -> np.ndarray:
+        """[t1-t0][D] bf16 bits of one KV head (cheaper than kv_bits for long runs)."""
+        key = self.key_k if which == "k" else self.key_v
+        t = np.arange(t0, t1, dtype=np.int64)
+        tok = (self.src_request(b, t) << TOKEN_SHIFT) + t
+        idx = (tok * self.Hkv + kvh)[:, None] * self.D + np.arange(self.D, dtype=np.int64)[None, :]
+        return gen.normal_bf16(key, idx.reshape(-1).astype(np.uint64)).reshape(t1 - t0, self.D)
+
     def q_bits(self) -> np.ndarray:
         n = self.B * self.Hq * self.D
         return gen.normal_bf16(self.key_q, np.arange(n, dtype=np.uint64)).reshape(self.B, self.Hq, self.D)

@@ -1,0 +1,155 @@
+"""mla_decode_attn and validate_tables on the GPU against the oracle."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from synth import gen
+
+from gpu_helpers import assert_within_tolerance, pf, to_np_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+def _setup_mla(p, m):
+    from synth import device as sdev
+    if m.ckv_scale is None and int(m.context_lens.sum()) * m.Dqk <= (1 << 24):
+        m.set_scales_host()
+    st = sdev.setup_mla(m, lambda c, c4, s: p.kv_append_fp8(c, None, c4, None, s, m.ckv_scale))
+    p.kv_append_fp8(st.c_new, None, st.ckv_cache.view(m.num_pages, 1, m.P, m.Dqk), None, st.step_slots,
+                    m.ckv_scale)
+    return st
+
+
+def _run_mla(p, m, st, topk=True):
+    import torch
+    out = torch.empty((m.B, m.H, m.Dv), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((m.B, m.H), dtype=torch.float32, device="cuda")
+    ws = p.mla_decode_attn(out, st.q, st.ckv_cache, st.block_tables, st.context_lens,
+                           st.topk if topk else None, m.ckv_scale, m.softmax_scale, lse_out=lse)
+    torch.cuda.synchronize()
+    return to_np_bf16(out), lse.cpu().numpy(), p.workspace_status(ws)
+
+
+def _oracle_cache(m, rows_of=None):
+    c = np.zeros((m.num_pages, 1, m.P, m.Dqk), np.uint8)
+    for b in range(m.B):
+        L = int(m.context_lens[b])
+        oracle.kv_append(m.ckv_bits(b, 0, L), c, m.slots(b, 0, L), m.P, m.ckv_scale)
+    return c.reshape(m.num_pages, m.P, m.Dqk)
+
+
+@pytest.mark.parametrize("case", [
+    dict(H=128, lens=(300, 129), topk=64),
+    dict(H=128, lens=(64, 1000, 17), topk=0),
+    dict(H=16, lens=(2048, 70), topk=50),
+    dict(H=64, lens=(1, 65), topk=1),
+])
+def test_mla_small_cases_match_oracle(case):
+    p = pf()
+    m = synth.MlaWorkload("mla", B=len(case["lens"]), H=case["H"], context_lens=np.array(case["lens"]),
+                          topk_n=case["topk"], P=64, seed=8)
+    st = _setup_mla(p, m)
+    out, lse, status = _run_mla(p, m, st)
+    assert status == 0
+    c = _oracle_cache(m)
+    assert np.array_equal(st.ckv_cache.cpu().numpy(), c)
+    ref, ref_lse = oracle.mla_decode(m.q_bits(), c, m.block_tables, m.context_lens, m.topk, m.P, m.Dv,
+                                     m.ckv_scale, m.softmax_scale)
+    assert_within_tolerance(out, ref, "mla")
+    np.testing.assert_allclose(lse, ref_lse, rtol=2e-5, atol=2e-4)
+
+
+def test_mla_topk_padding_and_out_of_range_indices():
+    import torch
+    p = pf()
+    m = synth.MlaWorkload("mla", B=2, H=16, context_lens=np.array([100, 300]), topk_n=0, P=64, seed=5)
+    st = _setup_mla(p, m)
+    tk = np.full((2, 40), -1, np.int32)
+    tk[0, :10] = np.arange(0, 100, 10)
+    tk[1, 5:35] = np.arange(0, 300, 10)
+    st.topk = torch.from_numpy(tk).cuda()
+    out, _, status = _run_mla(p, m, st)
+    assert status == 0
+    c = _oracle_cache(m)
+    ref, _ = oracle.mla_decode(m.q_bits(), c, m.block_tables, m.context_lens, tk, m.P, m.Dv, m.ckv_scale,
+                               m.softmax_scale)
+    assert_within_tolerance(out, ref, "mla padding")
+    tk[1, 0] = 300  # == context length: skipped and flagged
+    st.topk = torch.from_numpy(tk).cuda()
+    out2, _, status = _run_mla(p, m, st)
+    assert status & p.DEVERR["BAD_TOPK"]
+    assert_within_tolerance(out2, ref, "mla bad index skipped")
+
+
+def test_config4_mla_full_size_sampled():
+    p = pf()
+    m = synth.config(4)
+    st = _setup_mla(p, m)
+    out, lse, status = _run_mla(p, m, st)
+    assert status == 0
+    q = m.q_bits()
+    cache = st.ckv_cache
+    gots, refs = [], []
+    for b in (0, 17, 63):
+        tok = m.topk[b]
+        rows = m.ckv_rows_bits(b, tok)  # [k][576] bf16 bits of the selected tokens
+        mini = np.zeros((len(tok), 1, 1, m.Dqk), np.uint8)
+        oracle.kv_append(rows[:, None, :], mini, np.arange(len(tok), dtype=np.int64), 1, m.ckv_scale)
+        mini = mini.reshape(len(tok), 1, m.Dqk)
+        import torch
+        pages = torch.as_tensor(m.block_tables[b, tok // m.P].astype(np.int64), device="cuda")
+        offs = torch.as_tensor((tok % m.P).astype(np.int64), device="cuda")
+        got_rows = cache[pages, offs].cpu().numpy()
+        assert np.array_equal(got_rows, mini[:, 0, :])
+        for h in (0, 77, 127):
+            ref, ref_lse = oracle.mla_decode_one(q[b, h], mini, np.arange(len(tok), dtype=np.int32),
+                                                 len(tok), None, 1, m.Dv, m.ckv_scale, m.softmax_scale)
+            gots.append(out[b, h])
+            refs.append(ref)
+            assert abs(lse[b, h] - ref_lse) <= 2e-4 + 2e-5 * abs(ref_lse)
+    assert_within_tolerance(np.stack(gots), np.stack(refs), "mla config 4 sampled")
+
+
+def test_validate_tables_flags_each_error_kind():
+    import torch
+    p = pf()
+    B, maxp, P, pages = 3, 4, 16, 10
+    bt = torch.tensor([[0, 1, 2, -1], [3, 4, -1, -1], [5, 6, 7, 8]], dtype=torch.int32, device="cuda")
+    cl = torch.tensor([40, 20, 64], dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    p.validate_tables(bt, cl, P, pages, err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    bt[2, 3] = 10
+    p.validate_tables(bt, cl, P, pages, err)
+    torch.cuda.synchronize()
+    assert err.item() == p.DEVERR["BAD_PAGE"]
+    bt[2, 3] = 8
+    cl[1] = 70
+    p.validate_tables(bt, cl, P, pages, err)
+    torch.cuda.synchronize()
+    assert err.item() & p.DEVERR["BAD_CONTEXT"]
+    cl[1] = 20
+    tk = torch.tensor([[0, 39], [19, 20], [1, -1]], dtype=torch.int32, device="cuda")
+    p.validate_tables(bt, cl, P, pages, err, topk_idx=tk)
+    torch.cuda.synchronize()
+    assert err.item() == p.DEVERR["BAD_TOPK"]
+    sl = torch.tensor([0, 159, 160], dtype=torch.int64, device="cuda")
+    p.validate_tables(bt, cl, P, pages, err, slot_mapping=sl)
+    torch.cuda.synchronize()
+    assert err.item() == p.DEVERR["BAD_SLOT"]
+
+
+def test_device_generator_matches_host_generator():
+    import torch
+    from synth import device as sdev
+    key = gen.make_key(0, gen.TENSOR_V)
+    base = (5 << 21) * 1024 + 12345
+    n = 1_000_003
+    t = torch.empty(n, dtype=torch.int16, device="cuda")
+    word = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sdev.fill_normal_bf16(t, key, base, word)
+    host = gen.normal_bf16(key, np.arange(base, base + n, dtype=np.uint64))
+    assert np.array_equal(t.cpu().numpy().view(np.uint16), host)
+    assert word.item() == int((host & 0x7FFF).max())
