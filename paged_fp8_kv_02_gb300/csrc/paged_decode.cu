@@ -44,7 +44,7 @@ namespace {
 constexpr int kD = 128;
 constexpr int kTile = 16;         // tokens per stage = MMA M (scores) / K (P.V)
 constexpr int kWarps = 4;         // independent worker warps per CTA
-constexpr int kStages = 4;        // TMA ring depth per warp
+constexpr int kStages = 3;        // TMA ring depth per warp
 constexpr int kPartialStride = 132;  // floats per (slot, head): m, l, -, -, o[128]
 constexpr int kMaxGrid = 1024;    // bound on persistent CTAs (sizes the workspace)
 constexpr int kMaxWarps = kMaxGrid * kWarps;
@@ -205,8 +205,16 @@ struct Geometry {
 };
 
 // --------------------------------------------------------------- main kernel
+// Lazy softmax rescale: the running reference max of a head is only raised when
+// a score exceeds it by more than kRescaleLog2 (log2 units); in between, p =
+// 2^(s - ref) stays <= 2^kRescaleLog2, which f16/bf16 P and the fp32
+// accumulators carry with unchanged relative precision.  The reference is a
+// pure re-parametrisation: (ref, l, o) describe the same state as the exact
+// running maximum would.
+constexpr float kRescaleLog2 = 8.f;
+
 template <bool kBf16, int NT>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 2)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const DecodeArgs a) {
   using Geo = Geometry<kBf16>;
@@ -217,13 +225,12 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int g = lane >> 2, t = lane & 3;
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t wbase = smem_base + warp * Geo::kWarpBytes;
-  uint32_t bar[kStages];
-#pragma unroll
-  for (int s = 0; s < kStages; ++s) bar[s] = smem_u32(&bars[warp][s]);
+  uint8_t* const wptr = smem_raw + (smem_base - smem_u32(smem_raw)) + warp * Geo::kWarpBytes;
+  const uint32_t bar0 = smem_u32(&bars[warp][0]);  // stage s: bar0 + 8 s
 
   if (lane == 0) {
 #pragma unroll
-    for (int s = 0; s < kStages; ++s) mbar_init(bar[s], 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
     fence_mbar_init();
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
@@ -236,34 +243,43 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int64_t f_begin = w * W / N, f_end = (w + 1) * W / N;
   if (f_begin >= f_end) return;
 
-  // --- producer: all lanes track the cursor, lane 0 issues.
+  // --- producer: all lanes track the cursor, lane 0 issues.  The block-table
+  // entry of the next tile to issue is loaded one issue ahead, so the TMA issue
+  // never waits on a dependent global load.
   Cursor pc;
   cursor_seek(pc, a, f_begin);
   int64_t f_issue = f_begin;
+  int next_page = 0;
+  auto load_page = [&]() {
+    if (lane == 0 && f_issue < f_end)
+      next_page = __ldg(a.block_tables + (int64_t)pc.b * a.max_pages + (pc.tile * kTile) / a.P);
+  };
+  load_page();
   auto issue = [&](int stage) {
     if (lane == 0) {
       const int tok0 = pc.tile * kTile;
-      const int lp = tok0 / a.P;
-      int page = a.block_tables[(int64_t)pc.b * a.max_pages + lp];
+      int page = next_page;
       if (page < 0 || (int64_t)page >= a.num_pages) {
         atomicOr(a.status, kErrBadPage);
         page = -1;  // the TMA box lands outside the tensor and reads zeros
       }
-      const int row = (page * a.Hkv + pc.kvh) * a.P + (tok0 - lp * a.P);
+      const int row = (page * a.Hkv + pc.kvh) * a.P + tok0 % a.P;
       const uint32_t dst = wbase + stage * Geo::kStageBytes;
-      mbar_arrive_expect_tx(bar[stage], Geo::kStageBytes);
+      const uint32_t bar = bar0 + 8 * stage;
+      mbar_arrive_expect_tx(bar, Geo::kStageBytes);
       if constexpr (kBf16) {
-        tma_load_3d(dst, &tmK, 0, 0, row, bar[stage]);
-        tma_load_3d(dst + 2048, &tmK, 0, 1, row, bar[stage]);
-        tma_load_3d(dst + Geo::kKBytes, &tmV, 0, 0, row, bar[stage]);
-        tma_load_3d(dst + Geo::kKBytes + 2048, &tmV, 0, 1, row, bar[stage]);
+        tma_load_3d(dst, &tmK, 0, 0, row, bar);
+        tma_load_3d(dst + 2048, &tmK, 0, 1, row, bar);
+        tma_load_3d(dst + Geo::kKBytes, &tmV, 0, 0, row, bar);
+        tma_load_3d(dst + Geo::kKBytes + 2048, &tmV, 0, 1, row, bar);
       } else {
-        tma_load_2d(dst, &tmK, 0, row, bar[stage]);
-        tma_load_2d(dst + Geo::kKBytes, &tmV, 0, row, bar[stage]);
+        tma_load_2d(dst, &tmK, 0, row, bar);
+        tma_load_2d(dst + Geo::kKBytes, &tmV, 0, row, bar);
       }
     }
     cursor_next(pc, a);
     ++f_issue;
+    load_page();
   };
 #pragma unroll
   for (int s = 0; s < kStages; ++s)
@@ -272,15 +288,18 @@ __global__ void __launch_bounds__(kWarps * 32)
   // --- consumer state
   Cursor cc;
   cursor_seek(cc, a, f_begin);
-  float m[NT][2], l[NT][2], o[NT][8][4];
+  float mref[NT][2];   // reference max per head (log2 domain, scaled scores)
+  float rthr[NT][2];   // raw-score threshold that forces a rescale
+  float l[NT][2], o[NT][8][4];
   uint32_t qf[NT][8][2];
   int L = 0;
+  int chunk_left = 0;  // tiles left in the current unit, including the current one
   int64_t seg_begin = f_begin;
-  bool timed_out = false;
+  const float sc = a.score_scale;
 
   auto flush = [&](int64_t f_stop) {
-    // f_stop: first flattened tile after this segment
-    const int b = cc.b, kvh = cc.kvh;  // cursor still on the segment's last tile
+    // f_stop: first flattened tile after this segment; cc is on its last tile
+    const int b = cc.b, kvh = cc.kvh;
     const int ntiles = cc.ntiles;
     const int chunk = cc.tile / a.chunk_tiles;
     const int64_t ts = a.tile_start[b];
@@ -333,11 +352,11 @@ __global__ void __launch_bounds__(kWarps * 32)
             *reinterpret_cast<uint4*>(dst + 16 * g) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             *reinterpret_cast<uint4*>(dst + 16 * g + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
           }
-          if (a.lse && g == 0) a.lse[head] = (m[j][e] + __log2f(l[j][e])) * kLn2;
+          if (a.lse && g == 0) a.lse[head] = (mref[j][e] + __log2f(l[j][e])) * kLn2;
         } else {
           float* dst = a.partials + (slot * a.G + hl) * kPartialStride;
           if (g == 0) {
-            dst[0] = m[j][e];
+            dst[0] = mref[j][e];
             dst[1] = l[j][e];
           }
           float4* o4 = reinterpret_cast<float4*>(dst + 4);
@@ -357,9 +376,12 @@ __global__ void __launch_bounds__(kWarps * 32)
 
   auto start_unit = [&]() {
     L = clamp_len(a, cc.b);
+    const int into = cc.tile % a.chunk_tiles;
+    chunk_left = min(a.chunk_tiles - into, cc.ntiles - cc.tile);
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
-      m[j][0] = m[j][1] = -INFINITY;
+      mref[j][0] = mref[j][1] = -INFINITY;
+      rthr[j][0] = rthr[j][1] = -INFINITY;
       l[j][0] = l[j][1] = 0.f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) o[j][i][0] = o[j][i][1] = o[j][i][2] = o[j][i][3] = 0.f;
@@ -398,30 +420,33 @@ __global__ void __launch_bounds__(kWarps * 32)
 
   int stage = 0;
   uint32_t phase = 0;
+  int64_t f_stop_at = f_end;  // first tile not consumed (differs from f_end on a timeout)
+  bool timed_out = false;
+  bool need_start = true;
   for (int64_t f = f_begin; f < f_end; ++f) {
-    if (f == f_begin || cc.tile % a.chunk_tiles == 0) {
-      if (f != f_begin) {
-        // the cursor has moved on: flush used the previous tile's identity
-      }
+    if (need_start) {
       start_unit();
       seg_begin = f;
+      need_start = false;
     }
-    if (!mbar_wait(bar[stage], phase)) {
+    if (!mbar_wait(bar0 + 8 * stage, phase)) {
       timed_out = true;
+      f_stop_at = f;
       break;
     }
-    const uint32_t kb = wbase + stage * Geo::kStageBytes;
-    const uint32_t vb = kb + Geo::kKBytes;
+    const uint8_t* kb = wptr + stage * Geo::kStageBytes;
+    const uint8_t* vb = kb + Geo::kKBytes;
     const int tok0 = cc.tile * kTile;
+    const bool partial = tok0 + kTile > L;  // warp-uniform: only the last tile of a request
 
-    // ---------------- S^T = K . Q^T  (rows: tokens, cols: heads)
+    // ---------------- S^T = K . Q^T  (rows: tokens, cols: heads), raw units
     float s[NT][4];
 #pragma unroll
     for (int j = 0; j < NT; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
     if constexpr (kBf16) {
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
-        const uint32_t hb = kb + h2 * 2048;
+        const uint8_t* hb = kb + h2 * 2048;
         const uint4 x0 = lds128(hb + swz(g, 2 * t)), x1 = lds128(hb + swz(g, 2 * t + 1));
         const uint4 y0 = lds128(hb + swz(g + 8, 2 * t)), y1 = lds128(hb + swz(g + 8, 2 * t + 1));
         const uint32_t xr[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
@@ -442,45 +467,62 @@ __global__ void __launch_bounds__(kWarps * 32)
       const uint32_t yr[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t a0 = e4m3x2_to_f16x2(xr[ks] & 0xFFFFu);
-        const uint32_t a1 = e4m3x2_to_f16x2(yr[ks] & 0xFFFFu);
-        const uint32_t a2 = e4m3x2_to_f16x2(xr[ks] >> 16);
-        const uint32_t a3 = e4m3x2_to_f16x2(yr[ks] >> 16);
+        uint32_t a0, a1, a2, a3;
+        e4m3x4_to_f16x2x2(xr[ks], a0, a2);
+        e4m3x4_to_f16x2x2(yr[ks], a1, a3);
 #pragma unroll
         for (int j = 0; j < NT; ++j) mma_f16(s[j], a0, a1, a2, a3, qf[j][ks][0], qf[j][ks][1]);
       }
     }
 
-    // ---------------- masking + online softmax (exp2 domain)
-    const bool va = tok0 + g < L, vb8 = tok0 + g + 8 < L;
+    // ---------------- mask (last tile only), lazy online softmax (exp2 domain)
+    if (partial) {
+      const bool va = tok0 + g < L, vb8 = tok0 + g + 8 < L;
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        if (!va) s[j][0] = s[j][1] = -INFINITY;
+        if (!vb8) s[j][2] = s[j][3] = -INFINITY;
+      }
+    }
+    bool grow = false;
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+      grow |= (fmaxf(s[j][0], s[j][2]) > rthr[j][0]) | (fmaxf(s[j][1], s[j][3]) > rthr[j][1]);
+    if (__any_sync(0xFFFFFFFFu, grow)) {
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        float mx0 = fmaxf(s[j][0], s[j][2]), mx1 = fmaxf(s[j][1], s[j][3]);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, off));
+        }
+        const float mn0 = fmaxf(mref[j][0], mx0 * sc), mn1 = fmaxf(mref[j][1], mx1 * sc);
+        const float al0 = fast_exp2(mref[j][0] - mn0), al1 = fast_exp2(mref[j][1] - mn1);
+        l[j][0] *= al0;
+        l[j][1] *= al1;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          o[j][i][0] *= al0;
+          o[j][i][1] *= al1;
+          o[j][i][2] *= al0;
+          o[j][i][3] *= al1;
+        }
+        mref[j][0] = mn0;
+        mref[j][1] = mn1;
+        rthr[j][0] = (mn0 + kRescaleLog2) / sc;
+        rthr[j][1] = (mn1 + kRescaleLog2) / sc;
+      }
+    }
     uint32_t pb[NT][2];
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
-      const float s0 = va ? s[j][0] * a.score_scale : -INFINITY;
-      const float s1 = va ? s[j][1] * a.score_scale : -INFINITY;
-      const float s2 = vb8 ? s[j][2] * a.score_scale : -INFINITY;
-      const float s3 = vb8 ? s[j][3] * a.score_scale : -INFINITY;
-      float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, off));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, off));
-      }
-      const float mn0 = fmaxf(m[j][0], mx0), mn1 = fmaxf(m[j][1], mx1);
-      const float al0 = fast_exp2(m[j][0] - mn0), al1 = fast_exp2(m[j][1] - mn1);
-      const float p0 = fast_exp2(s0 - mn0), p1 = fast_exp2(s1 - mn1);
-      const float p2 = fast_exp2(s2 - mn0), p3 = fast_exp2(s3 - mn1);
-      l[j][0] = l[j][0] * al0 + (p0 + p2);
-      l[j][1] = l[j][1] * al1 + (p1 + p3);
-      m[j][0] = mn0;
-      m[j][1] = mn1;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        o[j][i][0] *= al0;
-        o[j][i][1] *= al1;
-        o[j][i][2] *= al0;
-        o[j][i][3] *= al1;
-      }
+      const float p0 = fast_exp2(fmaf(s[j][0], sc, -mref[j][0]));
+      const float p1 = fast_exp2(fmaf(s[j][1], sc, -mref[j][1]));
+      const float p2 = fast_exp2(fmaf(s[j][2], sc, -mref[j][0]));
+      const float p3 = fast_exp2(fmaf(s[j][3], sc, -mref[j][1]));
+      l[j][0] += p0 + p2;
+      l[j][1] += p1 + p3;
       if constexpr (kBf16) {
         pb[j][0] = movmatrix_trans(pack_bf16x2(p0, p1));
         pb[j][1] = movmatrix_trans(pack_bf16x2(p2, p3));
@@ -491,21 +533,20 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
 
     // ---------------- O^T += V^T . P^T  (rows: head_dim, cols: heads)
-    const bool partial = tok0 + kTile > L;
-    const bool v0ok = tok0 + 2 * t < L, v1ok = tok0 + 2 * t + 1 < L;
-    const bool v2ok = tok0 + 2 * t + 8 < L, v3ok = tok0 + 2 * t + 9 < L;
+    // Rows past the context hold arbitrary bytes (even NaN codes); they are
+    // zeroed so that p = 0 cannot meet a NaN in the MMA.
     if constexpr (kBf16) {
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
-        const uint32_t hb = vb + h2 * 2048;
+        const uint8_t* hb = vb + h2 * 2048;
         uint4 r0 = lds128(hb + swz(2 * t, g)), r1 = lds128(hb + swz(2 * t + 1, g));
         uint4 r2 = lds128(hb + swz(2 * t + 8, g)), r3 = lds128(hb + swz(2 * t + 9, g));
         if (partial) {
           const uint4 z = make_uint4(0, 0, 0, 0);
-          if (!v0ok) r0 = z;
-          if (!v1ok) r1 = z;
-          if (!v2ok) r2 = z;
-          if (!v3ok) r3 = z;
+          if (tok0 + 2 * t >= L) r0 = z;
+          if (tok0 + 2 * t + 1 >= L) r1 = z;
+          if (tok0 + 2 * t + 8 >= L) r2 = z;
+          if (tok0 + 2 * t + 9 >= L) r3 = z;
         }
         const uint32_t R0[4] = {r0.x, r0.y, r0.z, r0.w}, R1[4] = {r1.x, r1.y, r1.z, r1.w};
         const uint32_t R2[4] = {r2.x, r2.y, r2.z, r2.w}, R3[4] = {r3.x, r3.y, r3.z, r3.w};
@@ -523,20 +564,19 @@ __global__ void __launch_bounds__(kWarps * 32)
       uint4 r2 = lds128(vb + swz(2 * t + 8, g)), r3 = lds128(vb + swz(2 * t + 9, g));
       if (partial) {
         const uint4 z = make_uint4(0, 0, 0, 0);
-        if (!v0ok) r0 = z;
-        if (!v1ok) r1 = z;
-        if (!v2ok) r2 = z;
-        if (!v3ok) r3 = z;
+        if (tok0 + 2 * t >= L) r0 = z;
+        if (tok0 + 2 * t + 1 >= L) r1 = z;
+        if (tok0 + 2 * t + 8 >= L) r2 = z;
+        if (tok0 + 2 * t + 9 >= L) r3 = z;
       }
       const uint32_t R0[4] = {r0.x, r0.y, r0.z, r0.w}, R1[4] = {r1.x, r1.y, r1.z, r1.w};
       const uint32_t R2[4] = {r2.x, r2.y, r2.z, r2.w}, R3[4] = {r3.x, r3.y, r3.z, r3.w};
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
-        const uint32_t x01 = prmt(R0[i >> 1], R1[i >> 1], sel);
-        const uint32_t x23 = prmt(R2[i >> 1], R3[i >> 1], sel);
-        const uint32_t A0 = e4m3x2_to_f16x2(x01 & 0xFFFFu), A1 = e4m3x2_to_f16x2(x01 >> 16);
-        const uint32_t A2 = e4m3x2_to_f16x2(x23 & 0xFFFFu), A3 = e4m3x2_to_f16x2(x23 >> 16);
+        uint32_t A0, A1, A2, A3;
+        e4m3x4_to_f16x2x2(prmt(R0[i >> 1], R1[i >> 1], sel), A0, A1);
+        e4m3x4_to_f16x2x2(prmt(R2[i >> 1], R3[i >> 1], sel), A2, A3);
 #pragma unroll
         for (int j = 0; j < NT; ++j) mma_f16(o[j][i], A0, A1, A2, A3, pb[j][0], pb[j][1]);
       }
@@ -554,75 +594,123 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
 
     // ---------------- end of a unit segment?
-    const int64_t fn = f + 1;
-    bool boundary = (fn == f_end);
-    if (!boundary) {
-      const int nt = cc.tile + 1;
-      boundary = (nt == cc.ntiles) || (nt % a.chunk_tiles == 0);
+    if (--chunk_left == 0 || f + 1 == f_end) {
+      flush(f + 1);
+      need_start = true;
     }
-    if (boundary) flush(fn);
     cursor_next(cc, a);
   }
 
   if (timed_out) {
     if (lane == 0) atomicOr(a.status, kErrWaitTimeout);
-    // let every copy still in flight land before the CTA's memory is released
-    for (int s = 0; s < kStages; ++s) (void)mbar_wait(bar[s], 0), (void)mbar_wait(bar[s], 1);
+    // let every copy still in flight land (bounded waits) before the CTA's
+    // shared memory is released
+    int st = stage;
+    uint32_t ph = phase;
+    for (int64_t k = 0; k < f_issue - f_stop_at; ++k) {
+      (void)mbar_wait(bar0 + 8 * st, ph);
+      if (++st == kStages) {
+        st = 0;
+        ph ^= 1u;
+      }
+    }
   }
 }
 
 // -------------------------------------------------------------- merge kernel
-// One CTA per (request, KV head); G warps, one per query head, each lane owns
-// four head_dim values.  Combines the fp32 partials of every segment with the
-// log-sum-exp rule: M = max m_k, out = sum 2^{m_k-M} o_k / sum 2^{m_k-M} l_k.
-__global__ void __launch_bounds__(512) merge_kernel(const DecodeArgs a, int64_t N) {
-  const int b = blockIdx.x / a.Hkv, kvh = blockIdx.x % a.Hkv;
-  const int hl = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (hl >= a.G) return;
-  const int64_t head = (int64_t)b * a.Hq + (int64_t)kvh * a.G + hl;
-  uint2* out2 = reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.out) + head * kD) + lane;
+// One CTA per (request, query head): 4 warps split the segments of that head's
+// (request, KV head) between them, each lane owning four head_dim values, and
+// combine them with the log-sum-exp rule
+//   M = max_k m_k,  out = sum_k 2^{m_k-M} o_k / sum_k 2^{m_k-M} l_k.
+constexpr int kMergeWarps = 4;
+
+struct SegRange {
+  int64_t s_u, e_u;
+};
+
+__device__ __forceinline__ SegRange unit_range(const DecodeArgs& a, int64_t ts, int ntiles, int c) {
+  SegRange r;
+  r.s_u = ts + (int64_t)c * a.chunk_tiles;
+  r.e_u = r.s_u + a.chunk_tiles;
+  if (r.e_u > ts + ntiles) r.e_u = ts + ntiles;
+  return r;
+}
+
+__global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const DecodeArgs a, int64_t N) {
+  __shared__ float red_m[kMergeWarps];
+  __shared__ float4 red_o[kMergeWarps][32];
+  __shared__ float red_l[kMergeWarps];
+  const int bh = blockIdx.x;
+  const int b = bh / a.Hq, h = bh % a.Hq;
+  const int kvh = h / a.G, hl = h % a.G;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t head = (int64_t)b * a.Hq + h;
   const int ntiles = ntiles_of(a, b);
+  uint2* out2 = reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.out) + head * kD) + lane;
   if (ntiles == 0) {
-    *out2 = make_uint2(0, 0);
-    if (a.lse && lane == 0) a.lse[head] = -INFINITY;
+    if (warp == 0) {
+      *out2 = make_uint2(0, 0);
+      if (a.lse && lane == 0) a.lse[head] = -INFINITY;
+    }
     return;
   }
   const int64_t W = a.tile_start[a.B];
   const int nchunks = (int)((a.unit_start[b + 1] - a.unit_start[b]) / a.Hkv);
   const int64_t ts = a.tile_start[b] + (int64_t)kvh * ntiles;
   const int64_t u0 = a.unit_start[b] + (int64_t)kvh * nchunks;
-  if (nchunks == 1 && owner_of(ts, W, N) == owner_of(ts + ntiles - 1, W, N)) return;  // direct
+  if (nchunks == 1 && owner_of(ts, W, N) == owner_of(ts + ntiles - 1, W, N)) return;  // written directly
 
+  // pass 1: running maximum over all segments (threads stride over chunks)
   float M = -INFINITY;
-  for (int c = 0; c < nchunks; ++c) {
-    const int64_t s_u = ts + (int64_t)c * a.chunk_tiles;
-    const int64_t e_u = min(s_u + a.chunk_tiles, ts + ntiles);
-    const int64_t w1 = owner_of(e_u - 1, W, N);
-    for (int64_t w = owner_of(s_u, W, N); w <= w1; ++w) {
+  for (int c = threadIdx.x; c < nchunks; c += blockDim.x) {
+    const SegRange r = unit_range(a, ts, ntiles, c);
+    const int64_t w1 = owner_of(r.e_u - 1, W, N);
+    for (int64_t w = owner_of(r.s_u, W, N); w <= w1; ++w) {
       if (w * W / N == (w + 1) * W / N) continue;  // a warp with no tiles wrote nothing
       const int64_t slot = w + u0 + c;
       if (slot < a.capacity) M = fmaxf(M, a.partials[(slot * a.G + hl) * kPartialStride]);
     }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+  if (lane == 0) red_m[warp] = M;
+  __syncthreads();
+  M = red_m[0];
+#pragma unroll
+  for (int k = 1; k < kMergeWarps; ++k) M = fmaxf(M, red_m[k]);
+
+  // pass 2: weighted sums, warps striding over chunks
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float den = 0.f;
-  for (int c = 0; c < nchunks; ++c) {
-    const int64_t s_u = ts + (int64_t)c * a.chunk_tiles;
-    const int64_t e_u = min(s_u + a.chunk_tiles, ts + ntiles);
-    const int64_t w1 = owner_of(e_u - 1, W, N);
-    for (int64_t w = owner_of(s_u, W, N); w <= w1; ++w) {
+  for (int c = warp; c < nchunks; c += kMergeWarps) {
+    const SegRange r = unit_range(a, ts, ntiles, c);
+    const int64_t w1 = owner_of(r.e_u - 1, W, N);
+    for (int64_t w = owner_of(r.s_u, W, N); w <= w1; ++w) {
       if (w * W / N == (w + 1) * W / N) continue;
       const int64_t slot = w + u0 + c;
       if (slot >= a.capacity) continue;
       const float* p = a.partials + (slot * a.G + hl) * kPartialStride;
       const float wt = fast_exp2(p[0] - M);
-      den += wt * p[1];
       const float4 v = reinterpret_cast<const float4*>(p + 4)[lane];
+      den += wt * p[1];
       acc.x += wt * v.x;
       acc.y += wt * v.y;
       acc.z += wt * v.z;
       acc.w += wt * v.w;
     }
+  }
+  red_o[warp][lane] = acc;
+  if (lane == 0) red_l[warp] = den;
+  __syncthreads();
+  if (warp != 0) return;
+#pragma unroll
+  for (int k = 1; k < kMergeWarps; ++k) {
+    const float4 v = red_o[k][lane];
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+    den += red_l[k];
   }
   const float inv = a.out_scale / den;
   *out2 = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
@@ -666,7 +754,7 @@ int launch_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const DecodeAr
   if (grid > kMaxGrid) grid = kMaxGrid;
   plan_kernel<<<1, 1024, 0, stream>>>(a);
   kern<<<grid, kWarps * 32, Geo::kSmemBytes, stream>>>(tmK, tmV, a);
-  merge_kernel<<<a.B * a.Hkv, a.G * 32, 0, stream>>>(a, (int64_t)grid * kWarps);
+  merge_kernel<<<a.B * a.Hq, kMergeWarps * 32, 0, stream>>>(a, (int64_t)grid * kWarps);
   return check_cuda("paged_decode launch");
 }
 

@@ -94,7 +94,7 @@ def setup_paged(w: PagedWorkload, append, bf16_cache: bool = False, chunk_tokens
     slots)` writes rows into the caches (the product's append call)."""
     import torch
     dev = "cuda"
-    if w.k_scale is None or w.v_scale is None:
+    if not bf16_cache and (w.k_scale is None or w.v_scale is None):
         if scales_on_device:
             w.k_scale = scale_from_amax(device_amax_paged(w, "k"))
             w.v_scale = scale_from_amax(device_amax_paged(w, "v"))
