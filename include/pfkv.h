@@ -154,6 +154,36 @@ PFKV_API int pfkv_paged_decode_attn(void *out, const void *q, const void *k_cach
                            int kv_split_tokens, void *workspace, size_t workspace_bytes,
                            float *lse_out, pfkv_stream_t stream);
 
+/* paged_decode_attn_noalloc -- the same computation as pfkv_paged_decode_attn
+ * for callers that cannot allocate device memory where decode runs (an engine
+ * that reserves all device memory up front and hands out every byte from its
+ * own pool, or a per-token path that cannot afford the synchronisation and
+ * latency of cudaMalloc).  The source pages have no counterpart of this call;
+ * it exists for such callers only.
+ *  - Scratch is a fixed 64 MiB array inside the library's device module,
+ *    present on every GPU that loads the library until the process exits.
+ *    A call whose pfkv_paged_decode_workspace_size(batch, num_q_heads,
+ *    num_kv_heads, head_dim, kv_split_tokens, max_total_chunks) exceeds 64 MiB
+ *    fails with PFKV_ERR_WORKSPACE and enqueues nothing.
+ *  - The call allocates nothing (no cudaMalloc, no allocating library call).
+ *    Its first call on a device looks up the array's device address on that
+ *    device (cudaGetSymbolAddress); make that first call before any stream
+ *    capture begins.
+ *  - All calls share the one array.  Two calls whose work overlaps on the GPU
+ *    (different streams without ordering between them) race on it; order them.
+ *  - status_out: optional device int32 that receives the device status word
+ *    (PFKV_DEVERR_* bits) of this call, copied after the decode on `stream`.
+ *  - Other arguments, layouts and errors as pfkv_paged_decode_attn. */
+PFKV_API int pfkv_paged_decode_attn_noalloc(void *out, const void *q, const void *k_cache,
+                                            const void *v_cache, pfkv_cache_dtype cache_dtype,
+                                            const int32_t *block_tables, int max_pages_per_seq,
+                                            const int32_t *context_lens, int batch, int num_q_heads,
+                                            int num_kv_heads, int head_dim, int page_size,
+                                            int64_t num_pages, float k_scale, float v_scale,
+                                            float softmax_scale, int kv_split_tokens,
+                                            int64_t max_total_chunks, float *lse_out,
+                                            int32_t *status_out, pfkv_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* mla_decode_attn -- MLA absorbed-latent decode over one shared e4m3 latent
  * row per token, optionally restricted to a top-k token list.

@@ -19,7 +19,8 @@ from . import _build
 
 __all__ = [
     "PfkvError", "load", "lib_path", "kv_append_fp8", "kv_append_bf16",
-    "paged_decode_workspace_size", "paged_decode_attn", "mla_decode_workspace_size",
+    "paged_decode_workspace_size", "paged_decode_attn", "paged_decode_attn_noalloc",
+    "mla_decode_workspace_size",
     "mla_decode_attn", "validate_tables", "workspace_status", "last_error", "version",
     "CACHE_FP8_E4M3", "CACHE_BF16", "DEVERR",
 ]
@@ -64,6 +65,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             "pfkv_paged_decode_workspace_size": (sz, [i32, i32, i32, i32, i32, i64]),
             "pfkv_paged_decode_attn": (i32, [vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, i32,
                                              i64, f32, f32, f32, i32, vp, sz, vp, vp]),
+            "pfkv_paged_decode_attn_noalloc": (i32, [vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32,
+                                                     i32, i64, f32, f32, f32, i32, i64, vp, vp, vp]),
             "pfkv_mla_decode_workspace_size": (sz, [i32, i32, i32, i32]),
             "pfkv_mla_decode_attn": (i32, [vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32,
                                            i64, f32, f32, vp, sz, vp, vp]),
@@ -158,6 +161,26 @@ def paged_decode_attn(out, q, k_cache, v_cache, block_tables, context_lens, k_sc
                                        workspace.numel(), _ptr(lse_out), _stream(stream))
     _check("paged_decode_attn", rc)
     return workspace
+
+
+def paged_decode_attn_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, k_scale: float,
+                              v_scale: float, softmax_scale: float, kv_split_tokens: int = 0,
+                              max_total_chunks: int = 0, lse_out=None, status_out=None, stream=None):
+    """paged_decode_attn without a workspace: for callers that cannot allocate
+    device memory on the decode path.  The library's fixed 64 MiB device
+    scratch is used instead (shared by all calls; order calls that could
+    overlap).  status_out: optional int32 device tensor of one element."""
+    import torch
+    B, Hq, D = q.shape
+    pages, Hkv, P, _ = k_cache.shape
+    dt = CACHE_BF16 if k_cache.dtype == torch.bfloat16 else CACHE_FP8_E4M3
+    rc = load().pfkv_paged_decode_attn_noalloc(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), dt,
+                                               _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+                                               B, Hq, Hkv, D, P, pages, float(k_scale), float(v_scale),
+                                               float(softmax_scale), int(kv_split_tokens),
+                                               int(max_total_chunks), _ptr(lse_out), _ptr(status_out),
+                                               _stream(stream))
+    _check("paged_decode_attn_noalloc", rc)
 
 
 def mla_decode_workspace_size(batch: int, num_heads: int, d_latent: int = 512, topk: int = 0) -> int:

@@ -871,3 +871,82 @@ int pfkv_paged_decode_attn(void* out, const void* q, const void* k_cache, const 
 }
 
 }  // extern "C"
+
+// --------------------------------------------------- no-allocation variant
+// Some callers cannot allocate device memory at the point where they run
+// decode: a serving engine that reserves the whole device up front and owns
+// every byte through its own pool, or a per-token path that must not take the
+// synchronisation and latency of cudaMalloc.  For them the scratch that
+// paged_decode_attn needs lives in one file-scope device array of fixed size
+// that is part of the loaded module; each GPU that loads this library keeps
+// it until the process exits.
+#include <mutex>
+
+namespace pfkv {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = (size_t)64 << 20;  // 64 MiB
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device.  The host-side
+// name of the array is only a stand-in: the address must come from the
+// runtime, once per device, with that device current.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return check_cuda("paged_decode_attn_noalloc: cudaGetDevice");
+  if (dev < 0 || dev >= kNoAllocMaxDevices)
+    return fail(PFKV_ERR_UNSUPPORTED, "paged_decode_attn_noalloc: device %d beyond %d", dev,
+                kNoAllocMaxDevices);
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr)
+      return fail(PFKV_ERR_CUDA, "paged_decode_attn_noalloc: cudaGetSymbolAddress failed: %s",
+                  cudaGetErrorString(e));
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return PFKV_OK;
+}
+
+}  // namespace
+}  // namespace pfkv
+
+extern "C" int pfkv_paged_decode_attn_noalloc(
+    void* out, const void* q, const void* k_cache, const void* v_cache, pfkv_cache_dtype cache_dtype,
+    const int32_t* block_tables, int max_pages_per_seq, const int32_t* context_lens, int batch,
+    int num_q_heads, int num_kv_heads, int head_dim, int page_size, int64_t num_pages, float k_scale,
+    float v_scale, float softmax_scale, int kv_split_tokens, int64_t max_total_chunks, float* lse_out,
+    int32_t* status_out, pfkv_stream_t stream) {
+  using namespace pfkv;
+  clear_error();
+  const size_t need = pfkv_paged_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
+                                                       kv_split_tokens, max_total_chunks);
+  if (need == 0)
+    return fail(PFKV_ERR_INVALID_ARG, "paged_decode_attn_noalloc: bad batch or head counts");
+  if (need > kNoAllocScratchBytes)
+    return fail(PFKV_ERR_WORKSPACE,
+                "paged_decode_attn_noalloc: this call needs %zu bytes of scratch; the built-in "
+                "scratch holds %zu bytes (64 MiB) -- use pfkv_paged_decode_attn with a workspace",
+                need, kNoAllocScratchBytes);
+  void* ws = nullptr;
+  int rc = noalloc_scratch(&ws);
+  if (rc != PFKV_OK) return rc;
+  // The decode path itself zeroes the status word at the start of the
+  // scratch and writes every other scratch byte it later reads, so the
+  // contents left by the previous call need no clearing here.
+  rc = pfkv_paged_decode_attn(out, q, k_cache, v_cache, cache_dtype, block_tables, max_pages_per_seq,
+                              context_lens, batch, num_q_heads, num_kv_heads, head_dim, page_size,
+                              num_pages, k_scale, v_scale, softmax_scale, kv_split_tokens, ws,
+                              kNoAllocScratchBytes, lse_out, stream);
+  if (rc != PFKV_OK || status_out == nullptr || batch == 0) return rc;
+  if (cudaMemcpyAsync(status_out, ws, sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                      reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return check_cuda("paged_decode_attn_noalloc: status copy");
+  return PFKV_OK;
+}
