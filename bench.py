@@ -232,26 +232,30 @@ class MlaStep:
 
 
 def time_events(fn, iters, flush=None):
-    """Median device time (s) of fn over iters launches, L2 flushed before each."""
+    """Median device time (s) of fn: iters launches enqueued back to back (the
+    host stays ahead of the GPU), L2 flushed before each by READING a buffer
+    larger than L2 (a write flush would leave dirty lines for the timed kernel
+    to write back), one sync at the end."""
     import torch
-    ts = []
+    evs = []
+    sink = torch.empty((), dtype=torch.float32, device="cuda") if flush is not None else None
     for _ in range(iters):
         if flush is not None:
-            flush.zero_()
+            torch.sum(flush, dim=0, out=sink)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         fn()
         b.record()
-        torch.cuda.synchronize()
-        ts.append(a.elapsed_time(b) * 1e-3)
-    return statistics.median(ts)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) * 1e-3 for a, b in evs)
 
 
 def other_workloads(pf, peak_gbs, peak_tf, iters=10):
     import torch
     import synth
     res = {}
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")  # > L2 (129 MB)
+    flush = torch.ones(128 << 20, dtype=torch.float32, device="cuda")  # 512 MB > L2 (129 MB)
 
     def paged(name, w, bf16=False):
         s = PagedStep(pf, w, bf16_cache=bf16)

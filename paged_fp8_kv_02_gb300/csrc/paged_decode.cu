@@ -61,7 +61,8 @@ struct DecodeArgs {
   int64_t* tile_start;  // [B+1] exclusive prefix of Hkv * ceil(L_b / 16)
   int64_t* unit_start;  // [B+1] exclusive prefix of Hkv * chunks_b
   float* partials;      // [capacity][G][kPartialStride]
-  int64_t capacity;
+  int64_t capacity;     // partial slots (and the bound on units)
+  int64_t nwarps;       // warps of the tile kernel's grid
   int B, Hq, Hkv, G, P, max_pages;
   int64_t num_pages;
   int chunk_tiles;      // tiles per split unit
@@ -146,6 +147,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeArgs a) {
   if (threadIdx.x == 0) {
     a.tile_start[a.B] = carry_tiles;
     a.unit_start[a.B] = carry_units;
+    if (carry_units > a.capacity) atomicOr(a.status, kErrWorkspace);
   }
 }
 
@@ -618,103 +620,163 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 2)
 }
 
 // -------------------------------------------------------------- merge kernel
-// One CTA per (request, query head): 4 warps split the segments of that head's
-// (request, KV head) between them, each lane owning four head_dim values, and
-// combine them with the log-sum-exp rule
+// One CTA per (request, KV head).  Its segments -- one per (chunk, covering
+// warp) -- are enumerated in batches of chunks (threads find each chunk's first
+// covering warp and segment count; a block scan numbers the segments in shared
+// memory).  The G heads' partial states of one segment are contiguous, so a
+// warp reads all of them with coalesced loads; warps split the segments and
+// fold them with an online maximum per head, and warp e then combines the
+// warps' states of head e with the log-sum-exp rule
 //   M = max_k m_k,  out = sum_k 2^{m_k-M} o_k / sum_k 2^{m_k-M} l_k.
-constexpr int kMergeWarps = 4;
+constexpr int kMergeWarps = 8;
+constexpr int kMergeThreads = kMergeWarps * 32;
+constexpr int kMergeBatch = kMergeThreads;  // chunks enumerated per batch
 
-struct SegRange {
-  int64_t s_u, e_u;
-};
-
-__device__ __forceinline__ SegRange unit_range(const DecodeArgs& a, int64_t ts, int ntiles, int c) {
-  SegRange r;
-  r.s_u = ts + (int64_t)c * a.chunk_tiles;
-  r.e_u = r.s_u + a.chunk_tiles;
-  if (r.e_u > ts + ntiles) r.e_u = ts + ntiles;
-  return r;
-}
-
-__global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const DecodeArgs a, int64_t N) {
-  __shared__ float red_m[kMergeWarps];
-  __shared__ float4 red_o[kMergeWarps][32];
-  __shared__ float red_l[kMergeWarps];
-  const int bh = blockIdx.x;
-  const int b = bh / a.Hq, h = bh % a.Hq;
-  const int kvh = h / a.G, hl = h % a.G;
+// kHeads query heads of one (request, KV head) per CTA: 1 for many small CTAs
+// (MHA, or long requests cut into many chunks), 8 to read a segment's heads
+// with one coalesced sweep (GQA without chunking).
+template <int kMergeHeads>
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeArgs a) {
+  __shared__ float4 red_o[kMergeWarps][kMergeHeads][32];
+  __shared__ float red_m[kMergeWarps][kMergeHeads], red_l[kMergeWarps][kMergeHeads];
+  __shared__ int32_t seg_base[kMergeBatch + 1];
+  __shared__ int32_t first_w[kMergeBatch];
+  __shared__ int16_t seg_chunk[kMergeBatch + kMaxWarps];  // batch-local chunk of each segment
+  __shared__ int32_t scan_tmp[kMergeWarps];
+  const int groups = (a.G + kMergeHeads - 1) / kMergeHeads;
+  const int bk = blockIdx.x / groups;
+  const int g_lo = (blockIdx.x % groups) * kMergeHeads;  // first head of this CTA
+  const int g_hi = min(a.G, g_lo + kMergeHeads);
+  const int b = bk / a.Hkv, kvh = bk % a.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t head = (int64_t)b * a.Hq + h;
+  const int64_t head0 = (int64_t)b * a.Hq + (int64_t)kvh * a.G;
   const int ntiles = ntiles_of(a, b);
-  uint2* out2 = reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.out) + head * kD) + lane;
   if (ntiles == 0) {
-    if (warp == 0) {
-      *out2 = make_uint2(0, 0);
-      if (a.lse && lane == 0) a.lse[head] = -INFINITY;
+    for (int e = g_lo + warp; e < g_hi; e += kMergeWarps) {
+      reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.out) + (head0 + e) * kD)[lane] = make_uint2(0, 0);
+      if (a.lse && lane == 0) a.lse[head0 + e] = -INFINITY;
     }
     return;
   }
-  const int64_t W = a.tile_start[a.B];
+  const int64_t W = a.tile_start[a.B], N = a.nwarps;
   const int nchunks = (int)((a.unit_start[b + 1] - a.unit_start[b]) / a.Hkv);
   const int64_t ts = a.tile_start[b] + (int64_t)kvh * ntiles;
   const int64_t u0 = a.unit_start[b] + (int64_t)kvh * nchunks;
-  if (nchunks == 1 && owner_of(ts, W, N) == owner_of(ts + ntiles - 1, W, N)) return;  // written directly
+  if (nchunks == 1 && owner_of(ts, W, N) == owner_of(ts + ntiles - 1, W, N)) return;  // direct
 
-  // pass 1: running maximum over all segments (threads stride over chunks)
-  float M = -INFINITY;
-  for (int c = threadIdx.x; c < nchunks; c += blockDim.x) {
-    const SegRange r = unit_range(a, ts, ntiles, c);
-    const int64_t w1 = owner_of(r.e_u - 1, W, N);
-    for (int64_t w = owner_of(r.s_u, W, N); w <= w1; ++w) {
-      if (w * W / N == (w + 1) * W / N) continue;  // a warp with no tiles wrote nothing
-      const int64_t slot = w + u0 + c;
-      if (slot < a.capacity) M = fmaxf(M, a.partials[(slot * a.G + hl) * kPartialStride]);
+  {
+    const int e0 = g_lo;
+    const int ne = g_hi - g_lo;
+    float M[kMergeHeads], den[kMergeHeads];
+    float4 acc[kMergeHeads];
+#pragma unroll
+    for (int e = 0; e < kMergeHeads; ++e) {
+      M[e] = -INFINITY;
+      den[e] = 0.f;
+      acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int c0 = 0; c0 < nchunks; c0 += kMergeBatch) {
+      const int nb = min(kMergeBatch, nchunks - c0);
+      // ---- enumerate this batch's segments
+      int32_t nseg = 0;
+      if (threadIdx.x < nb) {
+        const int c = c0 + threadIdx.x;
+        const int64_t s_c = ts + (int64_t)c * a.chunk_tiles;
+        const int64_t e_c = min(s_c + (int64_t)a.chunk_tiles, ts + ntiles);
+        const int64_t first = owner_of(s_c, W, N), last = owner_of(e_c - 1, W, N);
+        // W >= N: every warp owns tiles, owners are consecutive; W < N: one tile per warp
+        nseg = (int32_t)(W >= N ? last - first + 1 : e_c - s_c);
+        first_w[threadIdx.x] = (int32_t)first;
+      }
+      int32_t x = nseg;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) scan_tmp[warp] = x;
+      __syncthreads();
+      int32_t pre = 0;
+      for (int k = 0; k < warp; ++k) pre += scan_tmp[k];
+      if (threadIdx.x < nb) {
+        seg_base[threadIdx.x] = pre + x - nseg;
+        for (int32_t k = 0; k < nseg; ++k)
+          if (pre + x - nseg + k < kMergeBatch + kMaxWarps)
+            seg_chunk[pre + x - nseg + k] = (int16_t)threadIdx.x;
+      }
+      if (threadIdx.x == kMergeThreads - 1) seg_base[nb] = pre + x;
+      __syncthreads();
+      const int32_t total = min(seg_base[nb], (int32_t)(kMergeBatch + kMaxWarps));
+      // ---- fold: warps stride over segments; lane l owns head_dim 4l..4l+3
+      for (int32_t sg = warp; sg < total; sg += kMergeWarps) {
+        const int lo = seg_chunk[sg];
+        const int32_t k = sg - seg_base[lo];
+        const int c = c0 + lo;
+        const int64_t w = W >= N ? (int64_t)first_w[lo] + k
+                                 : owner_of(ts + (int64_t)c * a.chunk_tiles + k, W, N);
+        const int64_t slot = w + u0 + c;
+        if (slot >= a.capacity) continue;
+        const float* p = a.partials + (slot * a.G + e0) * kPartialStride;
+        float mk[kMergeHeads], lk[kMergeHeads];
+        float4 ok[kMergeHeads];
+#pragma unroll
+        for (int e = 0; e < kMergeHeads; ++e) {
+          if (e < ne) {
+            mk[e] = p[e * kPartialStride];
+            lk[e] = p[e * kPartialStride + 1];
+            ok[e] = reinterpret_cast<const float4*>(p + e * kPartialStride + 4)[lane];
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < kMergeHeads; ++e) {
+          if (e >= ne) continue;
+          const float Mn = fmaxf(M[e], mk[e]);
+          const float al = fast_exp2(M[e] - Mn), wt = fast_exp2(mk[e] - Mn);
+          den[e] = den[e] * al + wt * lk[e];
+          acc[e].x = acc[e].x * al + wt * ok[e].x;
+          acc[e].y = acc[e].y * al + wt * ok[e].y;
+          acc[e].z = acc[e].z * al + wt * ok[e].z;
+          acc[e].w = acc[e].w * al + wt * ok[e].w;
+          M[e] = Mn;
+        }
+      }
+      __syncthreads();  // seg_base / first_w / seg_chunk are rewritten by the next batch
+    }
+    // ---- combine the warps' states; warp e finishes head e0 + e
+#pragma unroll
+    for (int e = 0; e < kMergeHeads; ++e) {
+      red_o[warp][e][lane] = acc[e];
+      if (lane == 0) {
+        red_m[warp][e] = M[e];
+        red_l[warp][e] = den[e];
+      }
+    }
+    __syncthreads();
+    if (warp < ne) {
+      const int e = warp;
+      float Mt = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < kMergeWarps; ++k) Mt = fmaxf(Mt, red_m[k][e]);
+      float4 tot = make_float4(0.f, 0.f, 0.f, 0.f);
+      float dt = 0.f;
+#pragma unroll
+      for (int k = 0; k < kMergeWarps; ++k) {
+        if (red_m[k][e] == -INFINITY) continue;
+        const float wt = fast_exp2(red_m[k][e] - Mt);
+        const float4 v = red_o[k][e][lane];
+        tot.x += wt * v.x;
+        tot.y += wt * v.y;
+        tot.z += wt * v.z;
+        tot.w += wt * v.w;
+        dt += wt * red_l[k][e];
+      }
+      const int64_t head = head0 + e0 + e;
+      const float inv = a.out_scale / dt;
+      reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.out) + head * kD)[lane] =
+          make_uint2(pack_bf16x2(tot.x * inv, tot.y * inv), pack_bf16x2(tot.z * inv, tot.w * inv));
+      if (a.lse && lane == 0) a.lse[head] = (Mt + __log2f(dt)) * kLn2;
     }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
-  if (lane == 0) red_m[warp] = M;
-  __syncthreads();
-  M = red_m[0];
-#pragma unroll
-  for (int k = 1; k < kMergeWarps; ++k) M = fmaxf(M, red_m[k]);
-
-  // pass 2: weighted sums, warps striding over chunks
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float den = 0.f;
-  for (int c = warp; c < nchunks; c += kMergeWarps) {
-    const SegRange r = unit_range(a, ts, ntiles, c);
-    const int64_t w1 = owner_of(r.e_u - 1, W, N);
-    for (int64_t w = owner_of(r.s_u, W, N); w <= w1; ++w) {
-      if (w * W / N == (w + 1) * W / N) continue;
-      const int64_t slot = w + u0 + c;
-      if (slot >= a.capacity) continue;
-      const float* p = a.partials + (slot * a.G + hl) * kPartialStride;
-      const float wt = fast_exp2(p[0] - M);
-      const float4 v = reinterpret_cast<const float4*>(p + 4)[lane];
-      den += wt * p[1];
-      acc.x += wt * v.x;
-      acc.y += wt * v.y;
-      acc.z += wt * v.z;
-      acc.w += wt * v.w;
-    }
-  }
-  red_o[warp][lane] = acc;
-  if (lane == 0) red_l[warp] = den;
-  __syncthreads();
-  if (warp != 0) return;
-#pragma unroll
-  for (int k = 1; k < kMergeWarps; ++k) {
-    const float4 v = red_o[k][lane];
-    acc.x += v.x;
-    acc.y += v.y;
-    acc.z += v.z;
-    acc.w += v.w;
-    den += red_l[k];
-  }
-  const float inv = a.out_scale / den;
-  *out2 = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
-  if (a.lse && lane == 0) a.lse[head] = (M + __log2f(den)) * kLn2;
 }
 
 // ------------------------------------------------------------------- host
@@ -723,6 +785,9 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct WsLayout {
   size_t tile_off, unit_off, part_off;
 };
+
+// Bytes per partial slot: the fp32 states of G heads.
+size_t slot_bytes(int G) { return (size_t)G * kPartialStride * sizeof(float); }
 
 WsLayout ws_layout(int B) {
   WsLayout L;
@@ -744,17 +809,30 @@ int launch_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const DecodeAr
       return check_cuda("paged_decode set smem attribute");
     attr_set = true;
   }
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * 32, Geo::kSmemBytes) !=
-      cudaSuccess)
-    return check_cuda("paged_decode occupancy");
-  if (per_sm < 1) per_sm = 1;
-  int grid = device_sm_count() * per_sm;
-  if (grid < 1) grid = 1;
-  if (grid > kMaxGrid) grid = kMaxGrid;
-  plan_kernel<<<1, 1024, 0, stream>>>(a);
-  kern<<<grid, kWarps * 32, Geo::kSmemBytes, stream>>>(tmK, tmV, a);
-  merge_kernel<<<a.B * a.Hq, kMergeWarps * 32, 0, stream>>>(a, (int64_t)grid * kWarps);
+  // persistent grid: every SM filled with resident CTAs (cached per device)
+  static int grid_of_device[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return check_cuda("paged_decode cudaGetDevice");
+  int grid = (dev >= 0 && dev < 64) ? grid_of_device[dev] : 0;
+  if (grid == 0) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * 32, Geo::kSmemBytes) !=
+        cudaSuccess)
+      return check_cuda("paged_decode occupancy");
+    if (per_sm < 1) per_sm = 1;
+    grid = device_sm_count() * per_sm;
+    if (grid < 1) grid = 1;
+    if (grid > kMaxGrid) grid = kMaxGrid;
+    if (dev >= 0 && dev < 64) grid_of_device[dev] = grid;
+  }
+  DecodeArgs args = a;
+  args.nwarps = (int64_t)grid * kWarps;
+  plan_kernel<<<1, 1024, 0, stream>>>(args);
+  kern<<<grid, kWarps * 32, Geo::kSmemBytes, stream>>>(tmK, tmV, args);
+  if (a.chunk_tiles < (1 << 30) || a.G < 8)
+    merge_kernel<1><<<a.B * a.Hq, kMergeThreads, 0, stream>>>(args);
+  else
+    merge_kernel<8><<<a.B * a.Hkv * ((a.G + 7) / 8), kMergeThreads, 0, stream>>>(args);
   return check_cuda("paged_decode launch");
 }
 
@@ -772,7 +850,7 @@ size_t pfkv_paged_decode_workspace_size(int batch, int num_q_heads, int num_kv_h
   if (kv_split_tokens > 0 && max_total_chunks > units) units = max_total_chunks;
   const pfkv::WsLayout L = pfkv::ws_layout(batch);
   const int64_t slots = pfkv::kMaxWarps + (int64_t)num_kv_heads * units;
-  return L.part_off + (size_t)slots * G * pfkv::kPartialStride * sizeof(float);
+  return L.part_off + (size_t)slots * pfkv::slot_bytes(G) + 1024;
 }
 
 int pfkv_paged_decode_attn(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -813,9 +891,11 @@ int pfkv_paged_decode_attn(void* out, const void* q, const void* k_cache, const 
     return fail(PFKV_ERR_INVALID_ARG, "paged_decode: misaligned pointer");
   const WsLayout L = ws_layout(batch);
   const size_t per_slot = (size_t)G * kPartialStride * sizeof(float);
-  if (workspace_bytes < L.part_off + per_slot * ((size_t)kMaxWarps + (size_t)num_kv_heads * batch))
+  if (workspace_bytes <
+      L.part_off + slot_bytes(G) * ((size_t)kMaxWarps + (size_t)num_kv_heads * batch) + 1024)
     return fail(PFKV_ERR_WORKSPACE, "paged_decode: workspace of %zu bytes is too small",
                 workspace_bytes);
+  const int64_t cap = (int64_t)((workspace_bytes - L.part_off - 1024) / slot_bytes(G));
 
   DecodeArgs a;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -828,7 +908,8 @@ int pfkv_paged_decode_attn(void* out, const void* q, const void* k_cache, const 
   a.tile_start = reinterpret_cast<int64_t*>(ws + L.tile_off);
   a.unit_start = reinterpret_cast<int64_t*>(ws + L.unit_off);
   a.partials = reinterpret_cast<float*>(ws + L.part_off);
-  a.capacity = (int64_t)((workspace_bytes - L.part_off) / per_slot);
+  a.capacity = cap;
+  a.nwarps = 0;
   a.B = batch;
   a.Hq = num_q_heads;
   a.Hkv = num_kv_heads;
