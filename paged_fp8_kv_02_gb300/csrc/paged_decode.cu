@@ -890,7 +890,6 @@ int pfkv_paged_decode_attn(void* out, const void* q, const void* k_cache, const 
       (lse_out && !aligned(lse_out, 4)))
     return fail(PFKV_ERR_INVALID_ARG, "paged_decode: misaligned pointer");
   const WsLayout L = ws_layout(batch);
-  const size_t per_slot = (size_t)G * kPartialStride * sizeof(float);
   if (workspace_bytes <
       L.part_off + slot_bytes(G) * ((size_t)kMaxWarps + (size_t)num_kv_heads * batch) + 1024)
     return fail(PFKV_ERR_WORKSPACE, "paged_decode: workspace of %zu bytes is too small",
