@@ -148,13 +148,28 @@ def barrier(ws):
         dist.barrier()
 
 
-def max_over_ranks(x, ws, device):
+def max_over_ranks(x, ws, device=None):
+    """Maximum of a per-rank float over all ranks (gloo: CPU tensor; nccl: device)."""
     if ws == 1:
         return x
     import torch
     import torch.distributed as dist
+    if dist.get_backend() == "gloo":
+        device = "cpu"
     t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, ws, device=None):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    if dist.get_backend() == "gloo":
+        device = "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
     return float(t.item())
 
 
@@ -388,36 +403,46 @@ def oracle_baseline(w, n_requests, steps=1, warmup=0):
             "seconds_per_step": dt, "query_tokens_per_s": n_requests / dt}
 
 
-def scale_sample_workload(w):
-    """The headline workload's per-tensor scales, from the device generator when
-    a GPU is present, else from the host generator (identical bits)."""
+def reference_scales(w, n_requests):
+    """Per-tensor scales of the headline workload for the reference arm: the
+    full-tensor amax from the device generator when a GPU is present (the same
+    scales the native arm uses), else the amax of the sampled requests only
+    (host generator; the full tensor would take minutes on the host)."""
+    from synth.workloads import scale_from_amax
     try:
         import torch
         if torch.cuda.is_available():
             from synth import device as sdev
-            from synth.workloads import scale_from_amax
             w.k_scale = scale_from_amax(sdev.device_amax_paged(w, "k"))
             w.v_scale = scale_from_amax(sdev.device_amax_paged(w, "v"))
-            return w
+            return "full-tensor amax (device generator)"
     except OSError:
         pass
-    w.set_scales_host()
-    return w
+    from synth import gen
+    m = {"k": 0, "v": 0}
+    for which in ("k", "v"):
+        key = w.key_k if which == "k" else w.key_v
+        for b in range(n_requests):
+            for a, z, base in w.kv_runs(b, 0, int(w.context_lens[b])):
+                m[which] = max(m[which], int((gen.normal_bf16_range(key, base, (z - a) * w.Hkv * w.D)
+                                              & np.uint16(0x7FFF)).max()))
+    from synth.workloads import amax_from_bits
+    w.k_scale = scale_from_amax(amax_from_bits(m["k"]))
+    w.v_scale = scale_from_amax(amax_from_bits(m["v"]))
+    return "amax of the sampled requests (host generator; no GPU present)"
 
 
 # ---------------------------------------------------------------------- main
 def run_reference(args, rank, ws):
+    """The reference arm: the CPU oracle (plain C, fp64) on this host's cores,
+    on a bounded sample of the headline workload.  Under torchrun only rank 0
+    runs and prints; the other ranks exit without work."""
     import synth
     if rank != 0:
         return
     w = synth.config(HEADLINE)
-    if w.k_scale is None:
-        # the reference arm needs no GPU: the host generator gives the same scales
-        try:
-            scale_sample_workload(w)
-        except Exception:
-            w.set_scales_host()
     n_req = args.oracle_requests
+    scales = reference_scales(w, n_req)
     res = oracle_baseline(w, n_req, steps=max(1, args.steps), warmup=min(1, args.warmup))
     line = {
         "impl": "reference", "metric": METRIC, "value": round(res["value"], 4), "unit": "GB/s",
@@ -426,7 +451,7 @@ def run_reference(args, rank, ws):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": synth.CONFIG_NAMES[HEADLINE], "batch": w.B, "q_heads": w.Hq,
                    "kv_heads": w.Hkv, "head_dim": w.D, "context": int(w.context_lens[0]), "page_size": w.P,
-                   "cache": "e4m3", "sample_requests": n_req},
+                   "cache": "e4m3", "sample_requests": n_req, "scales": scales},
         "query_tokens_per_s": round(res["query_tokens_per_s"], 3),
         "cpu_baseline": {k: res[k] for k in ("value", "unit", "cores", "kind", "sample")},
         "e2e": {"value": round(res["value"], 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -20,6 +20,11 @@ Generator (both sides):
 """
 from __future__ import annotations
 
+import ctypes
+import os
+import subprocess
+import threading
+
 import numpy as np
 
 GOLDEN = np.uint64(0x9E3779B97F4A7C15)
@@ -85,8 +90,80 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
-def normal_bf16(key: int, idx: np.ndarray) -> np.ndarray:
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_HOST_SRC = os.path.join(_HERE, "csrc", "synth_host.c")
+_HOST_LIB = os.path.join(_HERE, "_build", "libsynth_host.so")
+_host = None
+_host_lock = threading.Lock()
+
+
+def build_host() -> str:
+    """Compile the host C twin of this generator (gcc, strict IEEE)."""
+    os.makedirs(os.path.dirname(_HOST_LIB), exist_ok=True)
+    if os.path.exists(_HOST_LIB) and os.path.getmtime(_HOST_LIB) >= os.path.getmtime(_HOST_SRC):
+        return _HOST_LIB
+    tmp = _HOST_LIB + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+                    "-o", tmp, _HOST_SRC], check=True)
+    os.replace(tmp, _HOST_LIB)
+    return _HOST_LIB
+
+
+def _host_lib():
+    global _host
+    with _host_lock:
+        if _host is None:
+            try:
+                L = ctypes.CDLL(build_host())
+            except (OSError, subprocess.CalledProcessError):
+                _host = False
+                return None
+            L.synth_normal_bf16_idx.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_int64]
+            L.synth_normal_bf16_range.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint64,
+                                                  ctypes.c_int64]
+            L.synth_normal_bf16_rows.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint64,
+                                                 ctypes.c_int64, ctypes.c_int64, ctypes.c_uint64]
+            _host = L
+    return _host or None
+
+
+def normal_bf16_numpy(key: int, idx: np.ndarray) -> np.ndarray:
     return f32_to_bf16_bits(normal_f32(key, idx))
+
+
+def normal_bf16(key: int, idx: np.ndarray) -> np.ndarray:
+    """bf16 normals at counters idx (C twin when available; same bits)."""
+    idx = np.ascontiguousarray(np.asarray(idx, dtype=np.uint64))
+    L = _host_lib()
+    if L is None:
+        return normal_bf16_numpy(key, idx)
+    out = np.empty(idx.shape, dtype=np.uint16)
+    L.synth_normal_bf16_idx(out.ctypes.data_as(ctypes.c_void_p), np.uint64(key), idx.ctypes.data_as(ctypes.c_void_p),
+                            idx.size)
+    return out
+
+
+def normal_bf16_range(key: int, base: int, n: int) -> np.ndarray:
+    """bf16 normals at counters base .. base + n - 1."""
+    L = _host_lib()
+    if L is None:
+        return normal_bf16_numpy(key, np.arange(base, base + n, dtype=np.uint64))
+    out = np.empty(n, dtype=np.uint16)
+    L.synth_normal_bf16_range(out.ctypes.data_as(ctypes.c_void_p), np.uint64(key), np.uint64(base), n)
+    return out
+
+
+def normal_bf16_rows(key: int, base: int, rows: int, row_len: int, row_stride: int) -> np.ndarray:
+    """[rows][row_len] bf16 normals; row r covers counters base + r*row_stride + (0..row_len-1)."""
+    L = _host_lib()
+    if L is None:
+        idx = (np.uint64(base) + np.arange(rows, dtype=np.uint64)[:, None] * np.uint64(row_stride)
+               + np.arange(row_len, dtype=np.uint64)[None, :])
+        return normal_bf16_numpy(key, idx.reshape(-1)).reshape(rows, row_len)
+    out = np.empty((rows, row_len), dtype=np.uint16)
+    L.synth_normal_bf16_rows(out.ctypes.data_as(ctypes.c_void_p), np.uint64(key), np.uint64(base), rows, row_len,
+                             np.uint64(row_stride))
+    return out
 
 
 def uniform_u64(key: int, idx: np.ndarray) -> np.ndarray:

@@ -134,20 +134,20 @@ class PagedWorkload:
 
     def kv_bits(self, which: str, b: int, t0: int, t1: int) -> np.ndarray:
         key = self.key_k if which == "k" else self.key_v
-        return gen.normal_bf16(key, self.kv_index(b, t0, t1).reshape(-1).astype(np.uint64)).reshape(
-            t1 - t0, self.Hkv, self.D)
+        parts = [gen.normal_bf16_range(key, base, (z - a) * self.Hkv * self.D) for a, z, base in self.kv_runs(b, t0, t1)]
+        flat = np.concatenate(parts) if parts else np.zeros(0, np.uint16)
+        return flat.reshape(t1 - t0, self.Hkv, self.D)
 
     def kv_head_bits(self, which: str, b: int, kvh: int, t0: int, t1: int) -> np.ndarray:
         """[t1-t0][D] bf16 bits of one KV head (cheaper than kv_bits for long runs)."""
         key = self.key_k if which == "k" else self.key_v
-        t = np.arange(t0, t1, dtype=np.int64)
-        tok = (self.src_request(b, t) << TOKEN_SHIFT) + t
-        idx = (tok * self.Hkv + kvh)[:, None] * self.D + np.arange(self.D, dtype=np.int64)[None, :]
-        return gen.normal_bf16(key, idx.reshape(-1).astype(np.uint64)).reshape(t1 - t0, self.D)
+        parts = [gen.normal_bf16_rows(key, base + kvh * self.D, z - a, self.D, self.Hkv * self.D)
+                 for a, z, base in self.kv_runs(b, t0, t1)]
+        return np.concatenate(parts) if parts else np.zeros((0, self.D), np.uint16)
 
     def q_bits(self) -> np.ndarray:
         n = self.B * self.Hq * self.D
-        return gen.normal_bf16(self.key_q, np.arange(n, dtype=np.uint64)).reshape(self.B, self.Hq, self.D)
+        return gen.normal_bf16_range(self.key_q, 0, n).reshape(self.B, self.Hq, self.D)
 
     # ----------------------------------------------------------------- slots
     def slots(self, b: int, t0: int, t1: int) -> np.ndarray:
@@ -177,10 +177,10 @@ class PagedWorkload:
         m = 0
         for b in range(self.B):
             t0 = self.shared_tokens if 0 < b < self.shared_requests else 0
-            idx = self.kv_index(b, t0, int(self.context_lens[b])).reshape(-1).astype(np.uint64)
-            bits = gen.normal_bf16(key, idx) & np.uint16(0x7FFF)
-            if bits.size:
-                m = max(m, int(bits.max()))
+            for a, z, base in self.kv_runs(b, t0, int(self.context_lens[b])):
+                bits = gen.normal_bf16_range(key, base, (z - a) * self.Hkv * self.D) & np.uint16(0x7FFF)
+                if bits.size:
+                    m = max(m, int(bits.max()))
         return amax_from_bits(m)
 
     def set_scales_host(self):
@@ -261,9 +261,7 @@ class MlaWorkload:
         return ((b << TOKEN_SHIFT) + t0) * self.Dqk
 
     def ckv_bits(self, b: int, t0: int, t1: int) -> np.ndarray:
-        base = self.ckv_run_base(b, t0)
-        n = (t1 - t0) * self.Dqk
-        return gen.normal_bf16(self.key_c, np.arange(base, base + n, dtype=np.uint64)).reshape(
+        return gen.normal_bf16_range(self.key_c, self.ckv_run_base(b, t0), (t1 - t0) * self.Dqk).reshape(
             t1 - t0, 1, self.Dqk)
 
     def ckv_rows_bits(self, b: int, tokens: np.ndarray) -> np.ndarray:
@@ -272,8 +270,7 @@ class MlaWorkload:
         return gen.normal_bf16(self.key_c, idx.reshape(-1).astype(np.uint64)).reshape(len(t), self.Dqk)
 
     def q_bits(self) -> np.ndarray:
-        n = self.B * self.H * self.Dqk
-        return gen.normal_bf16(self.key_q, np.arange(n, dtype=np.uint64)).reshape(self.B, self.H, self.Dqk)
+        return gen.normal_bf16_range(self.key_q, 0, self.B * self.H * self.Dqk).reshape(self.B, self.H, self.Dqk)
 
     def slots(self, b: int, t0: int, t1: int) -> np.ndarray:
         t = np.arange(t0, t1, dtype=np.int64)

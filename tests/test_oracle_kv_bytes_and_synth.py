@@ -110,3 +110,27 @@ def test_slots_follow_block_tables_and_shared_tokens_map_to_request_0():
     assert not np.array_equal(w.kv_bits("k", 7, 2048, 2050), w.kv_bits("k", 0, 2048, 2050))
     runs = list(w.kv_runs(3, 2040, 2060))
     assert len(runs) == 2 and runs[0][1] == 2048
+
+
+def test_host_c_generator_twin_matches_numpy_definition():
+    key = gen.make_key(3, gen.TENSOR_V)
+    idx = (np.arange(200_000, dtype=np.uint64) * np.uint64(977)) + np.uint64(1 << 40)
+    assert np.array_equal(gen.normal_bf16(key, idx), gen.normal_bf16_numpy(key, idx))
+    assert np.array_equal(gen.normal_bf16_range(key, 5, 3000),
+                          gen.normal_bf16_numpy(key, np.arange(5, 3005, dtype=np.uint64)))
+    rows = gen.normal_bf16_rows(key, 11, 40, 16, 1000)
+    ref = gen.normal_bf16_numpy(key, (np.uint64(11) + np.arange(40, dtype=np.uint64)[:, None] * np.uint64(1000)
+                                      + np.arange(16, dtype=np.uint64)[None, :]).reshape(-1)).reshape(40, 16)
+    assert np.array_equal(rows, ref)
+
+
+def test_workload_rows_follow_the_documented_counter_layout():
+    w = synth.config(3)
+    b, t0, t1 = 20, 100, 131
+    idx = (((np.int64(b) << 21) + np.arange(t0, t1))[:, None] * (w.Hkv * w.D)
+           + np.arange(w.Hkv * w.D)[None, :]).astype(np.uint64)
+    ref = gen.normal_bf16_numpy(w.key_k, idx.reshape(-1)).reshape(t1 - t0, w.Hkv, w.D)
+    assert np.array_equal(w.kv_bits("k", b, t0, t1), ref)
+    assert np.array_equal(w.kv_head_bits("k", b, 5, t0, t1), ref[:, 5, :])
+    # shared prefix tokens of request 3 are request 0's
+    assert np.array_equal(w.kv_head_bits("v", 3, 2, 2040, 2056)[:8], w.kv_head_bits("v", 0, 2, 2040, 2048))
