@@ -82,6 +82,7 @@ __device__ __forceinline__ int clamp_len(const DecodeArgs& a, int b) {
 __global__ void __launch_bounds__(1024) plan_kernel(const DecodeArgs a) {
   __shared__ int64_t warp_tiles[32], warp_units[32];
   __shared__ int64_t carry_tiles, carry_units;
+  grid_launch_dependents();  // the tile kernel may start its prologue now
   if (threadIdx.x == 0) {
     *a.status = 0;
     carry_tiles = 0;
@@ -238,6 +239,8 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 2)
     prefetch_tensormap(&tmV);
   }
   __syncwarp();
+  grid_launch_dependents();  // the merge kernel may be scheduled as CTAs retire
+  grid_dependency_wait();    // the plan's prefix sums are complete and visible
 
   const int64_t N = (int64_t)gridDim.x * kWarps;
   const int64_t w = (int64_t)blockIdx.x * kWarps + warp;
@@ -643,6 +646,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeArgs a
   __shared__ int32_t first_w[kMergeBatch];
   __shared__ int16_t seg_chunk[kMergeBatch + kMaxWarps];  // batch-local chunk of each segment
   __shared__ int32_t scan_tmp[kMergeWarps];
+  grid_dependency_wait();  // every partial state of the tile kernel is visible
   const int groups = (a.G + kMergeHeads - 1) / kMergeHeads;
   const int bk = blockIdx.x / groups;
   const int g_lo = (blockIdx.x % groups) * kMergeHeads;  // first head of this CTA
@@ -828,11 +832,31 @@ int launch_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const DecodeAr
   DecodeArgs args = a;
   args.nwarps = (int64_t)grid * kWarps;
   plan_kernel<<<1, 1024, 0, stream>>>(args);
-  kern<<<grid, kWarps * 32, Geo::kSmemBytes, stream>>>(tmK, tmV, args);
-  if (a.chunk_tiles < (1 << 30) || a.G < 8)
-    merge_kernel<1><<<a.B * a.Hq, kMergeThreads, 0, stream>>>(args);
-  else
-    merge_kernel<8><<<a.B * a.Hkv * ((a.G + 7) / 8), kMergeThreads, 0, stream>>>(args);
+  // the tile kernel and the merge kernel are launched as programmatic
+  // dependents, so their launch overlaps the tail of the kernel before them;
+  // each waits (griddepcontrol.wait) before reading what that kernel wrote
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = Geo::kSmemBytes;
+  if (cudaLaunchKernelEx(&cfg, kern, tmK, tmV, args) != cudaSuccess) return check_cuda("paged_decode launch");
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = 0;
+  cudaError_t e;
+  if (a.chunk_tiles < (1 << 30) || a.G < 8) {
+    cfg.gridDim = dim3(a.B * a.Hq);
+    e = cudaLaunchKernelEx(&cfg, merge_kernel<1>, args);
+  } else {
+    cfg.gridDim = dim3(a.B * a.Hkv * ((a.G + 7) / 8));
+    e = cudaLaunchKernelEx(&cfg, merge_kernel<8>, args);
+  }
+  if (e != cudaSuccess) return check_cuda("paged_decode merge launch");
   return check_cuda("paged_decode launch");
 }
 
