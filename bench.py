@@ -595,8 +595,46 @@ def measure_e2e(pf, s, iters):
             "query_tokens_per_s": round(w.B / dt, 1)}
 
 
+PROFILE_CASES = {
+    # name: (description, factory)
+    "mha_b8_l8192": "MHA, 8 requests x 48 heads x 8192 tokens, page 16 (a quarter of the headline batch)",
+    "gqa_prefix_b64": "GQA 64/8 heads, 64 requests, lognormal contexts, 16 share a 2048-token prefix",
+    "long_b2_l262144": "GQA 64/8 heads, 2 requests x 262144 tokens, page 64, 4096-token chunks",
+    "mla_b16_topk2048": "MLA 128 heads x 576, 16 requests x 65536 tokens, top-k 2048, page 64",
+}
+
+
+def run_profile_case(name):
+    """Set up one small case, run its decode call three times and exit: the
+    program that ncu captures (inputs larger than L2, about 1 GB on the device)."""
+    import torch
+    import paged_fp8_kv_02_gb300 as pf
+    import synth
+    pf.load()
+    if name == "mha_b8_l8192":
+        s = PagedStep(pf, synth.PagedWorkload("mha_b8", B=8, Hq=48, Hkv=48, D=128, P=16,
+                                              context_lens=np.full(8, 8192), n_new=1))
+    elif name == "gqa_prefix_b64":
+        s = PagedStep(pf, synth.config(3))
+    elif name == "long_b2_l262144":
+        s = PagedStep(pf, synth.PagedWorkload("long_b2", B=2, Hq=64, Hkv=8, D=128, P=64,
+                                              context_lens=np.full(2, 262144), n_new=8, kv_split_tokens=4096))
+    elif name == "mla_b16_topk2048":
+        s = MlaStep(pf, synth.MlaWorkload("mla_b16", B=16, H=128, context_lens=np.full(16, 65536), topk_n=2048,
+                                          P=64))
+    else:
+        raise SystemExit(f"unknown profile case {name}; choose from {sorted(PROFILE_CASES)}")
+    s.append()
+    for _ in range(3):
+        s.decode()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": name, "what": PROFILE_CASES[name], "status": "ok"}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default=None,
+                    help="run one small case three times and exit (for ncu)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
@@ -607,6 +645,11 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.profile_case:
+        import torch
+        torch.cuda.set_device(0)
+        run_profile_case(args.profile_case)
+        return
     rank, ws, local = dist_init(args)
     if args.impl == "reference":
         run_reference(args, rank, ws)

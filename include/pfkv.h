@@ -231,6 +231,13 @@ PFKV_API int pfkv_validate_tables(const int32_t *block_tables, int max_pages_per
  * synchronising `stream`.  Returns PFKV_OK, or PFKV_ERR_CUDA. */
 PFKV_API int pfkv_workspace_status(const void *workspace, int32_t *status, pfkv_stream_t stream);
 
+/* Diagnostic: one thread waits, with the bounded wait every kernel uses, on a
+ * barrier that nothing completes; after about one second it gives up and
+ * writes PFKV_DEVERR_WAIT_TIMEOUT to *d_status (device int32).  Shows that an
+ * expired wait ends the kernel with a status instead of hanging the GPU.  The
+ * pages have no counterpart of this call. */
+PFKV_API int pfkv_selftest_barrier_timeout(int32_t *d_status, pfkv_stream_t stream);
+
 /* Message describing the last error on the calling thread ("" if none). */
 PFKV_API const char *pfkv_last_error(void);
 

@@ -21,7 +21,8 @@ __all__ = [
     "PfkvError", "load", "lib_path", "kv_append_fp8", "kv_append_bf16",
     "paged_decode_workspace_size", "paged_decode_attn", "paged_decode_attn_noalloc",
     "mla_decode_workspace_size",
-    "mla_decode_attn", "validate_tables", "workspace_status", "last_error", "version",
+    "mla_decode_attn", "validate_tables", "workspace_status", "selftest_barrier_timeout", "last_error",
+    "version",
     "CACHE_FP8_E4M3", "CACHE_BF16", "DEVERR",
 ]
 
@@ -72,6 +73,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                            i64, f32, f32, vp, sz, vp, vp]),
             "pfkv_validate_tables": (i32, [vp, i32, vp, i32, i32, i64, vp, i32, vp, i32, vp, vp]),
             "pfkv_workspace_status": (i32, [vp, vp, vp]),
+            "pfkv_selftest_barrier_timeout": (i32, [vp, vp]),
             "pfkv_last_error": (ctypes.c_char_p, []),
             "pfkv_version": (ctypes.c_char_p, []),
         }
@@ -216,6 +218,11 @@ def validate_tables(block_tables, context_lens, page_size: int, num_pages: int, 
                                      page_size, num_pages, _ptr(topk_idx), k, _ptr(slot_mapping), ns,
                                      _ptr(err_word), _stream(stream))
     _check("validate_tables", rc)
+
+
+def selftest_barrier_timeout(status, stream=None):
+    """Run the bounded-wait self-test; `status` is an int32 device tensor of one element."""
+    _check("selftest_barrier_timeout", load().pfkv_selftest_barrier_timeout(_ptr(status), _stream(stream)))
 
 
 def workspace_status(workspace, stream=None) -> int:

@@ -4,6 +4,7 @@
 #include <string.h>
 
 #include "pfkv_internal.h"
+#include "pfkv_ptx.cuh"
 
 namespace pfkv {
 
@@ -55,9 +56,29 @@ int encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, cuuint32_t ra
   return PFKV_OK;
 }
 
+namespace {
+// One thread waits, through the same bounded wait the kernels use, on an
+// mbarrier that nothing ever arrives on; the wait gives up after about one
+// second and the kernel reports the timeout bit.
+__global__ void barrier_timeout_selftest_kernel(int32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  fence_mbar_init();
+  *status = mbar_wait(b, 0) ? 0 : kErrWaitTimeout;
+}
+}  // namespace
+
 }  // namespace pfkv
 
 extern "C" {
+
+int pfkv_selftest_barrier_timeout(int32_t* d_status, pfkv_stream_t stream) {
+  pfkv::clear_error();
+  if (d_status == nullptr) return pfkv::fail(PFKV_ERR_INVALID_ARG, "selftest: null status pointer");
+  pfkv::barrier_timeout_selftest_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(d_status);
+  return pfkv::check_cuda("selftest launch");
+}
 
 const char* pfkv_last_error(void) { return pfkv::g_msg; }
 

@@ -153,3 +153,16 @@ def test_device_generator_matches_host_generator():
     host = gen.normal_bf16(key, np.arange(base, base + n, dtype=np.uint64))
     assert np.array_equal(t.cpu().numpy().view(np.uint16), host)
     assert word.item() == int((host & 0x7FFF).max())
+
+
+def test_bounded_barrier_wait_times_out_with_a_status():
+    """A wait on a barrier that nothing completes gives up (about one second)
+    and reports the timeout bit; the context stays usable afterwards."""
+    import torch
+    p = pf()
+    st = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    p.selftest_barrier_timeout(st)
+    torch.cuda.synchronize()
+    assert st.item() == p.DEVERR["WAIT_TIMEOUT"]
+    x = torch.arange(10, device="cuda").sum()  # the context still works
+    assert x.item() == 45
