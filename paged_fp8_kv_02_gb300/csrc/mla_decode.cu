@@ -1,5 +1,6 @@
 // mla_decode.cu -- MLA absorbed-latent decode over one shared e4m3 latent row
-// per token, optionally restricted to a top-k token list.
+// per token, optionally restricted to a top-k token list, on the fifth-
+// generation tensor cores (tcgen05, accumulators in tensor memory).
 //
 // kLLM article (快手万擎大模型推理成本和性能优化实践), §5.1.1: DSA selects the
 // top-k historical tokens that take part in attention and MLA stores a
@@ -7,49 +8,104 @@
 // (it cannot be split by head the way GQA KV heads can).  Absorbed reading: the
 // whole Dqk = 576-wide row is the key, its first 512 entries are the value.
 //
-// Kernel: one CTA per (request, 32 query heads).  A producer warp gathers the
-// 64 latent rows of each token tile straight from their pages with bulk copies
-// (cp.async.bulk, one 576-byte row each) into a ring of shared-memory stages;
-// the consumer warps run both contractions on warp-level tensor-core MMA
-// (m16n8k16, f32 accumulate) with the e4m3 -> f16 conversion fused into the
-// fragment build:
-//   S[32 heads x 64 tokens] = Q . C^T  (K = 576; the head_dim sum is permuted
-//                                       consistently in Q and in C's fragments)
-//   O[32 heads x 512]      += P . C[:, 0:512]
-// with an exp2 online softmax whose reference maximum is only raised when a
-// score exceeds it by more than 2^8 (an exact re-parametrisation).  Sixteen
-// consumer warps: for the scores each owns a 16-head x 8-token tile, for the
-// output 32 columns of all 32 heads.
+// Per request a cluster of two CTAs.  The fp32 output O[128 heads][512] alone
+// fills one SM's tensor memory, so CTA r keeps O[:, 256 r .. 256 r + 255] and
+// the pair splits the score contraction instead of repeating it: CTA r
+// contracts latent columns 256 r .. 256 r + 255 (Q held in tensor memory as
+// the A operand) and rope columns 512 + 32 r .. 512 + 32 r + 31 (Q in shared
+// memory).  The partial score tiles cross between the pair through
+// distributed shared memory, one bulk copy per tile, as 16-bit fixed point
+// over the row's range in the tile (an fp32 row minimum, a power-of-two step
+// with range / step <= 65535, one u16 code per token: error <= range / 65535
+// in log2 units).  Each CTA adds its own exact fp32 partial to the peer's
+// decoded one, runs the online softmax over the sum and multiplies its P tile
+// into its own output columns; each half is normalised by its own running sum.
+//
+// Per 32-token tile, with four tiles in flight (scores and P in tensor
+// memory, the widened latent tile in shared memory):
+//   producer warp   resolves the cache rows of 1024 list positions at a time
+//                   (top-k entry -> block table, cached in shared memory ->
+//                   row) into a double-buffered shared table;
+//   loader warps    (8 rows of every tile each) gather this CTA's 288 bytes of
+//                   each row with 16-byte asynchronous copies five tiles
+//                   ahead (the rate of random row gathers grows with the
+//                   number of issuing warps), then widen their rows to f16
+//                   (exact) in the 128-byte-swizzled layout the MMA reads,
+//                   K-major for the scores and MN-major for the output;
+//   MMA thread      S[128 x 32] = Q . C^T (18 K steps), and two tiles later
+//                   O += P . C[:, own 256] (2 K steps, N = 256);
+//   sender warps    read S, encode it and copy it to the peer;
+//   softmax warps   (one TMEM lane per head) add the peer's partial, take the
+//                   exp2 online softmax with a reference maximum that moves
+//                   only when a score exceeds it by more than 2^8 (then O is
+//                   rescaled in tensor memory) and store P as f16 pairs over
+//                   the score columns, where the MMA reads it as its A operand;
+//   ack warp        tells the peer when a received tile has been read.
+// Every wait is bounded; a wait that gives up sets PFKV_DEVERR_WAIT_TIMEOUT
+// and the CTA still runs to its end, so the pair always meets at the final
+// cluster barrier and frees its tensor memory.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
 
 #include "pfkv_internal.h"
 #include "pfkv_ptx.cuh"
+#include "pfkv_tc.cuh"
 
 namespace pfkv {
 namespace {
 
 constexpr int kDqk = 576, kDv = 512;
-constexpr int kHeads = 32;                    // query heads per CTA (2 MMA row tiles)
-constexpr int kTok = 64;                      // tokens per tile
-constexpr int kStages = 3;                    // latent-row ring depth
-constexpr int kConsumers = 16;                // MMA warps
-constexpr int kThreads = (kConsumers + 1) * 32;
-constexpr int kRowBytes = 592;                // staged row stride (576 + 16: bank spread)
-constexpr int kStageBytes = kTok * kRowBytes;
-constexpr int kQStride = kDqk * 2 + 16;       // bytes per staged Q row (f16, padded)
-constexpr int kPStride = kTok * 2 + 16;       // bytes per P row (f16, padded)
+constexpr int kRows = 128;            // MMA rows: query heads, zero-padded
+constexpr int kTok = 32;              // tokens per tile
+constexpr int kBufs = 4;              // tiles in flight: score/P buffers and widened latent tiles
+constexpr int kAhead = 5;             // tiles a loader warp gathers ahead of the one it widens
+constexpr int kXDepth = 3;            // exchange buffers per direction
+constexpr int kLatCols = 256;         // latent columns one CTA contracts (and outputs)
+constexpr int kRopeCols = 32;         // rope columns one CTA contracts
+constexpr int kRowCopy = kLatCols + kRopeCols;  // 288 staged bytes per token row
+constexpr int kRowChunks = kRowCopy / 16;        // 18; chunk c of staged row r sits at (c + r) % 18
+constexpr int kLoadRows = kTok / 4;               // rows per loader warp
+constexpr int kSlotBytes = kLoadRows * kRowCopy;   // one loader warp's rows of one tile, e4m3
+constexpr int kStageBytes = 4 * (kAhead + 1) * kSlotBytes;  // all loader warps' staging
+constexpr int kAtomBytes = kTok * 128;           // [32 tokens][64 f16 columns], 128-byte swizzle
+constexpr int kCBufBytes = 5 * kAtomBytes;       // 4 latent atoms + the rope atom
+constexpr int kQRopeBytes = kRows * 128;         // [128 heads][64 rope columns] f16
+constexpr int kXCodes = kRows * kTok * 2;        // exchanged partial scores: [128][32] u16 codes
+constexpr int kXBytes = kXCodes + kRows * 4 + kRows;  // + [128] fp32 row minima + [128] step exponents
+constexpr int kRowTab = 1024;                    // list positions per half of the row table
+constexpr int kRowTabTiles = kRowTab / kTok;
+constexpr int kBtCache = 2048;                   // block-table entries cached in shared memory
+
+constexpr int kOffQRope = 0;
+constexpr int kOffC = kOffQRope + kQRopeBytes;
+constexpr int kOffStage = kOffC + kBufs * kCBufBytes;
+constexpr int kOffSend = kOffStage + kStageBytes;
+constexpr int kOffRecv = kOffSend + kXDepth * kXBytes;
+constexpr int kOffRows = kOffRecv + kXDepth * kXBytes;
+constexpr int kOffBt = kOffRows + 2 * kRowTab * 4;
+constexpr int kOffBars = kOffBt + kBtCache * 4;
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemO = 0;        // 256 columns: this CTA's output columns, fp32
+constexpr uint32_t kTmemS = 256;      // 4 x 32 columns: scores, then P (f16 pairs) in the first 16
+constexpr uint32_t kTmemQ = 384;      // 128 columns: this CTA's 256 latent Q columns as f16 pairs
+
+constexpr int kLoadWarp0 = 0;         // warps 0-3
+constexpr int kSoftWarp0 = 4;         // warps 4-7: TMEM lane quadrants 0-3
+constexpr int kSendWarp0 = 8;         // warps 8-11: TMEM lane quadrants 0-3
+constexpr int kProdWarp = 12;
+constexpr int kMmaWarp = 13;
+constexpr int kAckWarp = 14;
+constexpr int kThreads = 15 * 32;
+constexpr int kPvLag = 2;             // the MMA thread issues O += P(j - 2) C(j - 2) after S(j)
+
+constexpr uint32_t kIdescQK = tc::idesc_f16(kRows, kTok, false);
+constexpr uint32_t kIdescPV = tc::idesc_f16(kRows, kLatCols, true);
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.f;
-
-constexpr int kSmemQ = kHeads * kQStride;                 // 37,376
-constexpr int kSmemRows = kStages * kStageBytes;          // 113,664
-constexpr int kSmemP = kHeads * kPStride;                 //  4,608
-constexpr int kMaxRows = 2048;                            // rows resolved per pass
-constexpr int kSmemSrc = kMaxRows * 8;                    // 16,384: row offsets (or -1)
-constexpr size_t kSmemBytes = (size_t)kSmemQ + kSmemRows + kSmemP + kSmemSrc + 128;
 
 struct MlaArgs {
   __nv_bfloat16* out;
@@ -66,53 +122,74 @@ struct MlaArgs {
   float out_scale;    // ckv_scale
 };
 
-// head_dim index of fragment k-index kk (0..15) in k-step s (0..35): within each
-// 128-wide block thread t of a quad owns 32 contiguous bytes (16 in the last,
-// 64-wide block), four per k-step: k = 2t, 2t+1, 2t+8, 2t+9 -> bytes 0..3.
-__device__ __forceinline__ int perm_d(int s, int kk) {
-  const int t = (kk & 7) >> 1;
-  const int j = (kk & 1) | ((kk >> 3) << 1);
-  if (s < 32) return 128 * (s >> 3) + 32 * t + 4 * (s & 7) + j;
-  return 512 + 16 * t + 4 * (s - 32) + j;
-}
+struct __align__(8) Bars {
+  uint64_t rows_ready[2], rows_free[2];  // the two halves of the row table
+  uint64_t cfull[kBufs], sfull[kBufs], pfull[kBufs], pvdone[kBufs];
+  uint64_t sent[kBufs];      // the sender warps have read the scores of a tile
+  uint64_t qready;
+  uint64_t xfull[kXDepth];   // the peer's partial scores of a tile have landed
+  uint64_t xack[kXDepth];    // the peer has read a tile this CTA sent
+  uint64_t rdone[kXDepth];   // this CTA's softmax warps have read a received tile
+  uint32_t cmask[kBufs];  // bit i: token row i of the tile takes part (byte w from loader warp w)
+  uint8_t vmask[4][kAhead + 1];  // loader warp w: which of its rows of a staged tile take part
+  uint32_t tmem_base;
+};
+constexpr size_t kSmemBytes = (size_t)kOffBars + sizeof(Bars) + 1024;  // + alignment of the base to 1024
+static_assert(kSmemBytes <= 232448, "shared memory over the per-CTA limit");
 
-__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                            uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr)
-               : "memory");
+// 16-byte global -> shared copy through L2 only; completion is tracked per
+// thread by commit groups.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most kAhead of this thread's committed groups are still landing.
+__device__ __forceinline__ void cp_async_wait_ahead() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(kAhead) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
-__device__ __forceinline__ void bulk_row(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) { return pack_f16x2(bf16_lo(v), bf16_hi(v)); }
+
+// Shared memory of this CTA -> shared memory of a peer CTA, completion
+// counted in bytes on the peer's mbarrier.
+__device__ __forceinline__ void bulk_to_peer(uint32_t dst_cluster, uint32_t src, uint32_t bytes, uint32_t bar_cluster) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst_cluster),
+      "r"(src), "r"(bytes), "r"(bar_cluster)
       : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+__device__ __forceinline__ uint4 lds128_u32(uint32_t addr) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(addr) : "memory");
+  return r;
 }
 
-__device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
+// The four sender warps only.
+__device__ __forceinline__ void sender_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ uint4 ldg_nc(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const MlaArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* qs = smem;                                  // [32][kQStride] f16, permuted head_dim
-  uint8_t* rows = smem + kSmemQ;                       // [kStages][64][kRowBytes] e4m3
-  uint8_t* ps = rows + kSmemRows;                      // [32][kPStride] f16
-  int64_t* srcs = reinterpret_cast<int64_t*>(ps + kSmemP);  // [kMaxRows] cache row, -1 if none
-  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages];
-  __shared__ int valid[kStages][kTok];
-  __shared__ float red_max[2][8][16], red_l[2][8][16], alpha[kHeads];
-  __shared__ int grow_flag;
+// Byte offset of 16-byte unit c (0..3) of row t in an exchange buffer
+// ([128][64 bytes], rows paired per 128-byte line): conflict-free for eight
+// consecutive rows.
+__device__ __forceinline__ uint32_t xunit(int t, int c) { return t * 64 + 16 * (c ^ ((t >> 1) & 3)); }
 
-  const int b = blockIdx.x, h0 = blockIdx.y * kHeads;
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_decode_kernel(const MlaArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  Bars& bs = *reinterpret_cast<Bars*>(smem + kOffBars);
+
+  const uint32_t rank = tc::cluster_ctarank();
+  const uint32_t peer = rank ^ 1u;
+  const int b = blockIdx.x >> 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
 
   int L = a.context_lens[b];
   if (L < 0) L = 0;
@@ -121,291 +198,436 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const MlaArgs a
   const int ntiles = (n + kTok - 1) / kTok;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&full_bar[s]), 1);
-      mbar_init(smem_u32(&empty_bar[s]), kConsumers);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bs.rows_ready[i]), 1);
+      mbar_init(smem_u32(&bs.rows_free[i]), 4);
+    }
+    for (int i = 0; i < kBufs; ++i) {
+      mbar_init(smem_u32(&bs.cfull[i]), 4);
+      mbar_init(smem_u32(&bs.sfull[i]), 1);
+      mbar_init(smem_u32(&bs.pfull[i]), 4);
+      mbar_init(smem_u32(&bs.pvdone[i]), 1);
+      mbar_init(smem_u32(&bs.sent[i]), 4);
+    }
+    mbar_init(smem_u32(&bs.qready), 4);
+    for (int i = 0; i < kXDepth; ++i) {
+      mbar_init(smem_u32(&bs.xfull[i]), 1);
+      mbar_init(smem_u32(&bs.xack[i]), 1);
+      mbar_init(smem_u32(&bs.rdone[i]), 4);
     }
     fence_mbar_init();
   }
-  // stage Q (bf16 -> f16) with the head_dim permutation used by the fragments
-  for (int i = threadIdx.x; i < kHeads * kDqk; i += kThreads) {
-    const int hr = i / kDqk, c = i % kDqk;  // c = 16 s + kk
-    const int d = perm_d(c >> 4, c & 15);
-    const int head = h0 + hr;
-    float v = 0.f;
-    if (head < a.H)
-      v = __bfloat162float(a.q[((int64_t)b * a.H + head) * kDqk + d]);
-    reinterpret_cast<__half*>(qs + hr * kQStride)[c] = __float2half_rn(v);
+  if (warp == kMmaWarp) {
+    tc::tmem_alloc(smem_u32(&bs.tmem_base), kTmemCols);
+    tc::tmem_relinquish();
   }
-  __syncthreads();
+  tc::fence_before_sync();
+  tc::cluster_sync();  // both CTAs' barriers initialised before any remote arrival
+  tc::fence_after_sync();
+  const uint32_t tmem = bs.tmem_base;
+  bool to = false;  // this thread gave up a wait
 
-  bool timed_out = false;
-  if (warp == kConsumers) {
+  if (warp == kProdWarp) {
     // ------------------------------------------------------------ producer
-    // Rows are resolved (top-k index -> block-table entry -> cache row) for
-    // up to kMaxRows tokens at a time with independent loads from all lanes,
-    // so the gather loop below only waits for free stages and issues copies.
-    uint32_t ph_empty = 1;  // a fresh barrier's preceding phase counts as complete
-    for (int it = 0; it < ntiles; ++it) {
-      const int t0 = it * kTok;
-      if (t0 % kMaxRows == 0) {
-        __syncwarp();
-        for (int r = lane; r < kMaxRows && t0 + r < n; r += 32) {
-          const int tok = a.topk ? a.topk[(int64_t)b * a.topk_n + t0 + r] : t0 + r;
-          int64_t row = -1;
-          if (tok >= L && a.topk) atomicOr(a.status, kErrBadTopk);
-          if (tok >= 0 && tok < L) {
-            const int page = a.block_tables[(int64_t)b * a.max_pages + tok / a.P];
-            if (page < 0 || (int64_t)page >= a.num_pages)
-              atomicOr(a.status, kErrBadPage);
-            else
-              row = (int64_t)page * a.P + tok % a.P;
-          }
-          srcs[r] = row;
-        }
-        __syncwarp();
-      }
-      const int st = it % kStages;
-      if (it > 0 && st == 0) ph_empty ^= 1u;
-      if (!mbar_wait(smem_u32(&empty_bar[st]), ph_empty)) {
-        timed_out = true;
-        break;
-      }
-      uint8_t* sbase = rows + st * kStageBytes;
-      int64_t srow[2];
-      bool ok[2];
+    // Row table half c % 2 <- list positions 1024 c .. 1024 c + 1023: top-k
+    // entry -> page -> cache row (-1: padding, past the list, or rejected).
+    const int64_t tbase = (int64_t)b * a.topk_n;
+    const int32_t* bt = a.block_tables + (int64_t)b * a.max_pages;
+    int32_t* bt_s = reinterpret_cast<int32_t*>(smem + kOffBt);
+    const int npages = (L + a.P - 1) / a.P;
+    const int ncached = npages < kBtCache ? npages : kBtCache;
+#pragma unroll 1
+    for (int i0 = 0; i0 < ncached; i0 += 32 * 16) {
+      int v[16];
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int r = lane + 32 * k;
-        srow[k] = (t0 + r < n) ? srcs[(t0 + r) % kMaxRows] : -1;
-        ok[k] = srow[k] >= 0;
-        valid[st][r] = ok[k];
-        if (!ok[k]) {  // rows that take no part are zero, so that p = 0 meets no NaN
-          uint4* z = reinterpret_cast<uint4*>(sbase + r * kRowBytes);
-          for (int w = 0; w < kDqk / 16; ++w) z[w] = make_uint4(0, 0, 0, 0);
-        }
-      }
-      const uint32_t cnt = __popc(__ballot_sync(0xFFFFFFFFu, ok[0])) + __popc(__ballot_sync(0xFFFFFFFFu, ok[1]));
-      fence_proxy_async_smem();  // zero rows (generic stores) before later bulk copies
-      __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(smem_u32(&full_bar[st]), cnt * kDqk);
-      __syncwarp();
-#pragma unroll
-      for (int k = 0; k < 2; ++k)
-        if (ok[k])
-          bulk_row(smem_u32(sbase + (lane + 32 * k) * kRowBytes), a.ckv + srow[k] * kDqk, kDqk,
-                   smem_u32(&full_bar[st]));
-    }
-    if (timed_out && lane == 0) atomicOr(a.status, kErrWaitTimeout);
-    return;
-  }
-
-  // -------------------------------------------------------------- consumers
-  const int mt = warp & 1, nt = warp >> 1;  // scores: head tile, 8-token column tile
-  const float sc = a.score_scale;
-  float mref[2] = {-INFINITY, -INFINITY};  // rows g, g+8 of head tile mt
-  float rthr[2] = {-INFINITY, -INFINITY};
-  float lpart[2] = {0.f, 0.f};
-  float o[2][4][4];  // [head tile][n-tile of this warp's 32 columns][frag]
-#pragma unroll
-  for (int i = 0; i < 2; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) o[i][j][0] = o[i][j][1] = o[i][j][2] = o[i][j][3] = 0.f;
-  const uint32_t qs_u = smem_u32(qs), ps_u = smem_u32(ps);
-  // ldmatrix row address of this lane for a 16x16 tile at (row0, col0 halves)
-  const int lm_row = (lane & 7) + ((lane >> 3) & 1) * 8, lm_col = (lane >> 4) * 8;
-
-  uint32_t ph_full = 0;
-  for (int it = 0; it < ntiles; ++it) {
-    const int st = it % kStages;
-    if (it > 0 && st == 0) ph_full ^= 1u;
-    // Every consumer warp runs the same sequence of named barriers whatever
-    // happens: after a timed-out wait a warp stops waiting (and computes on
-    // whatever the stage holds; the status word reports it) but keeps
-    // iterating, so no warp is ever left at a barrier the others skipped.
-    if (!timed_out && !mbar_wait(smem_u32(&full_bar[st]), ph_full)) timed_out = true;
-    const uint8_t* sb = rows + st * kStageBytes;
-
-    // ---- S = Q . C^T for head tile mt, tokens 8 nt .. 8 nt + 7; four
-    // interleaved partial accumulators keep the MMA dependency chains short
-    float sacc[4][4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) sacc[k][0] = sacc[k][1] = sacc[k][2] = sacc[k][3] = 0.f;
-    const uint8_t* r0 = sb + (8 * nt + g) * kRowBytes;
-    const uint32_t qa = qs_u + (16 * mt + lm_row) * kQStride + lm_col * 2;
-    uint32_t an[4];  // A fragment of the next k-step, loaded one step ahead
-    ldmatrix_x4(qa, an[0], an[1], an[2], an[3]);
-#pragma unroll
-    for (int blk = 0; blk < 5; ++blk) {
-      const int nsteps = blk < 4 ? 8 : 4;
-      const int off = blk < 4 ? 128 * blk + 32 * t : 512 + 16 * t;
-      uint32_t w0[8];
-      {
-        const uint4 x = *reinterpret_cast<const uint4*>(r0 + off);
-        w0[0] = x.x; w0[1] = x.y; w0[2] = x.z; w0[3] = x.w;
-      }
-      if (blk < 4) {
-        const uint4 x = *reinterpret_cast<const uint4*>(r0 + off + 16);
-        w0[4] = x.x; w0[5] = x.y; w0[6] = x.z; w0[7] = x.w;
+      for (int m = 0; m < 16; ++m) {
+        const int i = i0 + lane + 32 * m;
+        v[m] = i < ncached ? bt[i] : 0;
       }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (j >= nsteps) break;
-        const int ks = (blk < 4 ? 8 * blk : 32) + j;
-        const uint32_t a0 = an[0], a1 = an[1], a2 = an[2], a3 = an[3];
-        if (ks + 1 < kDqk / 16) ldmatrix_x4(qa + 32 * (ks + 1), an[0], an[1], an[2], an[3]);
-        uint32_t b0, b1;
-        e4m3x4_to_f16x2x2(w0[j], b0, b1);
-        mma_f16(sacc[ks & 3], a0, a1, a2, a3, b0, b1);
+      for (int m = 0; m < 16; ++m) {
+        const int i = i0 + lane + 32 * m;
+        if (i < ncached) bt_s[i] = v[m];
       }
-    }
-    float s[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) s[e] = (sacc[0][e] + sacc[1][e]) + (sacc[2][e] + sacc[3][e]);
-
-    // ---- mask, tile maximum across the eight column tiles, lazy rescale
-    const int* vld = valid[st];
-    {
-      const int c0 = 8 * nt + 2 * t;
-      if (!vld[c0]) s[0] = s[2] = -INFINITY;
-      if (!vld[c0 + 1]) s[1] = s[3] = -INFINITY;
-    }
-    float mx0 = fmaxf(s[0], s[1]);  // row g
-    float mx1 = fmaxf(s[2], s[3]);  // row g + 8
-#pragma unroll
-    for (int off = 1; off < 4; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, off));
-    }
-    if (t == 0) {
-      red_max[mt][nt][g] = mx0;
-      red_max[mt][nt][g + 8] = mx1;
-    }
-    if (threadIdx.x == 0) grow_flag = 0;
-    consumer_sync();
-    float tm0 = red_max[mt][0][g], tm1 = red_max[mt][0][g + 8];
-#pragma unroll
-    for (int k = 1; k < 8; ++k) {
-      tm0 = fmaxf(tm0, red_max[mt][k][g]);
-      tm1 = fmaxf(tm1, red_max[mt][k][g + 8]);
-    }
-    float al0 = 1.f, al1 = 1.f;
-    if (tm0 > rthr[0] || tm1 > rthr[1]) {  // identical in every warp of this head tile
-      const float mn0 = fmaxf(mref[0], tm0 * sc), mn1 = fmaxf(mref[1], tm1 * sc);
-      al0 = fast_exp2(mref[0] - mn0);
-      al1 = fast_exp2(mref[1] - mn1);
-      mref[0] = mn0;
-      mref[1] = mn1;
-      rthr[0] = (mn0 + kRescaleLog2) / sc;
-      rthr[1] = (mn1 + kRescaleLog2) / sc;
-      lpart[0] *= al0;
-      lpart[1] *= al1;
-      if (nt == 0 && t == 0) grow_flag = 1;
-    }
-    if (nt == 0 && t == 0) {
-      alpha[16 * mt + g] = al0;
-      alpha[16 * mt + g + 8] = al1;
-    }
-    // ---- P = 2^(s*scale - ref) -> f16 tile [head][token]
-    {
-      const float p0 = fast_exp2(fmaf(s[0], sc, -mref[0]));
-      const float p1 = fast_exp2(fmaf(s[1], sc, -mref[0]));
-      const float p2 = fast_exp2(fmaf(s[2], sc, -mref[1]));
-      const float p3 = fast_exp2(fmaf(s[3], sc, -mref[1]));
-      lpart[0] += p0 + p1;
-      lpart[1] += p2 + p3;
-      const int col = 8 * nt + 2 * t;
-      *reinterpret_cast<uint32_t*>(ps + (16 * mt + g) * kPStride + col * 2) = pack_f16x2(p0, p1);
-      *reinterpret_cast<uint32_t*>(ps + (16 * mt + g + 8) * kPStride + col * 2) = pack_f16x2(p2, p3);
-    }
-    consumer_sync();
-
-    // ---- O[:, 32 w .. 32 w + 31] += P . C  (both head tiles)
-    if (grow_flag) {
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const float a_lo = alpha[16 * i + g], a_hi = alpha[16 * i + g + 8];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          o[i][j][0] *= a_lo;
-          o[i][j][1] *= a_lo;
-          o[i][j][2] *= a_hi;
-          o[i][j][3] *= a_hi;
-        }
-      }
-    }
-#pragma unroll
-    for (int kstep = 0; kstep < kTok / 16; ++kstep) {
-      uint32_t pa[2][4];
-#pragma unroll
-      for (int i = 0; i < 2; ++i)
-        ldmatrix_x4(ps_u + (16 * i + lm_row) * kPStride + (16 * kstep + lm_col) * 2, pa[i][0], pa[i][1],
-                    pa[i][2], pa[i][3]);
-      // rows (tokens) 2t, 2t+1, 2t+8, 2t+9 of this k-step, 4 bytes at head_dim 32 w + 4 g:
-      // n-tile j column g <-> head_dim 32 w + 4 g + j
-      const uint8_t* base = sb + (16 * kstep) * kRowBytes + 32 * warp + 4 * g;
-      const uint32_t v0 = *reinterpret_cast<const uint32_t*>(base + (2 * t) * kRowBytes);
-      const uint32_t v1 = *reinterpret_cast<const uint32_t*>(base + (2 * t + 1) * kRowBytes);
-      const uint32_t v2 = *reinterpret_cast<const uint32_t*>(base + (2 * t + 8) * kRowBytes);
-      const uint32_t v3 = *reinterpret_cast<const uint32_t*>(base + (2 * t + 9) * kRowBytes);
-      uint32_t bl[4], bh[4];  // b0b1 (tokens 2t, 2t+1) and b2b3 (tokens 2t+8, 2t+9) per n-tile
-      e4m3x4_to_f16x2x2(prmt(v0, v1, 0x5140), bl[0], bl[1]);
-      e4m3x4_to_f16x2x2(prmt(v0, v1, 0x7362), bl[2], bl[3]);
-      e4m3x4_to_f16x2x2(prmt(v2, v3, 0x5140), bh[0], bh[1]);
-      e4m3x4_to_f16x2x2(prmt(v2, v3, 0x7362), bh[2], bh[3]);
-#pragma unroll
-      for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) mma_f16(o[i][j], pa[i][0], pa[i][1], pa[i][2], pa[i][3], bl[j], bh[j]);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
-    consumer_sync();  // P and red_max are rewritten by the next tile
-  }
-
-  // ---- finish: l per head across the column tiles, O / l, lse
-  float l0 = lpart[0], l1 = lpart[1];
+    const int nchunks = (n + kRowTab - 1) / kRowTab;
+    for (int c = 0; c < nchunks; ++c) {
+      if (c >= 2 && !to) to = !mbar_wait(smem_u32(&bs.rows_free[c & 1]), ((c - 2) >> 1) & 1);
+      int32_t* rowtab = reinterpret_cast<int32_t*>(smem + kOffRows) + (c & 1) * kRowTab;
+#pragma unroll 1
+      for (int half = 0; half < kRowTab / 1024; ++half) {
+        const int p0 = c * kRowTab + 32 * 32 * half + lane;
+        int tok[32];
 #pragma unroll
-  for (int off = 1; off < 4; off <<= 1) {
-    l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, off);
-    l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, off);
-  }
-  if (t == 0) {
-    red_l[mt][nt][g] = l0;
-    red_l[mt][nt][g + 8] = l1;
-    if (nt == 0) {
-      red_max[mt][0][g] = mref[0];  // the reference maxima, shared with the output warps
-      red_max[mt][0][g + 8] = mref[1];
-    }
-  }
-  consumer_sync();
-  if (timed_out && lane == 0) atomicOr(a.status, kErrWaitTimeout);
-#pragma unroll
-  for (int i = 0; i < 2; ++i)
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int hr = 16 * i + g + 8 * hh;
-      const int head = h0 + hr;
-      float lt = 0.f;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) lt += red_l[i][k][g + 8 * hh];
-      const float inv = lt > 0.f ? a.out_scale / lt : 0.f;
-      if (head < a.H) {
-        // n-tile j, columns 2t, 2t+1 of the fragment <-> head_dim 32 w + 4 (2t..2t+1) + j
-        uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) + ((int64_t)b * a.H + head) * kDv + 32 * warp;
-        uint32_t pk[4];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          pk[2 * c] = pack_bf16x2(o[i][0][2 * hh + c] * inv, o[i][1][2 * hh + c] * inv);
-          pk[2 * c + 1] = pack_bf16x2(o[i][2][2 * hh + c] * inv, o[i][3][2 * hh + c] * inv);
+        for (int m = 0; m < 32; ++m) {
+          const int p = p0 + 32 * m;
+          tok[m] = p < n ? (a.topk ? a.topk[tbase + p] : p) : -1;
         }
-        *reinterpret_cast<uint2*>(dst + 4 * (2 * t)) = make_uint2(pk[0], pk[1]);
-        *reinterpret_cast<uint2*>(dst + 4 * (2 * t + 1)) = make_uint2(pk[2], pk[3]);
-        if (a.lse && warp == 0 && t == 0)
-          a.lse[(int64_t)b * a.H + head] =
-              lt > 0.f ? (red_max[i][0][g + 8 * hh] + __log2f(lt)) * kLn2 : -INFINITY;
+#pragma unroll
+        for (int m = 0; m < 32; ++m) {
+          int32_t row = -1;
+          const int tk = tok[m];
+          if (tk >= L) {
+            if (a.topk) atomicOr(a.status, kErrBadTopk);
+          } else if (tk >= 0) {
+            const int pi = tk / a.P;
+            const int pg = pi < kBtCache ? bt_s[pi] : bt[pi];
+            if (pg < 0 || (int64_t)pg >= a.num_pages)
+              atomicOr(a.status, kErrBadPage);
+            else
+              row = pg * a.P + (tk - pi * a.P);
+          }
+          rowtab[32 * 32 * half + lane + 32 * m] = row;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.rows_ready[c & 1]));
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      if (!to) to = !mbar_wait(smem_u32(&bs.qready), 0);
+      tc::fence_after_sync();
+      const uint32_t cbase0 = smem_u32(smem + kOffC), qrope = smem_u32(smem + kOffQRope);
+      for (int j = 0; j < ntiles + kPvLag; ++j) {
+        if (j < ntiles) {  // S(j) = Q . C(j)^T
+          const int cb = j % kBufs;
+          if (!to) to = !mbar_wait(smem_u32(&bs.cfull[cb]), (j / kBufs) & 1);
+          tc::fence_after_sync();
+          const uint32_t cbuf = cbase0 + cb * kCBufBytes;
+          const uint32_t d = tmem + kTmemS + kTok * cb;
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            tc::mma_ts(d, tmem + kTmemQ + 8 * k, tc::desc_sw128(cbuf + (k >> 2) * kAtomBytes + 32 * (k & 3), 16, 1024),
+                       kIdescQK, k > 0);
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const uint32_t koff = 32 * (2 * rank + k);
+            tc::mma_ss(d, tc::desc_sw128(qrope + koff, 16, 1024),
+                       tc::desc_sw128(cbuf + 4 * kAtomBytes + koff, 16, 1024), kIdescQK, 1);
+          }
+          tc::mma_commit(smem_u32(&bs.sfull[cb]));
+        }
+        if (j >= kPvLag) {  // O += P(pj) . C(pj)[:, own columns]
+          const int pj = j - kPvLag, pb = pj % kBufs;
+          if (!to) to = !mbar_wait(smem_u32(&bs.pfull[pb]), (pj / kBufs) & 1);
+          tc::fence_after_sync();
+          const uint32_t cbuf = cbase0 + pb * kCBufBytes;
+#pragma unroll
+          for (int k = 0; k < kTok / 16; ++k)
+            tc::mma_ts(tmem + kTmemO, tmem + kTmemS + kTok * pb + 8 * k,
+                       tc::desc_sw128(cbuf + 2048 * k, kAtomBytes, 1024), kIdescPV, (pj > 0 || k > 0));
+          tc::mma_commit(smem_u32(&bs.pvdone[pb]));
+        }
+      }
+      // no MMA may still be running when the tensor memory is freed
+      if (ntiles > 0 && !to)
+        to = !mbar_wait(smem_u32(&bs.pvdone[(ntiles - 1) % kBufs]), ((ntiles - 1) / kBufs) & 1);
+    }
+    __syncwarp();
+  } else if (warp == kAckWarp) {
+    // ------------------------------------------------------------- ack warp
+    if (lane == 0) {
+      for (int j = 0; j < ntiles; ++j) {
+        const int xb = j % kXDepth;
+        if (!to) to = !mbar_wait(smem_u32(&bs.rdone[xb]), (j / kXDepth) & 1);
+        tc::mbar_arrive_remote(tc::mapa(smem_u32(&bs.xack[xb]), peer));
       }
     }
+    __syncwarp();
+  } else if (warp < kLoadWarp0 + 4) {
+    // --------------------------------------------------------- loader warps
+    // Warp w owns token rows 8 w .. 8 w + 7 of every tile: it gathers them
+    // (e4m3, 18 chunks of 16 bytes per row: 16 latent, 2 rope) into staging
+    // slot (tile % 6) five tiles ahead, then widens them to f16 in the
+    // swizzled atoms of latent buffer tile % 4.
+    const int w = warp - kLoadWarp0;
+    const uint8_t* src_lat = a.ckv + kLatCols * rank;
+    const uint8_t* src_rope = a.ckv + kDv + kRopeCols * rank;
+    uint8_t* stage = smem + kOffStage + w * (kAhead + 1) * kSlotBytes;
+    const int32_t* rowtab0 = reinterpret_cast<const int32_t*>(smem + kOffRows);
+    auto issue = [&](int jj) {  // gather this warp's rows of tile jj (nothing past the list)
+      if (jj < ntiles) {
+        const int c = jj / kRowTabTiles;
+        if (jj % kRowTabTiles == 0 && !to) to = !mbar_wait(smem_u32(&bs.rows_ready[c & 1]), (c >> 1) & 1);
+        const int32_t* rt = rowtab0 + (c & 1) * kRowTab + kTok * (jj % kRowTabTiles) + kLoadRows * w;
+        const uint32_t sdst = smem_u32(stage + (jj % (kAhead + 1)) * kSlotBytes);
+#pragma unroll
+        for (int k = 0; k < (kLoadRows * kRowChunks + 31) / 32; ++k) {
+          const int i = lane + 32 * k;
+          if (i < kLoadRows * kRowChunks) {
+            const int r = i / kRowChunks, ch = i - r * kRowChunks;
+            const int32_t row = rt[r];
+            const int u = ch + r < kRowChunks ? ch + r : ch + r - kRowChunks;  // rotated: no bank conflicts
+            if (row >= 0)
+              cp_async16(sdst + r * kRowCopy + 16 * u,
+                         (ch < 16 ? src_lat + 16 * ch : src_rope + 16 * (ch - 16)) + (int64_t)row * kDqk);
+          }
+        }
+        const uint32_t vm = __ballot_sync(0xFFFFFFFFu, lane < kLoadRows && rt[lane < kLoadRows ? lane : 0] >= 0);
+        if (lane == 0) bs.vmask[w][jj % (kAhead + 1)] = (uint8_t)vm;
+        __syncwarp();
+        const bool last_of_chunk = (jj % kRowTabTiles == kRowTabTiles - 1) || jj == ntiles - 1;
+        if (last_of_chunk && lane == 0) tc::mbar_arrive_local(smem_u32(&bs.rows_free[c & 1]));
+      }
+      cp_async_commit();  // one group per tile, empty past the list
+    };
+    for (int jj = 0; jj < kAhead; ++jj) issue(jj);
+    // widening: lane l takes row l % 8, chunks l / 8 + 4 m
+    const int wr = lane & 7, wc0 = lane >> 3;
+    const uint32_t swz = (kLoadRows * w + wr) & 7;
+    for (int j = 0; j < ntiles; ++j) {
+      const int cb = j % kBufs;
+      issue(j + kAhead);
+      cp_async_wait_ahead();  // this lane's copies of tile j have landed
+      __syncwarp();           // ... and every lane's
+      if (j >= kBufs && !to) to = !mbar_wait(smem_u32(&bs.pvdone[cb]), ((j - kBufs) / kBufs) & 1);
+      const uint32_t bits = bs.vmask[w][j % (kAhead + 1)];
+      const bool valid = (bits >> wr) & 1;
+      const uint8_t* src = stage + (j % (kAhead + 1)) * kSlotBytes + wr * kRowCopy;
+      uint8_t* cbuf = smem + kOffC + cb * kCBufBytes + (kLoadRows * w + wr) * 128;
+#pragma unroll
+      for (int m = 0; m < 5; ++m) {
+        const int ch = wc0 + 4 * m;
+        if (ch < kRowChunks) {
+          uint4 v = make_uint4(0, 0, 0, 0);
+          const int u = ch + wr < kRowChunks ? ch + wr : ch + wr - kRowChunks;
+          if (valid) v = lds128(src + 16 * u);
+          uint4 o0, o1;
+          e4m3x4_to_f16x2x2(v.x, o0.x, o0.y);
+          e4m3x4_to_f16x2x2(v.y, o0.z, o0.w);
+          e4m3x4_to_f16x2x2(v.z, o1.x, o1.y);
+          e4m3x4_to_f16x2x2(v.w, o1.z, o1.w);
+          const int atom = ch < 16 ? (ch >> 2) : 4;
+          const uint32_t unit = ch < 16 ? 2 * (ch & 3) : 4 * rank + 2 * (ch - 16);
+          uint8_t* dst = cbuf + atom * kAtomBytes;
+          *reinterpret_cast<uint4*>(dst + 16 * (unit ^ swz)) = o0;
+          *reinterpret_cast<uint4*>(dst + 16 * ((unit + 1) ^ swz)) = o1;
+        }
+      }
+      fence_proxy_async_smem();  // generic writes -> visible to the tensor core
+      __syncwarp();
+      if (lane == 0) {
+        reinterpret_cast<uint8_t*>(&bs.cmask[cb])[w] = (uint8_t)bits;
+        tc::mbar_arrive_local(smem_u32(&bs.cfull[cb]));
+      }
+    }
+    cp_async_wait_all();  // nothing may still be landing when the CTA retires
+  } else if (warp >= kSendWarp0) {
+    // --------------------------------------------------------- sender warps
+    // Tile j: this CTA's partial scores (log2 units) -> 16-bit fixed point in
+    // send buffer j % 3 -> one bulk copy into the peer's receive buffer.
+    const int t = threadIdx.x - kSendWarp0 * 32;  // head row = TMEM lane
+    const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const float sc = a.score_scale;
+    const uint32_t send0 = smem_u32(smem + kOffSend);
+    const uint32_t peer_recv0 = tc::mapa(smem_u32(smem + kOffRecv), peer);
+    for (int j = 0; j < ntiles; ++j) {
+      const int sb = j % kBufs, xb = j % kXDepth;
+      if (!to) to = !mbar_wait(smem_u32(&bs.sfull[sb]), (j / kBufs) & 1);
+      // the copy of tile j - 3 out of this buffer has landed and been read
+      if (j >= kXDepth && !to) to = !tc::mbar_wait_cluster(smem_u32(&bs.xack[xb]), ((j - kXDepth) / kXDepth) & 1);
+      tc::fence_after_sync();
+      float x[32];
+      {
+        uint32_t v[32];
+        tc::tmem_ld32(tl + kTmemS + kTok * sb, v);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(v[i]) * sc;
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.sent[sb]));  // the softmax may overwrite S with P
+      float lo = x[0], hi = x[0];
+#pragma unroll
+      for (int i = 1; i < 32; ++i) {
+        lo = fminf(lo, x[i]);
+        hi = fmaxf(hi, x[i]);
+      }
+      // step = 2^(e - 127), the smallest power of two with (hi - lo) / step <= 65535
+      const uint32_t rb = __float_as_uint((hi - lo) * (1.f / 65535.f));
+      uint32_t e = ((rb >> 23) & 0xFFu) + ((rb & 0x7FFFFFu) != 0u);
+      e = e < 1u ? 1u : (e > 253u ? 253u : e);
+      const float inv = __uint_as_float((254u - e) << 23);  // 1 / step, exact
+      const uint32_t buf = send0 + xb * kXBytes;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t q0 = min(__float2uint_rn((x[8 * c + 2 * k] - lo) * inv), 65535u);
+          const uint32_t q1 = min(__float2uint_rn((x[8 * c + 2 * k + 1] - lo) * inv), 65535u);
+          w[k] = q0 | (q1 << 16);
+        }
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(buf + xunit(t, c)), "r"(w[0]), "r"(w[1]),
+                     "r"(w[2]), "r"(w[3])
+                     : "memory");
+      }
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(buf + kXCodes + 4 * t), "f"(lo) : "memory");
+      asm volatile("st.shared.u8 [%0], %1;" ::"r"(buf + kXCodes + 4 * kRows + t), "r"(e) : "memory");
+      fence_proxy_async_smem();
+      sender_sync();
+      if (t == 0) {
+        mbar_arrive_expect_tx(smem_u32(&bs.xfull[xb]), kXBytes);  // the peer's tile j, into recv buffer xb
+        bulk_to_peer(peer_recv0 + xb * kXBytes, buf, kXBytes, tc::mapa(smem_u32(&bs.xfull[xb]), peer));
+      }
+    }
+  } else {
+    // ------------------------------------------------------- softmax warps
+    const int t = threadIdx.x - kSoftWarp0 * 32;  // head row = TMEM lane
+    const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    {  // Q: this CTA's latent columns into tensor memory, the rope into shared memory
+      const bool have = t < a.H;
+      const __nv_bfloat16* qrow = a.q + ((int64_t)b * a.H + (have ? t : 0)) * kDqk;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          uint4 x = make_uint4(0, 0, 0, 0);
+          if (have) x = ldg_nc(qrow + kLatCols * rank + 64 * c + 8 * u);
+          v[4 * u + 0] = bf16x2_to_f16x2(x.x);
+          v[4 * u + 1] = bf16x2_to_f16x2(x.y);
+          v[4 * u + 2] = bf16x2_to_f16x2(x.z);
+          v[4 * u + 3] = bf16x2_to_f16x2(x.w);
+        }
+        tc::tmem_st32(tl + kTmemQ + 32 * c, v);
+      }
+      uint8_t* qr = smem + kOffQRope + t * 128;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        uint4 x = make_uint4(0, 0, 0, 0);
+        if (have) x = ldg_nc(qrow + kDv + 8 * u);
+        const uint4 y = make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z),
+                                   bf16x2_to_f16x2(x.w));
+        *reinterpret_cast<uint4*>(qr + 16 * (u ^ (t & 7))) = y;
+      }
+      tc::tmem_st_wait();
+      fence_proxy_async_smem();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.qready));
+    }
+
+    const float sc = a.score_scale;
+    const uint32_t recv0 = smem_u32(smem + kOffRecv);
+    float mref = -INFINITY, l = 0.f;
+    for (int j = 0; j < ntiles; ++j) {
+      const int sb = j % kBufs, xb = j % kXDepth;
+      if (!to) to = !mbar_wait(smem_u32(&bs.sfull[sb]), (j / kBufs) & 1);
+      if (!to) to = !mbar_wait(smem_u32(&bs.cfull[sb]), (j / kBufs) & 1);
+      if (!to) to = !tc::mbar_wait_cluster(smem_u32(&bs.xfull[xb]), (j / kXDepth) & 1);
+      tc::fence_after_sync();
+      // ---- s = own exact partial + the peer's decoded partial
+      float s[32];
+      {
+        uint32_t v[32];
+        tc::tmem_ld32(tl + kTmemS + kTok * sb, v);
+        tc::tmem_ld_wait();
+        const uint32_t theirs = recv0 + xb * kXBytes;
+        float plo;
+        uint32_t pe;
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(plo) : "r"(theirs + kXCodes + 4 * t) : "memory");
+        asm volatile("ld.shared.u8 %0, [%1];" : "=r"(pe) : "r"(theirs + kXCodes + 4 * kRows + t) : "memory");
+        const float pstep = __uint_as_float(pe << 23);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 hq = lds128_u32(theirs + xunit(t, c));
+          const uint32_t wq[4] = {hq.x, hq.y, hq.z, hq.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float p0 = fmaf(__uint2float_rn(wq[k] & 0xFFFFu), pstep, plo);
+            const float p1 = fmaf(__uint2float_rn(wq[k] >> 16), pstep, plo);
+            s[8 * c + 2 * k] = fmaf(__uint_as_float(v[8 * c + 2 * k]), sc, p0);
+            s[8 * c + 2 * k + 1] = fmaf(__uint_as_float(v[8 * c + 2 * k + 1]), sc, p1);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.rdone[xb]));  // the ack warp frees it at the peer
+
+      // ---- mask, tile maximum, lazy reference update
+      const uint32_t mask = bs.cmask[sb];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        s[i] = ((mask >> i) & 1) ? s[i] : -INFINITY;
+        mx = fmaxf(mx, s[i]);
+      }
+      const bool grow = mx > mref + kRescaleLog2;
+      float alpha = 1.f;
+      if (grow) {
+        alpha = fast_exp2(mref - mx);  // 0 when there was no reference yet
+        mref = mx;
+        l *= alpha;
+      }
+      if (j > 0 && __any_sync(0xFFFFFFFFu, grow)) {  // O *= alpha once PV(j-1) has landed
+        if (!to) to = !mbar_wait(smem_u32(&bs.pvdone[(j - 1) % kBufs]), ((j - 1) / kBufs) & 1);
+        tc::fence_after_sync();
+#pragma unroll 1
+        for (int c = 0; c < kLatCols / 32; ++c) {
+          uint32_t v[32];
+          tc::tmem_ld32(tl + kTmemO + 32 * c, v);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+          tc::tmem_st32(tl + kTmemO + 32 * c, v);
+        }
+      }
+      // ---- P = 2^(s - ref) as f16 pairs over the score columns
+      const float moff = mref == -INFINITY ? 0.f : mref;
+      uint32_t pk[16];
+      float lsum = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float p0 = fast_exp2(s[2 * i] - moff), p1 = fast_exp2(s[2 * i + 1] - moff);
+        lsum += p0 + p1;
+        pk[i] = pack_f16x2(p0, p1);
+      }
+      l += lsum;
+      if (!to) to = !mbar_wait(smem_u32(&bs.sent[sb]), (j / kBufs) & 1);  // the sender has read S(j)
+      tc::fence_after_sync();
+      tc::tmem_st16(tl + kTmemS + kTok * sb, pk);
+      tc::tmem_st_wait();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.pfull[sb]));
+    }
+
+    // ---- epilogue: O / l -> bf16, this CTA's 256 columns; lse from rank 0
+    if (ntiles > 0 && !to)
+      to = !mbar_wait(smem_u32(&bs.pvdone[(ntiles - 1) % kBufs]), ((ntiles - 1) / kBufs) & 1);
+    tc::fence_after_sync();
+    const float inv = l > 0.f ? a.out_scale / l : 0.f;
+    uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) + ((int64_t)b * a.H + t) * kDv + kLatCols * rank;
+#pragma unroll 1
+    for (int c = 0; c < kLatCols / 32; ++c) {
+      uint32_t v[32];
+      if (ntiles > 0) {
+        tc::tmem_ld32(tl + kTmemO + 32 * c, v);
+        tc::tmem_ld_wait();
+      }
+      if (t < a.H) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = l > 0.f ? pack_bf16x2(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv) : 0u;
+        uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      }
+    }
+    if (rank == 0 && a.lse && t < a.H)
+      a.lse[(int64_t)b * a.H + t] = l > 0.f ? (mref + __log2f(l)) * kLn2 : -INFINITY;
+  }
+
+  if (to) atomicOr(a.status, kErrWaitTimeout);
+  tc::fence_before_sync();
+  tc::cluster_sync();  // the peer no longer touches this CTA's shared memory
+  tc::fence_after_sync();
+  if (warp == kMmaWarp) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
@@ -433,12 +655,14 @@ int pfkv_mla_decode_attn(void* out, const void* q, const void* ckv_cache, const 
     return fail(PFKV_ERR_INVALID_ARG, "mla_decode: bad sizes");
   if (d_latent != kDv || d_rope != kDqk - kDv)
     return fail(PFKV_ERR_UNSUPPORTED, "mla_decode: only d_latent 512 + d_rope 64 supported");
-  if (num_heads % 16 != 0 || num_heads > 128)
+  if (num_heads % 16 != 0 || num_heads > kRows)
     return fail(PFKV_ERR_UNSUPPORTED, "mla_decode: num_heads must be a multiple of 16, <= 128");
   if (page_size % 16 != 0)
     return fail(PFKV_ERR_UNSUPPORTED, "mla_decode: page_size must be a multiple of 16");
   if (!isfinite(ckv_scale) || !isfinite(softmax_scale) || !(softmax_scale > 0.f))
     return fail(PFKV_ERR_INVALID_ARG, "mla_decode: scales must be finite");
+  if (num_pages > (int64_t)INT32_MAX / page_size)
+    return fail(PFKV_ERR_UNSUPPORTED, "mla_decode: more than 2^31 cache rows");
   if (batch == 0) return PFKV_OK;
   if (!out || !q || !ckv_cache || !block_tables || !context_lens || !workspace)
     return fail(PFKV_ERR_INVALID_ARG, "mla_decode: null pointer");
@@ -472,8 +696,7 @@ int pfkv_mla_decode_attn(void* out, const void* q, const void* ckv_cache, const 
   }
   if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), s) != cudaSuccess)
     return check_cuda("mla_decode status reset");
-  dim3 grid(batch, (num_heads + kHeads - 1) / kHeads);
-  mla_decode_kernel<<<grid, kThreads, kSmemBytes, s>>>(a);
+  mla_decode_kernel<<<dim3(2 * batch), kThreads, kSmemBytes, s>>>(a);
   return check_cuda("mla_decode launch");
 }
 
