@@ -10,11 +10,13 @@
 //
 // Per request a cluster of two CTAs.  The fp32 output O[128 heads][512] alone
 // fills one SM's tensor memory, so CTA r keeps O[:, 256 r .. 256 r + 255] and
-// the pair splits the score contraction instead of repeating it: CTA r
-// contracts latent columns 256 r .. 256 r + 255 (Q held in tensor memory as
-// the A operand) and rope columns 512 + 32 r .. 512 + 32 r + 31 (Q in shared
-// memory).  The partial score tiles cross between the pair through
-// distributed shared memory, one bulk copy per tile, as 16-bit fixed point
+// the pair splits the score contraction instead of repeating it: CTA 0
+// contracts latent columns 0 .. 255, CTA 1 latent columns 256 .. 511 and the
+// 64 rope columns (Q's latent part held in tensor memory as the A operand,
+// the rope part in shared memory), so each CTA reads one contiguous span of
+// every row (256 or 320 bytes).  The partial score tiles cross between the
+// pair through distributed shared memory (asynchronous remote stores that
+// count their bytes on the receiver's mbarrier) as 16-bit fixed point
 // over the row's range in the tile (an fp32 row minimum, a power-of-two step
 // with range / step <= 65535, one u16 code per token: error <= range / 65535
 // in log2 units).  Each CTA adds its own exact fp32 partial to the peer's
@@ -23,18 +25,18 @@
 //
 // Per 32-token tile, with four tiles in flight (scores and P in tensor
 // memory, the widened latent tile in shared memory):
-//   producer warp   resolves the cache rows of 1024 list positions at a time
+//   producer warp   resolves the cache rows of 2048 list positions at a time
 //                   (top-k entry -> block table, cached in shared memory ->
-//                   row) into a double-buffered shared table;
-//   loader warps    (8 rows of every tile each) gather this CTA's 288 bytes of
-//                   each row with 16-byte asynchronous copies five tiles
-//                   ahead (the rate of random row gathers grows with the
-//                   number of issuing warps), then widen their rows to f16
-//                   (exact) in the 128-byte-swizzled layout the MMA reads,
-//                   K-major for the scores and MN-major for the output;
-//   MMA thread      S[128 x 32] = Q . C^T (18 K steps), and two tiles later
+//                   row) into a shared table and gathers this CTA's span of
+//                   each row with TMA four-row gathers (tile::gather4) into a
+//                   5-stage e4m3 ring;
+//   converter warps widen the tile to f16 (exact) in the 128-byte-swizzled
+//                   layout the MMA reads, K-major for the scores and MN-major
+//                   for the output product;
+//   MMA thread      S[128 x 32] = Q . C^T (16 or 20 K steps), and two tiles later
 //                   O += P . C[:, own 256] (2 K steps, N = 256);
-//   sender warps    read S, encode it and copy it to the peer;
+//   sender warps    read S, encode it and store it into the peer's receive
+//                   buffer;
 //   softmax warps   (one TMEM lane per head) add the peer's partial, take the
 //                   exp2 online softmax with a reference maximum that moves
 //                   only when a score exceeds it by more than 2^8 (then O is
@@ -59,31 +61,27 @@ constexpr int kDqk = 576, kDv = 512;
 constexpr int kRows = 128;            // MMA rows: query heads, zero-padded
 constexpr int kTok = 32;              // tokens per tile
 constexpr int kBufs = 4;              // tiles in flight: score/P buffers and widened latent tiles
-constexpr int kAhead = 5;             // tiles a loader warp gathers ahead of the one it widens
+constexpr int kStages = 5;            // e4m3 staging ring
 constexpr int kXDepth = 3;            // exchange buffers per direction
 constexpr int kLatCols = 256;         // latent columns one CTA contracts (and outputs)
-constexpr int kRopeCols = 32;         // rope columns one CTA contracts
-constexpr int kRowCopy = kLatCols + kRopeCols;  // 288 staged bytes per token row
-constexpr int kRowChunks = kRowCopy / 16;        // 18; chunk c of staged row r sits at (c + r) % 18
-constexpr int kLoadRows = kTok / 4;               // rows per loader warp
-constexpr int kSlotBytes = kLoadRows * kRowCopy;   // one loader warp's rows of one tile, e4m3
-constexpr int kStageBytes = 4 * (kAhead + 1) * kSlotBytes;  // all loader warps' staging
+constexpr int kSpan0 = 256, kSpan1 = 320;  // bytes of each row CTA 0 / CTA 1 reads
+constexpr int kStageBytes = kTok * kSpan1;
 constexpr int kAtomBytes = kTok * 128;           // [32 tokens][64 f16 columns], 128-byte swizzle
 constexpr int kCBufBytes = 5 * kAtomBytes;       // 4 latent atoms + the rope atom
 constexpr int kQRopeBytes = kRows * 128;         // [128 heads][64 rope columns] f16
 constexpr int kXCodes = kRows * kTok * 2;        // exchanged partial scores: [128][32] u16 codes
-constexpr int kXBytes = kXCodes + kRows * 4 + kRows;  // + [128] fp32 row minima + [128] step exponents
-constexpr int kRowTab = 1024;                    // list positions per half of the row table
+constexpr int kXMeta = kRows * 8;                // per row: fp32 minimum, u32 step exponent
+constexpr int kXBytes = kXCodes + kXMeta;
+constexpr int kRowTab = 2048;                    // list positions resolved per pass
 constexpr int kRowTabTiles = kRowTab / kTok;
 constexpr int kBtCache = 2048;                   // block-table entries cached in shared memory
 
 constexpr int kOffQRope = 0;
 constexpr int kOffC = kOffQRope + kQRopeBytes;
 constexpr int kOffStage = kOffC + kBufs * kCBufBytes;
-constexpr int kOffSend = kOffStage + kStageBytes;
-constexpr int kOffRecv = kOffSend + kXDepth * kXBytes;
+constexpr int kOffRecv = kOffStage + kStages * kStageBytes;
 constexpr int kOffRows = kOffRecv + kXDepth * kXBytes;
-constexpr int kOffBt = kOffRows + 2 * kRowTab * 4;
+constexpr int kOffBt = kOffRows + kRowTab * 4;
 constexpr int kOffBars = kOffBt + kBtCache * 4;
 
 constexpr uint32_t kTmemCols = 512;
@@ -91,7 +89,7 @@ constexpr uint32_t kTmemO = 0;        // 256 columns: this CTA's output columns,
 constexpr uint32_t kTmemS = 256;      // 4 x 32 columns: scores, then P (f16 pairs) in the first 16
 constexpr uint32_t kTmemQ = 384;      // 128 columns: this CTA's 256 latent Q columns as f16 pairs
 
-constexpr int kLoadWarp0 = 0;         // warps 0-3
+constexpr int kConvWarp0 = 0;         // warps 0-3
 constexpr int kSoftWarp0 = 4;         // warps 4-7: TMEM lane quadrants 0-3
 constexpr int kSendWarp0 = 8;         // warps 8-11: TMEM lane quadrants 0-3
 constexpr int kProdWarp = 12;
@@ -117,48 +115,53 @@ struct MlaArgs {
   float* lse;
   int32_t* status;
   int topk_n, B, H, P, max_pages;
+  int p_shift;        // log2(P) when P is a power of two, else -1
   int64_t num_pages;
   float score_scale;  // ckv_scale * softmax_scale * log2(e)
   float out_scale;    // ckv_scale
 };
 
 struct __align__(8) Bars {
-  uint64_t rows_ready[2], rows_free[2];  // the two halves of the row table
+  uint64_t stage_full[kStages], stage_empty[kStages];
   uint64_t cfull[kBufs], sfull[kBufs], pfull[kBufs], pvdone[kBufs];
   uint64_t sent[kBufs];      // the sender warps have read the scores of a tile
   uint64_t qready;
   uint64_t xfull[kXDepth];   // the peer's partial scores of a tile have landed
   uint64_t xack[kXDepth];    // the peer has read a tile this CTA sent
   uint64_t rdone[kXDepth];   // this CTA's softmax warps have read a received tile
-  uint32_t cmask[kBufs];  // bit i: token row i of the tile takes part (byte w from loader warp w)
-  uint8_t vmask[4][kAhead + 1];  // loader warp w: which of its rows of a staged tile take part
+  uint32_t stage_mask[kStages], cmask[kBufs];  // bit i: token row i of the tile takes part
   uint32_t tmem_base;
 };
 constexpr size_t kSmemBytes = (size_t)kOffBars + sizeof(Bars) + 1024;  // + alignment of the base to 1024
 static_assert(kSmemBytes <= 232448, "shared memory over the per-CTA limit");
 
-// 16-byte global -> shared copy through L2 only; completion is tracked per
-// thread by commit groups.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+// Four rows (y0..y3) of a 2D tensor map, columns x .. x + box - 1, into
+// consecutive box-wide rows of shared memory; completion counted in bytes on
+// the mbarrier.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int y0, int y1, int y2,
+                                            int y3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
+      : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// Wait until at most kAhead of this thread's committed groups are still landing.
-__device__ __forceinline__ void cp_async_wait_ahead() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(kAhead) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) { return pack_f16x2(bf16_lo(v), bf16_hi(v)); }
 
-// Shared memory of this CTA -> shared memory of a peer CTA, completion
-// counted in bytes on the peer's mbarrier.
-__device__ __forceinline__ void bulk_to_peer(uint32_t dst_cluster, uint32_t src, uint32_t bytes, uint32_t bar_cluster) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst_cluster),
-      "r"(src), "r"(bytes), "r"(bar_cluster)
-      : "memory");
+// Remote stores into a peer CTA's shared memory whose bytes are counted on
+// the peer's mbarrier when they land (no separate arrival needed).
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   addr),
+               "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void st_async_v2(uint32_t addr, uint32_t a, uint32_t b, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(addr),
+               "r"(a), "r"(b), "r"(bar)
+               : "memory");
 }
 
 __device__ __forceinline__ uint4 lds128_u32(uint32_t addr) {
@@ -167,8 +170,34 @@ __device__ __forceinline__ uint4 lds128_u32(uint32_t addr) {
   return r;
 }
 
-// The four sender warps only.
-__device__ __forceinline__ void sender_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Maximum / minimum of 32 values as a tree (short dependency chains).
+__device__ __forceinline__ float tree_max32(const float (&x)[32]) {
+  float m[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m[i] = fmaxf(x[2 * i], x[2 * i + 1]);
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+  return m[0];
+}
+__device__ __forceinline__ float tree_min32(const float (&x)[32]) {
+  float m[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m[i] = fminf(x[2 * i], x[2 * i + 1]);
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) m[i] = fminf(m[i], m[i + w]);
+  return m[0];
+}
+// u16 codes <-> floats through the 2^23 bias: for 0 <= v <= 65535 the fp32
+// sum v + 2^23 holds round(v) in its low mantissa bits, and the float with
+// exponent 2^23 and low bits q equals 2^23 + q exactly.
+constexpr float kTwo23 = 8388608.f;
+__device__ __forceinline__ uint32_t biased_code(float v) { return __float_as_uint(v + kTwo23); }
+__device__ __forceinline__ float code_lo(uint32_t w) { return __uint_as_float(prmt(w, 0x4B000000u, 0x7410)) - kTwo23; }
+__device__ __forceinline__ float code_hi(uint32_t w) { return __uint_as_float(prmt(w, 0x4B000000u, 0x7432)) - kTwo23; }
 
 __device__ __forceinline__ uint4 ldg_nc(const void* p) {
   uint4 r;
@@ -181,7 +210,10 @@ __device__ __forceinline__ uint4 ldg_nc(const void* p) {
 // consecutive rows.
 __device__ __forceinline__ uint32_t xunit(int t, int c) { return t * 64 + 16 * (c ^ ((t >> 1) & 3)); }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_decode_kernel(const MlaArgs a) {
+// tm0 / tm1: the cache as [rows][288 u16], boxes of 128 / 160 columns (CTA 0 / CTA 1).
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    mla_decode_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
+                      const MlaArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Bars& bs = *reinterpret_cast<Bars*>(smem + kOffBars);
@@ -198,9 +230,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_dec
   const int ntiles = (n + kTok - 1) / kTok;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&bs.rows_ready[i]), 1);
-      mbar_init(smem_u32(&bs.rows_free[i]), 4);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&bs.stage_full[s]), 1);
+      mbar_init(smem_u32(&bs.stage_empty[s]), 4);
     }
     for (int i = 0; i < kBufs; ++i) {
       mbar_init(smem_u32(&bs.cfull[i]), 4);
@@ -229,61 +261,86 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_dec
 
   if (warp == kProdWarp) {
     // ------------------------------------------------------------ producer
-    // Row table half c % 2 <- list positions 1024 c .. 1024 c + 1023: top-k
-    // entry -> page -> cache row (-1: padding, past the list, or rejected).
     const int64_t tbase = (int64_t)b * a.topk_n;
     const int32_t* bt = a.block_tables + (int64_t)b * a.max_pages;
+    int32_t* rowtab = reinterpret_cast<int32_t*>(smem + kOffRows);
     int32_t* bt_s = reinterpret_cast<int32_t*>(smem + kOffBt);
+    const CUtensorMap* tm = rank ? &tm1 : &tm0;
+    const int span = rank ? kSpan1 : kSpan0;
+    const int x0 = rank ? kLatCols / 2 : 0;  // first u16 column of this CTA's span
     const int npages = (L + a.P - 1) / a.P;
     const int ncached = npages < kBtCache ? npages : kBtCache;
+    for (int j = 0; j < ntiles; ++j) {
+      if (j % kRowTabTiles == 0) {
+        // Resolve list positions 32 j .. 32 j + 2047: top-k entry -> page ->
+        // cache row (-1: padding, past the list, or rejected).  Each lane
+        // keeps 32 loads in flight; the block table is cached on first use.
 #pragma unroll 1
-    for (int i0 = 0; i0 < ncached; i0 += 32 * 16) {
-      int v[16];
+        for (int half = 0; half < kRowTab / 1024; ++half) {
+          const int p0 = j * kTok + 1024 * half + lane;
+          int tok[32];
 #pragma unroll
-      for (int m = 0; m < 16; ++m) {
-        const int i = i0 + lane + 32 * m;
-        v[m] = i < ncached ? bt[i] : 0;
-      }
-#pragma unroll
-      for (int m = 0; m < 16; ++m) {
-        const int i = i0 + lane + 32 * m;
-        if (i < ncached) bt_s[i] = v[m];
-      }
-    }
-    __syncwarp();
-    const int nchunks = (n + kRowTab - 1) / kRowTab;
-    for (int c = 0; c < nchunks; ++c) {
-      if (c >= 2 && !to) to = !mbar_wait(smem_u32(&bs.rows_free[c & 1]), ((c - 2) >> 1) & 1);
-      int32_t* rowtab = reinterpret_cast<int32_t*>(smem + kOffRows) + (c & 1) * kRowTab;
-#pragma unroll 1
-      for (int half = 0; half < kRowTab / 1024; ++half) {
-        const int p0 = c * kRowTab + 32 * 32 * half + lane;
-        int tok[32];
-#pragma unroll
-        for (int m = 0; m < 32; ++m) {
-          const int p = p0 + 32 * m;
-          tok[m] = p < n ? (a.topk ? a.topk[tbase + p] : p) : -1;
-        }
-#pragma unroll
-        for (int m = 0; m < 32; ++m) {
-          int32_t row = -1;
-          const int tk = tok[m];
-          if (tk >= L) {
-            if (a.topk) atomicOr(a.status, kErrBadTopk);
-          } else if (tk >= 0) {
-            const int pi = tk / a.P;
-            const int pg = pi < kBtCache ? bt_s[pi] : bt[pi];
-            if (pg < 0 || (int64_t)pg >= a.num_pages)
-              atomicOr(a.status, kErrBadPage);
-            else
-              row = pg * a.P + (tk - pi * a.P);
+          for (int m = 0; m < 32; ++m) {
+            const int p = p0 + 32 * m;
+            tok[m] = p < n ? (a.topk ? a.topk[tbase + p] : p) : -1;
           }
-          rowtab[32 * 32 * half + lane + 32 * m] = row;
+          if (j == 0 && half == 0) {
+#pragma unroll 1
+            for (int i0 = 0; i0 < ncached; i0 += 32 * 16) {
+              int v[16];
+#pragma unroll
+              for (int m = 0; m < 16; ++m) {
+                const int i = i0 + lane + 32 * m;
+                v[m] = i < ncached ? bt[i] : 0;
+              }
+#pragma unroll
+              for (int m = 0; m < 16; ++m) {
+                const int i = i0 + lane + 32 * m;
+                if (i < ncached) bt_s[i] = v[m];
+              }
+            }
+            __syncwarp();
+          }
+#pragma unroll
+          for (int m = 0; m < 32; ++m) {
+            int32_t row = -1;
+            const int tk = tok[m];
+            if (tk >= L) {
+              if (a.topk) atomicOr(a.status, kErrBadTopk);
+            } else if (tk >= 0) {
+              const int pi = a.p_shift >= 0 ? tk >> a.p_shift : tk / a.P;
+              const int pg = pi < kBtCache ? bt_s[pi] : bt[pi];
+              if (pg < 0 || (int64_t)pg >= a.num_pages)
+                atomicOr(a.status, kErrBadPage);
+              else
+                row = pg * a.P + (tk - pi * a.P);
+            }
+            rowtab[1024 * half + lane + 32 * m] = row;
+          }
         }
+        __syncwarp();
+      }
+      const int st = j % kStages;
+      if (j >= kStages && !to) to = !mbar_wait(smem_u32(&bs.stage_empty[st]), ((j / kStages) - 1) & 1);
+      const int32_t* rt = rowtab + kTok * (j % kRowTabTiles);
+      const uint32_t mask = __ballot_sync(0xFFFFFFFFu, rt[lane] >= 0);
+      const uint32_t full = smem_u32(&bs.stage_full[st]);
+      if (lane == 0) {
+        bs.stage_mask[st] = mask;
+        mbar_arrive_expect_tx(full, (uint32_t)(kTok * span));
       }
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.rows_ready[c & 1]));
+      if (lane < kTok / 4) {  // rows that take no part fetch row 0 and are zeroed when widened
+        const int r = 4 * lane;
+        const int y0 = rt[r] >= 0 ? rt[r] : 0, y1 = rt[r + 1] >= 0 ? rt[r + 1] : 0;
+        const int y2 = rt[r + 2] >= 0 ? rt[r + 2] : 0, y3 = rt[r + 3] >= 0 ? rt[r + 3] : 0;
+        tma_gather4(smem_u32(smem + kOffStage + st * kStageBytes + r * span), tm, x0, y0, y1, y2, y3, full);
+      }
+      __syncwarp();  // the row table may be rewritten after this tile
     }
+    // no copy may still be landing when the CTA retires
+    for (int j = ntiles > kStages ? ntiles - kStages : 0; j < ntiles; ++j)
+      if (!to) to = !mbar_wait(smem_u32(&bs.stage_full[j % kStages]), (j / kStages) & 1);
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
@@ -301,11 +358,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_dec
           for (int k = 0; k < 16; ++k)
             tc::mma_ts(d, tmem + kTmemQ + 8 * k, tc::desc_sw128(cbuf + (k >> 2) * kAtomBytes + 32 * (k & 3), 16, 1024),
                        kIdescQK, k > 0);
+          if (rank) {  // the 64 rope columns
 #pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            const uint32_t koff = 32 * (2 * rank + k);
-            tc::mma_ss(d, tc::desc_sw128(qrope + koff, 16, 1024),
-                       tc::desc_sw128(cbuf + 4 * kAtomBytes + koff, 16, 1024), kIdescQK, 1);
+            for (int k = 0; k < 4; ++k)
+              tc::mma_ss(d, tc::desc_sw128(qrope + 32 * k, 16, 1024),
+                         tc::desc_sw128(cbuf + 4 * kAtomBytes + 32 * k, 16, 1024), kIdescQK, 1);
           }
           tc::mma_commit(smem_u32(&bs.sfull[cb]));
         }
@@ -336,72 +393,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_dec
       }
     }
     __syncwarp();
-  } else if (warp < kLoadWarp0 + 4) {
-    // --------------------------------------------------------- loader warps
-    // Warp w owns token rows 8 w .. 8 w + 7 of every tile: it gathers them
-    // (e4m3, 18 chunks of 16 bytes per row: 16 latent, 2 rope) into staging
-    // slot (tile % 6) five tiles ahead, then widens them to f16 in the
-    // swizzled atoms of latent buffer tile % 4.
-    const int w = warp - kLoadWarp0;
-    const uint8_t* src_lat = a.ckv + kLatCols * rank;
-    const uint8_t* src_rope = a.ckv + kDv + kRopeCols * rank;
-    uint8_t* stage = smem + kOffStage + w * (kAhead + 1) * kSlotBytes;
-    const int32_t* rowtab0 = reinterpret_cast<const int32_t*>(smem + kOffRows);
-    auto issue = [&](int jj) {  // gather this warp's rows of tile jj (nothing past the list)
-      if (jj < ntiles) {
-        const int c = jj / kRowTabTiles;
-        if (jj % kRowTabTiles == 0 && !to) to = !mbar_wait(smem_u32(&bs.rows_ready[c & 1]), (c >> 1) & 1);
-        const int32_t* rt = rowtab0 + (c & 1) * kRowTab + kTok * (jj % kRowTabTiles) + kLoadRows * w;
-        const uint32_t sdst = smem_u32(stage + (jj % (kAhead + 1)) * kSlotBytes);
-#pragma unroll
-        for (int k = 0; k < (kLoadRows * kRowChunks + 31) / 32; ++k) {
-          const int i = lane + 32 * k;
-          if (i < kLoadRows * kRowChunks) {
-            const int r = i / kRowChunks, ch = i - r * kRowChunks;
-            const int32_t row = rt[r];
-            const int u = ch + r < kRowChunks ? ch + r : ch + r - kRowChunks;  // rotated: no bank conflicts
-            if (row >= 0)
-              cp_async16(sdst + r * kRowCopy + 16 * u,
-                         (ch < 16 ? src_lat + 16 * ch : src_rope + 16 * (ch - 16)) + (int64_t)row * kDqk);
-          }
-        }
-        const uint32_t vm = __ballot_sync(0xFFFFFFFFu, lane < kLoadRows && rt[lane < kLoadRows ? lane : 0] >= 0);
-        if (lane == 0) bs.vmask[w][jj % (kAhead + 1)] = (uint8_t)vm;
-        __syncwarp();
-        const bool last_of_chunk = (jj % kRowTabTiles == kRowTabTiles - 1) || jj == ntiles - 1;
-        if (last_of_chunk && lane == 0) tc::mbar_arrive_local(smem_u32(&bs.rows_free[c & 1]));
-      }
-      cp_async_commit();  // one group per tile, empty past the list
-    };
-    for (int jj = 0; jj < kAhead; ++jj) issue(jj);
-    // widening: lane l takes row l % 8, chunks l / 8 + 4 m
-    const int wr = lane & 7, wc0 = lane >> 3;
-    const uint32_t swz = (kLoadRows * w + wr) & 7;
+  } else if (warp < kConvWarp0 + 4) {
+    // ---------------------------------------------------------- converters
+    // 16-byte chunk i of the staged tile (row i / nch, chunk i % nch; chunks
+    // 0-15 latent, 16-19 rope) -> e4m3 -> f16 -> the swizzled atoms.
+    // Consecutive threads read consecutive chunks of a row.
+    const int nch = rank ? kSpan1 / 16 : kSpan0 / 16;
+    const int span = rank ? kSpan1 : kSpan0;
     for (int j = 0; j < ntiles; ++j) {
-      const int cb = j % kBufs;
-      issue(j + kAhead);
-      cp_async_wait_ahead();  // this lane's copies of tile j have landed
-      __syncwarp();           // ... and every lane's
+      const int st = j % kStages, cb = j % kBufs;
+      if (!to) to = !mbar_wait(smem_u32(&bs.stage_full[st]), (j / kStages) & 1);
       if (j >= kBufs && !to) to = !mbar_wait(smem_u32(&bs.pvdone[cb]), ((j - kBufs) / kBufs) & 1);
-      const uint32_t bits = bs.vmask[w][j % (kAhead + 1)];
-      const bool valid = (bits >> wr) & 1;
-      const uint8_t* src = stage + (j % (kAhead + 1)) * kSlotBytes + wr * kRowCopy;
-      uint8_t* cbuf = smem + kOffC + cb * kCBufBytes + (kLoadRows * w + wr) * 128;
+      const uint32_t mask = bs.stage_mask[st];
+      const uint8_t* stage = smem + kOffStage + st * kStageBytes;
+      uint8_t* cbuf = smem + kOffC + cb * kCBufBytes;
 #pragma unroll
-      for (int m = 0; m < 5; ++m) {
-        const int ch = wc0 + 4 * m;
-        if (ch < kRowChunks) {
+      for (int m = 0; m < kSpan1 / 16 * kTok / 128; ++m) {
+        const int i = threadIdx.x - kConvWarp0 * 32 + 128 * m;
+        if (i < nch * kTok) {
+          const int row = rank ? i / (kSpan1 / 16) : i / (kSpan0 / 16);
+          const int ch = i - row * nch;
           uint4 v = make_uint4(0, 0, 0, 0);
-          const int u = ch + wr < kRowChunks ? ch + wr : ch + wr - kRowChunks;
-          if (valid) v = lds128(src + 16 * u);
+          if ((mask >> row) & 1) v = lds128(stage + row * span + 16 * ch);
           uint4 o0, o1;
           e4m3x4_to_f16x2x2(v.x, o0.x, o0.y);
           e4m3x4_to_f16x2x2(v.y, o0.z, o0.w);
           e4m3x4_to_f16x2x2(v.z, o1.x, o1.y);
           e4m3x4_to_f16x2x2(v.w, o1.z, o1.w);
           const int atom = ch < 16 ? (ch >> 2) : 4;
-          const uint32_t unit = ch < 16 ? 2 * (ch & 3) : 4 * rank + 2 * (ch - 16);
-          uint8_t* dst = cbuf + atom * kAtomBytes;
+          const uint32_t unit = ch < 16 ? 2 * (ch & 3) : 2 * (ch - 16);
+          const uint32_t swz = row & 7;
+          uint8_t* dst = cbuf + atom * kAtomBytes + row * 128;
           *reinterpret_cast<uint4*>(dst + 16 * (unit ^ swz)) = o0;
           *reinterpret_cast<uint4*>(dst + 16 * ((unit + 1) ^ swz)) = o1;
         }
@@ -409,24 +431,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_dec
       fence_proxy_async_smem();  // generic writes -> visible to the tensor core
       __syncwarp();
       if (lane == 0) {
-        reinterpret_cast<uint8_t*>(&bs.cmask[cb])[w] = (uint8_t)bits;
+        if (warp == kConvWarp0) bs.cmask[cb] = mask;
+        tc::mbar_arrive_local(smem_u32(&bs.stage_empty[st]));
         tc::mbar_arrive_local(smem_u32(&bs.cfull[cb]));
       }
     }
-    cp_async_wait_all();  // nothing may still be landing when the CTA retires
   } else if (warp >= kSendWarp0) {
     // --------------------------------------------------------- sender warps
-    // Tile j: this CTA's partial scores (log2 units) -> 16-bit fixed point in
-    // send buffer j % 3 -> one bulk copy into the peer's receive buffer.
+    // Tile j: this CTA's partial scores (log2 units) -> 16-bit fixed point,
+    // stored straight into the peer's receive buffer j % 3.
     const int t = threadIdx.x - kSendWarp0 * 32;  // head row = TMEM lane
     const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     const float sc = a.score_scale;
-    const uint32_t send0 = smem_u32(smem + kOffSend);
     const uint32_t peer_recv0 = tc::mapa(smem_u32(smem + kOffRecv), peer);
     for (int j = 0; j < ntiles; ++j) {
       const int sb = j % kBufs, xb = j % kXDepth;
       if (!to) to = !mbar_wait(smem_u32(&bs.sfull[sb]), (j / kBufs) & 1);
-      // the copy of tile j - 3 out of this buffer has landed and been read
+      // the peer has read tile j - 3 out of the buffer this tile goes to
       if (j >= kXDepth && !to) to = !tc::mbar_wait_cluster(smem_u32(&bs.xack[xb]), ((j - kXDepth) / kXDepth) & 1);
       tc::fence_after_sync();
       float x[32];
@@ -440,39 +461,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_dec
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.sent[sb]));  // the softmax may overwrite S with P
-      float lo = x[0], hi = x[0];
-#pragma unroll
-      for (int i = 1; i < 32; ++i) {
-        lo = fminf(lo, x[i]);
-        hi = fmaxf(hi, x[i]);
-      }
+      const float lo = tree_min32(x), hi = tree_max32(x);
       // step = 2^(e - 127), the smallest power of two with (hi - lo) / step <= 65535
       const uint32_t rb = __float_as_uint((hi - lo) * (1.f / 65535.f));
       uint32_t e = ((rb >> 23) & 0xFFu) + ((rb & 0x7FFFFFu) != 0u);
       e = e < 1u ? 1u : (e > 253u ? 253u : e);
       const float inv = __uint_as_float((254u - e) << 23);  // 1 / step, exact
-      const uint32_t buf = send0 + xb * kXBytes;
+      const uint32_t dst = peer_recv0 + xb * kXBytes;
+      const uint32_t rbar = tc::mapa(smem_u32(&bs.xfull[xb]), peer);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t w[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const uint32_t q0 = min(__float2uint_rn((x[8 * c + 2 * k] - lo) * inv), 65535u);
-          const uint32_t q1 = min(__float2uint_rn((x[8 * c + 2 * k + 1] - lo) * inv), 65535u);
-          w[k] = q0 | (q1 << 16);
+          // (x - lo) * inv is exact and <= (hi - lo) * inv <= 65535: no clamp needed
+          const uint32_t q0 = biased_code((x[8 * c + 2 * k] - lo) * inv);
+          const uint32_t q1 = biased_code((x[8 * c + 2 * k + 1] - lo) * inv);
+          w[k] = prmt(q0, q1, 0x5410);
         }
-        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(buf + xunit(t, c)), "r"(w[0]), "r"(w[1]),
-                     "r"(w[2]), "r"(w[3])
-                     : "memory");
+        st_async_v4(dst + xunit(t, c), w[0], w[1], w[2], w[3], rbar);
       }
-      asm volatile("st.shared.f32 [%0], %1;" ::"r"(buf + kXCodes + 4 * t), "f"(lo) : "memory");
-      asm volatile("st.shared.u8 [%0], %1;" ::"r"(buf + kXCodes + 4 * kRows + t), "r"(e) : "memory");
-      fence_proxy_async_smem();
-      sender_sync();
-      if (t == 0) {
-        mbar_arrive_expect_tx(smem_u32(&bs.xfull[xb]), kXBytes);  // the peer's tile j, into recv buffer xb
-        bulk_to_peer(peer_recv0 + xb * kXBytes, buf, kXBytes, tc::mapa(smem_u32(&bs.xfull[xb]), peer));
-      }
+      st_async_v2(dst + kXCodes + 8 * t, __float_as_uint(lo), e, rbar);
     }
   } else {
     // ------------------------------------------------------- softmax warps
@@ -497,7 +506,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_dec
       }
       uint8_t* qr = smem + kOffQRope + t * 128;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < 8 * (int)rank; ++u) {
         uint4 x = make_uint4(0, 0, 0, 0);
         if (have) x = ldg_nc(qrow + kDv + 8 * u);
         const uint4 y = make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z),
@@ -514,11 +523,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_dec
     const float sc = a.score_scale;
     const uint32_t recv0 = smem_u32(smem + kOffRecv);
     float mref = -INFINITY, l = 0.f;
+    // Receive buffer xb expects the peer's tile j only once its tile j - 3 has
+    // been taken, so the expectation never lands in an earlier phase.
+    if (t == 0)
+      for (int j = 0; j < kXDepth && j < ntiles; ++j) mbar_arrive_expect_tx(smem_u32(&bs.xfull[j]), kXBytes);
     for (int j = 0; j < ntiles; ++j) {
       const int sb = j % kBufs, xb = j % kXDepth;
       if (!to) to = !mbar_wait(smem_u32(&bs.sfull[sb]), (j / kBufs) & 1);
       if (!to) to = !mbar_wait(smem_u32(&bs.cfull[sb]), (j / kBufs) & 1);
       if (!to) to = !tc::mbar_wait_cluster(smem_u32(&bs.xfull[xb]), (j / kXDepth) & 1);
+      if (t == 0 && j + kXDepth < ntiles) mbar_arrive_expect_tx(smem_u32(&bs.xfull[xb]), kXBytes);
       tc::fence_after_sync();
       // ---- s = own exact partial + the peer's decoded partial
       float s[32];
@@ -529,8 +543,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_dec
         const uint32_t theirs = recv0 + xb * kXBytes;
         float plo;
         uint32_t pe;
-        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(plo) : "r"(theirs + kXCodes + 4 * t) : "memory");
-        asm volatile("ld.shared.u8 %0, [%1];" : "=r"(pe) : "r"(theirs + kXCodes + 4 * kRows + t) : "memory");
+        uint32_t plo_bits;
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(plo_bits), "=r"(pe) : "r"(theirs + kXCodes + 8 * t) : "memory");
+        plo = __uint_as_float(plo_bits);
         const float pstep = __uint_as_float(pe << 23);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -538,8 +553,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_dec
           const uint32_t wq[4] = {hq.x, hq.y, hq.z, hq.w};
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const float p0 = fmaf(__uint2float_rn(wq[k] & 0xFFFFu), pstep, plo);
-            const float p1 = fmaf(__uint2float_rn(wq[k] >> 16), pstep, plo);
+            const float p0 = fmaf(code_lo(wq[k]), pstep, plo);
+            const float p1 = fmaf(code_hi(wq[k]), pstep, plo);
             s[8 * c + 2 * k] = fmaf(__uint_as_float(v[8 * c + 2 * k]), sc, p0);
             s[8 * c + 2 * k + 1] = fmaf(__uint_as_float(v[8 * c + 2 * k + 1]), sc, p1);
           }
@@ -550,12 +565,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_dec
 
       // ---- mask, tile maximum, lazy reference update
       const uint32_t mask = bs.cmask[sb];
-      float mx = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        s[i] = ((mask >> i) & 1) ? s[i] : -INFINITY;
-        mx = fmaxf(mx, s[i]);
-      }
+      for (int i = 0; i < 32; ++i) s[i] = ((mask >> i) & 1) ? s[i] : -INFINITY;
+      const float mx = tree_max32(s);
       const bool grow = mx > mref + kRescaleLog2;
       float alpha = 1.f;
       if (grow) {
@@ -683,6 +695,7 @@ int pfkv_mla_decode_attn(void* out, const void* q, const void* ckv_cache, const 
   a.B = batch;
   a.H = num_heads;
   a.P = page_size;
+  a.p_shift = (page_size & (page_size - 1)) == 0 ? __builtin_ctz((unsigned)page_size) : -1;
   a.max_pages = max_pages_per_seq;
   a.num_pages = num_pages;
   a.score_scale = ckv_scale * softmax_scale * kLog2e;
@@ -696,7 +709,18 @@ int pfkv_mla_decode_attn(void* out, const void* q, const void* ckv_cache, const 
   }
   if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), s) != cudaSuccess)
     return check_cuda("mla_decode status reset");
-  mla_decode_kernel<<<dim3(2 * batch), kThreads, kSmemBytes, s>>>(a);
+  // The cache as [rows][288 u16]: CTA 0 reads u16 columns 0..127, CTA 1 128..287.
+  const cuuint64_t dims[2] = {kDqk / 2, (cuuint64_t)num_pages * page_size};
+  const cuuint64_t strides[1] = {kDqk};
+  CUtensorMap tm0, tm1;
+  const cuuint32_t box0[2] = {kSpan0 / 2, 1}, box1[2] = {kSpan1 / 2, 1};
+  int rc = encode_tensor_map(&tm0, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(ckv_cache), dims, strides,
+                             box0, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (rc == PFKV_OK)
+    rc = encode_tensor_map(&tm1, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(ckv_cache), dims, strides,
+                           box1, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (rc != PFKV_OK) return rc;
+  mla_decode_kernel<<<dim3(2 * batch), kThreads, kSmemBytes, s>>>(tm0, tm1, a);
   return check_cuda("mla_decode launch");
 }
 
