@@ -24,7 +24,8 @@
 // into its own output columns; each half is normalised by its own running sum.
 //
 // Per 32-token tile, with four tiles in flight (scores and P in tensor
-// memory, the widened latent tile in shared memory):
+// memory, the widened latent tiles in shared memory, two tiles per buffer so
+// that the scores of a tile pair come from one N = 64 MMA sequence):
 //   producer warp   resolves the cache rows of 2048 list positions at a time
 //                   (top-k entry -> block table, cached in shared memory ->
 //                   row) into a shared table and gathers this CTA's span of
@@ -33,8 +34,9 @@
 //   converter warps widen the tile to f16 (exact) in the 128-byte-swizzled
 //                   layout the MMA reads, K-major for the scores and MN-major
 //                   for the output product;
-//   MMA thread      S[128 x 32] = Q . C^T (16 or 20 K steps), and two tiles later
-//                   O += P . C[:, own 256] (2 K steps, N = 256);
+//   MMA thread      S[128 x 64] = Q . C^T for a tile pair (16 or 20 K steps) and
+//                   O += P . C[:, own 256] (2 K steps, N = 256), each issued
+//                   as soon as its inputs are ready;
 //   sender warps    read S, encode it and store it into the peer's receive
 //                   buffer;
 //   softmax warps   (one TMEM lane per head) add the peer's partial, take the
@@ -66,8 +68,9 @@ constexpr int kXDepth = 3;            // exchange buffers per direction
 constexpr int kLatCols = 256;         // latent columns one CTA contracts (and outputs)
 constexpr int kSpan0 = 256, kSpan1 = 320;  // bytes of each row CTA 0 / CTA 1 reads
 constexpr int kStageBytes = kTok * kSpan1;
-constexpr int kAtomBytes = kTok * 128;           // [32 tokens][64 f16 columns], 128-byte swizzle
-constexpr int kCBufBytes = 5 * kAtomBytes;       // 4 latent atoms + the rope atom
+constexpr int kAtomBytes = 2 * kTok * 128;       // [64 tokens: a tile pair][64 f16 columns], 128-byte swizzle
+constexpr int kCBufBytes = 5 * kAtomBytes;       // 4 latent atoms + the rope atom, for a tile pair
+constexpr int kPairs = kBufs / 2;                // pair buffers
 constexpr int kQRopeBytes = kRows * 128;         // [128 heads][64 rope columns] f16
 constexpr int kXCodes = kRows * kTok * 2;        // exchanged partial scores: [128][32] u16 codes
 constexpr int kXMeta = kRows * 8;                // per row: fp32 minimum, u32 step exponent
@@ -78,7 +81,7 @@ constexpr int kBtCache = 2048;                   // block-table entries cached i
 
 constexpr int kOffQRope = 0;
 constexpr int kOffC = kOffQRope + kQRopeBytes;
-constexpr int kOffStage = kOffC + kBufs * kCBufBytes;
+constexpr int kOffStage = kOffC + kPairs * kCBufBytes;
 constexpr int kOffRecv = kOffStage + kStages * kStageBytes;
 constexpr int kOffRows = kOffRecv + kXDepth * kXBytes;
 constexpr int kOffBt = kOffRows + kRowTab * 4;
@@ -96,9 +99,8 @@ constexpr int kProdWarp = 12;
 constexpr int kMmaWarp = 13;
 constexpr int kAckWarp = 14;
 constexpr int kThreads = 15 * 32;
-constexpr int kPvLag = 2;             // the MMA thread issues O += P(j - 2) C(j - 2) after S(j)
 
-constexpr uint32_t kIdescQK = tc::idesc_f16(kRows, kTok, false);
+constexpr uint32_t kIdescQK = tc::idesc_f16(kRows, 2 * kTok, false);
 constexpr uint32_t kIdescPV = tc::idesc_f16(kRows, kLatCols, true);
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -343,44 +345,63 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!to) to = !mbar_wait(smem_u32(&bs.stage_full[j % kStages]), (j / kStages) & 1);
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
+    // Issues O += P(j) . C(j)[:, own columns] as soon as P(j) is stored (first:
+    // it frees a widened tile buffer), and S = Q . C^T for a tile pair as soon
+    // as both tiles are widened and their score columns are free; the scores
+    // run up to four tiles ahead.
     if (lane == 0) {
       if (!to) to = !mbar_wait(smem_u32(&bs.qready), 0);
       tc::fence_after_sync();
-      const uint32_t cbase0 = smem_u32(smem + kOffC), qrope = smem_u32(smem + kOffQRope);
-      for (int j = 0; j < ntiles + kPvLag; ++j) {
-        if (j < ntiles) {  // S(j) = Q . C(j)^T
-          const int cb = j % kBufs;
-          if (!to) to = !mbar_wait(smem_u32(&bs.cfull[cb]), (j / kBufs) & 1);
+      const uint32_t cbase0 = smem_u32(smem + kOffC);
+      const uint64_t qdesc = tc::desc_sw128(smem_u32(smem + kOffQRope), 16, 1024);
+      int qn = 0, pn = 0;  // next tile for the scores (even: a pair) / for the output
+      long long idle_since = clock64();
+      while (pn < ntiles && !to) {
+        bool issued = false;
+        if (pn < qn && mbar_test_wait(smem_u32(&bs.pfull[pn % kBufs]), (pn / kBufs) & 1)) {
           tc::fence_after_sync();
-          const uint32_t cbuf = cbase0 + cb * kCBufBytes;
-          const uint32_t d = tmem + kTmemS + kTok * cb;
+          const uint64_t vdesc =
+              tc::desc_sw128(cbase0 + ((pn / 2) % kPairs) * kCBufBytes + (pn & 1) * kTok * 128, kAtomBytes, 1024);
+#pragma unroll
+          for (int k = 0; k < kTok / 16; ++k)
+            tc::mma_ts(tmem + kTmemO, tmem + kTmemS + kTok * (pn % kBufs) + 8 * k, vdesc + (uint64_t)((2048 * k) >> 4),
+                       kIdescPV, (pn > 0 || k > 0));
+          tc::mma_commit(smem_u32(&bs.pvdone[pn % kBufs]));
+          ++pn;
+          issued = true;
+        }
+        // the pair's score columns held P(qn - 4) and P(qn - 3): both products issued
+        if (qn < ntiles && pn >= qn - 2 && mbar_test_wait(smem_u32(&bs.cfull[qn % kBufs]), (qn / kBufs) & 1) &&
+            (qn + 1 >= ntiles || mbar_test_wait(smem_u32(&bs.cfull[(qn + 1) % kBufs]), ((qn + 1) / kBufs) & 1))) {
+          tc::fence_after_sync();
+          // descriptors built once; K steps add constant offsets to the address field
+          const uint64_t bdesc = tc::desc_sw128(cbase0 + ((qn / 2) % kPairs) * kCBufBytes, 16, 1024);
+          const uint32_t d = tmem + kTmemS + kTok * (qn % kBufs);
 #pragma unroll
           for (int k = 0; k < 16; ++k)
-            tc::mma_ts(d, tmem + kTmemQ + 8 * k, tc::desc_sw128(cbuf + (k >> 2) * kAtomBytes + 32 * (k & 3), 16, 1024),
+            tc::mma_ts(d, tmem + kTmemQ + 8 * k, bdesc + (uint64_t)(((k >> 2) * kAtomBytes + 32 * (k & 3)) >> 4),
                        kIdescQK, k > 0);
           if (rank) {  // the 64 rope columns
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              tc::mma_ss(d, tc::desc_sw128(qrope + 32 * k, 16, 1024),
-                         tc::desc_sw128(cbuf + 4 * kAtomBytes + 32 * k, 16, 1024), kIdescQK, 1);
+              tc::mma_ss(d, qdesc + (uint64_t)((32 * k) >> 4), bdesc + (uint64_t)((4 * kAtomBytes + 32 * k) >> 4),
+                         kIdescQK, 1);
           }
-          tc::mma_commit(smem_u32(&bs.sfull[cb]));
+          tc::mma_commit(smem_u32(&bs.sfull[qn % kBufs]));
+          if (qn + 1 < ntiles) tc::mma_commit(smem_u32(&bs.sfull[(qn + 1) % kBufs]));
+          qn += 2;
+          issued = true;
         }
-        if (j >= kPvLag) {  // O += P(pj) . C(pj)[:, own columns]
-          const int pj = j - kPvLag, pb = pj % kBufs;
-          if (!to) to = !mbar_wait(smem_u32(&bs.pfull[pb]), (pj / kBufs) & 1);
-          tc::fence_after_sync();
-          const uint32_t cbuf = cbase0 + pb * kCBufBytes;
-#pragma unroll
-          for (int k = 0; k < kTok / 16; ++k)
-            tc::mma_ts(tmem + kTmemO, tmem + kTmemS + kTok * pb + 8 * k,
-                       tc::desc_sw128(cbuf + 2048 * k, kAtomBytes, 1024), kIdescPV, (pj > 0 || k > 0));
-          tc::mma_commit(smem_u32(&bs.pvdone[pb]));
+        if (issued) {
+          idle_since = clock64();
+        } else {
+          __nanosleep(32);  // leave issue slots to the warps sharing this scheduler
+          if (clock64() - idle_since > kWaitLimitCycles) to = true;
         }
       }
       // no MMA may still be running when the tensor memory is freed
-      if (ntiles > 0 && !to)
-        to = !mbar_wait(smem_u32(&bs.pvdone[(ntiles - 1) % kBufs]), ((ntiles - 1) / kBufs) & 1);
+      if (ntiles > 0 && pn > 0 && !mbar_wait(smem_u32(&bs.pvdone[(pn - 1) % kBufs]), ((pn - 1) / kBufs) & 1))
+        to = true;
     }
     __syncwarp();
   } else if (warp == kAckWarp) {
@@ -397,35 +418,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- converters
     // 16-byte chunk i of the staged tile (row i / nch, chunk i % nch; chunks
     // 0-15 latent, 16-19 rope) -> e4m3 -> f16 -> the swizzled atoms.
-    // Consecutive threads read consecutive chunks of a row.
+    // Consecutive threads read consecutive chunks of a row; the offsets are
+    // the same for every tile.
     const int nch = rank ? kSpan1 / 16 : kSpan0 / 16;
     const int span = rank ? kSpan1 : kSpan0;
+    constexpr int kChunksPerThread = kSpan1 / 16 * kTok / 128;  // 5
+    int src_off[kChunksPerThread], dst_off[kChunksPerThread], crow[kChunksPerThread];
+#pragma unroll
+    for (int m = 0; m < kChunksPerThread; ++m) {
+      const int i = threadIdx.x - kConvWarp0 * 32 + 128 * m;
+      const int row = i / nch, ch = i - (i / nch) * nch;
+      const int atom = ch < 16 ? (ch >> 2) : 4;
+      const uint32_t unit = ch < 16 ? 2 * (ch & 3) : 2 * (ch - 16);
+      crow[m] = i < nch * kTok ? row : -1;
+      src_off[m] = row * span + 16 * ch;
+      dst_off[m] = atom * kAtomBytes + row * 128 + 16 * (unit ^ (row & 7));  // unit + 1: ^ 16
+    }
     for (int j = 0; j < ntiles; ++j) {
       const int st = j % kStages, cb = j % kBufs;
       if (!to) to = !mbar_wait(smem_u32(&bs.stage_full[st]), (j / kStages) & 1);
       if (j >= kBufs && !to) to = !mbar_wait(smem_u32(&bs.pvdone[cb]), ((j - kBufs) / kBufs) & 1);
       const uint32_t mask = bs.stage_mask[st];
       const uint8_t* stage = smem + kOffStage + st * kStageBytes;
-      uint8_t* cbuf = smem + kOffC + cb * kCBufBytes;
+      uint8_t* cbuf = smem + kOffC + ((j / 2) % kPairs) * kCBufBytes + (j & 1) * kTok * 128;
 #pragma unroll
-      for (int m = 0; m < kSpan1 / 16 * kTok / 128; ++m) {
-        const int i = threadIdx.x - kConvWarp0 * 32 + 128 * m;
-        if (i < nch * kTok) {
-          const int row = rank ? i / (kSpan1 / 16) : i / (kSpan0 / 16);
-          const int ch = i - row * nch;
+      for (int m = 0; m < kChunksPerThread; ++m) {
+        if (crow[m] >= 0) {
           uint4 v = make_uint4(0, 0, 0, 0);
-          if ((mask >> row) & 1) v = lds128(stage + row * span + 16 * ch);
+          if ((mask >> crow[m]) & 1) v = lds128(stage + src_off[m]);
           uint4 o0, o1;
           e4m3x4_to_f16x2x2(v.x, o0.x, o0.y);
           e4m3x4_to_f16x2x2(v.y, o0.z, o0.w);
           e4m3x4_to_f16x2x2(v.z, o1.x, o1.y);
           e4m3x4_to_f16x2x2(v.w, o1.z, o1.w);
-          const int atom = ch < 16 ? (ch >> 2) : 4;
-          const uint32_t unit = ch < 16 ? 2 * (ch & 3) : 2 * (ch - 16);
-          const uint32_t swz = row & 7;
-          uint8_t* dst = cbuf + atom * kAtomBytes + row * 128;
-          *reinterpret_cast<uint4*>(dst + 16 * (unit ^ swz)) = o0;
-          *reinterpret_cast<uint4*>(dst + 16 * ((unit + 1) ^ swz)) = o1;
+          // units u and u + 1 (u even) differ in bit 0, so their swizzled
+          // positions differ by exactly 16 bytes
+          *reinterpret_cast<uint4*>(cbuf + dst_off[m]) = o0;
+          *reinterpret_cast<uint4*>(cbuf + (dst_off[m] ^ 16)) = o1;
         }
       }
       fence_proxy_async_smem();  // generic writes -> visible to the tensor core
@@ -447,8 +476,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int j = 0; j < ntiles; ++j) {
       const int sb = j % kBufs, xb = j % kXDepth;
       if (!to) to = !mbar_wait(smem_u32(&bs.sfull[sb]), (j / kBufs) & 1);
-      // the peer has read tile j - 3 out of the buffer this tile goes to
-      if (j >= kXDepth && !to) to = !tc::mbar_wait_cluster(smem_u32(&bs.xack[xb]), ((j - kXDepth) / kXDepth) & 1);
       tc::fence_after_sync();
       float x[32];
       {
@@ -461,6 +488,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.sent[sb]));  // the softmax may overwrite S with P
+      // the peer has read tile j - 3 out of the buffer this tile goes to
+      if (j >= kXDepth && !to) to = !tc::mbar_wait_cluster(smem_u32(&bs.xack[xb]), ((j - kXDepth) / kXDepth) & 1);
       const float lo = tree_min32(x), hi = tree_max32(x);
       // step = 2^(e - 127), the smallest power of two with (hi - lo) / step <= 65535
       const uint32_t rb = __float_as_uint((hi - lo) * (1.f / 65535.f));
@@ -565,8 +594,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
       // ---- mask, tile maximum, lazy reference update
       const uint32_t mask = bs.cmask[sb];
+      if (mask != 0xFFFFFFFFu) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) s[i] = ((mask >> i) & 1) ? s[i] : -INFINITY;
+        for (int i = 0; i < 32; ++i) s[i] = ((mask >> i) & 1) ? s[i] : -INFINITY;
+      }
       const float mx = tree_max32(s);
       const bool grow = mx > mref + kRescaleLog2;
       float alpha = 1.f;
