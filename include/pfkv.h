@@ -202,8 +202,14 @@ PFKV_API int pfkv_paged_decode_attn_noalloc(void *out, const void *q, const void
  *   topk_idx   int32 [batch][topk] or NULL
  *   lse_out    optional fp32 [batch][num_heads]
  * Supported: d_latent 512, d_rope 64, num_heads 128 or fewer and a multiple of
- * 16, page_size a multiple of 16.  Listed indices >= L_b are skipped and set
- * PFKV_DEVERR_BAD_TOPK. */
+ * 16, page_size a multiple of 16, num_pages * page_size < 2^31.  Listed
+ * indices >= L_b are skipped and set PFKV_DEVERR_BAD_TOPK.
+ * Numerics: f16 operands (the latent exactly; q rounded from bf16, exact for
+ * 2^-14 <= |q| <= 65504) with f32 accumulation.  Each request runs on a pair
+ * of SMs that each contract part of the 576 columns; a score is one SM's
+ * exact f32 partial plus the other's partial carried as 16-bit fixed point
+ * over its range within a 32-token tile (at most range / 65535 added error,
+ * in log2 units).  The workspace holds only the status word. */
 PFKV_API size_t pfkv_mla_decode_workspace_size(int batch, int num_heads, int d_latent, int topk);
 PFKV_API int pfkv_mla_decode_attn(void *out, const void *q, const void *ckv_cache,
                          const int32_t *block_tables, int max_pages_per_seq,
