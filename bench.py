@@ -280,10 +280,28 @@ def other_workloads(pf, peak_gbs, peak_tf, iters=10):
         t_dec = time_events(s.decode, iters, flush)
         t_app = time_events(s.append, iters, flush)
         gbs = s.decode_bytes() / t_dec / 1e9
+        # opt-in page-tag integrity check over the same block tables (one tag per page)
+        st = s.st
+        page_tags = (torch.arange(w.num_pages, dtype=torch.int64, device="cuda") * 2654435761 % (1 << 31)).to(torch.int32)
+        table_tags = page_tags[st.block_tables.clamp(min=0).long()].contiguous()
+        req_status = torch.empty(w.B, dtype=torch.int32, device="cuda")
+        check = lambda: pf.verify_page_tags(st.block_tables, table_tags, st.context_lens, w.P, page_tags, req_status)
+        check()
+        t_chk = time_events(check, iters, flush)
+
+        def checked_decode():
+            check()
+            s.decode()
+        t_both = time_events(checked_decode, iters, flush)
         res[name] = {"decode_us": round(t_dec * 1e6, 2), "append_us": round(t_app * 1e6, 2),
                      "kv_bytes": s.bytes()["kv"], "decode_GBs": round(gbs, 1),
                      "frac_of_hbm_peak": round(gbs / peak_gbs, 4),
-                     "query_tokens_per_s": round(w.B / (t_dec + t_app), 1)}
+                     "query_tokens_per_s": round(w.B / (t_dec + t_app), 1),
+                     "page_tag_check_us": round(t_chk * 1e6, 2),
+                     "page_tag_check_pct_of_decode": round(100 * t_chk / t_dec, 3),
+                     "decode_with_page_tag_check_us": round(t_both * 1e6, 2),
+                     "page_tag_check_added_pct": round(100 * (t_both - t_dec) / t_dec, 3),
+                     "page_tag_check_flagged": int((req_status != 0).sum().item())}
         del s
         torch.cuda.empty_cache()
 

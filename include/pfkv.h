@@ -233,6 +233,34 @@ PFKV_API int pfkv_validate_tables(const int32_t *block_tables, int max_pages_per
                          const int32_t *topk_idx, int topk, const int64_t *slot_mapping,
                          int num_slots, int32_t *d_err_word, pfkv_stream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* verify_page_tags -- KV page integrity check before decode (Workers AI post,
+ * §3 "共用 KV キャッシュの保護", 動作原理): every physical page carries a tag
+ * that changes each time the page is handed out again; right before decode
+ * reads the cache, each request's pages are checked against the tags the
+ * request recorded when it mapped them, and a request that fails is aborted
+ * instead of reading another request's data.  A separate batched kernel, not
+ * fused into attention (the post's cost argument).
+ *   block_tables    int32  [batch][max_pages_per_seq]  device
+ *   table_tags      uint32 [batch][max_pages_per_seq]  device: tag recorded with each entry
+ *   context_lens    int32  [batch]                     device
+ *   page_tags       uint32 [num_pages]                 device: current tag of each page
+ *   request_status  int32  [batch]                     device, written: 0 (ok) or an OR of
+ *     PFKV_REQ_TAG_MISMATCH  a page the request reads (entry i < ceil(L / page_size)) carries
+ *                            a different tag now
+ *     PFKV_REQ_BAD_INDEX     such an entry is outside [0, num_pages), or L < 0 or
+ *                            L > max_pages_per_seq * page_size
+ * Entries past a request's context are not read and not checked.  Asynchronous
+ * on `stream`; the caller reads request_status after the stream reaches this
+ * point and leaves flagged requests out of the decode call.  Returns PFKV_OK,
+ * PFKV_ERR_INVALID_ARG or PFKV_ERR_CUDA. */
+#define PFKV_REQ_TAG_MISMATCH 0x1
+#define PFKV_REQ_BAD_INDEX 0x2
+PFKV_API int pfkv_verify_page_tags(const int32_t *block_tables, const uint32_t *table_tags,
+                                   int max_pages_per_seq, const int32_t *context_lens, int batch,
+                                   int page_size, const uint32_t *page_tags, int64_t num_pages,
+                                   int32_t *request_status, pfkv_stream_t stream);
+
 /* Copy the workspace status word (bits PFKV_DEVERR_*) to *status after
  * synchronising `stream`.  Returns PFKV_OK, or PFKV_ERR_CUDA. */
 PFKV_API int pfkv_workspace_status(const void *workspace, int32_t *status, pfkv_stream_t stream);

@@ -85,6 +85,8 @@ def lib():
             L.orc_mla_decode.restype = i32
             L.orc_mla_decode.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32,
                                          i32, i64, f32, f32, i64, i64]
+            L.orc_verify_page_tags.restype = i32
+            L.orc_verify_page_tags.argtypes = [vp, vp, i32, vp, i32, i32, vp, i64, vp]
             L.orc_kv_bytes.restype = i64
             L.orc_kv_bytes.argtypes = [i64, i64, i64, i64, i64]
             _lib = L
@@ -229,3 +231,19 @@ def mla_decode_one(q_head_bf16, ckv_cache, bt_row, L: int, topk_row, page_size: 
 
 def kv_bytes(layers: int, kv_heads: int, head_dim: int, tokens: int, bytes_per_elem: int) -> int:
     return int(lib().orc_kv_bytes(layers, kv_heads, head_dim, tokens, bytes_per_elem))
+
+
+REQ_TAG_MISMATCH = 0x1
+REQ_BAD_INDEX = 0x2
+
+
+def verify_page_tags(block_tables, table_tags, context_lens, page_size: int, page_tags) -> np.ndarray:
+    """Per-request status of the page-tag check: 0 or an OR of REQ_TAG_MISMATCH / REQ_BAD_INDEX."""
+    bt = _c(block_tables, np.int32)
+    tt = _c(np.asarray(table_tags).astype(np.uint32, copy=False), np.uint32)
+    cl = _c(context_lens, np.int32)
+    pt = _c(np.asarray(page_tags).astype(np.uint32, copy=False), np.uint32)
+    status = np.zeros(cl.shape[0], np.int32)
+    _chk(lib().orc_verify_page_tags(_ptr(bt), _ptr(tt), bt.shape[1], _ptr(cl), cl.shape[0], page_size,
+                                    _ptr(pt), pt.shape[0], _ptr(status)))
+    return status

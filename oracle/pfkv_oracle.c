@@ -449,3 +449,41 @@ int64_t orc_kv_bytes(int64_t layers, int64_t kv_heads, int64_t head_dim, int64_t
 {
     return 2 * layers * kv_heads * head_dim * tokens * bytes_per_elem;
 }
+
+/* ------------------------------------------------------------------------- */
+/* KV page integrity check (Workers AI post, section 3 "共用 KV キャッシュの保護",
+ * 動作原理): every physical page has a tag that changes whenever the page is
+ * handed out again; before decode, each request's pages are compared with the
+ * tags it recorded when it mapped them.  The request reads the entries
+ * i < ceil(L / P) of its block-table row.  status[b] = 0, or the OR of
+ * ORC_REQ_TAG_MISMATCH (a read page now carries another tag) and
+ * ORC_REQ_BAD_INDEX (a read entry outside [0, num_pages), or L outside
+ * [0, max_pages * P]; then the row is checked up to the clamped length). */
+int orc_verify_page_tags(const int32_t *block_tables, const uint32_t *table_tags, int max_pages,
+                         const int32_t *context_lens, int B, int P, const uint32_t *page_tags,
+                         int64_t num_pages, int32_t *status)
+{
+    if (B < 0 || max_pages <= 0 || P <= 0 || num_pages <= 0)
+        return ORC_ERR_ARG;
+    for (int b = 0; b < B; b++) {
+        int32_t flags = 0;
+        int64_t L = context_lens[b];
+        if (L < 0) {
+            flags |= ORC_REQ_BAD_INDEX;
+            L = 0;
+        } else if (L > (int64_t)max_pages * P) {
+            flags |= ORC_REQ_BAD_INDEX;
+            L = (int64_t)max_pages * P;
+        }
+        int64_t used = (L + P - 1) / P;
+        for (int64_t i = 0; i < used; i++) {
+            int32_t page = block_tables[(int64_t)b * max_pages + i];
+            if (page < 0 || page >= num_pages)
+                flags |= ORC_REQ_BAD_INDEX;
+            else if (page_tags[page] != table_tags[(int64_t)b * max_pages + i])
+                flags |= ORC_REQ_TAG_MISMATCH;
+        }
+        status[b] = flags;
+    }
+    return ORC_OK;
+}

@@ -49,6 +49,11 @@ int orc_mla_decode(double *out, double *lse, const uint16_t *q, const uint8_t *c
                    int64_t num_pages, float ckv_scale, float softmax_scale,
                    int64_t u_begin, int64_t u_end);
 
+#define ORC_REQ_TAG_MISMATCH 0x1
+#define ORC_REQ_BAD_INDEX 0x2
+int orc_verify_page_tags(const int32_t *block_tables, const uint32_t *table_tags, int max_pages,
+                         const int32_t *context_lens, int B, int P, const uint32_t *page_tags,
+                         int64_t num_pages, int32_t *status);
 int64_t orc_kv_bytes(int64_t layers, int64_t kv_heads, int64_t head_dim, int64_t tokens,
                      int64_t bytes_per_elem);
 

@@ -21,9 +21,9 @@ __all__ = [
     "PfkvError", "load", "lib_path", "kv_append_fp8", "kv_append_bf16",
     "paged_decode_workspace_size", "paged_decode_attn", "paged_decode_attn_noalloc",
     "mla_decode_workspace_size",
-    "mla_decode_attn", "validate_tables", "workspace_status", "selftest_barrier_timeout", "last_error",
-    "version",
-    "CACHE_FP8_E4M3", "CACHE_BF16", "DEVERR",
+    "mla_decode_attn", "validate_tables", "verify_page_tags", "workspace_status", "selftest_barrier_timeout",
+    "last_error", "version",
+    "CACHE_FP8_E4M3", "CACHE_BF16", "DEVERR", "REQ_TAG_MISMATCH", "REQ_BAD_INDEX",
 ]
 
 CACHE_FP8_E4M3 = 0
@@ -32,6 +32,9 @@ DEVERR = {
     "WAIT_TIMEOUT": 0x01, "BAD_PAGE": 0x02, "BAD_CONTEXT": 0x04, "WORKSPACE": 0x08,
     "BAD_TOPK": 0x10, "BAD_SLOT": 0x20,
 }
+
+REQ_TAG_MISMATCH = 0x1  # verify_page_tags: a page the request reads carries another tag
+REQ_BAD_INDEX = 0x2     # verify_page_tags: a page id or context length out of range
 
 _lock = threading.Lock()
 _lib = None
@@ -72,6 +75,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             "pfkv_mla_decode_attn": (i32, [vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32,
                                            i64, f32, f32, vp, sz, vp, vp]),
             "pfkv_validate_tables": (i32, [vp, i32, vp, i32, i32, i64, vp, i32, vp, i32, vp, vp]),
+            "pfkv_verify_page_tags": (i32, [vp, vp, i32, vp, i32, i32, vp, i64, vp, vp]),
             "pfkv_workspace_status": (i32, [vp, vp, vp]),
             "pfkv_selftest_barrier_timeout": (i32, [vp, vp]),
             "pfkv_last_error": (ctypes.c_char_p, []),
@@ -218,6 +222,20 @@ def validate_tables(block_tables, context_lens, page_size: int, num_pages: int, 
                                      page_size, num_pages, _ptr(topk_idx), k, _ptr(slot_mapping), ns,
                                      _ptr(err_word), _stream(stream))
     _check("validate_tables", rc)
+
+
+def verify_page_tags(block_tables, table_tags, context_lens, page_size: int, page_tags, request_status,
+                     stream=None):
+    """Page-tag integrity check before decode: request_status[b] (int32, device) receives 0 or an
+    OR of REQ_TAG_MISMATCH / REQ_BAD_INDEX.  table_tags (uint32 or int32 bits) has the shape of
+    block_tables; page_tags holds one tag per physical page."""
+    B = context_lens.shape[0]
+    if tuple(table_tags.shape) != tuple(block_tables.shape):
+        raise ValueError("table_tags must have the shape of block_tables")
+    rc = load().pfkv_verify_page_tags(_ptr(block_tables), _ptr(table_tags), block_tables.shape[1],
+                                      _ptr(context_lens), B, page_size, _ptr(page_tags), page_tags.shape[0],
+                                      _ptr(request_status), _stream(stream))
+    _check("verify_page_tags", rc)
 
 
 def selftest_barrier_timeout(status, stream=None):

@@ -56,6 +56,57 @@ __global__ void __launch_bounds__(256) validate_kernel(const ValidateArgs a) {
   if (bits && (threadIdx.x & 31) == 0) atomicOr(a.err, bits);
 }
 
+// Page generation tags: request b reads pages block_tables[b][0 .. used-1];
+// each must still carry the tag the request recorded when it mapped it.
+struct TagArgs {
+  const int32_t* block_tables;
+  const uint32_t* table_tags;
+  const int32_t* context_lens;
+  const uint32_t* page_tags;
+  int32_t* status;
+  int max_pages, P;
+  int64_t num_pages;
+};
+
+// One CTA per request; each thread keeps kTagUnroll block-table loads and then
+// kTagUnroll tag loads in flight, so a row of up to 8192 entries costs two
+// memory round trips.  The CTA writes the request's status itself.
+constexpr int kTagThreads = 1024, kTagUnroll = 8;
+__global__ void __launch_bounds__(kTagThreads) verify_tags_kernel(const TagArgs a) {
+  const int b = blockIdx.x;
+  int bad = 0, mismatch = 0;
+  int L = a.context_lens[b];
+  if (L < 0 || L > a.max_pages * a.P) {
+    bad = 1;
+    L = L < 0 ? 0 : a.max_pages * a.P;
+  }
+  const int used = (L + a.P - 1) / a.P;
+  const int64_t row = (int64_t)b * a.max_pages;
+  for (int base = 0; base < used; base += kTagThreads * kTagUnroll) {
+    int page[kTagUnroll];
+    uint32_t want[kTagUnroll];
+#pragma unroll
+    for (int k = 0; k < kTagUnroll; ++k) {
+      const int i = base + threadIdx.x + kTagThreads * k;
+      page[k] = i < used ? a.block_tables[row + i] : 0;
+      want[k] = i < used ? a.table_tags[row + i] : 0;
+    }
+    uint32_t have[kTagUnroll];
+#pragma unroll
+    for (int k = 0; k < kTagUnroll; ++k) {
+      const int i = base + threadIdx.x + kTagThreads * k;
+      const bool in_pool = page[k] >= 0 && page[k] < a.num_pages;
+      if (i < used && !in_pool) bad = 1;
+      have[k] = (i < used && in_pool) ? a.page_tags[page[k]] : want[k];
+    }
+#pragma unroll
+    for (int k = 0; k < kTagUnroll; ++k) mismatch |= have[k] != want[k];
+  }
+  bad = __syncthreads_or(bad);
+  mismatch = __syncthreads_or(mismatch);
+  if (threadIdx.x == 0) a.status[b] = (mismatch ? PFKV_REQ_TAG_MISMATCH : 0) | (bad ? PFKV_REQ_BAD_INDEX : 0);
+}
+
 }  // namespace
 }  // namespace pfkv
 
@@ -98,4 +149,21 @@ extern "C" int pfkv_validate_tables(const int32_t* block_tables, int max_pages_p
   dim3 grid(gx, batch + 1);
   validate_kernel<<<grid, 256, 0, s>>>(a);
   return check_cuda("validate_tables launch");
+}
+
+extern "C" int pfkv_verify_page_tags(const int32_t* block_tables, const uint32_t* table_tags,
+                                     int max_pages_per_seq, const int32_t* context_lens, int batch,
+                                     int page_size, const uint32_t* page_tags, int64_t num_pages,
+                                     int32_t* request_status, pfkv_stream_t stream) {
+  using namespace pfkv;
+  clear_error();
+  if (batch < 0 || max_pages_per_seq <= 0 || page_size <= 0 || num_pages <= 0)
+    return fail(PFKV_ERR_INVALID_ARG, "verify_page_tags: bad sizes");
+  if (batch == 0) return PFKV_OK;
+  if (!block_tables || !table_tags || !context_lens || !page_tags || !request_status)
+    return fail(PFKV_ERR_INVALID_ARG, "verify_page_tags: null pointer");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  TagArgs a{block_tables, table_tags, context_lens, page_tags, request_status, max_pages_per_seq, page_size, num_pages};
+  verify_tags_kernel<<<batch, kTagThreads, 0, s>>>(a);
+  return check_cuda("verify_page_tags launch");
 }
