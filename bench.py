@@ -306,6 +306,7 @@ def other_workloads(pf, peak_gbs, peak_tf, iters=10):
         torch.cuda.empty_cache()
 
     paged("gqa_prefix_b64_h64kv8_p16", synth.config(3))
+    res["page_pool_config3_host"] = page_pool_timing(pf, synth.config(3))
     w5 = synth.config(5)
     paged("long_splitkv_b8_h64kv8_p64_chunk4096", w5)
     paged("mha_b32_h48_l8192_p16_bf16_cache", synth.config(2), bf16=True)
@@ -326,6 +327,39 @@ def other_workloads(pf, peak_gbs, peak_tf, iters=10):
     del s
     torch.cuda.empty_cache()
     return res
+
+
+def page_pool_timing(pf, w, repeats=5):
+    """Host time of the page pool + prefix cache building config 3's block
+    tables from token streams (requests 0-15 share a 2048-token prefix), and of
+    releasing them; every page of the pool ends up used."""
+    import numpy as np
+    rng = np.random.default_rng(23)
+    shared = rng.integers(0, 32000, w.shared_tokens)
+    streams = []
+    for b in range(w.B):
+        L = int(w.context_lens[b])
+        tail = rng.integers(0, 32000, L - (w.shared_tokens if b < w.shared_requests else 0))
+        streams.append((np.concatenate([shared, tail]) if b < w.shared_requests else tail).astype(np.int32))
+    maxp = w.block_tables.shape[1]
+    t_map, t_rel, cached = [], [], 0
+    for _ in range(repeats):
+        pool = pf.PagePool(w.num_pages, w.P)
+        t0 = time.perf_counter()
+        rows = [pool.map_request(s, maxp) for s in streams]
+        t1 = time.perf_counter()
+        for (row, _, _), s in zip(rows, streams):
+            pool.release(row, (len(s) + w.P - 1) // w.P)
+        t2 = time.perf_counter()
+        t_map.append(t1 - t0)
+        t_rel.append(t2 - t1)
+        cached = sum(c for _, _, c in rows)
+        pool.close()
+    tokens = int(w.context_lens.sum())
+    return {"requests": w.B, "tokens": tokens, "pages": int(w.num_pages), "cached_tokens": cached,
+            "map_ms": round(1e3 * statistics.median(t_map), 3), "release_ms": round(1e3 * statistics.median(t_rel), 3),
+            "map_ns_per_token": round(1e9 * statistics.median(t_map) / tokens, 2),
+            "note": "host (CPU) time through the C ABI from Python; includes FNV-1a hashing of every full block"}
 
 
 # -------------------------------------------------------------- CPU oracle

@@ -62,7 +62,8 @@ typedef enum {
   PFKV_ERR_UNSUPPORTED = -2, /* valid but not implemented (head_dim, page size, ...) */
   PFKV_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed */
   PFKV_ERR_INDEX = -4,       /* an index error was found (status word set) */
-  PFKV_ERR_WORKSPACE = -5    /* workspace too small for this call */
+  PFKV_ERR_WORKSPACE = -5,   /* workspace too small for this call */
+  PFKV_ERR_NO_PAGES = -6     /* the page pool has too few free pages */
 } pfkv_status;
 
 typedef enum { PFKV_CACHE_FP8_E4M3 = 0, PFKV_CACHE_BF16 = 1 } pfkv_cache_dtype;
@@ -260,6 +261,56 @@ PFKV_API int pfkv_verify_page_tags(const int32_t *block_tables, const uint32_t *
                                    int max_pages_per_seq, const int32_t *context_lens, int batch,
                                    int page_size, const uint32_t *page_tags, int64_t num_pages,
                                    int32_t *request_status, pfkv_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Page pool and prefix cache (host side; no device memory, no CUDA calls).
+ * KV cache explainer, "PagedAttention の 2 つの原語": the cache is a pool of
+ * fixed-size pages plus per-request block tables; allocating is popping a page
+ * id off a free list and freeing is pushing it back (O(1), no device
+ * allocation); pages can be shared.  "Prefix Cache" section: each full block
+ * is identified by a hash of its tokens chained through its parent block's
+ * hash, a lookup walks a prompt's blocks in order and stops at the first miss,
+ * so the reused length is floored to whole blocks (100 shared tokens with
+ * 16-token blocks reuse 96).
+ * The pool keeps a reference count per page (a shared page returns to the free
+ * list when its last holder releases it, and then leaves the prefix table) and
+ * a generation tag per page that changes each time the page is handed out:
+ * the tags pfkv_verify_page_tags checks.  Not thread-safe.
+ * Block hash: 64-bit FNV-1a over the parent hash (8 bytes little endian) then
+ * the block's token ids (4 bytes each, little endian); the first block's
+ * parent is 0. */
+typedef struct pfkv_page_pool pfkv_page_pool;
+/* A pool of num_pages pages of page_size tokens, all free; NULL on bad sizes
+ * (message in pfkv_last_error).  Free pages are handed out lowest id first. */
+PFKV_API pfkv_page_pool *pfkv_pool_create(int64_t num_pages, int page_size);
+PFKV_API void pfkv_pool_destroy(pfkv_page_pool *pool);
+/* Free pages left (-1 for a NULL pool). */
+PFKV_API int64_t pfkv_pool_num_free(const pfkv_page_pool *pool);
+/* Holders of `page` (-1 if out of range). */
+PFKV_API int pfkv_pool_refcount(const pfkv_page_pool *pool, int32_t page);
+/* Current generation tag of every page into tags_out[num_pages] (host). */
+PFKV_API int pfkv_pool_page_tags(const pfkv_page_pool *pool, uint32_t *tags_out);
+/* Map a request's token stream (host int32 [n_tokens]) onto pages: the
+ * longest run of leading full blocks found in the prefix table is shared (each
+ * such page gains a holder), every other block gets a fresh page, and fresh
+ * full blocks enter the prefix table.  Writes block_table_row[max_pages]
+ * (page ids, -1 past the last page) and table_tags[max_pages] (the tag of each
+ * mapped page, 0 past it), and *cached_tokens = shared blocks x page_size.
+ * PFKV_ERR_NO_PAGES (nothing changed) if the free list is too short;
+ * PFKV_ERR_INVALID_ARG if the row is too short. */
+PFKV_API int pfkv_pool_map_request(pfkv_page_pool *pool, const int32_t *tokens, int n_tokens,
+                                   int32_t *block_table_row, uint32_t *table_tags, int max_pages,
+                                   int *cached_tokens);
+/* Release a request's first n_pages pages (one holder each); pages with no
+ * holder left return to the free list.  PFKV_ERR_INVALID_ARG (nothing
+ * changed) if an entry is not a held page. */
+PFKV_API int pfkv_pool_release(pfkv_page_pool *pool, const int32_t *block_table_row, int n_pages);
+/* The FNV-1a chain hash of one block (n tokens) given its parent's hash. */
+PFKV_API uint64_t pfkv_block_hash(uint64_t parent, const int32_t *tokens, int n);
+/* slots_out[k] = page * page_size + t % page_size for tokens t = first_token +
+ * k of a request (host arrays): the slot mapping kv_append_fp8 takes. */
+PFKV_API int pfkv_slots_from_table(const int32_t *block_table_row, int max_pages, int page_size,
+                                   int first_token, int n_tokens, int64_t *slots_out);
 
 /* Copy the workspace status word (bits PFKV_DEVERR_*) to *status after
  * synchronising `stream`.  Returns PFKV_OK, or PFKV_ERR_CUDA. */

@@ -24,6 +24,7 @@ __all__ = [
     "mla_decode_attn", "validate_tables", "verify_page_tags", "workspace_status", "selftest_barrier_timeout",
     "last_error", "version",
     "CACHE_FP8_E4M3", "CACHE_BF16", "DEVERR", "REQ_TAG_MISMATCH", "REQ_BAD_INDEX",
+    "PagePool", "block_hash", "slots_from_table",
 ]
 
 CACHE_FP8_E4M3 = 0
@@ -77,6 +78,15 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             "pfkv_validate_tables": (i32, [vp, i32, vp, i32, i32, i64, vp, i32, vp, i32, vp, vp]),
             "pfkv_verify_page_tags": (i32, [vp, vp, i32, vp, i32, i32, vp, i64, vp, vp]),
             "pfkv_workspace_status": (i32, [vp, vp, vp]),
+            "pfkv_pool_create": (vp, [i64, i32]),
+            "pfkv_pool_destroy": (None, [vp]),
+            "pfkv_pool_num_free": (i64, [vp]),
+            "pfkv_pool_refcount": (i32, [vp, ctypes.c_int32]),
+            "pfkv_pool_page_tags": (i32, [vp, vp]),
+            "pfkv_pool_map_request": (i32, [vp, vp, i32, vp, vp, i32, vp]),
+            "pfkv_pool_release": (i32, [vp, vp, i32]),
+            "pfkv_block_hash": (ctypes.c_uint64, [ctypes.c_uint64, vp, i32]),
+            "pfkv_slots_from_table": (i32, [vp, i32, i32, i32, i32, vp]),
             "pfkv_selftest_barrier_timeout": (i32, [vp, vp]),
             "pfkv_last_error": (ctypes.c_char_p, []),
             "pfkv_version": (ctypes.c_char_p, []),
@@ -248,3 +258,76 @@ def workspace_status(workspace, stream=None) -> int:
     rc = load().pfkv_workspace_status(_ptr(workspace), ctypes.byref(v), _stream(stream))
     _check("workspace_status", rc)
     return int(v.value)
+
+
+# ------------------------------------------------------ page pool (host side)
+def _host(a, dtype):
+    import numpy as np
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a, a.ctypes.data_as(ctypes.c_void_p)
+
+
+class PagePool:
+    """Host page pool with reference counts, generation tags and a block-hash
+    prefix cache (``pfkv_pool_*``).  Arrays are numpy, on the host."""
+
+    def __init__(self, num_pages: int, page_size: int):
+        self._h = load().pfkv_pool_create(num_pages, page_size)
+        if not self._h:
+            raise PfkvError("pool_create", -1, last_error())
+        self.num_pages, self.page_size = num_pages, page_size
+
+    def close(self):
+        if self._h:
+            load().pfkv_pool_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def num_free(self) -> int:
+        return int(load().pfkv_pool_num_free(self._h))
+
+    def refcount(self, page: int) -> int:
+        return int(load().pfkv_pool_refcount(self._h, page))
+
+    def page_tags(self):
+        import numpy as np
+        out = np.zeros(self.num_pages, np.uint32)
+        _check("pool_page_tags", load().pfkv_pool_page_tags(self._h, out.ctypes.data_as(ctypes.c_void_p)))
+        return out
+
+    def map_request(self, tokens, max_pages: int):
+        """-> (block-table row int32 [max_pages], tags uint32 [max_pages], cached token count)."""
+        import numpy as np
+        t, tp = _host(tokens, np.int32)
+        row = np.zeros(max_pages, np.int32)
+        tags = np.zeros(max_pages, np.uint32)
+        cached = ctypes.c_int(0)
+        rc = load().pfkv_pool_map_request(self._h, tp, t.shape[0], row.ctypes.data_as(ctypes.c_void_p),
+                                          tags.ctypes.data_as(ctypes.c_void_p), max_pages, ctypes.byref(cached))
+        _check("pool_map_request", rc)
+        return row, tags, int(cached.value)
+
+    def release(self, row, n_pages: int):
+        import numpy as np
+        r, rp = _host(row, np.int32)
+        _check("pool_release", load().pfkv_pool_release(self._h, rp, n_pages))
+
+
+def block_hash(parent: int, tokens) -> int:
+    import numpy as np
+    t, tp = _host(tokens, np.int32)
+    return int(load().pfkv_block_hash(ctypes.c_uint64(parent), tp, t.shape[0]))
+
+
+def slots_from_table(row, page_size: int, first_token: int, n_tokens: int):
+    import numpy as np
+    r, rp = _host(row, np.int32)
+    out = np.zeros(n_tokens, np.int64)
+    _check("slots_from_table", load().pfkv_slots_from_table(rp, r.shape[0], page_size, first_token, n_tokens,
+                                                            out.ctypes.data_as(ctypes.c_void_p)))
+    return out
