@@ -70,6 +70,12 @@ def lib():
             L.orc_kv_append.argtypes = [vp, vp, vp, i32, i32, i32, i32, i64, f32]
             L.orc_kv_append_bf16.restype = i32
             L.orc_kv_append_bf16.argtypes = [vp, vp, vp, i32, i32, i32, i32, i64]
+            L.orc_kv_append_head.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i64]
+            L.orc_kv_append_token.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i64]
+            L.orc_paged_decode_scaled_one.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, vp, i32, i32,
+                                                      i32, i32, i32, i64, f32]
+            L.orc_paged_decode_scaled.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, vp, i32, vp, i32,
+                                                  i32, i32, i32, i32, i64, f32, i64, i64]
             L.orc_paged_decode_one.restype = i32
             L.orc_paged_decode_one.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32,
                                                i64, f32, f32, f32]
@@ -154,7 +160,75 @@ def kv_append_bf16(x_new_bf16, cache, slot_mapping, page_size: int):
                                   cache.shape[0]))
 
 
+SCALE_TENSOR = 0
+SCALE_HEAD = 1
+SCALE_TOKEN = 2
+
+
+def kv_append_head(x_new_bf16, cache, slot_mapping, page_size: int, head_scales):
+    """In place: quantise x_new [T][H][D] with one scale per KV head (float32 [H])."""
+    x = _c(x_new_bf16, np.uint16)
+    T, H, D = x.shape
+    assert cache.dtype == np.uint8 and cache.flags.c_contiguous
+    hs = _c(head_scales, np.float32)
+    assert hs.shape == (H,)
+    sm = _c(slot_mapping, np.int64)
+    _chk(lib().orc_kv_append_head(_ptr(x), _ptr(cache), _ptr(hs), _ptr(sm), T, H, D, page_size,
+                                  cache.shape[0]))
+
+
+def kv_append_token(x_new_bf16, cache, scales, slot_mapping, page_size: int):
+    """In place: quantise x_new [T][H][D] with one scale per (token, KV head) row,
+    written to scales float32 [pages][H][P] beside the row."""
+    x = _c(x_new_bf16, np.uint16)
+    T, H, D = x.shape
+    assert cache.dtype == np.uint8 and cache.flags.c_contiguous
+    assert scales.dtype == np.float32 and scales.flags.c_contiguous
+    assert scales.shape == cache.shape[:3]
+    sm = _c(slot_mapping, np.int64)
+    _chk(lib().orc_kv_append_token(_ptr(x), _ptr(cache), _ptr(scales), _ptr(sm), T, H, D,
+                                   page_size, cache.shape[0]))
+
+
 # ------------------------------------------------------------------ attention
+def paged_decode_scaled(q_bf16, k_cache, v_cache, granularity: int, k_scales, v_scales,
+                        block_tables, context_lens, page_size: int, softmax_scale: float,
+                        num_kv_heads: int, units=None):
+    """Double-precision decode over an e4m3 cache with per-tensor ([1]), per-head
+    ([Hkv]) or per-token ([pages][Hkv][P]) float32 scales."""
+    q = _c(q_bf16, np.uint16)
+    B, Hq, D = q.shape
+    assert k_cache.dtype == np.uint8 and v_cache.dtype == np.uint8
+    ks = _c(k_scales, np.float32)
+    vs = _c(v_scales, np.float32)
+    bt = _c(block_tables, np.int32)
+    cl = _c(context_lens, np.int32)
+    out = np.zeros((B, Hq, D), np.float64)
+    lse = np.full((B, Hq), -np.inf, np.float64)
+    u0, u1 = (0, B * Hq) if units is None else units
+    _chk(lib().orc_paged_decode_scaled(_ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache),
+                                       _ptr(v_cache), granularity, _ptr(ks), _ptr(vs), _ptr(bt),
+                                       bt.shape[1], _ptr(cl), B, Hq, num_kv_heads, D, page_size,
+                                       k_cache.shape[0], softmax_scale, u0, u1))
+    return out, lse
+
+
+def paged_decode_scaled_one(q_head_bf16, k_cache, v_cache, granularity: int, k_scales, v_scales,
+                            bt_row, L: int, kvh: int, page_size: int, softmax_scale: float):
+    q = _c(q_head_bf16, np.uint16).reshape(-1)
+    D = q.shape[0]
+    ks = _c(k_scales, np.float32)
+    vs = _c(v_scales, np.float32)
+    bt = _c(bt_row, np.int32)
+    out = np.zeros(D, np.float64)
+    lse = ctypes.c_double(0.0)
+    _chk(lib().orc_paged_decode_scaled_one(_ptr(out), ctypes.byref(lse), _ptr(q), _ptr(k_cache),
+                                           _ptr(v_cache), granularity, _ptr(ks), _ptr(vs),
+                                           _ptr(bt), L, k_cache.shape[1], kvh, D, page_size,
+                                           k_cache.shape[0], softmax_scale))
+    return out, lse.value
+
+
 def paged_decode(q_bf16, k_cache, v_cache, block_tables, context_lens, page_size: int,
                  k_scale: float, v_scale: float, softmax_scale: float, num_kv_heads: int,
                  units=None):

@@ -18,7 +18,7 @@
  *         8-bit floating point in the e4m3 format and the attention kernel
  *         converts values when it reads them.
  *  [SCL]  explainer page, section "FP8 KV のエンジニアリング上の制約": scaling
- *         factors per tensor, per head or per token (this oracle: per tensor).
+ *         factors per tensor, per head or per token (all three here).
  *  [OSM]  Kuaishou kLLM article "快手万擎大模型推理成本和性能优化实践", §5.2.2
  *         "分块式 Ring Attention 实现": blockwise attention keeps the running
  *         maximum, normaliser and output (m, ℓ, O) so that the blockwise result
@@ -160,6 +160,85 @@ int orc_kv_append_bf16(const uint16_t *x_new, uint16_t *cache, const int64_t *sl
 }
 
 /* ------------------------------------------------------------------------- */
+/* Finer scale granularities ([SCL]): one scale per tensor, one per KV head, or
+ * one per token.  The section lists the three in order of increasing fineness,
+ * so "per token" is read as finer than "per head": one scale for each
+ * (token, KV head) row of D values.  Where the scales live:
+ *   ORC_SCALE_TENSOR  scales[0]
+ *   ORC_SCALE_HEAD    scales[h]                               h = KV head
+ *   ORC_SCALE_TOKEN   scales[(page * H + h) * P + off]   beside the cache row
+ * The per-token scale maps the row's largest magnitude onto the largest e4m3
+ * value, s = fp32(max_d |x_d|) / 448 (fp32 division), the same amax / 448 rule
+ * the per-tensor scale follows over a whole tensor; an all-zero row gets s = 0
+ * and zero codes (nothing to scale). */
+static double scale_at(int granularity, const float *scales, int64_t cache_row, int h)
+{
+    if (granularity == ORC_SCALE_TENSOR)
+        return (double)scales[0];
+    if (granularity == ORC_SCALE_HEAD)
+        return (double)scales[h];
+    return (double)scales[cache_row];
+}
+
+/* Append with one given scale per KV head: code = e4m3(fp32(x) / scales[h]). */
+int orc_kv_append_head(const uint16_t *x_new, uint8_t *cache, const float *head_scales,
+                       const int64_t *slot_mapping, int T, int H, int D, int P,
+                       int64_t num_pages)
+{
+    for (int t = 0; t < T; t++) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0)
+            continue;
+        if (slot >= num_pages * (int64_t)P)
+            return ORC_ERR_INDEX;
+        int64_t page = slot / P;
+        int64_t off = slot % P;
+        for (int h = 0; h < H; h++) {
+            for (int d = 0; d < D; d++) {
+                float x = orc_bf16_to_f32(x_new[((int64_t)t * H + h) * D + d]);
+                float y = x / head_scales[h];
+                cache[((page * H + h) * P + off) * D + d] = orc_e4m3_encode(y);
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+/* Append with one scale per (token, KV head) row, computed from the row and
+ * stored beside it in scales [num_pages][H][P]. */
+int orc_kv_append_token(const uint16_t *x_new, uint8_t *cache, float *scales,
+                        const int64_t *slot_mapping, int T, int H, int D, int P,
+                        int64_t num_pages)
+{
+    for (int t = 0; t < T; t++) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0)
+            continue;
+        if (slot >= num_pages * (int64_t)P)
+            return ORC_ERR_INDEX;
+        int64_t page = slot / P;
+        int64_t off = slot % P;
+        for (int h = 0; h < H; h++) {
+            const uint16_t *row = x_new + ((int64_t)t * H + h) * D;
+            int64_t crow = (page * H + h) * P + off;
+            float amax = 0.0f;
+            for (int d = 0; d < D; d++) {
+                float a = fabsf(orc_bf16_to_f32(row[d]));
+                if (a > amax)
+                    amax = a;
+            }
+            float s = amax / 448.0f;
+            scales[crow] = s;
+            for (int d = 0; d < D; d++) {
+                float x = orc_bf16_to_f32(row[d]);
+                cache[crow * D + d] = (s == 0.0f) ? 0 : orc_e4m3_encode(x / s);
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------- */
 /* Dequantised element of a cache row ([FP8]: converted when read). */
 static double cache_elem(const void *cache, int cache_dtype, int64_t idx, double scale)
 {
@@ -256,6 +335,94 @@ int orc_paged_decode(double *out, double *lse, const uint16_t *q,
                                       cache_dtype, block_tables + (int64_t)b * max_pages_per_seq,
                                       L, Hkv, h / G, D, P, num_pages, k_scale, v_scale,
                                       softmax_scale);
+        if (rc != ORC_OK)
+            return rc;
+        if (lse)
+            lse[u] = lse_bh;
+    }
+    return ORC_OK;
+}
+
+/* Decode attention as orc_paged_decode_one with an e4m3 cache whose elements
+ * are dequantised with the scale of their granularity ([SCL]):
+ *   K(t)[d] = e4m3(Kcode) * ks(t),  V(t)[d] = e4m3(Vcode) * vs(t)
+ * where ks/vs pick scales[0], scales[kvh] or the token row's own scale. */
+int orc_paged_decode_scaled_one(double *out, double *lse, const uint16_t *q,
+                                const uint8_t *k_cache, const uint8_t *v_cache, int granularity,
+                                const float *k_scales, const float *v_scales,
+                                const int32_t *bt_row, int L, int Hkv, int kvh, int D, int P,
+                                int64_t num_pages, float softmax_scale)
+{
+    for (int d = 0; d < D; d++)
+        out[d] = 0.0;
+    if (L <= 0) {
+        *lse = -INFINITY;
+        return ORC_OK;
+    }
+    double *s = (double *)malloc(sizeof(double) * (size_t)L);
+    if (!s)
+        return ORC_ERR_NOMEM;
+    for (int64_t t = 0; t < L; t++) {
+        int64_t row = token_row(bt_row, t, P, num_pages);
+        if (row < 0) {
+            free(s);
+            return ORC_ERR_INDEX;
+        }
+        int64_t crow = ((row / P) * Hkv + kvh) * (int64_t)P + row % P;
+        double ks = scale_at(granularity, k_scales, crow, kvh);
+        double acc = 0.0;
+        for (int d = 0; d < D; d++)
+            acc += (double)orc_bf16_to_f32(q[d]) * (orc_e4m3_value(k_cache[crow * D + d]) * ks);
+        s[t] = (double)softmax_scale * acc;
+    }
+    double m = -INFINITY;
+    for (int64_t t = 0; t < L; t++)
+        if (s[t] > m)
+            m = s[t];
+    double l = 0.0;
+    for (int64_t t = 0; t < L; t++) {
+        double p = exp(s[t] - m);
+        int64_t row = token_row(bt_row, t, P, num_pages);
+        int64_t crow = ((row / P) * Hkv + kvh) * (int64_t)P + row % P;
+        double vs = scale_at(granularity, v_scales, crow, kvh);
+        l += p;
+        for (int d = 0; d < D; d++)
+            out[d] += p * (orc_e4m3_value(v_cache[crow * D + d]) * vs);
+    }
+    for (int d = 0; d < D; d++)
+        out[d] /= l;
+    *lse = m + log(l);
+    free(s);
+    return ORC_OK;
+}
+
+/* Whole batch of orc_paged_decode_scaled_one, units [u_begin, u_end) as in
+ * orc_paged_decode. */
+int orc_paged_decode_scaled(double *out, double *lse, const uint16_t *q, const uint8_t *k_cache,
+                            const uint8_t *v_cache, int granularity, const float *k_scales,
+                            const float *v_scales, const int32_t *block_tables,
+                            int max_pages_per_seq, const int32_t *context_lens, int B, int Hq,
+                            int Hkv, int D, int P, int64_t num_pages, float softmax_scale,
+                            int64_t u_begin, int64_t u_end)
+{
+    if (Hkv <= 0 || Hq % Hkv != 0)
+        return ORC_ERR_ARG;
+    if (granularity != ORC_SCALE_TENSOR && granularity != ORC_SCALE_HEAD &&
+        granularity != ORC_SCALE_TOKEN)
+        return ORC_ERR_ARG;
+    int G = Hq / Hkv;
+    if (u_end > (int64_t)B * Hq)
+        u_end = (int64_t)B * Hq;
+    for (int64_t u = u_begin; u < u_end; u++) {
+        int b = (int)(u / Hq), h = (int)(u % Hq);
+        int L = context_lens[b];
+        if (L > max_pages_per_seq * P)
+            return ORC_ERR_INDEX;
+        double lse_bh;
+        int rc = orc_paged_decode_scaled_one(out + u * D, &lse_bh, q + u * D, k_cache, v_cache,
+                                             granularity, k_scales, v_scales,
+                                             block_tables + (int64_t)b * max_pages_per_seq, L,
+                                             Hkv, h / G, D, P, num_pages, softmax_scale);
         if (rc != ORC_OK)
             return rc;
         if (lse)

@@ -13,6 +13,7 @@ extern "C" {
 
 enum { ORC_OK = 0, ORC_ERR_ARG = -1, ORC_ERR_INDEX = -4, ORC_ERR_NOMEM = -5 };
 enum { ORC_CACHE_FP8_E4M3 = 0, ORC_CACHE_BF16 = 1 };
+enum { ORC_SCALE_TENSOR = 0, ORC_SCALE_HEAD = 1, ORC_SCALE_TOKEN = 2 };
 
 double orc_e4m3_value(uint8_t code);
 uint8_t orc_e4m3_encode(float x);
@@ -23,6 +24,12 @@ int orc_kv_append(const uint16_t *x_new, uint8_t *cache, const int64_t *slot_map
                   int T, int H, int D, int P, int64_t num_pages, float scale);
 int orc_kv_append_bf16(const uint16_t *x_new, uint16_t *cache, const int64_t *slot_mapping,
                        int T, int H, int D, int P, int64_t num_pages);
+int orc_kv_append_head(const uint16_t *x_new, uint8_t *cache, const float *head_scales,
+                       const int64_t *slot_mapping, int T, int H, int D, int P,
+                       int64_t num_pages);
+int orc_kv_append_token(const uint16_t *x_new, uint8_t *cache, float *scales,
+                        const int64_t *slot_mapping, int T, int H, int D, int P,
+                        int64_t num_pages);
 
 int orc_paged_decode_one(double *out, double *lse, const uint16_t *q,
                          const void *k_cache, const void *v_cache, int cache_dtype,
@@ -34,6 +41,17 @@ int orc_paged_decode(double *out, double *lse, const uint16_t *q,
                      const int32_t *context_lens, int B, int Hq, int Hkv, int D, int P,
                      int64_t num_pages, float k_scale, float v_scale, float softmax_scale,
                      int64_t u_begin, int64_t u_end);
+int orc_paged_decode_scaled_one(double *out, double *lse, const uint16_t *q,
+                                const uint8_t *k_cache, const uint8_t *v_cache, int granularity,
+                                const float *k_scales, const float *v_scales,
+                                const int32_t *bt_row, int L, int Hkv, int kvh, int D, int P,
+                                int64_t num_pages, float softmax_scale);
+int orc_paged_decode_scaled(double *out, double *lse, const uint16_t *q, const uint8_t *k_cache,
+                            const uint8_t *v_cache, int granularity, const float *k_scales,
+                            const float *v_scales, const int32_t *block_tables,
+                            int max_pages_per_seq, const int32_t *context_lens, int B, int Hq,
+                            int Hkv, int D, int P, int64_t num_pages, float softmax_scale,
+                            int64_t u_begin, int64_t u_end);
 int orc_paged_decode_split_one(double *out, double *lse, const uint16_t *q,
                                const void *k_cache, const void *v_cache, int cache_dtype,
                                const int32_t *bt_row, int L, int Hkv, int kvh, int D, int P,

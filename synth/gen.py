@@ -41,6 +41,7 @@ TENSOR_QMLA = 5
 TENSOR_CTX = 6
 TENSOR_PERM = 7
 TENSOR_TOPK = 8
+TENSOR_SPREAD = 9
 
 
 def mix64(z: np.ndarray) -> np.ndarray:

@@ -145,6 +145,28 @@ class PagedWorkload:
                  for a, z, base in self.kv_runs(b, t0, t1)]
         return np.concatenate(parts) if parts else np.zeros((0, self.D), np.uint16)
 
+    def spread_exponents(self, which: str, b: int, t0: int, t1: int, spread: int) -> np.ndarray:
+        """int [t1-t0][Hkv]: a power-of-two exponent per (token, KV head), uniform
+        in [-spread, spread], plus one per head in the same range."""
+        key = gen.make_key(self.seed, gen.TENSOR_SPREAD) ^ (0 if which == "k" else 0x5bd1e995)
+        t = np.arange(t0, t1, dtype=np.int64)
+        tok = (self.src_request(b, t) << TOKEN_SHIFT) + t
+        h = np.arange(self.Hkv, dtype=np.int64)
+        e_tok = gen.uniform_int(key, (tok[:, None] * self.Hkv + h[None, :]).astype(np.uint64),
+                                -spread, spread)
+        e_head = gen.uniform_int(key ^ 0x27d4eb2f165667c5, h.astype(np.uint64) + (1 << 62),
+                                 -spread, spread)
+        return e_tok + e_head[None, :]
+
+    def kv_spread_bits(self, which: str, b: int, t0: int, t1: int, spread: int = 6) -> np.ndarray:
+        """kv_bits with every (token, KV head) row multiplied by 2^e
+        (spread_exponents): magnitudes that differ between tokens and between
+        heads, the case that finer scale granularity serves.  A power of two
+        times a bf16 value is again an exact bf16 value."""
+        x = gen.bf16_bits_to_f32(self.kv_bits(which, b, t0, t1))
+        e = self.spread_exponents(which, b, t0, t1, spread)
+        return gen.f32_to_bf16_bits(np.ldexp(x, e[:, :, None]).astype(np.float32))
+
     def q_bits(self) -> np.ndarray:
         n = self.B * self.Hq * self.D
         return gen.normal_bf16_range(self.key_q, 0, n).reshape(self.B, self.Hq, self.D)
