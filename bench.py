@@ -305,6 +305,10 @@ def other_workloads(pf, peak_gbs, peak_tf, iters=10):
         del s
         torch.cuda.empty_cache()
 
+    res["scale_granularity_mha_b32_h48_l8192_p16"] = scale_granularity_timing(
+        pf, lambda: synth.config(2), peak_gbs, flush, iters)
+    res["scale_granularity_gqa_prefix_b64_h64kv8_p16"] = scale_granularity_timing(
+        pf, lambda: synth.config(3), peak_gbs, flush, iters)
     paged("gqa_prefix_b64_h64kv8_p16", synth.config(3))
     res["page_pool_config3_host"] = page_pool_timing(pf, synth.config(3))
     w5 = synth.config(5)
@@ -325,6 +329,68 @@ def other_workloads(pf, peak_gbs, peak_tf, iters=10):
         "frac_of_bf16_peak": round(m.flops() / t_dec / 1e12 / peak_tf, 4),
         "query_tokens_per_s": round(m.B / t_dec, 1)}
     del s
+    torch.cuda.empty_cache()
+    return res
+
+
+def scale_granularity_timing(pf, w_factory, peak_gbs, flush, iters):
+    """Decode (and append) time of one workload with per-tensor host scales,
+    per-tensor and per-head device scales (same codes), and per-token scales
+    (its own cache, filled by the per-token append), and the time each adds
+    over per-tensor host scales."""
+    import torch
+    from synth import device as sdev
+    res = {}
+    w = w_factory()
+    s = PagedStep(pf, w)
+    for _ in range(3):
+        s.step()
+    torch.cuda.synchronize()
+    t_ref = time_events(s.decode, iters, flush)
+    t_app_ref = time_events(s.append, iters, flush)
+    st = s.st
+    res["tensor_host_us"] = round(t_ref * 1e6, 2)
+    res["append_tensor_host_us"] = round(t_app_ref * 1e6, 2)
+    for name, gran, n in (("tensor_device", pf.SCALE_TENSOR, 1), ("head", pf.SCALE_HEAD, w.Hkv)):
+        ks = torch.full((n,), w.k_scale, dtype=torch.float32, device="cuda")
+        vs = torch.full((n,), w.v_scale, dtype=torch.float32, device="cuda")
+        fn = lambda: pf.paged_decode_attn_scaled(s.out, st.q, st.k_cache, st.v_cache, gran, ks, vs,
+                                                 st.block_tables, st.context_lens, w.softmax_scale,
+                                                 workspace=s.ws)
+        fn()
+        t = time_events(fn, iters, flush)
+        res[name + "_us"] = round(t * 1e6, 2)
+        res[name + "_added_pct"] = round(100 * (t - t_ref) / t_ref, 2)
+    kv_bytes = s.decode_bytes()
+    del s, st
+    torch.cuda.empty_cache()
+    w = w_factory()
+    shape = (w.num_pages, w.Hkv, w.P)
+    ks = torch.zeros(shape, dtype=torch.float32, device="cuda")
+    vs = torch.zeros_like(ks)
+    append = lambda k, v, kc, vc, sl: pf.kv_append_fp8_scaled(k, v, kc, vc, sl, pf.SCALE_TOKEN, ks, vs)
+    w.k_scale = w.v_scale = 1.0  # replaced by the per-token scales
+    st = sdev.setup_paged(w, append)
+    out = torch.empty_like(st.q)
+    ws = torch.empty(pf.paged_decode_workspace_size(w.B, w.Hq, w.Hkv, w.D), dtype=torch.uint8, device="cuda")
+    dec = lambda: pf.paged_decode_attn_scaled(out, st.q, st.k_cache, st.v_cache, pf.SCALE_TOKEN, ks, vs,
+                                              st.block_tables, st.context_lens, w.softmax_scale, workspace=ws)
+    app = lambda: append(st.k_new, st.v_new, st.k_cache, st.v_cache, st.step_slots)
+    for _ in range(3):
+        app()
+        dec()
+    torch.cuda.synchronize()
+    t = time_events(dec, iters, flush)
+    t_app = time_events(app, iters, flush)
+    scale_bytes = 2 * 4 * w.Hkv * w.unique_tokens
+    res["token_us"] = round(t * 1e6, 2)
+    res["token_added_pct"] = round(100 * (t - t_ref) / t_ref, 2)
+    res["token_scale_bytes"] = scale_bytes
+    res["token_scale_bytes_pct_of_codes"] = round(100 * scale_bytes / w.kv_bytes(), 3)
+    res["token_decode_GBs"] = round((kv_bytes + scale_bytes) / t / 1e9, 1)
+    res["token_frac_of_hbm_peak"] = round((kv_bytes + scale_bytes) / t / 1e9 / peak_gbs, 4)
+    res["append_token_us"] = round(t_app * 1e6, 2)
+    del st, ks, vs, out, ws
     torch.cuda.empty_cache()
     return res
 

@@ -110,6 +110,46 @@ PFKV_API int pfkv_kv_append_bf16(const void *k_new, const void *v_new, void *k_c
                         int head_dim, int page_size, int64_t num_pages, pfkv_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Scale granularity of an e4m3 cache.
+ *
+ * Explainer, section "FP8 KV のエンジニアリング上の制約": the scaling factor can
+ * be per tensor, per head or per token; the finer it is, the more precise the
+ * cache and the more extra work and memory traffic inside the decode kernel.
+ * The section lists the three from coarse to fine, so per token is read as
+ * finer than per head: one scale for every (token, KV head) row.  Scales are
+ * fp32 DEVICE arrays:
+ *   PFKV_SCALE_TENSOR  [1]
+ *   PFKV_SCALE_HEAD    [num_kv_heads]
+ *   PFKV_SCALE_TOKEN   [num_pages][num_kv_heads][page_size], entry
+ *                      (page * num_kv_heads + h) * page_size + offset beside
+ *                      the cache row it scales */
+typedef enum {
+  PFKV_SCALE_TENSOR = 0,
+  PFKV_SCALE_HEAD = 1,
+  PFKV_SCALE_TOKEN = 2
+} pfkv_scale_granularity;
+
+/* kv_append_fp8_scaled -- kv_append_fp8 with device-resident scales.
+ *  TENSOR, HEAD: k_scales / v_scales are READ (scale = scales[0] or
+ *      scales[h]); code = e4m3_rne_satfinite(fp32(x) / scale).  Scales must be
+ *      finite and > 0 (not checked: they live on the device).
+ *  TOKEN: k_scales / v_scales are WRITTEN, one entry per appended row:
+ *      s = fp32(max_d |x[i][h][d]|) / 448 (IEEE fp32 divide), then
+ *      code = e4m3_rne_satfinite(fp32(x) / s), so the row's largest magnitude
+ *      becomes the largest e4m3 value; an all-zero row stores s = 0 and zero
+ *      codes.  Inputs must be finite.
+ * Other arguments, layouts and skipped slots as kv_append_fp8; v_new = v_cache
+ * = v_scales = NULL appends K only.
+ * Supported: head_dim a multiple of 16 (TOKEN: at most 512); scale arrays
+ * 4-byte aligned.  Errors: PFKV_ERR_INVALID_ARG for an unknown granularity or
+ * a NULL scale array, plus those of kv_append_fp8. */
+PFKV_API int pfkv_kv_append_fp8_scaled(const void *k_new, const void *v_new, void *k_cache,
+                                       void *v_cache, const int64_t *slot_mapping, int num_tokens,
+                                       int num_kv_heads, int head_dim, int page_size,
+                                       int64_t num_pages, pfkv_scale_granularity granularity,
+                                       float *k_scales, float *v_scales, pfkv_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* paged_decode_attn -- one decode step of GQA/MHA attention over the paged
  * cache, dequantising on read, with split-KV and a log-sum-exp merge.
  *
@@ -184,6 +224,39 @@ PFKV_API int pfkv_paged_decode_attn_noalloc(void *out, const void *q, const void
                                             float softmax_scale, int kv_split_tokens,
                                             int64_t max_total_chunks, float *lse_out,
                                             int32_t *status_out, pfkv_stream_t stream);
+
+/* paged_decode_attn_scaled -- paged_decode_attn over an e4m3 cache whose
+ * scales are device arrays of the given granularity (see
+ * pfkv_scale_granularity):
+ *   s_t = softmax_scale * sum_d q[b][h][d] * e4m3(Kcode_t[d]) * ks(t)
+ *   out = sum_t e^{s_t - m} e4m3(Vcode_t[d]) * vs(t) / sum_t e^{s_t - m}
+ * with ks(t), vs(t) = scales[0], scales[kvh] or the scale stored beside row t.
+ * Per tensor and per head, the scales fold into the score and output factors
+ * of each work unit, so the tile loop is unchanged.  Per token, the 16 K and
+ * 16 V scales of each 16-token tile (2 x 64 bytes) are copied in with the
+ * tile: 8 extra bytes per (token, KV head) against 2 x head_dim bytes of
+ * codes; each K scale multiplies its raw score, and each V scale, relative to
+ * the largest V scale seen so far in the work unit, multiplies its token's
+ * probability before the f16 P.V product (the accumulator is rescaled when
+ * that largest scale grows, as for the running maximum of the softmax).
+ * Scales: finite and >= 0 (TENSOR, HEAD: > 0); not checked (device arrays).
+ * The scale of a token past L_b is never used.  Workspace: as
+ * pfkv_paged_decode_attn (pfkv_paged_decode_workspace_size).  Other arguments
+ * and device errors as pfkv_paged_decode_attn; a row outside the pool reads as
+ * zeros with zero scales.
+ * Supported: as pfkv_paged_decode_attn, e4m3 cache only; scale arrays 16-byte
+ * aligned. */
+PFKV_API int pfkv_paged_decode_attn_scaled(void *out, const void *q, const void *k_cache,
+                                           const void *v_cache,
+                                           pfkv_scale_granularity granularity,
+                                           const float *k_scales, const float *v_scales,
+                                           const int32_t *block_tables, int max_pages_per_seq,
+                                           const int32_t *context_lens, int batch,
+                                           int num_q_heads, int num_kv_heads, int head_dim,
+                                           int page_size, int64_t num_pages, float softmax_scale,
+                                           int kv_split_tokens, void *workspace,
+                                           size_t workspace_bytes, float *lse_out,
+                                           pfkv_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* mla_decode_attn -- MLA absorbed-latent decode over one shared e4m3 latent

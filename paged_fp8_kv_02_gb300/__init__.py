@@ -67,11 +67,15 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         sig = {
             "pfkv_kv_append_fp8": (i32, [vp, vp, vp, vp, vp, i32, i32, i32, i32, i64, f32, f32, vp]),
             "pfkv_kv_append_bf16": (i32, [vp, vp, vp, vp, vp, i32, i32, i32, i32, i64, vp]),
+            "pfkv_kv_append_fp8_scaled": (i32, [vp, vp, vp, vp, vp, i32, i32, i32, i32, i64, i32, vp, vp,
+                                                vp]),
             "pfkv_paged_decode_workspace_size": (sz, [i32, i32, i32, i32, i32, i64]),
             "pfkv_paged_decode_attn": (i32, [vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, i32,
                                              i64, f32, f32, f32, i32, vp, sz, vp, vp]),
             "pfkv_paged_decode_attn_noalloc": (i32, [vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32,
                                                      i32, i64, f32, f32, f32, i32, i64, vp, vp, vp]),
+            "pfkv_paged_decode_attn_scaled": (i32, [vp, vp, vp, vp, i32, vp, vp, vp, i32, vp, i32, i32, i32,
+                                                    i32, i32, i64, f32, i32, vp, sz, vp, vp]),
             "pfkv_mla_decode_workspace_size": (sz, [i32, i32, i32, i32]),
             "pfkv_mla_decode_attn": (i32, [vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32,
                                            i64, f32, f32, vp, sz, vp, vp]),
@@ -150,6 +154,24 @@ def kv_append_bf16(k_new, v_new, k_cache, v_cache, slot_mapping, stream=None):
     _check("kv_append_bf16", rc)
 
 
+SCALE_TENSOR = 0
+SCALE_HEAD = 1
+SCALE_TOKEN = 2
+
+
+def kv_append_fp8_scaled(k_new, v_new, k_cache, v_cache, slot_mapping, granularity: int, k_scales,
+                         v_scales=None, stream=None):
+    """kv_append_fp8 with float32 device scales: SCALE_TENSOR [1] / SCALE_HEAD
+    [H] are read; SCALE_TOKEN [pages][H][P] receives each appended row's
+    scale (its amax / 448)."""
+    T, H, D = k_new.shape
+    pages, _, P, _ = k_cache.shape
+    rc = load().pfkv_kv_append_fp8_scaled(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                          _ptr(slot_mapping), T, H, D, P, pages, int(granularity),
+                                          _ptr(k_scales), _ptr(v_scales), _stream(stream))
+    _check("kv_append_fp8_scaled", rc)
+
+
 # ---------------------------------------------------------------- decode
 def paged_decode_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int = 128,
                                 kv_split_tokens: int = 0, max_total_chunks: int = 0) -> int:
@@ -176,6 +198,29 @@ def paged_decode_attn(out, q, k_cache, v_cache, block_tables, context_lens, k_sc
                                        float(softmax_scale), int(kv_split_tokens), _ptr(workspace),
                                        workspace.numel(), _ptr(lse_out), _stream(stream))
     _check("paged_decode_attn", rc)
+    return workspace
+
+
+def paged_decode_attn_scaled(out, q, k_cache, v_cache, granularity: int, k_scales, v_scales,
+                             block_tables, context_lens, softmax_scale: float, kv_split_tokens: int = 0,
+                             workspace=None, lse_out=None, stream=None, max_total_chunks: int = 0):
+    """paged_decode_attn over an e4m3 cache with float32 device scales of the
+    given granularity (SCALE_TENSOR [1], SCALE_HEAD [Hkv], SCALE_TOKEN
+    [pages][Hkv][P]).  Returns the workspace used."""
+    import torch
+    B, Hq, D = q.shape
+    pages, Hkv, P, _ = k_cache.shape
+    if workspace is None:
+        n = paged_decode_workspace_size(B, Hq, Hkv, D, kv_split_tokens, max_total_chunks)
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
+    rc = load().pfkv_paged_decode_attn_scaled(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                              int(granularity), _ptr(k_scales), _ptr(v_scales),
+                                              _ptr(block_tables), block_tables.shape[1],
+                                              _ptr(context_lens), B, Hq, Hkv, D, P, pages,
+                                              float(softmax_scale), int(kv_split_tokens),
+                                              _ptr(workspace), workspace.numel(), _ptr(lse_out),
+                                              _stream(stream))
+    _check("paged_decode_attn_scaled", rc)
     return workspace
 
 

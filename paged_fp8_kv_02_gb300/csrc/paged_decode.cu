@@ -49,6 +49,10 @@ constexpr int kPartialStride = 132;  // floats per (slot, head): m, l, -, -, o[1
 constexpr int kMaxGrid = 1024;    // bound on persistent CTAs (sizes the workspace)
 constexpr int kMaxWarps = kMaxGrid * kWarps;
 constexpr float kLog2e = 1.4426950408889634f;
+// Where the K/V scales come from: host scalars in DecodeArgs, one device scale
+// per work unit (per tensor or per KV head), or one per token row.
+enum : int { kSclHost = 0, kSclUnit = 1, kSclToken = 2 };
+constexpr int kScaleStageBytes = 128;  // per-token mode: 16 K + 16 V fp32 scales per stage
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct DecodeArgs {
@@ -68,6 +72,10 @@ struct DecodeArgs {
   int chunk_tiles;      // tiles per split unit
   float score_scale;    // k_scale * softmax_scale * log2(e)
   float out_scale;      // v_scale
+  const float* k_scales;   // device scales (unit or token modes)
+  const float* v_scales;
+  int scale_head_stride;   // unit mode: 1 = one scale per KV head, 0 = one for all
+  float logit_scale;       // softmax_scale * log2(e)
 };
 
 __device__ __forceinline__ int clamp_len(const DecodeArgs& a, int b) {
@@ -199,12 +207,14 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
-template <bool kBf16>
+template <bool kBf16, int kScl = kSclHost>
 struct Geometry {
   static constexpr int kKBytes = kBf16 ? 4096 : 2048;  // one 16-token K slab
   static constexpr int kStageBytes = 2 * kKBytes;       // K + V
   static constexpr int kWarpBytes = kStages * kStageBytes;
-  static constexpr int kSmemBytes = kWarps * kWarpBytes + 1024;  // + alignment slack
+  // per-token scales sit after all warps' tiles (which keep their 1024-byte alignment)
+  static constexpr int kScaleWarpBytes = kScl == kSclToken ? kStages * kScaleStageBytes : 0;
+  static constexpr int kSmemBytes = kWarps * (kWarpBytes + kScaleWarpBytes) + 1024;  // + alignment slack
 };
 
 // --------------------------------------------------------------- main kernel
@@ -216,11 +226,12 @@ struct Geometry {
 // running maximum would.
 constexpr float kRescaleLog2 = 8.f;
 
-template <bool kBf16, int NT>
+template <bool kBf16, int NT, int kScl>
 __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 2)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const DecodeArgs a) {
-  using Geo = Geometry<kBf16>;
+  static_assert(!kBf16 || kScl == kSclHost, "device scales are for the e4m3 cache");
+  using Geo = Geometry<kBf16, kScl>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[kWarps][kStages];
 
@@ -229,6 +240,10 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 2)
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t wbase = smem_base + warp * Geo::kWarpBytes;
   uint8_t* const wptr = smem_raw + (smem_base - smem_u32(smem_raw)) + warp * Geo::kWarpBytes;
+  // per-token mode: this warp's kStages x (16 K + 16 V) fp32 scales
+  const uint32_t sbase = smem_base + kWarps * Geo::kWarpBytes + warp * Geo::kScaleWarpBytes;
+  float* const sptr = reinterpret_cast<float*>(wptr + (kWarps - warp) * Geo::kWarpBytes +
+                                               warp * Geo::kScaleWarpBytes);
   const uint32_t bar0 = smem_u32(&bars[warp][0]);  // stage s: bar0 + 8 s
 
   if (lane == 0) {
@@ -271,7 +286,24 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 2)
       const int row = (page * a.Hkv + pc.kvh) * a.P + tok0 % a.P;
       const uint32_t dst = wbase + stage * Geo::kStageBytes;
       const uint32_t bar = bar0 + 8 * stage;
-      mbar_arrive_expect_tx(bar, Geo::kStageBytes);
+      uint32_t tx = Geo::kStageBytes;
+      if constexpr (kScl == kSclToken) {
+        if (page >= 0) {
+          tx += kScaleStageBytes;
+        } else {  // a row outside the pool: zero scales beside its zero codes
+          float4* z = reinterpret_cast<float4*>(sptr + stage * (kScaleStageBytes / 4));
+#pragma unroll
+          for (int i = 0; i < kScaleStageBytes / 16; ++i) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      mbar_arrive_expect_tx(bar, tx);
+      if constexpr (kScl == kSclToken) {
+        if (page >= 0) {
+          const uint32_t sdst = sbase + stage * kScaleStageBytes;
+          bulk_load(sdst, a.k_scales + row, 64, bar);
+          bulk_load(sdst + 64, a.v_scales + row, 64, bar);
+        }
+      }
       if constexpr (kBf16) {
         tma_load_3d(dst, &tmK, 0, 0, row, bar);
         tma_load_3d(dst + 2048, &tmK, 0, 1, row, bar);
@@ -300,7 +332,9 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 2)
   int L = 0;
   int chunk_left = 0;  // tiles left in the current unit, including the current one
   int64_t seg_begin = f_begin;
-  const float sc = a.score_scale;
+  float sc = a.score_scale;  // unit mode: set per unit from the device K scale
+  float unit_vs = 1.f;       // unit mode: the unit's V scale
+  float vref = 0.f, vinv = 0.f;  // token mode: largest V scale of the unit so far, 1 / it
 
   auto flush = [&](int64_t f_stop) {
     // f_stop: first flattened tile after this segment; cc is on its last tile
@@ -314,6 +348,8 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 2)
     if (e_u > e_req) e_u = e_req;
     const int nchunks = (int)((a.unit_start[b + 1] - a.unit_start[b]) / a.Hkv);
     const bool final = (nchunks == 1) && seg_begin == s_u && f_stop == e_u;
+    // factor from accumulator units to dequantised V units
+    const float vmul = kScl == kSclUnit ? unit_vs : (kScl == kSclToken ? vref : 1.f);
 #pragma unroll
     for (int j = 0; j < NT; ++j)
 #pragma unroll
@@ -343,6 +379,10 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 2)
         for (int i = 0; i < 8; ++i) {
           vals[2 * i] = o[j][i][e];
           vals[2 * i + 1] = o[j][i][2 + e];
+        }
+        if constexpr (kScl != kSclHost) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) vals[i] *= vmul;
         }
         if (final) {
           const float inv = a.out_scale / l[j][e];
@@ -383,6 +423,15 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 2)
     L = clamp_len(a, cc.b);
     const int into = cc.tile % a.chunk_tiles;
     chunk_left = min(a.chunk_tiles - into, cc.ntiles - cc.tile);
+    if constexpr (kScl == kSclUnit) {
+      const int si = cc.kvh * a.scale_head_stride;
+      sc = __ldg(a.k_scales + si) * a.logit_scale;
+      unit_vs = __ldg(a.v_scales + si);
+    }
+    if constexpr (kScl == kSclToken) {
+      vref = 0.f;
+      vinv = 0.f;
+    }
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
       mref[j][0] = mref[j][1] = -INFINITY;
@@ -480,6 +529,23 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 2)
       }
     }
 
+    // ---------------- per-token scales: this thread's tokens are g and g + 8
+    float ks0 = 1.f, ks8 = 1.f, vs0 = 0.f, vs8 = 0.f;
+    if constexpr (kScl == kSclToken) {
+      const float* sp = sptr + stage * (kScaleStageBytes / 4);
+      ks0 = sp[g];
+      ks8 = sp[g + 8];
+      vs0 = sp[16 + g];
+      vs8 = sp[24 + g];
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        s[j][0] *= ks0;
+        s[j][1] *= ks0;
+        s[j][2] *= ks8;
+        s[j][3] *= ks8;
+      }
+    }
+
     // ---------------- mask (last tile only), lazy online softmax (exp2 domain)
     if (partial) {
       const bool va = tok0 + g < L, vb8 = tok0 + g + 8 < L;
@@ -487,6 +553,10 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 2)
       for (int j = 0; j < NT; ++j) {
         if (!va) s[j][0] = s[j][1] = -INFINITY;
         if (!vb8) s[j][2] = s[j][3] = -INFINITY;
+      }
+      if constexpr (kScl == kSclToken) {  // scales past the context are never used
+        if (!va) vs0 = 0.f;
+        if (!vb8) vs8 = 0.f;
       }
     }
     bool grow = false;
@@ -519,15 +589,47 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 2)
         rthr[j][1] = (mn1 + kRescaleLog2) / sc;
       }
     }
+    // per-token V scales enter as weights on p relative to vref, the largest V
+    // scale of the unit so far, so that p * weight <= p stays in f16 range;
+    // when vref grows the accumulator is rescaled like the running maximum
+    float w0 = 1.f, w8 = 1.f;
+    if constexpr (kScl == kSclToken) {
+      float vm = fmaxf(vs0, vs8);
+      vm = fmaxf(vm, __shfl_xor_sync(0xFFFFFFFFu, vm, 4));
+      vm = fmaxf(vm, __shfl_xor_sync(0xFFFFFFFFu, vm, 8));
+      vm = fmaxf(vm, __shfl_xor_sync(0xFFFFFFFFu, vm, 16));
+      if (vm > vref) {  // warp-uniform
+        const float r = vref / vm;
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            o[j][i][0] *= r;
+            o[j][i][1] *= r;
+            o[j][i][2] *= r;
+            o[j][i][3] *= r;
+          }
+        vref = vm;
+        vinv = 1.f / vm;
+      }
+      w0 = vs0 * vinv;
+      w8 = vs8 * vinv;
+    }
     uint32_t pb[NT][2];
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
-      const float p0 = fast_exp2(fmaf(s[j][0], sc, -mref[j][0]));
-      const float p1 = fast_exp2(fmaf(s[j][1], sc, -mref[j][1]));
-      const float p2 = fast_exp2(fmaf(s[j][2], sc, -mref[j][0]));
-      const float p3 = fast_exp2(fmaf(s[j][3], sc, -mref[j][1]));
+      float p0 = fast_exp2(fmaf(s[j][0], sc, -mref[j][0]));
+      float p1 = fast_exp2(fmaf(s[j][1], sc, -mref[j][1]));
+      float p2 = fast_exp2(fmaf(s[j][2], sc, -mref[j][0]));
+      float p3 = fast_exp2(fmaf(s[j][3], sc, -mref[j][1]));
       l[j][0] += p0 + p2;
       l[j][1] += p1 + p3;
+      if constexpr (kScl == kSclToken) {
+        p0 *= w0;
+        p1 *= w0;
+        p2 *= w8;
+        p3 *= w8;
+      }
       if constexpr (kBf16) {
         pb[j][0] = movmatrix_trans(pack_bf16x2(p0, p1));
         pb[j][1] = movmatrix_trans(pack_bf16x2(p2, p3));
@@ -801,11 +903,11 @@ WsLayout ws_layout(int B) {
   return L;
 }
 
-template <bool kBf16, int NT>
+template <bool kBf16, int NT, int kScl>
 int launch_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const DecodeArgs& a,
                   cudaStream_t stream) {
-  using Geo = Geometry<kBf16>;
-  auto kern = paged_decode_kernel<kBf16, NT>;
+  using Geo = Geometry<kBf16, kScl>;
+  auto kern = paged_decode_kernel<kBf16, NT, kScl>;
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Geo::kSmemBytes) !=
@@ -877,14 +979,21 @@ size_t pfkv_paged_decode_workspace_size(int batch, int num_q_heads, int num_kv_h
   return L.part_off + (size_t)slots * pfkv::slot_bytes(G) + 1024;
 }
 
-int pfkv_paged_decode_attn(void* out, const void* q, const void* k_cache, const void* v_cache,
-                           pfkv_cache_dtype cache_dtype, const int32_t* block_tables,
-                           int max_pages_per_seq, const int32_t* context_lens, int batch,
-                           int num_q_heads, int num_kv_heads, int head_dim, int page_size,
-                           int64_t num_pages, float k_scale, float v_scale, float softmax_scale,
-                           int kv_split_tokens, void* workspace, size_t workspace_bytes,
-                           float* lse_out, pfkv_stream_t stream) {
-  using namespace pfkv;
+}  // extern "C"
+
+namespace pfkv {
+namespace {
+
+// The decode entry for every scale mode: kSclHost takes k_scale / v_scale;
+// kSclUnit and kSclToken read the device arrays k_scales / v_scales (unit
+// mode: one scale per KV head when head_stride is 1, one for all when 0).
+int decode_entry(void* out, const void* q, const void* k_cache, const void* v_cache,
+                 pfkv_cache_dtype cache_dtype, const int32_t* block_tables, int max_pages_per_seq,
+                 const int32_t* context_lens, int batch, int num_q_heads, int num_kv_heads,
+                 int head_dim, int page_size, int64_t num_pages, float k_scale, float v_scale,
+                 float softmax_scale, int kv_split_tokens, void* workspace, size_t workspace_bytes,
+                 float* lse_out, pfkv_stream_t stream, int scl, const float* k_scales,
+                 const float* v_scales, int head_stride) {
   clear_error();
   if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || page_size <= 0 || num_pages <= 0 ||
       max_pages_per_seq <= 0)
@@ -900,6 +1009,13 @@ int pfkv_paged_decode_attn(void* out, const void* q, const void* k_cache, const 
     return fail(PFKV_ERR_INVALID_ARG, "paged_decode: kv_split_tokens must be a multiple of 16");
   if (cache_dtype != PFKV_CACHE_FP8_E4M3 && cache_dtype != PFKV_CACHE_BF16)
     return fail(PFKV_ERR_INVALID_ARG, "paged_decode: unknown cache dtype");
+  if (scl != kSclHost) {
+    if (cache_dtype != PFKV_CACHE_FP8_E4M3)
+      return fail(PFKV_ERR_UNSUPPORTED, "paged_decode_scaled: device scales need the e4m3 cache");
+    if (!k_scales || !v_scales) return fail(PFKV_ERR_INVALID_ARG, "paged_decode_scaled: null scale array");
+    if (!aligned(k_scales, 16) || !aligned(v_scales, 16))
+      return fail(PFKV_ERR_INVALID_ARG, "paged_decode_scaled: scale arrays must be 16-byte aligned");
+  }
   if ((int64_t)num_pages * num_kv_heads * page_size >= (int64_t)1 << 31)
     return fail(PFKV_ERR_UNSUPPORTED, "paged_decode: cache has 2^31 or more token rows");
   if ((int64_t)max_pages_per_seq * page_size >= (int64_t)1 << 30)
@@ -943,6 +1059,14 @@ int pfkv_paged_decode_attn(void* out, const void* q, const void* k_cache, const 
   a.chunk_tiles = kv_split_tokens > 0 ? kv_split_tokens / kTile : (1 << 30);
   a.score_scale = k_scale * softmax_scale * kLog2e;
   a.out_scale = v_scale;
+  a.k_scales = k_scales;
+  a.v_scales = v_scales;
+  a.scale_head_stride = head_stride;
+  a.logit_scale = softmax_scale * kLog2e;
+  if (scl != kSclHost) {  // the device scales carry K and V; the merge multiplies by 1
+    a.score_scale = a.logit_scale;
+    a.out_scale = 1.f;
+  }
 
   const bool bf16 = cache_dtype == PFKV_CACHE_BF16;
   const cuuint64_t rows = (cuuint64_t)num_pages * num_kv_heads * page_size;
@@ -970,8 +1094,58 @@ int pfkv_paged_decode_attn(void* out, const void* q, const void* k_cache, const 
   if (rc != PFKV_OK) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (bf16)
-    return G <= 8 ? launch_decode<true, 1>(tmK, tmV, a, s) : launch_decode<true, 2>(tmK, tmV, a, s);
-  return G <= 8 ? launch_decode<false, 1>(tmK, tmV, a, s) : launch_decode<false, 2>(tmK, tmV, a, s);
+    return G <= 8 ? launch_decode<true, 1, kSclHost>(tmK, tmV, a, s)
+                  : launch_decode<true, 2, kSclHost>(tmK, tmV, a, s);
+  if (scl == kSclUnit)
+    return G <= 8 ? launch_decode<false, 1, kSclUnit>(tmK, tmV, a, s)
+                  : launch_decode<false, 2, kSclUnit>(tmK, tmV, a, s);
+  if (scl == kSclToken)
+    return G <= 8 ? launch_decode<false, 1, kSclToken>(tmK, tmV, a, s)
+                  : launch_decode<false, 2, kSclToken>(tmK, tmV, a, s);
+  return G <= 8 ? launch_decode<false, 1, kSclHost>(tmK, tmV, a, s)
+                : launch_decode<false, 2, kSclHost>(tmK, tmV, a, s);
+}
+
+}  // namespace
+}  // namespace pfkv
+
+extern "C" {
+
+int pfkv_paged_decode_attn(void* out, const void* q, const void* k_cache, const void* v_cache,
+                           pfkv_cache_dtype cache_dtype, const int32_t* block_tables,
+                           int max_pages_per_seq, const int32_t* context_lens, int batch,
+                           int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+                           int64_t num_pages, float k_scale, float v_scale, float softmax_scale,
+                           int kv_split_tokens, void* workspace, size_t workspace_bytes,
+                           float* lse_out, pfkv_stream_t stream) {
+  return pfkv::decode_entry(out, q, k_cache, v_cache, cache_dtype, block_tables, max_pages_per_seq,
+                            context_lens, batch, num_q_heads, num_kv_heads, head_dim, page_size,
+                            num_pages, k_scale, v_scale, softmax_scale, kv_split_tokens, workspace,
+                            workspace_bytes, lse_out, stream, pfkv::kSclHost, nullptr, nullptr, 0);
+}
+
+int pfkv_paged_decode_attn_scaled(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                  pfkv_scale_granularity granularity, const float* k_scales,
+                                  const float* v_scales, const int32_t* block_tables,
+                                  int max_pages_per_seq, const int32_t* context_lens, int batch,
+                                  int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+                                  int64_t num_pages, float softmax_scale, int kv_split_tokens,
+                                  void* workspace, size_t workspace_bytes, float* lse_out,
+                                  pfkv_stream_t stream) {
+  using namespace pfkv;
+  int scl, stride = 0;
+  switch (granularity) {
+    case PFKV_SCALE_TENSOR: scl = kSclUnit; break;
+    case PFKV_SCALE_HEAD: scl = kSclUnit; stride = 1; break;
+    case PFKV_SCALE_TOKEN: scl = kSclToken; break;
+    default:
+      clear_error();
+      return fail(PFKV_ERR_INVALID_ARG, "paged_decode_scaled: unknown granularity %d", (int)granularity);
+  }
+  return decode_entry(out, q, k_cache, v_cache, PFKV_CACHE_FP8_E4M3, block_tables, max_pages_per_seq,
+                      context_lens, batch, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
+                      1.f, 1.f, softmax_scale, kv_split_tokens, workspace, workspace_bytes, lse_out,
+                      stream, scl, k_scales, v_scales, stride);
 }
 
 }  // extern "C"

@@ -104,6 +104,30 @@ def oracle_one_head(w, b, kvh, bf16=False):
     return kc, vc, np.arange(max(npg, 1), dtype=np.int32)
 
 
+def oracle_one_head_token(w, b, kvh):
+    """As oracle_one_head for per-token scales: the oracle's codes and scales
+    of one (request, KV head) in a private mini cache, plus its block-table row."""
+    L = int(w.context_lens[b])
+    P = w.P
+    npg = max((L + P - 1) // P, 1)
+    kc = np.zeros((npg, 1, P, w.D), np.uint8)
+    vc = np.zeros_like(kc)
+    ks = np.zeros((npg, 1, P), np.float32)
+    vs = np.zeros_like(ks)
+    slots = np.arange(L, dtype=np.int64)
+    oracle.kv_append_token(w.kv_head_bits("k", b, kvh, 0, L)[:, None, :], kc, ks, slots, P)
+    oracle.kv_append_token(w.kv_head_bits("v", b, kvh, 0, L)[:, None, :], vc, vs, slots, P)
+    return kc, vc, ks, vs, np.arange(npg, dtype=np.int32)
+
+
+def gpu_scales_of(scales_dev, bt_row, kvh, L, P):
+    """Per-token scales t < L of one KV head of one request -> host float32 [L]."""
+    import torch
+    npg = (L + P - 1) // P
+    pages = torch.as_tensor(bt_row[:npg].astype(np.int64), device=scales_dev.device)
+    return scales_dev.index_select(0, pages)[:, kvh].reshape(-1)[:L].cpu().numpy()
+
+
 def to_np_bf16(t):
     import torch
     return t.float().cpu().numpy().astype(np.float64) if t.dtype == torch.bfloat16 else t.cpu().numpy()

@@ -49,6 +49,67 @@ def oracle_fill_mla(m):
     return cache
 
 
+# ------------------------------------------------------- scale granularities
+def spread_rows(w, which, b, t0, t1, spread=6, zero_rows=False):
+    """bf16 rows [t1-t0][Hkv][D] whose magnitudes vary by token and head
+    (PagedWorkload.kv_spread_bits); zero_rows also blanks every 13th token of
+    head 0 (K) or every 11th (V) so that all-zero rows occur."""
+    x = w.kv_spread_bits(which, b, t0, t1, spread)
+    if zero_rows:
+        t = np.arange(t0, t1)
+        x[(t % (13 if which == "k" else 11)) == 0, 0, :] = 0
+    return x
+
+
+def spread_scales(w, gran, spread=6, zero_rows=False):
+    """Per-tensor [1] or per-head [Hkv] scales (amax / 448 in fp32) of the
+    spread rows of every attended token of w; None for per-token."""
+    if gran == oracle.SCALE_TOKEN:
+        return None, None
+    out = []
+    for which in ("k", "v"):
+        m = np.zeros(w.Hkv, np.float32)
+        for b in range(w.B):
+            L = int(w.context_lens[b])
+            t0 = w.shared_tokens if 0 < b < w.shared_requests else 0
+            if L > t0:
+                x = np.abs(gen.bf16_bits_to_f32(spread_rows(w, which, b, t0, L, spread, zero_rows)))
+                m = np.maximum(m, x.max(axis=(0, 2)))
+        if gran == oracle.SCALE_TENSOR:
+            m = np.array([m.max()], np.float32)
+        out.append((m / np.float32(448.0)).astype(np.float32))
+    return out[0], out[1]
+
+
+def oracle_fill_scaled(w, gran, spread=6, zero_rows=False):
+    """Caches [pages][Hkv][P][D] (u8) and scales of w filled by the oracle at
+    granularity gran from the spread rows: (kc, vc, ks, vs)."""
+    shape = (w.num_pages, w.Hkv, w.P, w.D)
+    kc, vc = np.zeros(shape, np.uint8), np.zeros(shape, np.uint8)
+    ks, vs = spread_scales(w, gran, spread, zero_rows)
+    if gran == oracle.SCALE_TOKEN:
+        ks = np.zeros(shape[:3], np.float32)
+        vs = np.zeros(shape[:3], np.float32)
+    for b in range(w.B):
+        L = int(w.context_lens[b])
+        t0 = w.shared_tokens if 0 < b < w.shared_requests else 0
+        if L <= t0:
+            continue
+        sl = w.slots(b, t0, L)
+        kb = spread_rows(w, "k", b, t0, L, spread, zero_rows)
+        vb = spread_rows(w, "v", b, t0, L, spread, zero_rows)
+        if gran == oracle.SCALE_TOKEN:
+            oracle.kv_append_token(kb, kc, ks, sl, w.P)
+            oracle.kv_append_token(vb, vc, vs, sl, w.P)
+        elif gran == oracle.SCALE_HEAD:
+            oracle.kv_append_head(kb, kc, sl, w.P, ks)
+            oracle.kv_append_head(vb, vc, sl, w.P, vs)
+        else:
+            oracle.kv_append(kb, kc, sl, w.P, float(ks[0]))
+            oracle.kv_append(vb, vc, sl, w.P, float(vs[0]))
+    return kc, vc, ks, vs
+
+
 # ------------------------------------------------------------- dense reference
 def torch_dequant_fp8(x_bits, scale):
     """fp32(x) / scale (IEEE fp32) cast by torch to float8_e4m3fn, back to float64 x scale."""

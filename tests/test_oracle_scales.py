@@ -25,7 +25,7 @@ import torch
 import oracle
 import synth
 from synth import gen
-from oracle_helpers import sdpa_dense
+from oracle_helpers import oracle_fill_scaled, sdpa_dense
 
 E4M3_MAX_CODE = 0x7E
 
@@ -135,29 +135,7 @@ def test_head_append_equals_per_tensor_append_of_each_head():
 
 
 def _filled(w, gran, spread=6):
-    """Caches and scales of workload w filled by the oracle at granularity gran."""
-    shape = (w.num_pages, w.Hkv, w.P, w.D)
-    kc, vc = np.zeros(shape, np.uint8), np.zeros(shape, np.uint8)
-    if gran == oracle.SCALE_TOKEN:
-        ks = np.zeros(shape[:3], np.float32)
-        vs = np.zeros(shape[:3], np.float32)
-    else:
-        ks = np.array([0.02, 0.05, 0.11, 0.3][: w.Hkv], np.float32)
-        vs = np.array([0.07, 0.015, 0.2, 0.04][: w.Hkv], np.float32)
-    for b in range(w.B):
-        L = int(w.context_lens[b])
-        t0 = w.shared_tokens if 0 < b < w.shared_requests else 0
-        if L <= t0:
-            continue
-        sl = w.slots(b, t0, L)
-        kb, vb = w.kv_spread_bits("k", b, t0, L, spread), w.kv_spread_bits("v", b, t0, L, spread)
-        if gran == oracle.SCALE_TOKEN:
-            oracle.kv_append_token(kb, kc, ks, sl, w.P)
-            oracle.kv_append_token(vb, vc, vs, sl, w.P)
-        else:
-            oracle.kv_append_head(kb, kc, sl, w.P, ks)
-            oracle.kv_append_head(vb, vc, sl, w.P, vs)
-    return kc, vc, ks, vs
+    return oracle_fill_scaled(w, gran, spread)
 
 
 def _workload(**kw):
