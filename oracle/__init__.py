@@ -74,6 +74,8 @@ def lib():
             L.orc_kv_append_token.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i64]
             L.orc_paged_decode_scaled_one.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, vp, i32, i32,
                                                       i32, i32, i32, i64, f32]
+            L.orc_paged_prefill.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, vp, vp, i32, i32, i32, i32,
+                                            i32, i64, f32, f32, f32, i64, i64]
             L.orc_paged_decode_scaled.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, vp, i32, vp, i32,
                                                   i32, i32, i32, i32, i64, f32, i64, i64]
             L.orc_paged_decode_one.restype = i32
@@ -245,6 +247,28 @@ def paged_decode(q_bf16, k_cache, v_cache, block_tables, context_lens, page_size
     _chk(lib().orc_paged_decode(_ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache), dt,
                                 _ptr(bt), bt.shape[1], _ptr(cl), B, Hq, num_kv_heads, D, page_size,
                                 k_cache.shape[0], k_scale, v_scale, softmax_scale, u0, u1))
+    return out, lse
+
+
+def paged_prefill(q_bf16, k_cache, v_cache, block_tables, context_lens, q_start, page_size: int,
+                  k_scale: float, v_scale: float, softmax_scale: float, num_kv_heads: int, rows=None):
+    """Several new query tokens per request, causal among themselves: q
+    [total_q][Hq][D] bf16 bits with request b's rows q_start[b] .. q_start[b+1]-1
+    at positions L_b - n_b + i.  Returns (out [total_q][Hq][D], lse [total_q][Hq])."""
+    q = _c(q_bf16, np.uint16)
+    T, Hq, D = q.shape
+    dt = ORC_CACHE_BF16 if k_cache.dtype == np.uint16 else ORC_CACHE_FP8_E4M3
+    bt = _c(block_tables, np.int32)
+    cl = _c(context_lens, np.int32)
+    qs = _c(q_start, np.int32)
+    B = cl.shape[0]
+    assert qs.shape == (B + 1,) and qs[-1] == T
+    out = np.zeros((T, Hq, D), np.float64)
+    lse = np.full((T, Hq), -np.inf, np.float64)
+    r0, r1 = (0, T * Hq) if rows is None else rows
+    _chk(lib().orc_paged_prefill(_ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache), dt,
+                                 _ptr(bt), bt.shape[1], _ptr(cl), _ptr(qs), B, Hq, num_kv_heads, D,
+                                 page_size, k_cache.shape[0], k_scale, v_scale, softmax_scale, r0, r1))
     return out, lse
 
 

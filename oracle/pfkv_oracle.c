@@ -23,6 +23,12 @@
  *         "分块式 Ring Attention 实现": blockwise attention keeps the running
  *         maximum, normaliser and output (m, ℓ, O) so that the blockwise result
  *         equals full attention.
+ *  [CHK]  explainer page, section "チャンク分割と、その大きさの決め方": chunked
+ *         prefill cuts a prompt into fixed-size chunks, one per step, writing
+ *         each chunk's KV before the next; its tokens attend the cached prefix
+ *         and each other causally.
+ *  [SPEC] same page, "Speculative Decoding" section: the target model checks
+ *         the gamma+1 drafted positions in one parallel forward pass.
  *  [MLA]  same article, §5.1.1/§5.1.2: MLA keeps one compressed latent cKV per
  *         token shared by all heads; DSA selects the top-k historical tokens that
  *         take part in attention.
@@ -427,6 +433,47 @@ int orc_paged_decode_scaled(double *out, double *lse, const uint16_t *q, const u
             return rc;
         if (lse)
             lse[u] = lse_bh;
+    }
+    return ORC_OK;
+}
+
+/* Several new query tokens per request ([CHK] chunked prefill / [SPEC]
+ * verification): request b's last n_b = q_start[b+1] - q_start[b] positions,
+ * L_b - n_b .. L_b - 1, are queries; query i sits at position L_b - n_b + i and
+ * attends the keys 0 .. L_b - n_b + i (causal within the new tokens).  That is
+ * decode attention (orc_paged_decode_one) over a context of L_b - n_b + i + 1
+ * tokens.  q / out rows are [q_start[b] + i][Hq][D]; lse [q_start[b] + i][Hq]. */
+int orc_paged_prefill(double *out, double *lse, const uint16_t *q, const void *k_cache,
+                      const void *v_cache, int cache_dtype, const int32_t *block_tables,
+                      int max_pages_per_seq, const int32_t *context_lens, const int32_t *q_start,
+                      int B, int Hq, int Hkv, int D, int P, int64_t num_pages, float k_scale,
+                      float v_scale, float softmax_scale, int64_t r_begin, int64_t r_end)
+{
+    if (Hkv <= 0 || Hq % Hkv != 0)
+        return ORC_ERR_ARG;
+    int G = Hq / Hkv;
+    int64_t total = q_start[B];
+    if (r_end > total * Hq)
+        r_end = total * Hq;
+    for (int64_t u = r_begin; u < r_end; u++) {
+        int64_t row = u / Hq; /* query token row in q */
+        int h = (int)(u % Hq);
+        int b = 0;
+        while (q_start[b + 1] <= row)
+            b++;
+        int n = q_start[b + 1] - q_start[b];
+        int L = context_lens[b];
+        int i = (int)(row - q_start[b]);
+        if (n > L || L > max_pages_per_seq * P)
+            return ORC_ERR_INDEX;
+        double lse_r;
+        int rc = orc_paged_decode_one(out + u * D, &lse_r, q + u * D, k_cache, v_cache, cache_dtype,
+                                      block_tables + (int64_t)b * max_pages_per_seq, L - n + i + 1,
+                                      Hkv, h / G, D, P, num_pages, k_scale, v_scale, softmax_scale);
+        if (rc != ORC_OK)
+            return rc;
+        if (lse)
+            lse[u] = lse_r;
     }
     return ORC_OK;
 }

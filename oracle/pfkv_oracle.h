@@ -52,6 +52,11 @@ int orc_paged_decode_scaled(double *out, double *lse, const uint16_t *q, const u
                             int max_pages_per_seq, const int32_t *context_lens, int B, int Hq,
                             int Hkv, int D, int P, int64_t num_pages, float softmax_scale,
                             int64_t u_begin, int64_t u_end);
+int orc_paged_prefill(double *out, double *lse, const uint16_t *q, const void *k_cache,
+                      const void *v_cache, int cache_dtype, const int32_t *block_tables,
+                      int max_pages_per_seq, const int32_t *context_lens, const int32_t *q_start,
+                      int B, int Hq, int Hkv, int D, int P, int64_t num_pages, float k_scale,
+                      float v_scale, float softmax_scale, int64_t r_begin, int64_t r_end);
 int orc_paged_decode_split_one(double *out, double *lse, const uint16_t *q,
                                const void *k_cache, const void *v_cache, int cache_dtype,
                                const int32_t *bt_row, int L, int Hkv, int kvh, int D, int P,

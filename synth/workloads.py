@@ -171,6 +171,26 @@ class PagedWorkload:
         n = self.B * self.Hq * self.D
         return gen.normal_bf16_range(self.key_q, 0, n).reshape(self.B, self.Hq, self.D)
 
+    def q_new_bits(self, q_lens=None) -> np.ndarray:
+        """[sum q_lens][Hq][D] bf16 bits: one query row per new token, request
+        b's rows at positions L_b - q_lens[b] .. L_b - 1 (q_lens defaults to
+        n_new for every request).  Row (b, position t) draws counters from its
+        own run, so any subset of positions regenerates the same values."""
+        q_lens = np.full(self.B, self.n_new) if q_lens is None else np.asarray(q_lens)
+        rows = []
+        for b in range(self.B):
+            L = int(self.context_lens[b])
+            for t in range(L - int(q_lens[b]), L):
+                base = ((1 << 40) + (b << TOKEN_SHIFT) + t) * self.Hq * self.D
+                rows.append(gen.normal_bf16_range(self.key_q, base, self.Hq * self.D))
+        if not rows:
+            return np.zeros((0, self.Hq, self.D), np.uint16)
+        return np.stack(rows).reshape(-1, self.Hq, self.D)
+
+    def q_start(self, q_lens=None) -> np.ndarray:
+        q_lens = np.full(self.B, self.n_new) if q_lens is None else np.asarray(q_lens)
+        return np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+
     # ----------------------------------------------------------------- slots
     def slots(self, b: int, t0: int, t1: int) -> np.ndarray:
         t = np.arange(t0, t1, dtype=np.int64)
