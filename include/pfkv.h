@@ -259,6 +259,56 @@ PFKV_API int pfkv_paged_decode_attn_scaled(void *out, const void *q, const void 
                                            pfkv_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* paged_prefill_attn -- several new query tokens per request over the paged
+ * e4m3 cache, causal among the new tokens: the attention of a chunked-prefill
+ * step or of a speculative-decoding verification pass.
+ *
+ * Explainer, section "チャンク分割と、その大きさの決め方": a chunked prefill
+ * writes each chunk's KV before the next, and the chunk's tokens attend the
+ * cached prefix and each other; "Speculative Decoding" section: the target
+ * model checks the gamma+1 drafted positions in one parallel forward pass.
+ * kLLM article, §5.2.2: chunks of a long context merge by (m, ℓ, O).
+ *
+ * Request b has n_b = q_start[b+1] - q_start[b] query tokens, at positions
+ * L_b - n_b .. L_b - 1 (their K/V must already be in the cache: append them
+ * first).  For query i of request b and query head h (kvh = h / (Hq / Hkv)):
+ *   s_t = softmax_scale * sum_d q[q_start[b]+i][h][d] * K(t)[d] * k_scale,
+ *         t = 0 .. L_b - n_b + i
+ *   out = sum_t e^{s_t - m} V(t) * v_scale / sum_t e^{s_t - m}
+ *   lse = m + ln sum_t e^{s_t - m}
+ * Products on the tensor cores in f16 (e4m3 widens exactly; q is rounded from
+ * bf16 to f16, exact for 2^-14 <= |q| <= 65504; P is f16 <= 2^8) with fp32
+ * accumulation.
+ *   out, q        bf16 [q_start[batch]][num_q_heads][head_dim]
+ *   q_start       int32 [batch + 1] (device), non-decreasing, q_start[0] = 0
+ *   max_q_len     host bound on every n_b; max_context_len host bound on
+ *                 every L_b (the grid is sized from them; larger values are
+ *                 clamped and flagged PFKV_DEVERR_BAD_CONTEXT, as is n_b > L_b)
+ *   kv_split_tokens  0: one pass over each request's context; > 0 (a
+ *                 multiple of 64): chunks of that many tokens run in parallel
+ *                 and are merged (workspace grows with batch * num_kv_heads *
+ *                 ceil(max_q_len * G / 128) * ceil(max_context_len / split))
+ *   workspace     >= pfkv_paged_prefill_workspace_size(...) bytes, 256-byte
+ *                 aligned; lse_out optional fp32 [q_start[batch]][num_q_heads]
+ * Other layouts as pfkv_paged_decode_attn.
+ * Supported: head_dim 128; e4m3 cache; page_size a multiple of 16;
+ * (num_q_heads / num_kv_heads) divides 128.
+ * Device errors: PFKV_DEVERR_BAD_PAGE (rows read as zeros),
+ * PFKV_DEVERR_BAD_CONTEXT, PFKV_DEVERR_WAIT_TIMEOUT. */
+PFKV_API size_t pfkv_paged_prefill_workspace_size(int batch, int num_q_heads, int num_kv_heads,
+                                                  int head_dim, int max_q_len, int max_context_len,
+                                                  int kv_split_tokens);
+PFKV_API int pfkv_paged_prefill_attn(void *out, const void *q, const void *k_cache,
+                                     const void *v_cache, const int32_t *block_tables,
+                                     int max_pages_per_seq, const int32_t *context_lens,
+                                     const int32_t *q_start, int batch, int num_q_heads,
+                                     int num_kv_heads, int head_dim, int page_size,
+                                     int64_t num_pages, int max_q_len, int max_context_len,
+                                     float k_scale, float v_scale, float softmax_scale,
+                                     int kv_split_tokens, void *workspace, size_t workspace_bytes,
+                                     float *lse_out, pfkv_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* mla_decode_attn -- MLA absorbed-latent decode over one shared e4m3 latent
  * row per token, optionally restricted to a top-k token list.
  *

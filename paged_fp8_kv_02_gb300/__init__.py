@@ -76,6 +76,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                                      i32, i64, f32, f32, f32, i32, i64, vp, vp, vp]),
             "pfkv_paged_decode_attn_scaled": (i32, [vp, vp, vp, vp, i32, vp, vp, vp, i32, vp, i32, i32, i32,
                                                     i32, i32, i64, f32, i32, vp, sz, vp, vp]),
+            "pfkv_paged_prefill_workspace_size": (sz, [i32, i32, i32, i32, i32, i32, i32]),
+            "pfkv_paged_prefill_attn": (i32, [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i64,
+                                              i32, i32, f32, f32, f32, i32, vp, sz, vp, vp]),
             "pfkv_mla_decode_workspace_size": (sz, [i32, i32, i32, i32]),
             "pfkv_mla_decode_attn": (i32, [vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32,
                                            i64, f32, f32, vp, sz, vp, vp]),
@@ -242,6 +245,34 @@ def paged_decode_attn_noalloc(out, q, k_cache, v_cache, block_tables, context_le
                                                int(max_total_chunks), _ptr(lse_out), _ptr(status_out),
                                                _stream(stream))
     _check("paged_decode_attn_noalloc", rc)
+
+
+def paged_prefill_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, max_q_len: int,
+                                 max_context_len: int, kv_split_tokens: int = 0, head_dim: int = 128) -> int:
+    return int(load().pfkv_paged_prefill_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_q_len,
+                                                        max_context_len, kv_split_tokens))
+
+
+def paged_prefill_attn(out, q, k_cache, v_cache, block_tables, context_lens, q_start, max_q_len: int,
+                       max_context_len: int, k_scale: float, v_scale: float, softmax_scale: float,
+                       kv_split_tokens: int = 0, workspace=None, lse_out=None, stream=None):
+    """Several new query tokens per request, causal among themselves: q/out
+    bf16 [q_start[B]][Hq][D]; q_start int32 [B+1]; caches uint8 (e4m3)
+    [pages][Hkv][P][D].  Returns the workspace used."""
+    import torch
+    T, Hq, D = q.shape
+    pages, Hkv, P, _ = k_cache.shape
+    B = context_lens.shape[0]
+    if workspace is None:
+        n = paged_prefill_workspace_size(B, Hq, Hkv, max_q_len, max_context_len, kv_split_tokens, D)
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+    rc = load().pfkv_paged_prefill_attn(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                        block_tables.shape[1], _ptr(context_lens), _ptr(q_start), B, Hq, Hkv, D,
+                                        P, pages, int(max_q_len), int(max_context_len), float(k_scale),
+                                        float(v_scale), float(softmax_scale), int(kv_split_tokens),
+                                        _ptr(workspace), workspace.numel(), _ptr(lse_out), _stream(stream))
+    _check("paged_prefill_attn", rc)
+    return workspace
 
 
 def mla_decode_workspace_size(batch: int, num_heads: int, d_latent: int = 512, topk: int = 0) -> int:

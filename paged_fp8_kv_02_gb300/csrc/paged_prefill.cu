@@ -1,0 +1,631 @@
+// paged_prefill.cu -- attention of several new query tokens per request over
+// the paged e4m3 cache, causal among the new tokens, on the fifth-generation
+// tensor cores (tcgen05, operands in shared and tensor memory).
+//
+// Inference-engine scheduling explainer (推論エンジンの実践), section
+// "チャンク分割と、その大きさの決め方": chunked prefill writes a prompt's KV chunk
+// by chunk, and each chunk's tokens attend the cached prefix and each other;
+// "Speculative Decoding" section: the target model checks the drafted
+// positions in one parallel forward pass.  Both are this operation: request b
+// has n_b query tokens at positions L_b - n_b .. L_b - 1, and query i attends
+// keys 0 .. L_b - n_b + i.
+//
+// With several queries per KV head the step becomes a dense contraction, so
+// the products run on tcgen05 (kind::f16, fp32 accumulation in tensor memory):
+//   * a work unit is (request, KV head, block of 128 rows, KV chunk), a row
+//     being one (query token, query head) pair of that KV head: 128 / G query
+//     tokens per block;
+//   * the producer warp gathers 64-token K and V tiles of e4m3 with TMA (four
+//     16-token boxes each, one block-table entry per box, loaded eight tiles
+//     ahead);
+//   * four converter warps widen them to f16 in 128-byte-swizzled atoms (the
+//     K tile is the K-major B operand of S = Q.K^T, the V tile the MN-major B
+//     operand of O = P.V);
+//   * one thread issues the MMAs: S for a tile into one of two 64-column
+//     tensor-memory buffers, then O += P.V with P read from tensor memory;
+//   * four softmax warps own one row each per lane: mask (causal and context
+//     end), lazy-reference exp2 online softmax (the reference moves only when a
+//     score exceeds it by more than 2^8; the accumulator in tensor memory is
+//     then rescaled), P as f16 pairs written over the row's scores, and the
+//     epilogue.
+// Long contexts are cut into chunks of kv_split_tokens; chunks write fp32
+// partial states (m, l, o) and a merge kernel combines them by the log-sum-exp
+// rule (kLLM article, §5.2.2).
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "pfkv_internal.h"
+#include "pfkv_ptx.cuh"
+#include "pfkv_tc.cuh"
+
+namespace pfkv {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kRows = 128;                    // MMA M: rows of a work unit
+constexpr int kTokN = 64;                     // KV tokens per tile
+constexpr int kBoxTok = 16;                   // tokens per TMA box
+constexpr int kBoxes = kTokN / kBoxTok;       // 4
+constexpr int kStages = 4;                    // e4m3 stage ring
+constexpr int kBoxBytes = kBoxTok * kD;       // 2 KB
+constexpr int kStageBytes = 2 * kTokN * kD;   // K + V e4m3: 16 KB
+constexpr int kKvAtom = kTokN * 128;          // [64 tokens][64 f16] swizzled atom: 8 KB
+constexpr int kKvBufBytes = 4 * kKvAtom;      // K (2 atoms) + V (2 atoms): 32 KB
+constexpr int kQAtom = kRows * 128;           // [128 rows][64 f16]: 16 KB
+constexpr int kPartStride = 132;              // floats per row of a partial state: m, l, -, -, o[128]
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.f;
+constexpr int kPageBatch = 8;                 // tiles whose block-table entries one load covers
+
+constexpr int kOffQ = 0;
+constexpr int kOffKv = kOffQ + 2 * kQAtom;
+constexpr int kOffStage = kOffKv + 2 * kKvBufBytes;
+constexpr int kOffBars = kOffStage + kStages * kStageBytes;
+constexpr int kSmemBytes = kOffBars + 256 + 1024;  // + 1024-byte alignment slack
+
+constexpr int kProdWarp = 0, kMmaWarp = 1, kConvWarp0 = 2, kSoftWarp0 = 6;
+constexpr int kThreads = 320;
+
+// tensor memory: S/P buffers at columns 0 and 64, O at 128..255
+constexpr uint32_t kTmemS = 0, kTmemO = 128, kTmemCols = 256;
+constexpr uint32_t kIdescQK = tc::idesc_f16(kRows, kTokN, false);
+constexpr uint32_t kIdescPV = tc::idesc_f16(kRows, kD, true);
+
+struct PrefillArgs {
+  __nv_bfloat16* out;
+  const __nv_bfloat16* q;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const int32_t* q_start;
+  float* lse;
+  int32_t* status;
+  float* partials;  // [units][kRows][kPartStride] when C > 1
+  int B, Hq, Hkv, G, P, max_pages;
+  int QB;           // row blocks per (request, KV head)
+  int C;            // KV chunks per (request, KV head)
+  int split;        // tokens per chunk
+  int max_q_len, max_ctx;
+  int64_t num_pages;
+  float score_scale;  // k_scale * softmax_scale * log2(e)
+  float out_scale;    // v_scale
+};
+
+struct Bars {
+  uint64_t stage_full[kStages], stage_empty[kStages];
+  uint64_t kvfull[2], sfull[2], pfull[2], pvdone[2];
+  uint64_t qready;
+  uint32_t tmem_base;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+
+// Geometry of one (request, KV head, row block, chunk) unit, the same in both
+// kernels.  Lengths are clamped to what the launch covers; the tile kernel
+// reports clamping in the status word.
+struct Unit {
+  int b, kvh, qb, c;
+  int L, n;          // clamped context length and query count
+  int i0, i1;        // query tokens [i0, i1) of this block
+  int rows;          // valid rows: (i1 - i0) * G
+  int t_lo, t_hi;    // KV tokens [t_lo, t_hi) this unit reads (t_hi may be <= t_lo)
+  int t_end_chunk;   // min(L, t_lo + split): the chunk's own end
+  int ntiles;
+  bool active;       // the unit exists (its block has queries and its chunk starts inside L)
+};
+
+__device__ __forceinline__ Unit unit_of(const PrefillArgs& a, int64_t u, bool report) {
+  Unit x;
+  x.qb = (int)(u % a.QB);
+  int64_t r = u / a.QB;
+  x.c = (int)(r % a.C);
+  r /= a.C;
+  x.kvh = (int)(r % a.Hkv);
+  x.b = (int)(r / a.Hkv);
+  const int L_raw = a.context_lens[x.b];
+  const int n_raw = a.q_start[x.b + 1] - a.q_start[x.b];
+  int cap = a.max_pages * a.P;
+  if (a.max_ctx < cap) cap = a.max_ctx;
+  int L = L_raw < 0 ? 0 : (L_raw > cap ? cap : L_raw);
+  int ncap = L < a.max_q_len ? L : a.max_q_len;
+  int n = n_raw < 0 ? 0 : (n_raw > ncap ? ncap : n_raw);
+  if (report && (L != L_raw || n != n_raw)) atomicOr(a.status, kErrBadContext);
+  x.L = L;
+  x.n = n;
+  const int tpb = kRows / a.G;
+  x.i0 = x.qb * tpb;
+  x.i1 = min(n, x.i0 + tpb);
+  x.rows = (x.i1 - x.i0) * a.G;
+  x.t_lo = x.c * a.split;
+  x.active = x.i0 < n && x.t_lo < L;
+  const int64_t chunk_end = (int64_t)x.t_lo + a.split;
+  x.t_end_chunk = (int)(chunk_end < L ? chunk_end : L);
+  const int qpos_max = L - n + x.i1 - 1;
+  x.t_hi = min(x.t_end_chunk, qpos_max + 1);
+  x.ntiles = x.active && x.t_hi > x.t_lo ? (x.t_hi - x.t_lo + kTokN - 1) / kTokN : 0;
+  return x;
+}
+
+// Bounded wait taken by every lane of a warp, with one verdict for all lanes
+// (so that a timeout never splits the warp).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
+  return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity));
+}
+
+// 128-byte-swizzled offset of 16-byte chunk c of row r in a TMA box written
+// with CU_TENSOR_MAP_SWIZZLE_128B (1024-byte aligned).
+__device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
+
+// Offset of f16 unit u (elements 8u .. 8u+7, u < 16) of row r in a pair of
+// 128-byte-swizzled K-major atoms [rows][64] (atom size atom_bytes).
+__device__ __forceinline__ uint32_t atom_off(int r, int u, int atom_bytes) {
+  return (uint32_t)((u >> 3) * atom_bytes + r * 128 + 16 * ((u & 7) ^ (r & 7)));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                   const PrefillArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* const smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  Bars& bs = *reinterpret_cast<Bars*>(smem + kOffBars);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int64_t u = blockIdx.x;
+  const Unit x = unit_of(a, u, threadIdx.x == 0 && (u % ((int64_t)a.QB * a.C * a.Hkv)) == 0);
+  if (!x.active) return;  // uniform over the CTA: nothing to compute or write
+  const int ntiles = x.ntiles;
+  const bool direct = a.C == 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&bs.stage_full[s]), 1);
+      mbar_init(smem_u32(&bs.stage_empty[s]), 4);
+    }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(smem_u32(&bs.kvfull[k]), 4);
+      mbar_init(smem_u32(&bs.sfull[k]), 1);
+      mbar_init(smem_u32(&bs.pfull[k]), 4);
+      mbar_init(smem_u32(&bs.pvdone[k]), 1);
+    }
+    mbar_init(smem_u32(&bs.qready), 4);
+    fence_mbar_init();
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  if (warp == kMmaWarp) {
+    tc::tmem_alloc(smem_u32(&bs.tmem_base), kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = bs.tmem_base;
+  bool to = false;  // a bounded wait gave up
+
+  if (warp == kProdWarp) {
+    // ------------------------------------------------------------ producer
+    // Lane l holds the block-table entry of box l % 4 of tile (batch + l / 4);
+    // the next batch is loaded while the current one is issued.
+    const int32_t* bt = a.block_tables + (int64_t)x.b * a.max_pages;
+    auto load_batch = [&](int j0) {
+      const int j = j0 + lane / kBoxes;
+      const int tb = x.t_lo + j * kTokN + (lane % kBoxes) * kBoxTok;
+      return (j < ntiles && tb < x.t_hi) ? __ldg(bt + tb / a.P) : 0;
+    };
+    int cur = load_batch(0), nxt = load_batch(kPageBatch);
+    for (int j = 0; j < ntiles && !to; ++j) {
+      if (j > 0 && j % kPageBatch == 0) {
+        cur = nxt;
+        nxt = load_batch(j + kPageBatch);
+      }
+      const int st = j % kStages;
+      if (j >= kStages && !warp_wait(smem_u32(&bs.stage_empty[st]), ((j / kStages) - 1) & 1)) {
+        to = true;
+        break;
+      }
+      const int tok0 = x.t_lo + j * kTokN;
+      const int nbox = min(kBoxes, (x.t_hi - tok0 + kBoxTok - 1) / kBoxTok);
+      const uint32_t bar = smem_u32(&bs.stage_full[st]);
+      if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(2 * nbox * kBoxBytes));
+      __syncwarp();
+      int page = __shfl_sync(0xFFFFFFFFu, cur, (j % kPageBatch) * kBoxes + (lane & 3));
+      if (lane < nbox) {
+        const int tb = tok0 + lane * kBoxTok;
+        if (page < 0 || (int64_t)page >= a.num_pages) {
+          atomicOr(a.status, kErrBadPage);
+          page = -1;  // the box lands outside the tensor and reads zeros
+        }
+        const int row = (page * a.Hkv + x.kvh) * a.P + tb % a.P;
+        const uint32_t dst = smem_u32(smem + kOffStage + st * kStageBytes) + lane * kBoxBytes;
+        tma_load_2d(dst, &tmK, 0, row, bar);
+        tma_load_2d(dst + kTokN * kD, &tmV, 0, row, bar);
+      }
+    }
+    // no copy may still be landing when the CTA retires
+    for (int j = ntiles > kStages ? ntiles - kStages : 0; j < ntiles; ++j)
+      if (!mbar_wait(smem_u32(&bs.stage_full[j % kStages]), (j / kStages) & 1)) to = true;
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0 && ntiles > 0) {
+      if (!mbar_wait(smem_u32(&bs.qready), 0)) to = true;
+      tc::fence_after_sync();
+      const uint64_t qdesc = tc::desc_sw128(smem_u32(smem + kOffQ), 16, 1024);
+      const uint32_t kv0 = smem_u32(smem + kOffKv);
+      int qn = 0, pn = 0;
+      long long idle_since = clock64();
+      while (pn < ntiles && !to) {
+        bool issued = false;
+        if (pn < qn && mbar_test_wait(smem_u32(&bs.pfull[pn & 1]), (pn >> 1) & 1)) {
+          tc::fence_after_sync();
+          const uint64_t vdesc = tc::desc_sw128(kv0 + (pn & 1) * kKvBufBytes + 2 * kKvAtom, kKvAtom, 1024);
+#pragma unroll
+          for (int k = 0; k < kTokN / 16; ++k)
+            tc::mma_ts(tmem + kTmemO, tmem + kTmemS + 64 * (pn & 1) + 8 * k, vdesc + (uint64_t)((2048 * k) >> 4),
+                       kIdescPV, (pn > 0 || k > 0) ? 1u : 0u);
+          tc::mma_commit(smem_u32(&bs.pvdone[pn & 1]));
+          ++pn;
+          issued = true;
+        }
+        // S(qn) reuses the buffer of P(qn - 2): issued after PV(qn - 2)
+        if (qn < ntiles && qn - pn < 2 && mbar_test_wait(smem_u32(&bs.kvfull[qn & 1]), (qn >> 1) & 1)) {
+          tc::fence_after_sync();
+          const uint64_t kdesc = tc::desc_sw128(kv0 + (qn & 1) * kKvBufBytes, 16, 1024);
+#pragma unroll
+          for (int k = 0; k < kD / 16; ++k)
+            tc::mma_ss(tmem + kTmemS + 64 * (qn & 1), qdesc + (uint64_t)(((k >> 2) * kQAtom + 32 * (k & 3)) >> 4),
+                       kdesc + (uint64_t)(((k >> 2) * kKvAtom + 32 * (k & 3)) >> 4), kIdescQK, k > 0 ? 1u : 0u);
+          tc::mma_commit(smem_u32(&bs.sfull[qn & 1]));
+          ++qn;
+          issued = true;
+        }
+        if (issued) {
+          idle_since = clock64();
+        } else {
+          __nanosleep(20);
+          if (clock64() - idle_since > kWaitLimitCycles) to = true;
+        }
+      }
+      // no MMA may still be running when the tensor memory is freed
+      if (pn > 0 && !mbar_wait(smem_u32(&bs.pvdone[(pn - 1) & 1]), ((pn - 1) >> 1) & 1)) to = true;
+    }
+    __syncwarp();
+  } else if (warp < kSoftWarp0) {
+    // ---------------------------------------------------------- converters
+    // Chunk i of the stage (K: i < 512, V: i >= 512; row (i % 512) / 8, 16-byte
+    // chunk i % 8) -> e4m3 -> f16 units 2(c % 4), 2(c % 4) + 1 of atom c / 4.
+    const int ct = threadIdx.x - kConvWarp0 * 32;
+    for (int j = 0; j < ntiles && !to; ++j) {
+      const int st = j % kStages, kb = j & 1;
+      if (!warp_wait(smem_u32(&bs.stage_full[st]), (j / kStages) & 1)) to = true;
+      if (j >= 2 && !to && !warp_wait(smem_u32(&bs.pvdone[kb]), ((j - 2) >> 1) & 1)) to = true;
+      if (to) break;
+      const int valid = min(kTokN, x.t_hi - (x.t_lo + j * kTokN));
+      const uint8_t* stage = smem + kOffStage + st * kStageBytes;
+      uint8_t* kv = smem + kOffKv + kb * kKvBufBytes;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int i = ct + 128 * m;
+        const int which = i >> 9, rem = i & 511;
+        const int row = rem >> 3, c = rem & 7;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (row < valid) v = lds128(stage + which * (kTokN * kD) + (row >> 4) * kBoxBytes + swz(row & 15, c));
+        uint4 o0, o1;
+        e4m3x4_to_f16x2x2(v.x, o0.x, o0.y);
+        e4m3x4_to_f16x2x2(v.y, o0.z, o0.w);
+        e4m3x4_to_f16x2x2(v.z, o1.x, o1.y);
+        e4m3x4_to_f16x2x2(v.w, o1.z, o1.w);
+        const uint32_t d = which * (2 * kKvAtom) + atom_off(row, 2 * c, kKvAtom);
+        *reinterpret_cast<uint4*>(kv + d) = o0;
+        *reinterpret_cast<uint4*>(kv + (d ^ 16)) = o1;  // unit 2(c%4) + 1: bit 0 of the unit flips
+      }
+      fence_proxy_async_smem();  // generic writes -> visible to the tensor core
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive_local(smem_u32(&bs.stage_empty[st]));
+        tc::mbar_arrive_local(smem_u32(&bs.kvfull[kb]));
+      }
+    }
+  } else {
+    // -------------------------------------------------- softmax + epilogue
+    const int quad = warp & 3;
+    const int r = 32 * quad + lane;  // this thread's row (tensor-memory lane)
+    const uint32_t trow = tmem + ((uint32_t)(32 * quad) << 16);
+    const bool row_ok = r < x.rows;
+    const int i = x.i0 + r / a.G, g = r % a.G;
+    const int64_t qrow = (int64_t)a.q_start[x.b] + i;
+    const int64_t head_row = qrow * a.Hq + (int64_t)x.kvh * a.G + g;  // row of q / out
+    // Q row -> f16 -> the swizzled K-major A operand
+    {
+      const uint4* qp = reinterpret_cast<const uint4*>(a.q + head_row * kD);
+#pragma unroll
+      for (int uu = 0; uu < 16; ++uu) {
+        uint4 w = make_uint4(0, 0, 0, 0);
+        if (row_ok) w = __ldg(qp + uu);
+        uint4 f;
+        f.x = pack_f16x2(bf16_lo(w.x), bf16_hi(w.x));
+        f.y = pack_f16x2(bf16_lo(w.y), bf16_hi(w.y));
+        f.z = pack_f16x2(bf16_lo(w.z), bf16_hi(w.z));
+        f.w = pack_f16x2(bf16_lo(w.w), bf16_hi(w.w));
+        *reinterpret_cast<uint4*>(smem + kOffQ + atom_off(r, uu, kQAtom)) = f;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.qready));
+    }
+    // keys t < lim are attended by this row
+    const int lim = row_ok ? min(x.L - x.n + i + 1, x.t_end_chunk) : x.t_lo;
+    const float sc = a.score_scale;
+    float mref = -INFINITY, rthr = -INFINITY, l = 0.f;
+    for (int j = 0; j < ntiles && !to; ++j) {
+      const int kb = j & 1;
+      if (!warp_wait(smem_u32(&bs.sfull[kb]), (j >> 1) & 1)) {
+        to = true;
+        break;
+      }
+      tc::fence_after_sync();
+      uint32_t sv[64];
+      {
+        uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
+        uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
+        tc::tmem_ld32(trow + kTmemS + 64 * kb, lo);
+        tc::tmem_ld32(trow + kTmemS + 64 * kb + 32, hi);
+        tc::tmem_ld_wait();
+      }
+      const int tok0 = x.t_lo + j * kTokN;
+      const int nvalid = lim - tok0;  // columns c < nvalid are attended
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 64; ++c)
+        if (c < nvalid) mx = fmaxf(mx, __uint_as_float(sv[c]));
+      const bool grow = mx > rthr;
+      if (__any_sync(0xFFFFFFFFu, grow)) {
+        const float mn = grow ? fmaxf(mref, mx * sc) : mref;
+        const float al = grow ? fast_exp2(mref - mn) : 1.f;  // 0 while mref is -inf
+        // the accumulator holds earlier tiles only once P(j - 1) was multiplied in
+        const bool rescale = __any_sync(0xFFFFFFFFu, grow && mref != -INFINITY);
+        if (rescale && j > 0) {
+          if (!warp_wait(smem_u32(&bs.pvdone[(j - 1) & 1]), ((j - 1) >> 1) & 1)) {
+            to = true;
+            break;
+          }
+          tc::fence_after_sync();
+#pragma unroll
+          for (int blk = 0; blk < 4; ++blk) {
+            uint32_t ov[32];
+            tc::tmem_ld32(trow + kTmemO + 32 * blk, ov);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * al);
+            tc::tmem_st32(trow + kTmemO + 32 * blk, ov);
+          }
+          tc::tmem_st_wait();
+        }
+        l *= al;
+        mref = mn;
+        rthr = (mn + kRescaleLog2) / sc;
+      }
+      uint32_t pv[32];
+      float ls = 0.f;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = 2 * c < nvalid ? fast_exp2(fmaf(__uint_as_float(sv[2 * c]), sc, -mref)) : 0.f;
+        const float p1 = 2 * c + 1 < nvalid ? fast_exp2(fmaf(__uint_as_float(sv[2 * c + 1]), sc, -mref)) : 0.f;
+        ls += p0 + p1;
+        pv[c] = pack_f16x2(p0, p1);
+      }
+      l += ls;
+      tc::tmem_st32(trow + kTmemS + 64 * kb, pv);
+      tc::tmem_st_wait();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.pfull[kb]));
+    }
+    // ---- epilogue: O (tensor memory) -> output row or partial state
+    if (!to && ntiles > 0 && !warp_wait(smem_u32(&bs.pvdone[(ntiles - 1) & 1]), ((ntiles - 1) >> 1) & 1))
+      to = true;
+    tc::fence_after_sync();
+    float* part = direct ? nullptr : a.partials + ((int64_t)u * kRows + r) * kPartStride;
+    const float inv = l > 0.f ? a.out_scale / l : 0.f;
+#pragma unroll
+    for (int blk = 0; blk < 4; ++blk) {
+      uint32_t ov[32];
+      if (ntiles > 0) {
+        tc::tmem_ld32(trow + kTmemO + 32 * blk, ov);
+        tc::tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) ov[c] = 0u;
+      }
+      if (!row_ok || to) continue;
+      if (direct) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          pk[c] = pack_bf16x2(__uint_as_float(ov[2 * c]) * inv, __uint_as_float(ov[2 * c + 1]) * inv);
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + head_row * kD + 32 * blk);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+      } else {
+        float4* dst = reinterpret_cast<float4*>(part + 4 + 32 * blk);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          dst[k] = make_float4(__uint_as_float(ov[4 * k]), __uint_as_float(ov[4 * k + 1]),
+                               __uint_as_float(ov[4 * k + 2]), __uint_as_float(ov[4 * k + 3]));
+      }
+    }
+    if (row_ok && !to) {
+      if (direct) {
+        if (a.lse) a.lse[head_row] = l > 0.f ? (mref + __log2f(l)) * kLn2 : -INFINITY;
+      } else {
+        part[0] = mref;
+        part[1] = l;
+      }
+    }
+  }
+
+  if (to) atomicOr(a.status, kErrWaitTimeout);
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// One warp per row of a (request, KV head, row block): folds the chunks'
+// partial states, M = max m_c, out = sum 2^(m_c - M) o_c / sum 2^(m_c - M) l_c.
+constexpr int kMergeWarps = 8;
+__global__ void __launch_bounds__(kMergeWarps * 32) prefill_merge_kernel(const PrefillArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t blk = blockIdx.x / (kRows / kMergeWarps);
+  const int r = (int)(blockIdx.x % (kRows / kMergeWarps)) * kMergeWarps + warp;
+  const int qb = (int)(blk % a.QB);
+  const int64_t bk = blk / a.QB;  // b * Hkv + kvh
+  const int64_t u0 = bk * a.C * a.QB + qb;  // unit of chunk 0
+  const Unit x = unit_of(a, u0, false);
+  if (!x.active || r >= x.rows) return;
+  const int nchunks = (x.L + a.split - 1) / a.split;
+  float M = -INFINITY, den = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c = 0; c < nchunks; ++c) {
+    const float* p = a.partials + ((u0 + (int64_t)c * a.QB) * kRows + r) * kPartStride;
+    const float mk = p[0], lk = p[1];
+    if (lk == 0.f) continue;  // a chunk this row does not reach
+    const float4 ok = reinterpret_cast<const float4*>(p + 4)[lane];
+    const float Mn = fmaxf(M, mk);
+    const float al = fast_exp2(M - Mn), wt = fast_exp2(mk - Mn);
+    den = den * al + wt * lk;
+    acc.x = acc.x * al + wt * ok.x;
+    acc.y = acc.y * al + wt * ok.y;
+    acc.z = acc.z * al + wt * ok.z;
+    acc.w = acc.w * al + wt * ok.w;
+    M = Mn;
+  }
+  const int i = x.i0 + r / a.G, g = r % a.G;
+  const int64_t head_row = ((int64_t)a.q_start[x.b] + i) * a.Hq + (int64_t)x.kvh * a.G + g;
+  const float inv = den > 0.f ? a.out_scale / den : 0.f;
+  reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.out) + head_row * kD)[lane] =
+      make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+  if (a.lse && lane == 0) a.lse[head_row] = den > 0.f ? (M + __log2f(den)) * kLn2 : -INFINITY;
+}
+
+constexpr size_t kStatusBytes = 256;
+
+int64_t units_of(int B, int Hkv, int QB, int C) { return (int64_t)B * Hkv * QB * C; }
+
+}  // namespace
+}  // namespace pfkv
+
+extern "C" {
+
+size_t pfkv_paged_prefill_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                         int max_q_len, int max_context_len, int kv_split_tokens) {
+  using namespace pfkv;
+  (void)head_dim;
+  if (batch < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads || max_q_len <= 0 ||
+      max_context_len <= 0 || kv_split_tokens < 0)
+    return 0;
+  const int G = num_q_heads / num_kv_heads;
+  if (G > kRows) return 0;
+  const int QB = (int)(((int64_t)max_q_len * G + kRows - 1) / kRows);
+  const int C = kv_split_tokens > 0 ? (max_context_len + kv_split_tokens - 1) / kv_split_tokens : 1;
+  if (C <= 1) return kStatusBytes;
+  return kStatusBytes + (size_t)units_of(batch, num_kv_heads, QB, C) * kRows * kPartStride * sizeof(float);
+}
+
+int pfkv_paged_prefill_attn(void* out, const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, int max_pages_per_seq, const int32_t* context_lens,
+                            const int32_t* q_start, int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                            int page_size, int64_t num_pages, int max_q_len, int max_context_len, float k_scale,
+                            float v_scale, float softmax_scale, int kv_split_tokens, void* workspace,
+                            size_t workspace_bytes, float* lse_out, pfkv_stream_t stream) {
+  using namespace pfkv;
+  clear_error();
+  if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || page_size <= 0 || num_pages <= 0 ||
+      max_pages_per_seq <= 0 || max_q_len <= 0 || max_context_len <= 0)
+    return fail(PFKV_ERR_INVALID_ARG, "paged_prefill: bad sizes");
+  if (num_q_heads % num_kv_heads != 0)
+    return fail(PFKV_ERR_INVALID_ARG, "paged_prefill: num_q_heads %% num_kv_heads != 0");
+  const int G = num_q_heads / num_kv_heads;
+  if (kRows % G != 0)
+    return fail(PFKV_ERR_UNSUPPORTED, "paged_prefill: group size %d does not divide 128", G);
+  if (head_dim != kD) return fail(PFKV_ERR_UNSUPPORTED, "paged_prefill: head_dim %d != 128", head_dim);
+  if (page_size % kBoxTok != 0)
+    return fail(PFKV_ERR_UNSUPPORTED, "paged_prefill: page_size %d not a multiple of 16", page_size);
+  if (kv_split_tokens < 0 || kv_split_tokens % kTokN != 0)
+    return fail(PFKV_ERR_INVALID_ARG, "paged_prefill: kv_split_tokens must be a multiple of 64");
+  if ((int64_t)num_pages * num_kv_heads * page_size >= (int64_t)1 << 31)
+    return fail(PFKV_ERR_UNSUPPORTED, "paged_prefill: cache has 2^31 or more token rows");
+  if ((int64_t)max_pages_per_seq * page_size >= (int64_t)1 << 30 || max_context_len >= (1 << 30))
+    return fail(PFKV_ERR_UNSUPPORTED, "paged_prefill: context too long");
+  if (!(softmax_scale > 0.f) || !isfinite(k_scale) || !isfinite(v_scale) || !isfinite(softmax_scale))
+    return fail(PFKV_ERR_INVALID_ARG, "paged_prefill: scales must be finite");
+  if (batch == 0) return PFKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !q_start || !workspace)
+    return fail(PFKV_ERR_INVALID_ARG, "paged_prefill: null pointer");
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(workspace, 256) || !aligned(block_tables, 4) || !aligned(context_lens, 4) ||
+      !aligned(q_start, 4) || (lse_out && !aligned(lse_out, 4)))
+    return fail(PFKV_ERR_INVALID_ARG, "paged_prefill: misaligned pointer");
+  const size_t need = pfkv_paged_prefill_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_q_len,
+                                                        max_context_len, kv_split_tokens);
+  if (need == 0 || workspace_bytes < need)
+    return fail(PFKV_ERR_WORKSPACE, "paged_prefill: workspace of %zu bytes is too small (%zu needed)",
+                workspace_bytes, need);
+
+  PrefillArgs a;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.q_start = q_start;
+  a.lse = lse_out;
+  a.status = reinterpret_cast<int32_t*>(ws);
+  a.partials = reinterpret_cast<float*>(ws + kStatusBytes);
+  a.B = batch;
+  a.Hq = num_q_heads;
+  a.Hkv = num_kv_heads;
+  a.G = G;
+  a.P = page_size;
+  a.max_pages = max_pages_per_seq;
+  a.QB = (int)(((int64_t)max_q_len * G + kRows - 1) / kRows);
+  a.C = kv_split_tokens > 0 ? (max_context_len + kv_split_tokens - 1) / kv_split_tokens : 1;
+  a.split = kv_split_tokens > 0 ? kv_split_tokens : (1 << 30);
+  a.max_q_len = max_q_len;
+  a.max_ctx = max_context_len;
+  a.num_pages = num_pages;
+  a.score_scale = k_scale * softmax_scale * kLog2e;
+  a.out_scale = v_scale;
+  const int64_t units = units_of(batch, num_kv_heads, a.QB, a.C);
+  if (units > 0x7FFFFFFF) return fail(PFKV_ERR_UNSUPPORTED, "paged_prefill: too many work units");
+
+  const cuuint64_t rows = (cuuint64_t)num_pages * num_kv_heads * page_size;
+  const cuuint64_t dims[2] = {128, rows};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {128, (cuuint32_t)kBoxTok};
+  CUtensorMap tmK, tmV;
+  int rc = encode_tensor_map(&tmK, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(k_cache), dims, strides,
+                             box, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc == PFKV_OK)
+    rc = encode_tensor_map(&tmV, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(v_cache), dims, strides,
+                           box, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != PFKV_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+        cudaSuccess)
+      return check_cuda("paged_prefill set smem attribute");
+    attr_set = true;
+  }
+  if (cudaMemsetAsync(a.status, 0, sizeof(int32_t), s) != cudaSuccess) return check_cuda("paged_prefill status");
+  prefill_kernel<<<(unsigned)units, kThreads, kSmemBytes, s>>>(tmK, tmV, a);
+  if (a.C > 1) {
+    const int64_t mblocks = (int64_t)batch * num_kv_heads * a.QB * (kRows / kMergeWarps);
+    prefill_merge_kernel<<<(unsigned)mblocks, kMergeWarps * 32, 0, s>>>(a);
+  }
+  return check_cuda("paged_prefill launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,165 @@
+"""paged_prefill_attn (several new query tokens per request, causal among them)
+on the GPU against the oracle.
+
+Small cases: caches encoded by the oracle from the host generator are
+uploaded and every output row is compared with the oracle (tolerance
+|err| <= 2e-3 * max|ref| + 1e-3 + half a bf16 ulp; lse to 2e-5 relative).
+Full size: config 5's cache is filled through the product's append from the
+device generator, its 8 appended tokens per request are the queries, and
+sampled (request, query, head) rows are recomputed by the oracle from the
+host generator in a private cache whose bytes are checked against the GPU's."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+from gpu_helpers import (append_fp8_fn, assert_within_tolerance, gpu_pages_of, oracle_one_head, pf,
+                         to_np_bf16)
+from oracle_helpers import oracle_fill_paged
+
+pytestmark = pytest.mark.gpu
+
+
+def _dev(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).to("cuda")
+
+
+def _dev_bits(bits):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to("cuda").view(torch.bfloat16)
+
+
+def _run(p, w, kc, vc, q_lens=None, split=0, max_q=None, max_ctx=None, bt=None, ctx=None):
+    import torch
+    qs = w.q_start(q_lens)
+    q = _dev_bits(w.q_new_bits(q_lens))
+    out = torch.zeros_like(q)
+    lse = torch.full((q.shape[0], w.Hq), float("nan"), dtype=torch.float32, device="cuda")
+    max_q = max_q or max(int(np.diff(qs).max(initial=1)), 1)
+    max_ctx = max_ctx or int(w.context_lens.max())
+    ws = p.paged_prefill_attn(out, q, kc, vc, _dev(w.block_tables if bt is None else bt),
+                              _dev(w.context_lens if ctx is None else ctx), _dev(qs), max_q, max_ctx,
+                              w.k_scale, w.v_scale, w.softmax_scale, kv_split_tokens=split, lse_out=lse)
+    torch.cuda.synchronize()
+    return to_np_bf16(out), lse.cpu().numpy(), p.workspace_status(ws)
+
+
+def _check_small(w, q_lens=None, split=0, **kw):
+    p = pf()
+    w.set_scales_host()
+    kc, vc = oracle_fill_paged(w)
+    out, lse, status = _run(p, w, _dev(kc), _dev(vc), q_lens, split, **kw)
+    assert status == 0
+    ref, ref_lse = oracle.paged_prefill(w.q_new_bits(q_lens), kc, vc, w.block_tables, w.context_lens,
+                                        w.q_start(q_lens), w.P, w.k_scale, w.v_scale, w.softmax_scale, w.Hkv)
+    if ref.shape[0]:
+        assert_within_tolerance(out, ref, f"{w.name} split {split}")
+        np.testing.assert_allclose(lse, ref_lse, rtol=2e-5, atol=2e-4)
+
+
+def _w(name, Hq, Hkv, lens, n_new, P=16, seed=31):
+    return synth.PagedWorkload(name, B=len(lens), Hq=Hq, Hkv=Hkv, D=128, P=P, context_lens=np.array(lens),
+                               n_new=n_new, seed=seed)
+
+
+@pytest.mark.parametrize("split", [0, 64, 192])
+def test_gqa_verification_sized(split):
+    _check_small(_w("g8", 16, 2, (9, 40, 77, 300), n_new=5), split=split)
+
+
+@pytest.mark.parametrize("split", [0, 128])
+def test_mha_two_row_blocks(split):
+    # G = 1: 128 query tokens per row block, 200 new tokens -> two blocks
+    _check_small(_w("mha", 4, 4, (200, 250, 333), n_new=200), split=split)
+
+
+def test_group16_page64_long():
+    _check_small(_w("g16", 16, 1, (8, 100, 700), n_new=8, P=64), split=128)
+
+
+def test_whole_prompt_is_new():
+    # prefill from an empty cache: n_b = L_b
+    w = _w("fresh", 8, 2, (1, 65, 130), n_new=1)
+    _check_small(w, q_lens=np.array([1, 65, 130]))
+
+
+def test_varlen_queries_including_none():
+    w = _w("varlen", 8, 2, (40, 16, 77, 5), n_new=1)
+    _check_small(w, q_lens=np.array([5, 0, 33, 1]), max_q=40)
+    _check_small(w, q_lens=np.array([5, 0, 33, 1]), split=64, max_q=40)
+
+
+def test_group4_many_requests():
+    lens = synth.gen.uniform_int(77, np.arange(40, dtype=np.uint64), 8, 400)
+    _check_small(_w("many", 16, 4, tuple(lens.tolist()), n_new=8), split=64)
+
+
+def test_bad_page_and_clamped_context_set_status():
+    p = pf()
+    w = _w("bad", 8, 2, (40, 90), n_new=4).set_scales_host()
+    kc, vc = oracle_fill_paged(w)
+    bt = w.block_tables.copy()
+    bt[1, 2] = w.num_pages + 5
+    out, _, status = _run(p, w, _dev(kc), _dev(vc), bt=bt)
+    assert status & p.DEVERR["BAD_PAGE"]
+    assert np.all(np.isfinite(out))
+    _, _, status = _run(p, w, _dev(kc), _dev(vc), max_ctx=64)  # request 1 holds 90 tokens
+    assert status & p.DEVERR["BAD_CONTEXT"]
+
+
+def test_bad_arguments_are_rejected():
+    import torch
+    p = pf()
+    w = _w("arg", 12, 2, (40,), n_new=4).set_scales_host()  # G = 6 does not divide 128
+    kc = torch.zeros((w.num_pages, 2, 16, 128), dtype=torch.uint8, device="cuda")
+    q = torch.zeros((4, 12, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(p.PfkvError) as e:
+        p.paged_prefill_attn(torch.empty_like(q), q, kc, kc, _dev(w.block_tables), _dev(w.context_lens),
+                             _dev(w.q_start()), 4, 40, 1.0, 1.0, 0.1)
+    assert e.value.code == -2
+    w = _w("arg2", 8, 2, (40,), n_new=4).set_scales_host()
+    q = torch.zeros((4, 8, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(p.PfkvError) as e:  # split not a multiple of 64
+        p.paged_prefill_attn(torch.empty_like(q), q, kc, kc, _dev(w.block_tables), _dev(w.context_lens),
+                             _dev(w.q_start()), 4, 40, 1.0, 1.0, 0.1, kv_split_tokens=48)
+    assert e.value.code == -1
+
+
+def test_config5_appended_tokens_full_size_sampled():
+    import torch
+    from synth import device as sdev
+    p = pf()
+    w = synth.config(5)
+    st = sdev.setup_paged(w, append_fp8_fn(p, w))
+    p.kv_append_fp8(st.k_new, st.v_new, st.k_cache, st.v_cache, st.step_slots, w.k_scale, w.v_scale)
+    qbits = w.q_new_bits()
+    q = _dev_bits(qbits)
+    out = torch.empty_like(q)
+    lse = torch.empty((q.shape[0], w.Hq), dtype=torch.float32, device="cuda")
+    ws = p.paged_prefill_attn(out, q, st.k_cache, st.v_cache, st.block_tables, st.context_lens,
+                              _dev(w.q_start()), w.n_new, int(w.context_lens.max()), w.k_scale, w.v_scale,
+                              w.softmax_scale, kv_split_tokens=w.kv_split_tokens, lse_out=lse)
+    torch.cuda.synchronize()
+    assert p.workspace_status(ws) == 0
+    out, lse = to_np_bf16(out), lse.cpu().numpy()
+    qs = w.q_start()
+    gots, refs = [], []
+    heads = {}
+    for b, i, h in [(0, 0, 0), (0, 7, 5), (3, 2, 17), (3, 6, 23)]:
+        kvh = h // w.G
+        L = int(w.context_lens[b])
+        if (b, kvh) not in heads:  # a 1M-token head takes seconds to regenerate
+            heads[(b, kvh)] = oracle_one_head(w, b, kvh)
+        kc, vc, bt_row = heads[(b, kvh)]
+        if i in (0, 2):
+            assert np.array_equal(gpu_pages_of(st.k_cache, w.block_tables[b], kvh, L, w.P), kc.reshape(-1, w.D)[:L])
+            assert np.array_equal(gpu_pages_of(st.v_cache, w.block_tables[b], kvh, L, w.P), vc.reshape(-1, w.D)[:L])
+        row = qs[b] + i
+        ref, ref_lse = oracle.paged_decode_one(qbits[row, h], kc, vc, bt_row, L - w.n_new + i + 1, 0, w.P,
+                                               w.k_scale, w.v_scale, w.softmax_scale)
+        gots.append(out[row, h])
+        refs.append(ref)
+        assert abs(lse[row, h] - ref_lse) <= 2e-4 + 2e-5 * abs(ref_lse)
+    assert_within_tolerance(np.stack(gots), np.stack(refs), "config 5 appended tokens sampled")
