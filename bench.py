@@ -305,6 +305,7 @@ def other_workloads(pf, peak_gbs, peak_tf, iters=10):
         del s
         torch.cuda.empty_cache()
 
+    res["prefill"] = prefill_timing(pf, peak_gbs, peak_tf, flush, iters)
     res["scale_granularity_mha_b32_h48_l8192_p16"] = scale_granularity_timing(
         pf, lambda: synth.config(2), peak_gbs, flush, iters)
     res["scale_granularity_gqa_prefix_b64_h64kv8_p16"] = scale_granularity_timing(
@@ -391,6 +392,73 @@ def scale_granularity_timing(pf, w_factory, peak_gbs, flush, iters):
     res["token_frac_of_hbm_peak"] = round((kv_bytes + scale_bytes) / t / 1e9 / peak_gbs, 4)
     res["append_token_us"] = round(t_app * 1e6, 2)
     del st, ks, vs, out, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def prefill_timing(pf, peak_gbs, peak_tf, flush, iters):
+    """paged_prefill_attn: (a) verification-sized, config 5's 8 appended tokens
+    per request as queries (HBM-bound); (b) a chunked-prefill step, 1024 new
+    tokens per request on a 7168-token cached prefix (tensor-bound)."""
+    import torch
+    import synth
+    res = {}
+
+    def setup(w):
+        s = PagedStep(pf, w)
+        s.append()
+        q = torch.from_numpy(w.q_new_bits().view(np.int16)).to("cuda").view(torch.bfloat16)
+        return s, q, torch.from_numpy(w.q_start()).to("cuda")
+
+    def causal_flops(w):
+        n = w.n_new
+        pos = sum(int(L) - n + i + 1 for L in w.context_lens for i in range(n))
+        return 4 * w.D * w.Hq * pos
+
+    # (a) verification-sized
+    w = synth.config(5)
+    s, q, qs = setup(w)
+    out = torch.empty_like(q)
+    st = s.st
+    best = None
+    sweep = {}
+    for split in (4096, 16384, 65536):
+        ws = torch.empty(pf.paged_prefill_workspace_size(w.B, w.Hq, w.Hkv, w.n_new, int(w.context_lens.max()), split),
+                         dtype=torch.uint8, device="cuda")
+        fn = lambda: pf.paged_prefill_attn(out, q, st.k_cache, st.v_cache, st.block_tables, st.context_lens, qs,
+                                           w.n_new, int(w.context_lens.max()), w.k_scale, w.v_scale, w.softmax_scale,
+                                           kv_split_tokens=split, workspace=ws)
+        fn()
+        t = time_events(fn, iters, flush)
+        sweep[str(split)] = round(t * 1e6, 1)
+        if best is None or t < best[0]:
+            best = (t, split)
+        del ws
+    t, split = best
+    nbytes = s.bytes()["kv"] + 2 * q.numel() * 2 + s.bytes()["tables"]
+    res["verify_long_b8_h64kv8_q8"] = {
+        "prefill_us": round(t * 1e6, 2), "kv_split_tokens": split, "split_sweep_us": sweep,
+        "GBs": round(nbytes / t / 1e9, 1), "frac_of_hbm_peak": round(nbytes / t / 1e9 / peak_gbs, 4),
+        "tflops": round(causal_flops(w) / t / 1e12, 2)}
+    del s, q, out, st
+    torch.cuda.empty_cache()
+    # (b) chunked prefill
+    w = synth.PagedWorkload("chunk", B=4, Hq=64, Hkv=8, D=128, P=16, context_lens=np.full(4, 8192), n_new=1024,
+                            seed=7)
+    s, q, qs = setup(w)
+    out = torch.empty_like(q)
+    st = s.st
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    fn = lambda: pf.paged_prefill_attn(out, q, st.k_cache, st.v_cache, st.block_tables, st.context_lens, qs,
+                                       w.n_new, 8192, w.k_scale, w.v_scale, w.softmax_scale, workspace=ws)
+    fn()
+    t = time_events(fn, iters, flush)
+    fl = causal_flops(w)
+    res["chunked_prefill_b4_n1024_l8192_h64kv8"] = {
+        "prefill_us": round(t * 1e6, 2), "causal_flop": fl, "tflops": round(fl / t / 1e12, 2),
+        "frac_of_bf16_peak": round(fl / t / 1e12 / peak_tf, 4),
+        "query_tokens_per_s": round(w.B * w.n_new / t, 1)}
+    del s, q, out, st, ws
     torch.cuda.empty_cache()
     return res
 

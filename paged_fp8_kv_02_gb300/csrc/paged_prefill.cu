@@ -46,7 +46,9 @@ constexpr int kRows = 128;                    // MMA M: rows of a work unit
 constexpr int kTokN = 64;                     // KV tokens per tile
 constexpr int kBoxTok = 16;                   // tokens per TMA box
 constexpr int kBoxes = kTokN / kBoxTok;       // 4
-constexpr int kStages = 4;                    // e4m3 stage ring
+constexpr int kStages = 5;                    // e4m3 stage ring
+constexpr int kKvBufs = 3;                    // widened f16 K/V tiles in flight
+constexpr int kSBufs = 4;                     // score / P buffers in tensor memory
 constexpr int kBoxBytes = kBoxTok * kD;       // 2 KB
 constexpr int kStageBytes = 2 * kTokN * kD;   // K + V e4m3: 16 KB
 constexpr int kKvAtom = kTokN * 128;          // [64 tokens][64 f16] swizzled atom: 8 KB
@@ -60,15 +62,15 @@ constexpr int kPageBatch = 8;                 // tiles whose block-table entries
 
 constexpr int kOffQ = 0;
 constexpr int kOffKv = kOffQ + 2 * kQAtom;
-constexpr int kOffStage = kOffKv + 2 * kKvBufBytes;
+constexpr int kOffStage = kOffKv + kKvBufs * kKvBufBytes;
 constexpr int kOffBars = kOffStage + kStages * kStageBytes;
 constexpr int kSmemBytes = kOffBars + 256 + 1024;  // + 1024-byte alignment slack
 
 constexpr int kProdWarp = 0, kMmaWarp = 1, kConvWarp0 = 2, kSoftWarp0 = 6;
 constexpr int kThreads = 320;
 
-// tensor memory: S/P buffers at columns 0 and 64, O at 128..255
-constexpr uint32_t kTmemS = 0, kTmemO = 128, kTmemCols = 256;
+// tensor memory: S/P buffers at columns 0, 64, 128, 192; O at 256..383
+constexpr uint32_t kTmemS = 0, kTmemO = 64 * kSBufs, kTmemCols = 512;
 constexpr uint32_t kIdescQK = tc::idesc_f16(kRows, kTokN, false);
 constexpr uint32_t kIdescPV = tc::idesc_f16(kRows, kD, true);
 
@@ -93,7 +95,7 @@ struct PrefillArgs {
 
 struct Bars {
   uint64_t stage_full[kStages], stage_empty[kStages];
-  uint64_t kvfull[2], sfull[2], pfull[2], pvdone[2];
+  uint64_t kvfull[kKvBufs], sfull[kSBufs], pfull[kSBufs], pvdone[kSBufs];
   uint64_t qready;
   uint32_t tmem_base;
 };
@@ -181,10 +183,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bs.stage_full[s]), 1);
       mbar_init(smem_u32(&bs.stage_empty[s]), 4);
     }
-    for (int k = 0; k < 2; ++k) {
-      mbar_init(smem_u32(&bs.kvfull[k]), 4);
+    for (int k = 0; k < kKvBufs; ++k) mbar_init(smem_u32(&bs.kvfull[k]), 4);
+    const int live_warps = min(4, (x.rows + 31) / 32);  // softmax warps with at least one real row
+    for (int k = 0; k < kSBufs; ++k) {
       mbar_init(smem_u32(&bs.sfull[k]), 1);
-      mbar_init(smem_u32(&bs.pfull[k]), 4);
+      mbar_init(smem_u32(&bs.pfull[k]), live_warps);
       mbar_init(smem_u32(&bs.pvdone[k]), 1);
     }
     mbar_init(smem_u32(&bs.qready), 4);
@@ -255,26 +258,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       long long idle_since = clock64();
       while (pn < ntiles && !to) {
         bool issued = false;
-        if (pn < qn && mbar_test_wait(smem_u32(&bs.pfull[pn & 1]), (pn >> 1) & 1)) {
+        if (pn < qn && mbar_test_wait(smem_u32(&bs.pfull[pn % kSBufs]), (pn / kSBufs) & 1)) {
           tc::fence_after_sync();
-          const uint64_t vdesc = tc::desc_sw128(kv0 + (pn & 1) * kKvBufBytes + 2 * kKvAtom, kKvAtom, 1024);
+          const uint64_t vdesc =
+              tc::desc_sw128(kv0 + (pn % kKvBufs) * kKvBufBytes + 2 * kKvAtom, kKvAtom, 1024);
 #pragma unroll
           for (int k = 0; k < kTokN / 16; ++k)
-            tc::mma_ts(tmem + kTmemO, tmem + kTmemS + 64 * (pn & 1) + 8 * k, vdesc + (uint64_t)((2048 * k) >> 4),
-                       kIdescPV, (pn > 0 || k > 0) ? 1u : 0u);
-          tc::mma_commit(smem_u32(&bs.pvdone[pn & 1]));
+            tc::mma_ts(tmem + kTmemO, tmem + kTmemS + 64 * (pn % kSBufs) + 8 * k,
+                       vdesc + (uint64_t)((2048 * k) >> 4), kIdescPV, (pn > 0 || k > 0) ? 1u : 0u);
+          tc::mma_commit(smem_u32(&bs.pvdone[pn % kSBufs]));
           ++pn;
           issued = true;
         }
-        // S(qn) reuses the buffer of P(qn - 2): issued after PV(qn - 2)
-        if (qn < ntiles && qn - pn < 2 && mbar_test_wait(smem_u32(&bs.kvfull[qn & 1]), (qn >> 1) & 1)) {
+        // S(qn) reuses the buffer of P(qn - kSBufs): issued after PV(qn - kSBufs)
+        if (qn < ntiles && qn - pn < kSBufs &&
+            mbar_test_wait(smem_u32(&bs.kvfull[qn % kKvBufs]), (qn / kKvBufs) & 1)) {
           tc::fence_after_sync();
-          const uint64_t kdesc = tc::desc_sw128(kv0 + (qn & 1) * kKvBufBytes, 16, 1024);
+          const uint64_t kdesc = tc::desc_sw128(kv0 + (qn % kKvBufs) * kKvBufBytes, 16, 1024);
 #pragma unroll
           for (int k = 0; k < kD / 16; ++k)
-            tc::mma_ss(tmem + kTmemS + 64 * (qn & 1), qdesc + (uint64_t)(((k >> 2) * kQAtom + 32 * (k & 3)) >> 4),
+            tc::mma_ss(tmem + kTmemS + 64 * (qn % kSBufs),
+                       qdesc + (uint64_t)(((k >> 2) * kQAtom + 32 * (k & 3)) >> 4),
                        kdesc + (uint64_t)(((k >> 2) * kKvAtom + 32 * (k & 3)) >> 4), kIdescQK, k > 0 ? 1u : 0u);
-          tc::mma_commit(smem_u32(&bs.sfull[qn & 1]));
+          tc::mma_commit(smem_u32(&bs.sfull[qn % kSBufs]));
           ++qn;
           issued = true;
         }
@@ -286,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // no MMA may still be running when the tensor memory is freed
-      if (pn > 0 && !mbar_wait(smem_u32(&bs.pvdone[(pn - 1) & 1]), ((pn - 1) >> 1) & 1)) to = true;
+      if (pn > 0 && !mbar_wait(smem_u32(&bs.pvdone[(pn - 1) % kSBufs]), ((pn - 1) / kSBufs) & 1)) to = true;
     }
     __syncwarp();
   } else if (warp < kSoftWarp0) {
@@ -295,9 +301,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // chunk i % 8) -> e4m3 -> f16 units 2(c % 4), 2(c % 4) + 1 of atom c / 4.
     const int ct = threadIdx.x - kConvWarp0 * 32;
     for (int j = 0; j < ntiles && !to; ++j) {
-      const int st = j % kStages, kb = j & 1;
+      const int st = j % kStages, kb = j % kKvBufs;
       if (!warp_wait(smem_u32(&bs.stage_full[st]), (j / kStages) & 1)) to = true;
-      if (j >= 2 && !to && !warp_wait(smem_u32(&bs.pvdone[kb]), ((j - 2) >> 1) & 1)) to = true;
+      // the buffer held tile j - kKvBufs: both of its products must be done
+      if (j >= kKvBufs && !to) {
+        const int jp = j - kKvBufs;
+        if (!warp_wait(smem_u32(&bs.pvdone[jp % kSBufs]), (jp / kSBufs) & 1)) to = true;
+      }
       if (to) break;
       const int valid = min(kTokN, x.t_hi - (x.t_lo + j * kTokN));
       const uint8_t* stage = smem + kOffStage + st * kStageBytes;
@@ -356,9 +366,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lim = row_ok ? min(x.L - x.n + i + 1, x.t_end_chunk) : x.t_lo;
     const float sc = a.score_scale;
     float mref = -INFINITY, rthr = -INFINITY, l = 0.f;
-    for (int j = 0; j < ntiles && !to; ++j) {
-      const int kb = j & 1;
-      if (!warp_wait(smem_u32(&bs.sfull[kb]), (j >> 1) & 1)) {
+    // a warp whose 32 rows are all padding has nothing to do after writing its
+    // zero Q rows (their scores are 0, which read as f16 pairs are P = 0)
+    const bool warp_live = 32 * quad < x.rows;
+    for (int j = 0; j < ntiles && !to && warp_live; ++j) {
+      const int kb = j % kSBufs;
+      if (!warp_wait(smem_u32(&bs.sfull[kb]), (j / kSBufs) & 1)) {
         to = true;
         break;
       }
@@ -373,10 +386,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int tok0 = x.t_lo + j * kTokN;
       const int nvalid = lim - tok0;  // columns c < nvalid are attended
+      const bool full = nvalid >= kTokN;
       float mx = -INFINITY;
+      if (full) {
 #pragma unroll
-      for (int c = 0; c < 64; ++c)
-        if (c < nvalid) mx = fmaxf(mx, __uint_as_float(sv[c]));
+        for (int c = 0; c < 64; ++c) mx = fmaxf(mx, __uint_as_float(sv[c]));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c < nvalid) mx = fmaxf(mx, __uint_as_float(sv[c]));
+      }
       const bool grow = mx > rthr;
       if (__any_sync(0xFFFFFFFFu, grow)) {
         const float mn = grow ? fmaxf(mref, mx * sc) : mref;
@@ -384,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the accumulator holds earlier tiles only once P(j - 1) was multiplied in
         const bool rescale = __any_sync(0xFFFFFFFFu, grow && mref != -INFINITY);
         if (rescale && j > 0) {
-          if (!warp_wait(smem_u32(&bs.pvdone[(j - 1) & 1]), ((j - 1) >> 1) & 1)) {
+          if (!warp_wait(smem_u32(&bs.pvdone[(j - 1) % kSBufs]), ((j - 1) / kSBufs) & 1)) {
             to = true;
             break;
           }
@@ -405,15 +424,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         rthr = (mn + kRescaleLog2) / sc;
       }
       uint32_t pv[32];
-      float ls = 0.f;
+      float ls0 = 0.f, ls1 = 0.f;
+      if (full) {
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float p0 = 2 * c < nvalid ? fast_exp2(fmaf(__uint_as_float(sv[2 * c]), sc, -mref)) : 0.f;
-        const float p1 = 2 * c + 1 < nvalid ? fast_exp2(fmaf(__uint_as_float(sv[2 * c + 1]), sc, -mref)) : 0.f;
-        ls += p0 + p1;
-        pv[c] = pack_f16x2(p0, p1);
+        for (int c = 0; c < 32; ++c) {
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * c]), sc, -mref));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * c + 1]), sc, -mref));
+          ls0 += p0;
+          ls1 += p1;
+          pv[c] = pack_f16x2(p0, p1);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float p0 = 2 * c < nvalid ? fast_exp2(fmaf(__uint_as_float(sv[2 * c]), sc, -mref)) : 0.f;
+          const float p1 = 2 * c + 1 < nvalid ? fast_exp2(fmaf(__uint_as_float(sv[2 * c + 1]), sc, -mref)) : 0.f;
+          ls0 += p0;
+          ls1 += p1;
+          pv[c] = pack_f16x2(p0, p1);
+        }
       }
-      l += ls;
+      l += ls0 + ls1;
       tc::tmem_st32(trow + kTmemS + 64 * kb, pv);
       tc::tmem_st_wait();
       tc::fence_before_sync();
@@ -421,44 +452,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.pfull[kb]));
     }
     // ---- epilogue: O (tensor memory) -> output row or partial state
-    if (!to && ntiles > 0 && !warp_wait(smem_u32(&bs.pvdone[(ntiles - 1) & 1]), ((ntiles - 1) >> 1) & 1))
-      to = true;
-    tc::fence_after_sync();
-    float* part = direct ? nullptr : a.partials + ((int64_t)u * kRows + r) * kPartStride;
-    const float inv = l > 0.f ? a.out_scale / l : 0.f;
+    if (warp_live) {
+      if (!to && ntiles > 0 &&
+          !warp_wait(smem_u32(&bs.pvdone[(ntiles - 1) % kSBufs]), ((ntiles - 1) / kSBufs) & 1))
+        to = true;
+      tc::fence_after_sync();
+      float* part = direct ? nullptr : a.partials + ((int64_t)u * kRows + r) * kPartStride;
+      const float inv = l > 0.f ? a.out_scale / l : 0.f;
 #pragma unroll
-    for (int blk = 0; blk < 4; ++blk) {
-      uint32_t ov[32];
-      if (ntiles > 0) {
-        tc::tmem_ld32(trow + kTmemO + 32 * blk, ov);
-        tc::tmem_ld_wait();
-      } else {
+      for (int blk = 0; blk < 4; ++blk) {
+        uint32_t ov[32];
+        if (ntiles > 0) {
+          tc::tmem_ld32(trow + kTmemO + 32 * blk, ov);
+          tc::tmem_ld_wait();
+        } else {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) ov[c] = 0u;
+          for (int c = 0; c < 32; ++c) ov[c] = 0u;
+        }
+        if (!row_ok || to) continue;
+        if (direct) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            pk[c] = pack_bf16x2(__uint_as_float(ov[2 * c]) * inv, __uint_as_float(ov[2 * c + 1]) * inv);
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + head_row * kD + 32 * blk);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+        } else {
+          float4* dst = reinterpret_cast<float4*>(part + 4 + 32 * blk);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            dst[k] = make_float4(__uint_as_float(ov[4 * k]), __uint_as_float(ov[4 * k + 1]),
+                                 __uint_as_float(ov[4 * k + 2]), __uint_as_float(ov[4 * k + 3]));
+        }
       }
-      if (!row_ok || to) continue;
-      if (direct) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          pk[c] = pack_bf16x2(__uint_as_float(ov[2 * c]) * inv, __uint_as_float(ov[2 * c + 1]) * inv);
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + head_row * kD + 32 * blk);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-      } else {
-        float4* dst = reinterpret_cast<float4*>(part + 4 + 32 * blk);
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          dst[k] = make_float4(__uint_as_float(ov[4 * k]), __uint_as_float(ov[4 * k + 1]),
-                               __uint_as_float(ov[4 * k + 2]), __uint_as_float(ov[4 * k + 3]));
-      }
-    }
-    if (row_ok && !to) {
-      if (direct) {
-        if (a.lse) a.lse[head_row] = l > 0.f ? (mref + __log2f(l)) * kLn2 : -INFINITY;
-      } else {
-        part[0] = mref;
-        part[1] = l;
+      if (row_ok && !to) {
+        if (direct) {
+          if (a.lse) a.lse[head_row] = l > 0.f ? (mref + __log2f(l)) * kLn2 : -INFINITY;
+        } else {
+          part[0] = mref;
+          part[1] = l;
+        }
       }
     }
   }
