@@ -787,7 +787,36 @@ PROFILE_CASES = {
     "gqa_prefix_b64": "GQA 64/8 heads, 64 requests, lognormal contexts, 16 share a 2048-token prefix",
     "long_b2_l262144": "GQA 64/8 heads, 2 requests x 262144 tokens, page 64, 4096-token chunks",
     "mla_b16_topk2048": "MLA 128 heads x 576, 16 requests x 65536 tokens, top-k 2048, page 64",
+    "prefill_chunk_b1_n1024_l8192": "multi-query: 1 request, 1024 new tokens on a 7168-token prefix, GQA 64/8",
+    "prefill_verify_b2_l262144_q8": "multi-query: 2 requests x 262144 tokens, 8 new tokens each, GQA 64/8, "
+                                    "page 64, 16384-token chunks",
 }
+
+
+class PrefillStep:
+    """Resident cache of a workload whose last n_new tokens per request are the
+    queries of paged_prefill_attn."""
+
+    def __init__(self, pf, w, split=0):
+        import torch
+        self.pf, self.w, self.split = pf, w, split
+        self.ps = PagedStep(pf, w)
+        self.ps.append()
+        self.q = torch.from_numpy(w.q_new_bits().view(np.int16)).to("cuda").view(torch.bfloat16)
+        self.qs = torch.from_numpy(w.q_start()).to("cuda")
+        self.out = torch.empty_like(self.q)
+        self.max_ctx = int(w.context_lens.max())
+        n = pf.paged_prefill_workspace_size(w.B, w.Hq, w.Hkv, w.n_new, self.max_ctx, split)
+        self.ws = torch.empty(max(n, 256), dtype=torch.uint8, device="cuda")
+
+    def append(self):
+        self.ps.append()
+
+    def decode(self):
+        st, w = self.ps.st, self.w
+        self.pf.paged_prefill_attn(self.out, self.q, st.k_cache, st.v_cache, st.block_tables, st.context_lens,
+                                   self.qs, w.n_new, self.max_ctx, w.k_scale, w.v_scale, w.softmax_scale,
+                                   kv_split_tokens=self.split, workspace=self.ws)
 
 
 def run_profile_case(name):
@@ -805,6 +834,12 @@ def run_profile_case(name):
     elif name == "long_b2_l262144":
         s = PagedStep(pf, synth.PagedWorkload("long_b2", B=2, Hq=64, Hkv=8, D=128, P=64,
                                               context_lens=np.full(2, 262144), n_new=8, kv_split_tokens=4096))
+    elif name == "prefill_chunk_b1_n1024_l8192":
+        s = PrefillStep(pf, synth.PagedWorkload("chunk_b1", B=1, Hq=64, Hkv=8, D=128, P=16,
+                                                context_lens=np.full(1, 8192), n_new=1024, seed=7))
+    elif name == "prefill_verify_b2_l262144_q8":
+        s = PrefillStep(pf, synth.PagedWorkload("verify_b2", B=2, Hq=64, Hkv=8, D=128, P=64,
+                                                context_lens=np.full(2, 262144), n_new=8), split=16384)
     elif name == "mla_b16_topk2048":
         s = MlaStep(pf, synth.MlaWorkload("mla_b16", B=16, H=128, context_lens=np.full(16, 65536), topk_n=2048,
                                           P=64))
