@@ -20,9 +20,11 @@
 //     ahead);
 //   * four converter warps widen them to f16 in 128-byte-swizzled atoms (the
 //     K tile is the K-major B operand of S = Q.K^T, the V tile the MN-major B
-//     operand of O = P.V);
-//   * one thread issues the MMAs: S for a tile into one of two 64-column
-//     tensor-memory buffers, then O += P.V with P read from tensor memory;
+//     operand of O = P.V), four tiles in flight;
+//   * one thread issues the MMAs: S for a tile into one of four 64-column
+//     tensor-memory buffers with Q (f16) as the A operand in tensor memory,
+//     then O += P.V with P read from tensor memory; blocks of at most 64 rows
+//     use half-height (M = 64) products;
 //   * four softmax warps own one row each per lane: mask (causal and context
 //     end), lazy-reference exp2 online softmax (the reference moves only when a
 //     score exceeds it by more than 2^8; the accumulator in tensor memory is
@@ -47,21 +49,19 @@ constexpr int kTokN = 64;                     // KV tokens per tile
 constexpr int kBoxTok = 16;                   // tokens per TMA box
 constexpr int kBoxes = kTokN / kBoxTok;       // 4
 constexpr int kStages = 5;                    // e4m3 stage ring
-constexpr int kKvBufs = 3;                    // widened f16 K/V tiles in flight
+constexpr int kKvBufs = 4;                    // widened f16 K/V tiles in flight
 constexpr int kSBufs = 4;                     // score / P buffers in tensor memory
 constexpr int kBoxBytes = kBoxTok * kD;       // 2 KB
 constexpr int kStageBytes = 2 * kTokN * kD;   // K + V e4m3: 16 KB
 constexpr int kKvAtom = kTokN * 128;          // [64 tokens][64 f16] swizzled atom: 8 KB
 constexpr int kKvBufBytes = 4 * kKvAtom;      // K (2 atoms) + V (2 atoms): 32 KB
-constexpr int kQAtom = kRows * 128;           // [128 rows][64 f16]: 16 KB
 constexpr int kPartStride = 132;              // floats per row of a partial state: m, l, -, -, o[128]
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kPageBatch = 8;                 // tiles whose block-table entries one load covers
 
-constexpr int kOffQ = 0;
-constexpr int kOffKv = kOffQ + 2 * kQAtom;
+constexpr int kOffKv = 0;
 constexpr int kOffStage = kOffKv + kKvBufs * kKvBufBytes;
 constexpr int kOffBars = kOffStage + kStages * kStageBytes;
 constexpr int kSmemBytes = kOffBars + 256 + 1024;  // + 1024-byte alignment slack
@@ -69,10 +69,17 @@ constexpr int kSmemBytes = kOffBars + 256 + 1024;  // + 1024-byte alignment slac
 constexpr int kProdWarp = 0, kMmaWarp = 1, kConvWarp0 = 2, kSoftWarp0 = 6;
 constexpr int kThreads = 320;
 
-// tensor memory: S/P buffers at columns 0, 64, 128, 192; O at 256..383
-constexpr uint32_t kTmemS = 0, kTmemO = 64 * kSBufs, kTmemCols = 512;
+// tensor memory: S/P buffers at columns 0, 64, 128, 192; O at 256..383; Q (the
+// A operand of the scores, f16 pairs) at 384..447
+constexpr uint32_t kTmemS = 0, kTmemO = 64 * kSBufs, kTmemQ = kTmemO + kD, kTmemCols = 512;
+static_assert(kTmemQ + kD / 2 <= kTmemCols, "tensor memory columns");
 constexpr uint32_t kIdescQK = tc::idesc_f16(kRows, kTokN, false);
 constexpr uint32_t kIdescPV = tc::idesc_f16(kRows, kD, true);
+// Units with at most 64 rows use M = 64 products: row m of the accumulator
+// (and of an A operand in tensor memory) then sits in lane (m % 16) + 32 (m / 16),
+// i.e. the first 16 lanes of each warp's quarter (checked on the device).
+constexpr uint32_t kIdescQK64 = tc::idesc_f16(64, kTokN, false);
+constexpr uint32_t kIdescPV64 = tc::idesc_f16(64, kD, true);
 
 struct PrefillArgs {
   __nv_bfloat16* out;
@@ -177,6 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!x.active) return;  // uniform over the CTA: nothing to compute or write
   const int ntiles = x.ntiles;
   const bool direct = a.C == 1;
+  const bool m64 = x.rows <= 64;  // half-height products
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -184,7 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bs.stage_empty[s]), 4);
     }
     for (int k = 0; k < kKvBufs; ++k) mbar_init(smem_u32(&bs.kvfull[k]), 4);
-    const int live_warps = min(4, (x.rows + 31) / 32);  // softmax warps with at least one real row
+    // softmax warps with at least one real row (16 rows per warp in half-height mode)
+    const int live_warps = m64 ? min(4, (x.rows + 15) / 16) : min(4, (x.rows + 31) / 32);
     for (int k = 0; k < kSBufs; ++k) {
       mbar_init(smem_u32(&bs.sfull[k]), 1);
       mbar_init(smem_u32(&bs.pfull[k]), live_warps);
@@ -252,8 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && ntiles > 0) {
       if (!mbar_wait(smem_u32(&bs.qready), 0)) to = true;
       tc::fence_after_sync();
-      const uint64_t qdesc = tc::desc_sw128(smem_u32(smem + kOffQ), 16, 1024);
       const uint32_t kv0 = smem_u32(smem + kOffKv);
+      const uint32_t idesc_qk = m64 ? kIdescQK64 : kIdescQK, idesc_pv = m64 ? kIdescPV64 : kIdescPV;
       int qn = 0, pn = 0;
       long long idle_since = clock64();
       while (pn < ntiles && !to) {
@@ -265,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < kTokN / 16; ++k)
             tc::mma_ts(tmem + kTmemO, tmem + kTmemS + 64 * (pn % kSBufs) + 8 * k,
-                       vdesc + (uint64_t)((2048 * k) >> 4), kIdescPV, (pn > 0 || k > 0) ? 1u : 0u);
+                       vdesc + (uint64_t)((2048 * k) >> 4), idesc_pv, (pn > 0 || k > 0) ? 1u : 0u);
           tc::mma_commit(smem_u32(&bs.pvdone[pn % kSBufs]));
           ++pn;
           issued = true;
@@ -277,18 +286,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t kdesc = tc::desc_sw128(kv0 + (qn % kKvBufs) * kKvBufBytes, 16, 1024);
 #pragma unroll
           for (int k = 0; k < kD / 16; ++k)
-            tc::mma_ss(tmem + kTmemS + 64 * (qn % kSBufs),
-                       qdesc + (uint64_t)(((k >> 2) * kQAtom + 32 * (k & 3)) >> 4),
-                       kdesc + (uint64_t)(((k >> 2) * kKvAtom + 32 * (k & 3)) >> 4), kIdescQK, k > 0 ? 1u : 0u);
+            tc::mma_ts(tmem + kTmemS + 64 * (qn % kSBufs), tmem + kTmemQ + 8 * k,
+                       kdesc + (uint64_t)(((k >> 2) * kKvAtom + 32 * (k & 3)) >> 4), idesc_qk, k > 0 ? 1u : 0u);
           tc::mma_commit(smem_u32(&bs.sfull[qn % kSBufs]));
           ++qn;
           issued = true;
         }
         if (issued) {
           idle_since = clock64();
-        } else {
-          __nanosleep(20);
-          if (clock64() - idle_since > kWaitLimitCycles) to = true;
+        } else if (clock64() - idle_since > kWaitLimitCycles) {
+          to = true;
         }
       }
       // no MMA may still be running when the tensor memory is freed
@@ -338,27 +345,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // -------------------------------------------------- softmax + epilogue
     const int quad = warp & 3;
-    const int r = 32 * quad + lane;  // this thread's row (tensor-memory lane)
     const uint32_t trow = tmem + ((uint32_t)(32 * quad) << 16);
-    const bool row_ok = r < x.rows;
+    // this thread's row: its own lane (full height) or, in half-height mode,
+    // row 16 quad + lane for lanes 0-15 (the lanes such products use)
+    const int r = m64 ? 16 * quad + (lane & 15) : 32 * quad + lane;
+    const bool row_ok = (!m64 || lane < 16) && r < x.rows;
     const int i = x.i0 + r / a.G, g = r % a.G;
-    const int64_t qrow = (int64_t)a.q_start[x.b] + i;
-    const int64_t head_row = qrow * a.Hq + (int64_t)x.kvh * a.G + g;  // row of q / out
-    // Q row -> f16 -> the swizzled K-major A operand
+    const int64_t head_row = ((int64_t)a.q_start[x.b] + i) * a.Hq + (int64_t)x.kvh * a.G + g;  // row of q / out
+    // Q row -> f16 pairs -> the A operand in tensor memory (zeros for padding rows)
     {
       const uint4* qp = reinterpret_cast<const uint4*>(a.q + head_row * kD);
 #pragma unroll
-      for (int uu = 0; uu < 16; ++uu) {
-        uint4 w = make_uint4(0, 0, 0, 0);
-        if (row_ok) w = __ldg(qp + uu);
-        uint4 f;
-        f.x = pack_f16x2(bf16_lo(w.x), bf16_hi(w.x));
-        f.y = pack_f16x2(bf16_lo(w.y), bf16_hi(w.y));
-        f.z = pack_f16x2(bf16_lo(w.z), bf16_hi(w.z));
-        f.w = pack_f16x2(bf16_lo(w.w), bf16_hi(w.w));
-        *reinterpret_cast<uint4*>(smem + kOffQ + atom_off(r, uu, kQAtom)) = f;
+      for (int half = 0; half < 2; ++half) {
+        uint32_t f[32];
+#pragma unroll
+        for (int uu = 0; uu < 8; ++uu) {
+          uint4 w = make_uint4(0, 0, 0, 0);
+          if (row_ok) w = __ldg(qp + 8 * half + uu);
+          f[4 * uu] = pack_f16x2(bf16_lo(w.x), bf16_hi(w.x));
+          f[4 * uu + 1] = pack_f16x2(bf16_lo(w.y), bf16_hi(w.y));
+          f[4 * uu + 2] = pack_f16x2(bf16_lo(w.z), bf16_hi(w.z));
+          f[4 * uu + 3] = pack_f16x2(bf16_lo(w.w), bf16_hi(w.w));
+        }
+        tc::tmem_st32(trow + kTmemQ + 32 * half, f);
       }
-      fence_proxy_async_smem();
+      tc::tmem_st_wait();
+      tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.qready));
     }
@@ -368,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float mref = -INFINITY, rthr = -INFINITY, l = 0.f;
     // a warp whose 32 rows are all padding has nothing to do after writing its
     // zero Q rows (their scores are 0, which read as f16 pairs are P = 0)
-    const bool warp_live = 32 * quad < x.rows;
+    const bool warp_live = (m64 ? 16 : 32) * quad < x.rows;
     for (int j = 0; j < ntiles && !to && warp_live; ++j) {
       const int kb = j % kSBufs;
       if (!warp_wait(smem_u32(&bs.sfull[kb]), (j / kSBufs) & 1)) {
@@ -388,13 +400,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nvalid = lim - tok0;  // columns c < nvalid are attended
       const bool full = nvalid >= kTokN;
       float mx = -INFINITY;
-      if (full) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) mx = fmaxf(mx, __uint_as_float(sv[c]));
+      if (!row_ok) {
+        // padding row or unused lane: P stays 0, nothing to track
       } else {
+        // eight independent chains, then a tree: no 64-long dependency chain
+        float m8[8];
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (c < nvalid) mx = fmaxf(mx, __uint_as_float(sv[c]));
+        for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
+        if (full) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sv[c]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (c < nvalid) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sv[c]));
+        }
+        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       }
       const bool grow = mx > rthr;
       if (__any_sync(0xFFFFFFFFu, grow)) {
@@ -424,14 +445,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         rthr = (mn + kRescaleLog2) / sc;
       }
       uint32_t pv[32];
-      float ls0 = 0.f, ls1 = 0.f;
-      if (full) {
+      float ls[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+      if (!row_ok) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) pv[c] = 0u;
+      } else if (full) {
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           const float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * c]), sc, -mref));
           const float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * c + 1]), sc, -mref));
-          ls0 += p0;
-          ls1 += p1;
+          ls[c & 3] += p0;
+          ls[4 + (c & 3)] += p1;
           pv[c] = pack_f16x2(p0, p1);
         }
       } else {
@@ -439,12 +465,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 32; ++c) {
           const float p0 = 2 * c < nvalid ? fast_exp2(fmaf(__uint_as_float(sv[2 * c]), sc, -mref)) : 0.f;
           const float p1 = 2 * c + 1 < nvalid ? fast_exp2(fmaf(__uint_as_float(sv[2 * c + 1]), sc, -mref)) : 0.f;
-          ls0 += p0;
-          ls1 += p1;
+          ls[c & 3] += p0;
+          ls[4 + (c & 3)] += p1;
           pv[c] = pack_f16x2(p0, p1);
         }
       }
-      l += ls0 + ls1;
+      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       tc::tmem_st32(trow + kTmemS + 64 * kb, pv);
       tc::tmem_st_wait();
       tc::fence_before_sync();
