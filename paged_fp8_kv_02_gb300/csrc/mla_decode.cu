@@ -75,17 +75,17 @@ constexpr int kQRopeBytes = kRows * 128;         // [128 heads][64 rope columns]
 constexpr int kXCodes = kRows * kTok * 2;        // exchanged partial scores: [128][32] u16 codes
 constexpr int kXMeta = kRows * 8;                // per row: fp32 minimum, u32 step exponent
 constexpr int kXBytes = kXCodes + kXMeta;
-constexpr int kRowTab = 2048;                    // list positions resolved per pass
-constexpr int kRowTabTiles = kRowTab / kTok;
-constexpr int kBtCache = 2048;                   // block-table entries cached in shared memory
+constexpr int kChunkTiles = 8;                   // tiles per chunk of resolved rows
+constexpr int kChunkPos = kChunkTiles * kTok;    // 256 list positions
+constexpr int kRowSlots = 8;                     // chunks of resolved rows in flight
+constexpr int kRowTab = kRowSlots * kChunkPos;   // 2048 entries
 
 constexpr int kOffQRope = 0;
 constexpr int kOffC = kOffQRope + kQRopeBytes;
 constexpr int kOffStage = kOffC + kPairs * kCBufBytes;
 constexpr int kOffRecv = kOffStage + kStages * kStageBytes;
 constexpr int kOffRows = kOffRecv + kXDepth * kXBytes;
-constexpr int kOffBt = kOffRows + kRowTab * 4;
-constexpr int kOffBars = kOffBt + kBtCache * 4;
+constexpr int kOffBars = kOffRows + kRowTab * 4;
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;        // 256 columns: this CTA's output columns, fp32
@@ -98,7 +98,8 @@ constexpr int kSendWarp0 = 8;         // warps 8-11: TMEM lane quadrants 0-3
 constexpr int kProdWarp = 12;
 constexpr int kMmaWarp = 13;
 constexpr int kAckWarp = 14;
-constexpr int kThreads = 15 * 32;
+constexpr int kResWarp = 15;          // resolves list positions to cache rows ahead of the producer
+constexpr int kThreads = 16 * 32;
 
 constexpr uint32_t kIdescQK = tc::idesc_f16(kRows, 2 * kTok, false);
 constexpr uint32_t kIdescPV = tc::idesc_f16(kRows, kLatCols, true);
@@ -131,6 +132,7 @@ struct __align__(8) Bars {
   uint64_t xfull[kXDepth];   // the peer's partial scores of a tile have landed
   uint64_t xack[kXDepth];    // the peer has read a tile this CTA sent
   uint64_t rdone[kXDepth];   // this CTA's softmax warps have read a received tile
+  uint64_t rows_full[kRowSlots], rows_empty[kRowSlots];  // a chunk of resolved rows written / issued
   uint32_t stage_mask[kStages], cmask[kBufs];  // bit i: token row i of the tile takes part
   uint32_t tmem_base;
 };
@@ -244,6 +246,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bs.sent[i]), 4);
     }
     mbar_init(smem_u32(&bs.qready), 4);
+    for (int i = 0; i < kRowSlots; ++i) {
+      mbar_init(smem_u32(&bs.rows_full[i]), 1);
+      mbar_init(smem_u32(&bs.rows_empty[i]), 1);
+    }
     for (int i = 0; i < kXDepth; ++i) {
       mbar_init(smem_u32(&bs.xfull[i]), 1);
       mbar_init(smem_u32(&bs.xack[i]), 1);
@@ -263,68 +269,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (warp == kProdWarp) {
     // ------------------------------------------------------------ producer
-    const int64_t tbase = (int64_t)b * a.topk_n;
-    const int32_t* bt = a.block_tables + (int64_t)b * a.max_pages;
-    int32_t* rowtab = reinterpret_cast<int32_t*>(smem + kOffRows);
-    int32_t* bt_s = reinterpret_cast<int32_t*>(smem + kOffBt);
+    // Rows come from the resolver warp in chunks of kChunkTiles tiles.
+    const int32_t* rowtab = reinterpret_cast<const int32_t*>(smem + kOffRows);
     const CUtensorMap* tm = rank ? &tm1 : &tm0;
     const int span = rank ? kSpan1 : kSpan0;
     const int x0 = rank ? kLatCols / 2 : 0;  // first u16 column of this CTA's span
-    const int npages = (L + a.P - 1) / a.P;
-    const int ncached = npages < kBtCache ? npages : kBtCache;
     for (int j = 0; j < ntiles; ++j) {
-      if (j % kRowTabTiles == 0) {
-        // Resolve list positions 32 j .. 32 j + 2047: top-k entry -> page ->
-        // cache row (-1: padding, past the list, or rejected).  Each lane
-        // keeps 32 loads in flight; the block table is cached on first use.
-#pragma unroll 1
-        for (int half = 0; half < kRowTab / 1024; ++half) {
-          const int p0 = j * kTok + 1024 * half + lane;
-          int tok[32];
-#pragma unroll
-          for (int m = 0; m < 32; ++m) {
-            const int p = p0 + 32 * m;
-            tok[m] = p < n ? (a.topk ? a.topk[tbase + p] : p) : -1;
-          }
-          if (j == 0 && half == 0) {
-#pragma unroll 1
-            for (int i0 = 0; i0 < ncached; i0 += 32 * 16) {
-              int v[16];
-#pragma unroll
-              for (int m = 0; m < 16; ++m) {
-                const int i = i0 + lane + 32 * m;
-                v[m] = i < ncached ? bt[i] : 0;
-              }
-#pragma unroll
-              for (int m = 0; m < 16; ++m) {
-                const int i = i0 + lane + 32 * m;
-                if (i < ncached) bt_s[i] = v[m];
-              }
-            }
-            __syncwarp();
-          }
-#pragma unroll
-          for (int m = 0; m < 32; ++m) {
-            int32_t row = -1;
-            const int tk = tok[m];
-            if (tk >= L) {
-              if (a.topk) atomicOr(a.status, kErrBadTopk);
-            } else if (tk >= 0) {
-              const int pi = a.p_shift >= 0 ? tk >> a.p_shift : tk / a.P;
-              const int pg = pi < kBtCache ? bt_s[pi] : bt[pi];
-              if (pg < 0 || (int64_t)pg >= a.num_pages)
-                atomicOr(a.status, kErrBadPage);
-              else
-                row = pg * a.P + (tk - pi * a.P);
-            }
-            rowtab[1024 * half + lane + 32 * m] = row;
-          }
-        }
-        __syncwarp();
-      }
+      const int chunk = j / kChunkTiles, slot = chunk % kRowSlots;
+      if (j % kChunkTiles == 0 && !to)
+        to = !__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bs.rows_full[slot]), (chunk / kRowSlots) & 1));
+      if (to) break;
       const int st = j % kStages;
       if (j >= kStages && !to) to = !mbar_wait(smem_u32(&bs.stage_empty[st]), ((j / kStages) - 1) & 1);
-      const int32_t* rt = rowtab + kTok * (j % kRowTabTiles);
+      const int32_t* rt = rowtab + slot * kChunkPos + kTok * (j % kChunkTiles);
       const uint32_t mask = __ballot_sync(0xFFFFFFFFu, rt[lane] >= 0);
       const uint32_t full = smem_u32(&bs.stage_full[st]);
       if (lane == 0) {
@@ -338,7 +295,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int y2 = rt[r + 2] >= 0 ? rt[r + 2] : 0, y3 = rt[r + 3] >= 0 ? rt[r + 3] : 0;
         tma_gather4(smem_u32(smem + kOffStage + st * kStageBytes + r * span), tm, x0, y0, y1, y2, y3, full);
       }
-      __syncwarp();  // the row table may be rewritten after this tile
+      __syncwarp();
+      // the chunk's rows have all been issued: the resolver may reuse its slot
+      if (lane == 0 && (j % kChunkTiles == kChunkTiles - 1 || j == ntiles - 1))
+        tc::mbar_arrive_local(smem_u32(&bs.rows_empty[slot]));
     }
     // no copy may still be landing when the CTA retires
     for (int j = ntiles > kStages ? ntiles - kStages : 0; j < ntiles; ++j)
@@ -464,6 +424,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc::mbar_arrive_local(smem_u32(&bs.stage_empty[st]));
         tc::mbar_arrive_local(smem_u32(&bs.cfull[cb]));
       }
+    }
+  } else if (warp == kResWarp) {
+    // ------------------------------------------------------------ resolver
+    // List position p -> top-k entry -> page -> cache row (-1: padding, past
+    // the list, or rejected), a chunk of 256 positions at a time (eight per
+    // lane, loads in flight together), up to kRowSlots chunks ahead of the
+    // producer.
+    const int64_t tbase = (int64_t)b * a.topk_n;
+    const int32_t* bt = a.block_tables + (int64_t)b * a.max_pages;
+    int32_t* rowtab = reinterpret_cast<int32_t*>(smem + kOffRows);
+    const int nchunks = (ntiles + kChunkTiles - 1) / kChunkTiles;
+    for (int c = 0; c < nchunks && !to; ++c) {
+      const int slot = c % kRowSlots;
+      if (c >= kRowSlots &&
+          !__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bs.rows_empty[slot]), ((c / kRowSlots) - 1) & 1))) {
+        to = true;
+        break;
+      }
+      int tok[8], pg[8];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int p = c * kChunkPos + lane + 32 * m;
+        tok[m] = p < n ? (a.topk ? a.topk[tbase + p] : p) : -1;
+      }
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int tk = tok[m];
+        pg[m] = (tk >= 0 && tk < L) ? bt[a.p_shift >= 0 ? tk >> a.p_shift : tk / a.P] : -1;
+      }
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        int32_t row = -1;
+        const int tk = tok[m];
+        if (tk >= L) {
+          if (a.topk) atomicOr(a.status, kErrBadTopk);
+        } else if (tk >= 0) {
+          const int pi = a.p_shift >= 0 ? tk >> a.p_shift : tk / a.P;
+          if (pg[m] < 0 || (int64_t)pg[m] >= a.num_pages)
+            atomicOr(a.status, kErrBadPage);
+          else
+            row = pg[m] * a.P + (tk - pi * a.P);
+        }
+        rowtab[slot * kChunkPos + lane + 32 * m] = row;
+      }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.rows_full[slot]));
     }
   } else if (warp >= kSendWarp0) {
     // --------------------------------------------------------- sender warps
