@@ -21,10 +21,10 @@
 //   * four converter warps widen them to f16 in 128-byte-swizzled atoms (the
 //     K tile is the K-major B operand of S = Q.K^T, the V tile the MN-major B
 //     operand of O = P.V), four tiles in flight;
-//   * one thread issues the MMAs: S for a tile into one of four 64-column
-//     tensor-memory buffers with Q (f16) as the A operand in tensor memory,
-//     then O += P.V with P read from tensor memory; blocks of at most 64 rows
-//     use half-height (M = 64) products;
+//   * one thread issues S for a tile into one of four 64-column
+//     tensor-memory buffers, with Q (f16) as the A operand in tensor memory,
+//     and a thread of another warp issues O += P.V with P read from tensor
+//     memory; blocks of at most 64 rows use half-height (M = 64) products;
 //   * four softmax warps own one row each per lane: mask (causal and context
 //     end), lazy-reference exp2 online softmax (the reference moves only when a
 //     score exceeds it by more than 2^8; the accumulator in tensor memory is
@@ -66,8 +66,8 @@ constexpr int kOffStage = kOffKv + kKvBufs * kKvBufBytes;
 constexpr int kOffBars = kOffStage + kStages * kStageBytes;
 constexpr int kSmemBytes = kOffBars + 256 + 1024;  // + 1024-byte alignment slack
 
-constexpr int kProdWarp = 0, kMmaWarp = 1, kConvWarp0 = 2, kSoftWarp0 = 6;
-constexpr int kThreads = 320;
+constexpr int kProdWarp = 0, kMmaWarp = 1, kConvWarp0 = 2, kSoftWarp0 = 6, kPvWarp = 10;
+constexpr int kThreads = 352;
 
 // tensor memory: S/P buffers at columns 0, 64, 128, 192; O at 256..383; Q (the
 // A operand of the scores, f16 pairs) at 384..447
@@ -257,46 +257,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = ntiles > kStages ? ntiles - kStages : 0; j < ntiles; ++j)
       if (!mbar_wait(smem_u32(&bs.stage_full[j % kStages]), (j / kStages) & 1)) to = true;
   } else if (warp == kMmaWarp) {
-    // ---------------------------------------------------------- MMA issuer
+    // ------------------------------------------------- score MMA issuer
+    // One thread issues S = Q.K^T per tile; the products O += P.V come from
+    // another warp, so that the two streams of (slow to issue) small MMAs
+    // overlap.  S(qn) reuses the buffer of P(qn - kSBufs): it waits until
+    // that product has completed.
     if (lane == 0 && ntiles > 0) {
       if (!mbar_wait(smem_u32(&bs.qready), 0)) to = true;
-      tc::fence_after_sync();
       const uint32_t kv0 = smem_u32(smem + kOffKv);
-      const uint32_t idesc_qk = m64 ? kIdescQK64 : kIdescQK, idesc_pv = m64 ? kIdescPV64 : kIdescPV;
-      int qn = 0, pn = 0;
-      long long idle_since = clock64();
-      while (pn < ntiles && !to) {
-        bool issued = false;
-        if (pn < qn && mbar_test_wait(smem_u32(&bs.pfull[pn % kSBufs]), (pn / kSBufs) & 1)) {
-          tc::fence_after_sync();
-          const uint64_t vdesc =
-              tc::desc_sw128(kv0 + (pn % kKvBufs) * kKvBufBytes + 2 * kKvAtom, kKvAtom, 1024);
-#pragma unroll
-          for (int k = 0; k < kTokN / 16; ++k)
-            tc::mma_ts(tmem + kTmemO, tmem + kTmemS + 64 * (pn % kSBufs) + 8 * k,
-                       vdesc + (uint64_t)((2048 * k) >> 4), idesc_pv, (pn > 0 || k > 0) ? 1u : 0u);
-          tc::mma_commit(smem_u32(&bs.pvdone[pn % kSBufs]));
-          ++pn;
-          issued = true;
+      const uint32_t idesc_qk = m64 ? kIdescQK64 : kIdescQK;
+      for (int qn = 0; qn < ntiles && !to; ++qn) {
+        if (!mbar_wait(smem_u32(&bs.kvfull[qn % kKvBufs]), (qn / kKvBufs) & 1)) to = true;
+        if (qn >= kSBufs && !to) {
+          const int jp = qn - kSBufs;
+          if (!mbar_wait(smem_u32(&bs.pvdone[jp % kSBufs]), (jp / kSBufs) & 1)) to = true;
         }
-        // S(qn) reuses the buffer of P(qn - kSBufs): issued after PV(qn - kSBufs)
-        if (qn < ntiles && qn - pn < kSBufs &&
-            mbar_test_wait(smem_u32(&bs.kvfull[qn % kKvBufs]), (qn / kKvBufs) & 1)) {
-          tc::fence_after_sync();
-          const uint64_t kdesc = tc::desc_sw128(kv0 + (qn % kKvBufs) * kKvBufBytes, 16, 1024);
+        if (to) break;
+        tc::fence_after_sync();
+        const uint64_t kdesc = tc::desc_sw128(kv0 + (qn % kKvBufs) * kKvBufBytes, 16, 1024);
 #pragma unroll
-          for (int k = 0; k < kD / 16; ++k)
-            tc::mma_ts(tmem + kTmemS + 64 * (qn % kSBufs), tmem + kTmemQ + 8 * k,
-                       kdesc + (uint64_t)(((k >> 2) * kKvAtom + 32 * (k & 3)) >> 4), idesc_qk, k > 0 ? 1u : 0u);
-          tc::mma_commit(smem_u32(&bs.sfull[qn % kSBufs]));
-          ++qn;
-          issued = true;
-        }
-        if (issued) {
-          idle_since = clock64();
-        } else if (clock64() - idle_since > kWaitLimitCycles) {
+        for (int k = 0; k < kD / 16; ++k)
+          tc::mma_ts(tmem + kTmemS + 64 * (qn % kSBufs), tmem + kTmemQ + 8 * k,
+                     kdesc + (uint64_t)(((k >> 2) * kKvAtom + 32 * (k & 3)) >> 4), idesc_qk, k > 0 ? 1u : 0u);
+        tc::mma_commit(smem_u32(&bs.sfull[qn % kSBufs]));
+      }
+    }
+    __syncwarp();
+  } else if (warp == kPvWarp) {
+    // ---------------------------------------------------- P.V MMA issuer
+    if (lane == 0 && ntiles > 0) {
+      const uint32_t kv0 = smem_u32(smem + kOffKv);
+      const uint32_t idesc_pv = m64 ? kIdescPV64 : kIdescPV;
+      int pn = 0;
+      for (; pn < ntiles && !to; ++pn) {
+        if (!mbar_wait(smem_u32(&bs.pfull[pn % kSBufs]), (pn / kSBufs) & 1)) {
           to = true;
+          break;
         }
+        tc::fence_after_sync();
+        const uint64_t vdesc = tc::desc_sw128(kv0 + (pn % kKvBufs) * kKvBufBytes + 2 * kKvAtom, kKvAtom, 1024);
+#pragma unroll
+        for (int k = 0; k < kTokN / 16; ++k)
+          tc::mma_ts(tmem + kTmemO, tmem + kTmemS + 64 * (pn % kSBufs) + 8 * k, vdesc + (uint64_t)((2048 * k) >> 4),
+                     idesc_pv, (pn > 0 || k > 0) ? 1u : 0u);
+        tc::mma_commit(smem_u32(&bs.pvdone[pn % kSBufs]));
       }
       // no MMA may still be running when the tensor memory is freed
       if (pn > 0 && !mbar_wait(smem_u32(&bs.pvdone[(pn - 1) % kSBufs]), ((pn - 1) / kSBufs) & 1)) to = true;
