@@ -737,13 +737,10 @@ int pfkv_mla_decode_attn(void* out, const void* q, const void* ckv_cache, const 
   a.num_pages = num_pages;
   a.score_scale = ckv_scale * softmax_scale * kLog2e;
   a.out_scale = ckv_scale;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes) != cudaSuccess)
-      return check_cuda("mla_decode set smem attribute");
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  const int smem_rc = set_max_dynamic_smem(reinterpret_cast<const void*>(mla_decode_kernel), (int)kSmemBytes, smem_set,
+                                       "mla_decode set smem attribute");
+  if (smem_rc != PFKV_OK) return smem_rc;
   if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), s) != cudaSuccess)
     return check_cuda("mla_decode status reset");
   // The cache as [rows][288 u16]: CTA 0 reads u16 columns 0..127, CTA 1 128..287.

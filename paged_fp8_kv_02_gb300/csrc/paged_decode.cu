@@ -908,13 +908,10 @@ int launch_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const DecodeAr
                   cudaStream_t stream) {
   using Geo = Geometry<kBf16, kScl>;
   auto kern = paged_decode_kernel<kBf16, NT, kScl>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Geo::kSmemBytes) !=
-        cudaSuccess)
-      return check_cuda("paged_decode set smem attribute");
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  const int rc = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), Geo::kSmemBytes, smem_set,
+                                      "paged_decode set smem attribute");
+  if (rc != PFKV_OK) return rc;
   // persistent grid: every SM filled with resident CTAs (cached per device)
   static int grid_of_device[64] = {};
   int dev = 0;

@@ -676,13 +676,10 @@ int pfkv_paged_prefill_attn(void* out, const void* q, const void* k_cache, const
                            box, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != PFKV_OK) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-        cudaSuccess)
-      return check_cuda("paged_prefill set smem attribute");
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  rc = set_max_dynamic_smem(reinterpret_cast<const void*>(prefill_kernel), kSmemBytes, smem_set,
+                            "paged_prefill set smem attribute");
+  if (rc != PFKV_OK) return rc;
   if (cudaMemsetAsync(a.status, 0, sizeof(int32_t), s) != cudaSuccess) return check_cuda("paged_prefill status");
   prefill_kernel<<<(unsigned)units, kThreads, kSmemBytes, s>>>(tmK, tmV, a);
   if (a.C > 1) {

@@ -28,6 +28,17 @@ int check_cuda(const char* what) {
   return PFKV_OK;
 }
 
+int set_max_dynamic_smem(const void* func, int bytes, std::atomic<uint64_t>& done, const char* what) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return check_cuda(what);
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return PFKV_OK;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return check_cuda(what);
+  if (bit) done.fetch_or(bit, std::memory_order_release);
+  return PFKV_OK;
+}
+
 int device_sm_count() {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;

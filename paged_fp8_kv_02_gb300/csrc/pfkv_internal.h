@@ -6,6 +6,8 @@
 #include <stdint.h>
 #include <stdio.h>
 
+#include <atomic>
+
 #include "pfkv.h"
 
 namespace pfkv {
@@ -21,6 +23,11 @@ inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintp
 
 // Number of SMs of the current device (queried each call; cheap).
 int device_sm_count();
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per device (the attribute belongs to each device's context);
+// `done` is the call site's mask of devices (0-63) already set.
+int set_max_dynamic_smem(const void* func, int bytes, std::atomic<uint64_t>& done, const char* what);
 
 // Encodes a tiled TMA descriptor through the driver entry point obtained from
 // the runtime (no link-time dependency on libcuda).
