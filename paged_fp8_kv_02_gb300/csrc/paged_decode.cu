@@ -769,6 +769,56 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeArgs a
   const int64_t ts = a.tile_start[b] + (int64_t)kvh * ntiles;
   const int64_t u0 = a.unit_start[b] + (int64_t)kvh * nchunks;
   if (nchunks == 1 && owner_of(ts, W, N) == owner_of(ts + ntiles - 1, W, N)) return;  // direct
+  if (nchunks == 1) {
+    // One unit (no explicit split): its segments are the consecutive warps
+    // first .. last (one warp per tile when there are fewer tiles than
+    // warps).  Warp k folds head g_lo + k alone (with one head per CTA, warp
+    // 0 does), four segments' loads in flight at a time, and writes it.
+    const int e = g_lo + (kMergeHeads == 1 ? 0 : warp);
+    if ((kMergeHeads == 1 && warp != 0) || e >= g_hi) return;
+    const int64_t first = owner_of(ts, W, N);
+    const int64_t nseg = W >= N ? owner_of(ts + ntiles - 1, W, N) - first + 1 : ntiles;
+    float M = -INFINITY, den = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t k0 = 0; k0 < nseg; k0 += 4) {
+      float mk[4], lk[4];
+      float4 ok[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int64_t k = k0 + q;
+        mk[q] = -INFINITY;
+        lk[q] = 0.f;
+        ok[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (k < nseg) {
+          const int64_t slot = (W >= N ? first + k : owner_of(ts + k, W, N)) + u0;
+          if (slot < a.capacity) {
+            const float* p = a.partials + (slot * a.G + e) * kPartialStride;
+            mk[q] = p[0];
+            lk[q] = p[1];
+            ok[q] = reinterpret_cast<const float4*>(p + 4)[lane];
+          }
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (mk[q] == -INFINITY) continue;
+        const float Mn = fmaxf(M, mk[q]);
+        const float al = fast_exp2(M - Mn), wt = fast_exp2(mk[q] - Mn);
+        den = den * al + wt * lk[q];
+        acc.x = acc.x * al + wt * ok[q].x;
+        acc.y = acc.y * al + wt * ok[q].y;
+        acc.z = acc.z * al + wt * ok[q].z;
+        acc.w = acc.w * al + wt * ok[q].w;
+        M = Mn;
+      }
+    }
+    const int64_t head = head0 + e;
+    const float inv = den > 0.f ? a.out_scale / den : 0.f;
+    reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.out) + head * kD)[lane] =
+        make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+    if (a.lse && lane == 0) a.lse[head] = den > 0.f ? (M + __log2f(den)) * kLn2 : -INFINITY;
+    return;
+  }
 
   {
     const int e0 = g_lo;
