@@ -32,7 +32,9 @@
 //     epilogue.
 // Long contexts are cut into chunks of kv_split_tokens; chunks write fp32
 // partial states (m, l, o) and a merge kernel combines them by the log-sum-exp
-// rule (kLLM article, §5.2.2).
+// rule (kLLM article, §5.2.2).  When a (request, KV head) has several row
+// blocks (a chunked-prefill step), prefill2_kernel takes two blocks per CTA
+// so that each widened tile feeds both and two softmax groups overlap.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -536,6 +538,423 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ------------------------------------------------ two row blocks per CTA
+// For several row blocks per (request, KV head) -- a chunked-prefill step --
+// a CTA takes two neighbouring blocks A and B over the same KV chunk: every
+// widened K/V tile feeds the products of both blocks, and two groups of four
+// softmax warps (each with its own rows, O accumulator and score buffers) run
+// side by side, so the softmax of one block overlaps the other's.
+//   tensor memory: block X in columns 256 X .. 256 X + 255: two 64-column
+//   score / P buffers, then O (128 columns); Q of both blocks in shared memory
+//   (the A operand of the score products).
+//   warps: 0 producer, 1 score MMAs, 2-5 widening, 6-9 softmax of block A,
+//   10-13 softmax of block B, 14 P.V MMAs.
+constexpr int k2KvBufs = 3;
+constexpr int k2Stages = 3;
+constexpr int k2SBufs = 2;
+constexpr int k2QAtom = kRows * 128;  // [128 rows][64 f16] swizzled atom: 16 KB
+constexpr int k2OffQ = 0;             // block X: 2 atoms at 2 X k2QAtom
+constexpr int k2OffKv = k2OffQ + 4 * k2QAtom;
+constexpr int k2OffStage = k2OffKv + k2KvBufs * kKvBufBytes;
+constexpr int k2OffBars = k2OffStage + k2Stages * kStageBytes;
+constexpr int k2SmemBytes = k2OffBars + 512 + 1024;
+constexpr int k2SoftWarp0 = 6, k2PvWarp = 14;
+constexpr int k2Threads = 15 * 32;
+static_assert(k2SmemBytes <= 232448, "shared memory over the per-CTA limit");
+
+struct Bars2 {
+  uint64_t stage_full[k2Stages], stage_empty[k2Stages];
+  uint64_t kvfull[k2KvBufs], kvfree[k2KvBufs];
+  uint64_t sfull[2][k2SBufs], pfull[2][k2SBufs], pvdone[2][k2SBufs];
+  uint64_t qready;
+  uint32_t tmem_base;
+};
+static_assert(sizeof(Bars2) <= 512, "barrier block");
+
+__global__ void __launch_bounds__(k2Threads, 1)
+    prefill2_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const PrefillArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* const smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  Bars2& bs = *reinterpret_cast<Bars2*>(smem + k2OffBars);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // CTA -> (request, KV head, chunk, block pair); the two blocks' units in the
+  // one-block numbering (partial states and the merge use it)
+  const int QB2 = (a.QB + 1) / 2;
+  const int64_t u2 = blockIdx.x;
+  const int qp = (int)(u2 % QB2);
+  const int64_t bkc = u2 / QB2;  // (b * Hkv + kvh) * C + c
+  const int64_t uA = bkc * a.QB + 2 * qp;
+  const bool hasB = 2 * qp + 1 < a.QB;
+  const Unit xa = unit_of(a, uA, threadIdx.x == 0 && (bkc % ((int64_t)a.C * a.Hkv)) == 0 && qp == 0);
+  if (!xa.active) return;  // uniform over the CTA
+  Unit xb = xa;
+  if (hasB) xb = unit_of(a, uA + 1, false);
+  const bool bact = hasB && xb.active;
+  const int ntiles = bact ? max(xa.ntiles, xb.ntiles) : xa.ntiles;
+  const int t_hi = bact ? max(xa.t_hi, xb.t_hi) : xa.t_hi;  // tokens the pair reads
+  const bool direct = a.C == 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < k2Stages; ++s) {
+      mbar_init(smem_u32(&bs.stage_full[s]), 1);
+      mbar_init(smem_u32(&bs.stage_empty[s]), 4);
+    }
+    for (int k = 0; k < k2KvBufs; ++k) {
+      mbar_init(smem_u32(&bs.kvfull[k]), 4);
+      mbar_init(smem_u32(&bs.kvfree[k]), 1);
+    }
+    for (int X = 0; X < 2; ++X) {
+      const int rows = X == 0 ? xa.rows : (bact ? xb.rows : 0);
+      const int live = max(1, min(4, (rows + 31) / 32));
+      for (int k = 0; k < k2SBufs; ++k) {
+        mbar_init(smem_u32(&bs.sfull[X][k]), 1);
+        mbar_init(smem_u32(&bs.pfull[X][k]), live);
+        mbar_init(smem_u32(&bs.pvdone[X][k]), 1);
+      }
+    }
+    mbar_init(smem_u32(&bs.qready), 8);
+    fence_mbar_init();
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  if (warp == kMmaWarp) {
+    tc::tmem_alloc(smem_u32(&bs.tmem_base), kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = bs.tmem_base;
+  bool to = false;  // a bounded wait gave up
+  const int nblk = bact ? 2 : 1;
+
+  if (warp == kProdWarp) {
+    // ------------------------------------------------------------ producer
+    const int32_t* bt = a.block_tables + (int64_t)xa.b * a.max_pages;
+    auto load_batch = [&](int j0) {
+      const int j = j0 + lane / kBoxes;
+      const int tb = xa.t_lo + j * kTokN + (lane % kBoxes) * kBoxTok;
+      return (j < ntiles && tb < t_hi) ? __ldg(bt + tb / a.P) : 0;
+    };
+    int cur = load_batch(0), nxt = load_batch(kPageBatch);
+    for (int j = 0; j < ntiles && !to; ++j) {
+      if (j > 0 && j % kPageBatch == 0) {
+        cur = nxt;
+        nxt = load_batch(j + kPageBatch);
+      }
+      const int st = j % k2Stages;
+      if (j >= k2Stages && !warp_wait(smem_u32(&bs.stage_empty[st]), ((j / k2Stages) - 1) & 1)) {
+        to = true;
+        break;
+      }
+      const int tok0 = xa.t_lo + j * kTokN;
+      const int nbox = min(kBoxes, (t_hi - tok0 + kBoxTok - 1) / kBoxTok);
+      const uint32_t bar = smem_u32(&bs.stage_full[st]);
+      if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(2 * nbox * kBoxBytes));
+      __syncwarp();
+      int page = __shfl_sync(0xFFFFFFFFu, cur, (j % kPageBatch) * kBoxes + (lane & 3));
+      if (lane < nbox) {
+        const int tb = tok0 + lane * kBoxTok;
+        if (page < 0 || (int64_t)page >= a.num_pages) {
+          atomicOr(a.status, kErrBadPage);
+          page = -1;  // the box lands outside the tensor and reads zeros
+        }
+        const int row = (page * a.Hkv + xa.kvh) * a.P + tb % a.P;
+        const uint32_t dst = smem_u32(smem + k2OffStage + st * kStageBytes) + lane * kBoxBytes;
+        tma_load_2d(dst, &tmK, 0, row, bar);
+        tma_load_2d(dst + kTokN * kD, &tmV, 0, row, bar);
+      }
+    }
+    for (int j = ntiles > k2Stages ? ntiles - k2Stages : 0; j < ntiles; ++j)
+      if (!mbar_wait(smem_u32(&bs.stage_full[j % k2Stages]), (j / k2Stages) & 1)) to = true;
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------- score MMA issuer
+    // S_X(j) = Q_X . K(j)^T for both blocks once the tile is widened and the
+    // block's score buffer is free (P.V_X(j - 2) has completed).
+    if (lane == 0 && ntiles > 0) {
+      if (!mbar_wait(smem_u32(&bs.qready), 0)) to = true;
+      const uint32_t kv0 = smem_u32(smem + k2OffKv);
+      for (int j = 0; j < ntiles && !to; ++j) {
+        if (!mbar_wait(smem_u32(&bs.kvfull[j % k2KvBufs]), (j / k2KvBufs) & 1)) {
+          to = true;
+          break;
+        }
+        const uint64_t kdesc = tc::desc_sw128(kv0 + (j % k2KvBufs) * kKvBufBytes, 16, 1024);
+        for (int X = 0; X < nblk && !to; ++X) {
+          if (j >= k2SBufs &&
+              !mbar_wait(smem_u32(&bs.pvdone[X][(j - k2SBufs) % k2SBufs]), ((j - k2SBufs) / k2SBufs) & 1)) {
+            to = true;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint64_t qdesc = tc::desc_sw128(smem_u32(smem + k2OffQ + 2 * X * k2QAtom), 16, 1024);
+#pragma unroll
+          for (int k = 0; k < kD / 16; ++k)
+            tc::mma_ss(tmem + 256 * X + 64 * (j % k2SBufs), qdesc + (uint64_t)(((k >> 2) * k2QAtom + 32 * (k & 3)) >> 4),
+                       kdesc + (uint64_t)(((k >> 2) * kKvAtom + 32 * (k & 3)) >> 4), kIdescQK, k > 0 ? 1u : 0u);
+          tc::mma_commit(smem_u32(&bs.sfull[X][j % k2SBufs]));
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == k2PvWarp) {
+    // ---------------------------------------------------- P.V MMA issuer
+    if (lane == 0 && ntiles > 0) {
+      const uint32_t kv0 = smem_u32(smem + k2OffKv);
+      int j = 0;
+      for (; j < ntiles && !to; ++j) {
+        const uint64_t vdesc = tc::desc_sw128(kv0 + (j % k2KvBufs) * kKvBufBytes + 2 * kKvAtom, kKvAtom, 1024);
+        for (int X = 0; X < nblk && !to; ++X) {
+          if (!mbar_wait(smem_u32(&bs.pfull[X][j % k2SBufs]), (j / k2SBufs) & 1)) {
+            to = true;
+            break;
+          }
+          tc::fence_after_sync();
+#pragma unroll
+          for (int k = 0; k < kTokN / 16; ++k)
+            tc::mma_ts(tmem + 256 * X + 128, tmem + 256 * X + 64 * (j % k2SBufs) + 8 * k,
+                       vdesc + (uint64_t)((2048 * k) >> 4), kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
+          tc::mma_commit(smem_u32(&bs.pvdone[X][j % k2SBufs]));
+        }
+        // both products of the tile issued: the widened tile frees once they (and its score products) complete
+        if (!to) tc::mma_commit(smem_u32(&bs.kvfree[j % k2KvBufs]));
+      }
+      // no MMA may still be running when the tensor memory is freed
+      if (j > 0)
+        for (int X = 0; X < nblk; ++X)
+          if (!mbar_wait(smem_u32(&bs.pvdone[X][(j - 1) % k2SBufs]), ((j - 1) / k2SBufs) & 1)) to = true;
+    }
+    __syncwarp();
+  } else if (warp < k2SoftWarp0) {
+    // ---------------------------------------------------------- converters
+    const int ct = threadIdx.x - kConvWarp0 * 32;
+    for (int j = 0; j < ntiles && !to; ++j) {
+      const int st = j % k2Stages, kb = j % k2KvBufs;
+      if (!warp_wait(smem_u32(&bs.stage_full[st]), (j / k2Stages) & 1)) to = true;
+      if (j >= k2KvBufs && !to && !warp_wait(smem_u32(&bs.kvfree[kb]), ((j - k2KvBufs) / k2KvBufs) & 1)) to = true;
+      if (to) break;
+      const int valid = min(kTokN, t_hi - (xa.t_lo + j * kTokN));
+      const uint8_t* stage = smem + k2OffStage + st * kStageBytes;
+      uint8_t* kv = smem + k2OffKv + kb * kKvBufBytes;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int i = ct + 128 * m;
+        const int which = i >> 9, rem = i & 511;
+        const int row = rem >> 3, c = rem & 7;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (row < valid) v = lds128(stage + which * (kTokN * kD) + (row >> 4) * kBoxBytes + swz(row & 15, c));
+        uint4 o0, o1;
+        e4m3x4_to_f16x2x2(v.x, o0.x, o0.y);
+        e4m3x4_to_f16x2x2(v.y, o0.z, o0.w);
+        e4m3x4_to_f16x2x2(v.z, o1.x, o1.y);
+        e4m3x4_to_f16x2x2(v.w, o1.z, o1.w);
+        const uint32_t d = which * (2 * kKvAtom) + atom_off(row, 2 * c, kKvAtom);
+        *reinterpret_cast<uint4*>(kv + d) = o0;
+        *reinterpret_cast<uint4*>(kv + (d ^ 16)) = o1;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive_local(smem_u32(&bs.stage_empty[st]));
+        tc::mbar_arrive_local(smem_u32(&bs.kvfull[kb]));
+      }
+    }
+  } else {
+    // ------------------------------------------- softmax + epilogue (block X)
+    const int X = (warp - k2SoftWarp0) >> 2;
+    const Unit& x = X == 0 ? xa : xb;
+    const int64_t ux = uA + X;
+    const int xrows = X == 0 ? xa.rows : (bact ? xb.rows : 0);
+    const int quad = warp & 3;
+    const int r = 32 * quad + lane;
+    const uint32_t trow = tmem + ((uint32_t)(32 * quad) << 16) + 256 * X;
+    const bool row_ok = r < xrows;
+    const int i = x.i0 + r / a.G, g = r % a.G;
+    const int64_t head_row = ((int64_t)a.q_start[x.b] + i) * a.Hq + (int64_t)x.kvh * a.G + g;
+    // Q row -> f16 -> the swizzled K-major A operand of this block (zeros for padding rows)
+    {
+      const uint4* qp4 = reinterpret_cast<const uint4*>(a.q + head_row * kD);
+#pragma unroll
+      for (int uu = 0; uu < 16; ++uu) {
+        uint4 w = make_uint4(0, 0, 0, 0);
+        if (row_ok) w = __ldg(qp4 + uu);
+        uint4 f;
+        f.x = pack_f16x2(bf16_lo(w.x), bf16_hi(w.x));
+        f.y = pack_f16x2(bf16_lo(w.y), bf16_hi(w.y));
+        f.z = pack_f16x2(bf16_lo(w.z), bf16_hi(w.z));
+        f.w = pack_f16x2(bf16_lo(w.w), bf16_hi(w.w));
+        *reinterpret_cast<uint4*>(smem + k2OffQ + 2 * X * k2QAtom + atom_off(r, uu, k2QAtom)) = f;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.qready));
+    }
+    const int lim = row_ok ? min(x.L - x.n + i + 1, x.t_end_chunk) : xa.t_lo;
+    const float sc = a.score_scale;
+    float mref = -INFINITY, rthr = -INFINITY, l = 0.f;
+    const bool warp_live = 32 * quad < xrows;
+    for (int j = 0; j < ntiles && !to && warp_live; ++j) {
+      const int kb = j % k2SBufs;
+      if (!warp_wait(smem_u32(&bs.sfull[X][kb]), (j / k2SBufs) & 1)) {
+        to = true;
+        break;
+      }
+      tc::fence_after_sync();
+      const int tok0 = xa.t_lo + j * kTokN;
+      const int nvalid = lim - tok0;
+      const bool full = nvalid >= kTokN;
+      // the scores are read twice, 32 columns at a time (once for the row
+      // maximum, once for P), to keep few registers live
+      float mx = -INFINITY;
+      {
+        float m8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t sv[32];
+          tc::tmem_ld32(trow + 64 * kb + 32 * h, sv);
+          tc::tmem_ld_wait();
+          if (row_ok) {
+            if (full) {
+#pragma unroll
+              for (int c = 0; c < 32; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sv[c]));
+            } else {
+#pragma unroll
+              for (int c = 0; c < 32; ++c)
+                if (32 * h + c < nvalid) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sv[c]));
+            }
+          }
+        }
+        if (row_ok)
+          mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      }
+      const bool grow = mx > rthr;
+      if (__any_sync(0xFFFFFFFFu, grow)) {
+        const float mn = grow ? fmaxf(mref, mx * sc) : mref;
+        const float al = grow ? fast_exp2(mref - mn) : 1.f;
+        const bool rescale = __any_sync(0xFFFFFFFFu, grow && mref != -INFINITY);
+        if (rescale && j > 0) {
+          if (!warp_wait(smem_u32(&bs.pvdone[X][(j - 1) % k2SBufs]), ((j - 1) / k2SBufs) & 1)) {
+            to = true;
+            break;
+          }
+          tc::fence_after_sync();
+#pragma unroll
+          for (int blk = 0; blk < 4; ++blk) {
+            uint32_t ov[32];
+            tc::tmem_ld32(trow + 128 + 32 * blk, ov);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * al);
+            tc::tmem_st32(trow + 128 + 32 * blk, ov);
+          }
+          tc::tmem_st_wait();
+        }
+        l *= al;
+        mref = mn;
+        rthr = (mn + kRescaleLog2) / sc;
+      }
+      float ls[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t sv[32];
+        tc::tmem_ld32(trow + 64 * kb + 32 * h, sv);
+        tc::tmem_ld_wait();
+        uint32_t pv[16];
+        if (!row_ok) {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) pv[c] = 0u;
+        } else if (full) {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * c]), sc, -mref));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * c + 1]), sc, -mref));
+            ls[c & 3] += p0;
+            ls[4 + (c & 3)] += p1;
+            pv[c] = pack_f16x2(p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int c0 = 32 * h + 2 * c;
+            const float p0 = c0 < nvalid ? fast_exp2(fmaf(__uint_as_float(sv[2 * c]), sc, -mref)) : 0.f;
+            const float p1 = c0 + 1 < nvalid ? fast_exp2(fmaf(__uint_as_float(sv[2 * c + 1]), sc, -mref)) : 0.f;
+            ls[c & 3] += p0;
+            ls[4 + (c & 3)] += p1;
+            pv[c] = pack_f16x2(p0, p1);
+          }
+        }
+        // P of columns 32 h .. 32 h + 31 overwrites scores 16 h .. 16 h + 15,
+        // which this half has already read (h = 0) or never needs again (h = 1)
+        tc::tmem_st16(trow + 64 * kb + 16 * h, pv);
+      }
+      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      tc::tmem_st_wait();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.pfull[X][kb]));
+    }
+    // ---- epilogue: O_X -> output rows or partial state
+    if (warp_live) {
+      if (!to && ntiles > 0 &&
+          !warp_wait(smem_u32(&bs.pvdone[X][(ntiles - 1) % k2SBufs]), ((ntiles - 1) / k2SBufs) & 1))
+        to = true;
+      tc::fence_after_sync();
+      float* part = direct ? nullptr : a.partials + (ux * kRows + r) * kPartStride;
+      const float inv = l > 0.f ? a.out_scale / l : 0.f;
+#pragma unroll
+      for (int blk = 0; blk < 4; ++blk) {
+        uint32_t ov[32];
+        if (ntiles > 0) {
+          tc::tmem_ld32(trow + 128 + 32 * blk, ov);
+          tc::tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) ov[c] = 0u;
+        }
+        if (!row_ok || to) continue;
+        if (direct) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            pk[c] = pack_bf16x2(__uint_as_float(ov[2 * c]) * inv, __uint_as_float(ov[2 * c + 1]) * inv);
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + head_row * kD + 32 * blk);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+        } else {
+          float4* dst = reinterpret_cast<float4*>(part + 4 + 32 * blk);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            dst[k] = make_float4(__uint_as_float(ov[4 * k]), __uint_as_float(ov[4 * k + 1]),
+                                 __uint_as_float(ov[4 * k + 2]), __uint_as_float(ov[4 * k + 3]));
+        }
+      }
+      if (row_ok && !to) {
+        if (direct) {
+          if (a.lse) a.lse[head_row] = l > 0.f ? (mref + __log2f(l)) * kLn2 : -INFINITY;
+        } else {
+          part[0] = mref;
+          part[1] = l;
+        }
+      }
+    }
+  }
+
+  if (to) atomicOr(a.status, kErrWaitTimeout);
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 // One warp per row of a (request, KV head, row block): folds the chunks'
 // partial states, M = max m_c, out = sum 2^(m_c - M) o_c / sum 2^(m_c - M) l_c.
 constexpr int kMergeWarps = 8;
@@ -681,7 +1100,17 @@ int pfkv_paged_prefill_attn(void* out, const void* q, const void* k_cache, const
                             "paged_prefill set smem attribute");
   if (rc != PFKV_OK) return rc;
   if (cudaMemsetAsync(a.status, 0, sizeof(int32_t), s) != cudaSuccess) return check_cuda("paged_prefill status");
-  prefill_kernel<<<(unsigned)units, kThreads, kSmemBytes, s>>>(tmK, tmV, a);
+  if (a.QB >= 2) {
+    // several row blocks per (request, KV head): two blocks per CTA
+    static std::atomic<uint64_t> smem2_set{0};
+    rc = set_max_dynamic_smem(reinterpret_cast<const void*>(prefill2_kernel), k2SmemBytes, smem2_set,
+                              "paged_prefill set smem attribute");
+    if (rc != PFKV_OK) return rc;
+    const int64_t units2 = (int64_t)batch * num_kv_heads * a.C * ((a.QB + 1) / 2);
+    prefill2_kernel<<<(unsigned)units2, k2Threads, k2SmemBytes, s>>>(tmK, tmV, a);
+  } else {
+    prefill_kernel<<<(unsigned)units, kThreads, kSmemBytes, s>>>(tmK, tmV, a);
+  }
   if (a.C > 1) {
     const int64_t mblocks = (int64_t)batch * num_kv_heads * a.QB * (kRows / kMergeWarps);
     prefill_merge_kernel<<<(unsigned)mblocks, kMergeWarps * 32, 0, s>>>(a);
