@@ -558,7 +558,7 @@ constexpr int k2OffKv = k2OffQ + 4 * k2QAtom;
 constexpr int k2OffStage = k2OffKv + k2KvBufs * kKvBufBytes;
 constexpr int k2OffBars = k2OffStage + k2Stages * kStageBytes;
 constexpr int k2SmemBytes = k2OffBars + 512 + 1024;
-constexpr int k2SoftWarp0 = 6, k2PvWarp = 14;
+constexpr int k2ProdWarp = 0, k2MmaWarp = 1, k2ConvWarp0 = 2, k2SoftWarp0 = 6, k2PvWarp = 14;
 constexpr int k2Threads = 15 * 32;
 static_assert(k2SmemBytes <= 232448, "shared memory over the per-CTA limit");
 
@@ -620,7 +620,7 @@ __global__ void __launch_bounds__(k2Threads, 1)
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
   }
-  if (warp == kMmaWarp) {
+  if (warp == k2MmaWarp) {
     tc::tmem_alloc(smem_u32(&bs.tmem_base), kTmemCols);
     tc::tmem_relinquish();
   }
@@ -631,7 +631,7 @@ __global__ void __launch_bounds__(k2Threads, 1)
   bool to = false;  // a bounded wait gave up
   const int nblk = bact ? 2 : 1;
 
-  if (warp == kProdWarp) {
+  if (warp == k2ProdWarp) {
     // ------------------------------------------------------------ producer
     const int32_t* bt = a.block_tables + (int64_t)xa.b * a.max_pages;
     auto load_batch = [&](int j0) {
@@ -670,7 +670,7 @@ __global__ void __launch_bounds__(k2Threads, 1)
     }
     for (int j = ntiles > k2Stages ? ntiles - k2Stages : 0; j < ntiles; ++j)
       if (!mbar_wait(smem_u32(&bs.stage_full[j % k2Stages]), (j / k2Stages) & 1)) to = true;
-  } else if (warp == kMmaWarp) {
+  } else if (warp == k2MmaWarp) {
     // ------------------------------------------------- score MMA issuer
     // S_X(j) = Q_X . K(j)^T for both blocks once the tile is widened and the
     // block's score buffer is free (P.V_X(j - 2) has completed).
@@ -730,7 +730,7 @@ __global__ void __launch_bounds__(k2Threads, 1)
     __syncwarp();
   } else if (warp < k2SoftWarp0) {
     // ---------------------------------------------------------- converters
-    const int ct = threadIdx.x - kConvWarp0 * 32;
+    const int ct = threadIdx.x - k2ConvWarp0 * 32;
     for (int j = 0; j < ntiles && !to; ++j) {
       const int st = j % k2Stages, kb = j % k2KvBufs;
       if (!warp_wait(smem_u32(&bs.stage_full[st]), (j / k2Stages) & 1)) to = true;
@@ -949,7 +949,7 @@ __global__ void __launch_bounds__(k2Threads, 1)
   if (to) atomicOr(a.status, kErrWaitTimeout);
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == k2MmaWarp) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
