@@ -955,6 +955,460 @@ __global__ void __launch_bounds__(k2Threads, 1)
   }
 }
 
+// ------------------------------------------ wide tiles for a few queries
+// When every row block holds at most 64 rows (a few query tokens per request:
+// speculative verification), prefillw_kernel uses 128-token tiles and
+// half-height (M = 64) products, so that one score instruction covers 128
+// tokens and each tile's fixed costs (waits, tensor-memory round trips) are
+// spread over twice as many tokens.  The softmax reads the 16 rows of each
+// warp with the 16-lane tensor-memory shape, so all 32 threads work (threads t
+// and t ^ 2 share a row, each holding the columns of one parity).  So that a
+// thread can pack its own P pairs, the contraction order of P.V swaps the
+// middle two tokens of every group of four: P column pair (4r + 2e, 4r + 2e + 1)
+// holds tokens (4r + e, 4r + e + 2), and row 4r + i of the widened V tile holds
+// token 4r + (i with its two low bits swapped).  Only two tiles fit in shared
+// memory, so each resource is released as soon as its last reader is done:
+//   * P has tensor-memory columns of its own: a score buffer is free once the
+//     softmax warps have read it, not once P.V has run;
+//   * the K and V halves of a widened tile are filled and freed separately
+//     (K after its score product, V after its P.V product).
+// tensor memory: two 128-column score buffers, O (128), Q (64), P (64).
+// shared memory: three 32 KB e4m3 stages, two 64 KB widened K/V tiles.
+constexpr int kWTok = 128;                      // tokens per tile
+constexpr int kWBoxes = kWTok / kBoxTok;        // 8 TMA boxes per tensor
+constexpr int kWStages = 3;
+constexpr int kWStageBytes = 2 * kWTok * kD;    // K + V e4m3: 32 KB
+constexpr int kWAtom = kWTok * 128;             // [128 tokens][64 f16]: 16 KB
+constexpr int kWBufBytes = 4 * kWAtom;          // K (2 atoms) + V (2 atoms): 64 KB
+constexpr int kWBufs = 2;
+constexpr int kWOffKv = 0;
+constexpr int kWOffStage = kWOffKv + kWBufs * kWBufBytes;
+constexpr int kWOffBars = kWOffStage + kWStages * kWStageBytes;
+constexpr int kWSmemBytes = kWOffBars + 512 + 1024;
+static_assert(kWSmemBytes <= 232448, "shared memory over the per-CTA limit");
+constexpr uint32_t kWTmemS = 0, kWTmemO = kWBufs * kWTok, kWTmemQ = kWTmemO + kD, kWTmemP = kWTmemQ + kD / 2;
+static_assert(kWTmemP + kWTok / 2 <= kTmemCols, "tensor memory columns");
+constexpr uint32_t kIdescQKW = tc::idesc_f16(64, kWTok, false);
+constexpr uint32_t kIdescPVW = tc::idesc_f16(64, kD, true);
+constexpr int kWConvWarps = 4;
+constexpr int kWProdWarp = 0, kWMmaWarp = 1, kWConvWarp0 = 2, kWSoftWarp0 = kWConvWarp0 + kWConvWarps,
+              kWPvWarp = kWSoftWarp0 + 4;
+constexpr int kWThreads = (kWPvWarp + 1) * 32;
+constexpr int kWChunks = kWTok * kD / 16 / (32 * kWConvWarps);  // 16-byte chunks of K (or V) per converter thread
+
+struct BarsW {
+  uint64_t stage_full[kWStages], stage_empty[kWStages];
+  uint64_t kfull[kWBufs], vfull[kWBufs];  // K / V half of a widened tile written
+  uint64_t sfull[kWBufs];                 // scores of a tile complete
+  uint64_t sread[kWBufs];                 // the softmax warps have read a score buffer
+  uint64_t pvdone[kWBufs];                // P.V of a tile complete (index: tile % 2)
+  uint64_t pfull;                         // P of the next tile written (one phase per tile)
+  uint64_t qready;
+  uint32_t tmem_base;
+};
+static_assert(sizeof(BarsW) <= 512, "barrier block");
+
+// Widens 16-byte chunk rows of K (which = 0) or V (which = 1) of a stage into
+// the tile's f16 atoms (V rows in the P.V contraction order); rows at or past
+// `valid` become zeros.  All loads are
+// issued before the first store: the compiler cannot move a load above a
+// store through another pointer into shared memory.
+__device__ __forceinline__ void widen_half(const uint8_t* stage, uint8_t* kv, int which, int ct, int valid) {
+  uint4 v[kWChunks];
+#pragma unroll
+  for (int m = 0; m < kWChunks; ++m) {
+    const int i = ct + 32 * kWConvWarps * m;  // chunk of this half: row i / 8, 16-byte chunk i % 8
+    const int row = i >> 3, c = i & 7;
+    v[m] = make_uint4(0, 0, 0, 0);
+    if (row < valid) v[m] = lds128(stage + which * (kWTok * kD) + (row >> 4) * kBoxBytes + swz(row & 15, c));
+  }
+#pragma unroll
+  for (int m = 0; m < kWChunks; ++m) {
+    const int i = ct + 32 * kWConvWarps * m;
+    const int row = i >> 3, c = i & 7;
+    uint4 o0, o1;
+    e4m3x4_to_f16x2x2(v[m].x, o0.x, o0.y);
+    e4m3x4_to_f16x2x2(v[m].y, o0.z, o0.w);
+    e4m3x4_to_f16x2x2(v[m].z, o1.x, o1.y);
+    e4m3x4_to_f16x2x2(v[m].w, o1.z, o1.w);
+    const int drow = which ? (row & ~3) | ((row & 1) << 1) | ((row >> 1) & 1) : row;
+    const uint32_t d = which * (2 * kWAtom) + atom_off(drow, 2 * c, kWAtom);
+    *reinterpret_cast<uint4*>(kv + d) = o0;
+    *reinterpret_cast<uint4*>(kv + (d ^ 16)) = o1;
+  }
+}
+
+__global__ void __launch_bounds__(kWThreads, 1)
+    prefillw_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const PrefillArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* const smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  BarsW& bs = *reinterpret_cast<BarsW*>(smem + kWOffBars);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int64_t u = blockIdx.x;
+  const Unit x = unit_of(a, u, threadIdx.x == 0 && (u % ((int64_t)a.QB * a.C * a.Hkv)) == 0);
+  if (!x.active) return;  // uniform over the CTA
+  const int ntiles = x.ntiles == 0 ? 0 : (x.t_hi - x.t_lo + kWTok - 1) / kWTok;
+  const bool direct = a.C == 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kWStages; ++s) {
+      mbar_init(smem_u32(&bs.stage_full[s]), 1);
+      mbar_init(smem_u32(&bs.stage_empty[s]), kWConvWarps);
+    }
+    const int live_warps = min(4, (x.rows + 15) / 16);
+    for (int k = 0; k < kWBufs; ++k) {
+      mbar_init(smem_u32(&bs.kfull[k]), kWConvWarps);
+      mbar_init(smem_u32(&bs.vfull[k]), kWConvWarps);
+      mbar_init(smem_u32(&bs.sfull[k]), 1);
+      mbar_init(smem_u32(&bs.sread[k]), live_warps);
+      mbar_init(smem_u32(&bs.pvdone[k]), 1);
+    }
+    mbar_init(smem_u32(&bs.pfull), live_warps);
+    mbar_init(smem_u32(&bs.qready), 4);
+    fence_mbar_init();
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  if (warp == kWMmaWarp) {
+    tc::tmem_alloc(smem_u32(&bs.tmem_base), kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = bs.tmem_base;
+  bool to = false;  // a bounded wait gave up
+
+  if (warp == kWProdWarp) {
+    // ------------------------------------------------------------ producer
+    // Lane l holds the block-table entry of box l % 8 of tile (batch + l / 8),
+    // four tiles per load, the next batch loaded while this one is issued.
+    constexpr int kBatch = 32 / kWBoxes;
+    const int32_t* bt = a.block_tables + (int64_t)x.b * a.max_pages;
+    auto load_batch = [&](int j0) {
+      const int j = j0 + lane / kWBoxes;
+      const int tb = x.t_lo + j * kWTok + (lane % kWBoxes) * kBoxTok;
+      return (j < ntiles && tb < x.t_hi) ? __ldg(bt + tb / a.P) : 0;
+    };
+    int cur = load_batch(0), nxt = load_batch(kBatch);
+    for (int j = 0; j < ntiles && !to; ++j) {
+      if (j > 0 && j % kBatch == 0) {
+        cur = nxt;
+        nxt = load_batch(j + kBatch);
+      }
+      const int st = j % kWStages;
+      if (j >= kWStages && !warp_wait(smem_u32(&bs.stage_empty[st]), ((j / kWStages) - 1) & 1)) {
+        to = true;
+        break;
+      }
+      const int tok0 = x.t_lo + j * kWTok;
+      const int nbox = min(kWBoxes, (x.t_hi - tok0 + kBoxTok - 1) / kBoxTok);
+      const uint32_t bar = smem_u32(&bs.stage_full[st]);
+      if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(2 * nbox * kBoxBytes));
+      __syncwarp();
+      int page = __shfl_sync(0xFFFFFFFFu, cur, (j % kBatch) * kWBoxes + (lane % kWBoxes));
+      if (lane < nbox) {
+        const int tb = tok0 + lane * kBoxTok;
+        if (page < 0 || (int64_t)page >= a.num_pages) {
+          atomicOr(a.status, kErrBadPage);
+          page = -1;  // the box lands outside the tensor and reads zeros
+        }
+        const int row = (page * a.Hkv + x.kvh) * a.P + tb % a.P;
+        const uint32_t dst = smem_u32(smem + kWOffStage + st * kWStageBytes) + lane * kBoxBytes;
+        tma_load_2d(dst, &tmK, 0, row, bar);
+        tma_load_2d(dst + kWTok * kD, &tmV, 0, row, bar);
+      }
+    }
+    for (int j = ntiles > kWStages ? ntiles - kWStages : 0; j < ntiles; ++j)
+      if (!mbar_wait(smem_u32(&bs.stage_full[j % kWStages]), (j / kWStages) & 1)) to = true;
+  } else if (warp == kWMmaWarp) {
+    // ------------------------------------------------- score MMA issuer
+    // S(j) = Q . K(j)^T (N = 128) into buffer j % 2, once K(j) is widened and
+    // the softmax warps have read S(j - 2) from that buffer.
+    if (lane == 0 && ntiles > 0) {
+      if (!mbar_wait(smem_u32(&bs.qready), 0)) to = true;
+      const uint32_t kv0 = smem_u32(smem + kWOffKv);
+      for (int qn = 0; qn < ntiles && !to; ++qn) {
+        const int kb = qn % kWBufs;
+        if (!mbar_wait(smem_u32(&bs.kfull[kb]), (qn / kWBufs) & 1)) to = true;
+        if (qn >= kWBufs && !to && !mbar_wait(smem_u32(&bs.sread[kb]), ((qn - kWBufs) / kWBufs) & 1)) to = true;
+        if (to) break;
+        tc::fence_after_sync();
+        const uint64_t kdesc = tc::desc_sw128(kv0 + kb * kWBufBytes, 16, 1024);
+#pragma unroll
+        for (int k = 0; k < kD / 16; ++k)
+          tc::mma_ts(tmem + kWTmemS + kWTok * kb, tmem + kWTmemQ + 8 * k,
+                     kdesc + (uint64_t)(((k >> 2) * kWAtom + 32 * (k & 3)) >> 4), kIdescQKW, k > 0 ? 1u : 0u);
+        tc::mma_commit(smem_u32(&bs.sfull[kb]));
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWPvWarp) {
+    // ---------------------------------------------------- P.V MMA issuer
+    if (lane == 0 && ntiles > 0) {
+      const uint32_t kv0 = smem_u32(smem + kWOffKv);
+      int pn = 0;
+      for (; pn < ntiles && !to; ++pn) {
+        const int kb = pn % kWBufs;
+        if (!mbar_wait(smem_u32(&bs.pfull), pn & 1) || !mbar_wait(smem_u32(&bs.vfull[kb]), (pn / kWBufs) & 1)) {
+          to = true;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint64_t vdesc = tc::desc_sw128(kv0 + kb * kWBufBytes + 2 * kWAtom, kWAtom, 1024);
+#pragma unroll
+        for (int k = 0; k < kWTok / 16; ++k)
+          tc::mma_ts(tmem + kWTmemO, tmem + kWTmemP + 8 * k, vdesc + (uint64_t)((2048 * k) >> 4), kIdescPVW,
+                     (pn > 0 || k > 0) ? 1u : 0u);
+        tc::mma_commit(smem_u32(&bs.pvdone[kb]));
+      }
+      if (pn > 0 && !mbar_wait(smem_u32(&bs.pvdone[(pn - 1) % kWBufs]), ((pn - 1) / kWBufs) & 1)) to = true;
+    }
+    __syncwarp();
+  } else if (warp < kWSoftWarp0) {
+    // ---------------------------------------------------------- converters
+    // K(j) once S(j - 2) has completed, V(j) once P.V(j - 2) has.
+    const int ct = threadIdx.x - kWConvWarp0 * 32;
+    for (int j = 0; j < ntiles && !to; ++j) {
+      const int st = j % kWStages, kb = j % kWBufs;
+      if (!warp_wait(smem_u32(&bs.stage_full[st]), (j / kWStages) & 1)) to = true;
+      if (j >= kWBufs && !to && !warp_wait(smem_u32(&bs.sfull[kb]), ((j - kWBufs) / kWBufs) & 1)) to = true;
+      if (to) break;
+      const int valid = min(kWTok, x.t_hi - (x.t_lo + j * kWTok));
+      const uint8_t* stage = smem + kWOffStage + st * kWStageBytes;
+      uint8_t* kv = smem + kWOffKv + kb * kWBufBytes;
+      widen_half(stage, kv, 0, ct, valid);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.kfull[kb]));
+      if (j >= kWBufs && !warp_wait(smem_u32(&bs.pvdone[kb]), ((j - kWBufs) / kWBufs) & 1)) {
+        to = true;
+        break;
+      }
+      widen_half(stage, kv, 1, ct, valid);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive_local(smem_u32(&bs.vfull[kb]));
+        tc::mbar_arrive_local(smem_u32(&bs.stage_empty[st]));
+      }
+    }
+  } else {
+    // -------------------------------------------------- softmax + epilogue
+    const int quad = warp & 3;
+    const uint32_t trow = tmem + ((uint32_t)(32 * quad) << 16);
+    // Q: thread t < 16 writes row 16 quad + t into its own lane (the lanes
+    // half-height products read), zeros elsewhere
+    {
+      const int rq = 16 * quad + (lane & 15);
+      const bool okq = lane < 16 && rq < x.rows;
+      const int64_t hq = ((int64_t)a.q_start[x.b] + x.i0 + rq / a.G) * a.Hq + (int64_t)x.kvh * a.G + rq % a.G;
+      const uint4* qp = reinterpret_cast<const uint4*>(a.q + hq * kD);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t f[32];
+#pragma unroll
+        for (int uu = 0; uu < 8; ++uu) {
+          uint4 w = make_uint4(0, 0, 0, 0);
+          if (okq) w = __ldg(qp + 8 * half + uu);
+          f[4 * uu] = pack_f16x2(bf16_lo(w.x), bf16_hi(w.x));
+          f[4 * uu + 1] = pack_f16x2(bf16_lo(w.y), bf16_hi(w.y));
+          f[4 * uu + 2] = pack_f16x2(bf16_lo(w.z), bf16_hi(w.z));
+          f[4 * uu + 3] = pack_f16x2(bf16_lo(w.w), bf16_hi(w.w));
+        }
+        tc::tmem_st32(trow + kWTmemQ + 32 * half, f);
+      }
+      tc::tmem_st_wait();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.qready));
+    }
+    // the 16-lane shape: thread t holds row 16 quad + Lm, Lm = (t >> 2) + 8 (t & 1),
+    // and the columns of parity par = (t >> 1) & 1 (register k of a 64-column
+    // read is column 2 k + par)
+    const int Lm = (lane >> 2) + 8 * (lane & 1), par = (lane >> 1) & 1;
+    const int rm = 16 * quad + Lm;
+    const bool okm = rm < x.rows;
+    const int im = x.i0 + rm / a.G;
+    const int limm = okm ? min(x.L - x.n + im + 1, x.t_end_chunk) : x.t_lo;
+    const float sc = a.score_scale;
+    float mref = -INFINITY, rthr = -INFINITY, lpart = 0.f;  // lpart: this thread's share of the row sum
+    // O row 16 quad + t (t < 16) sits in lane t of the quadrant; its statistics
+    // are held by thread 4 (t % 8) + t / 8
+    const int src = 4 * (lane & 7) + ((lane >> 3) & 1);
+    const bool live = 16 * quad < x.rows;
+    for (int j = 0; j < ntiles && !to && live; ++j) {
+      const int kb = j % kWBufs;
+      if (!warp_wait(smem_u32(&bs.sfull[kb]), (j / kWBufs) & 1)) {
+        to = true;
+        break;
+      }
+      tc::fence_after_sync();
+      // all 128 scores of the row half in registers: sv[32 h + k] is column
+      // 64 h + 2 k + par; the buffer is then free for S(j + 2)
+      uint32_t sv[64];
+      {
+        uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
+        uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
+        tc::tmem_ld16x64b_x32(trow + kWTmemS + kWTok * kb, s0);
+        tc::tmem_ld16x64b_x32(trow + kWTmemS + kWTok * kb + 64, s1);
+        tc::tmem_ld_wait();
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.sread[kb]));
+      // columns c < nv are attended (none for a padding row); every branch on
+      // `full` is warp-uniform and the masks are selects, so no lane diverges
+      const int nv = okm ? limm - (x.t_lo + j * kWTok) : 0;
+      const bool full = __all_sync(0xFFFFFFFFu, nv >= kWTok);
+      float mx;
+      {
+        float m8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
+        if (full) {
+#pragma unroll
+          for (int k = 0; k < 64; ++k) m8[k & 7] = fmaxf(m8[k & 7], __uint_as_float(sv[k]));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 64; ++k)
+            m8[k & 7] = fmaxf(m8[k & 7], 64 * (k >> 5) + 2 * (k & 31) + par < nv ? __uint_as_float(sv[k]) : -INFINITY);
+        }
+        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      }
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));  // the row's other half
+      const bool grow = mx > rthr;
+      float al = 1.f;
+      bool rescale = false;
+      if (__any_sync(0xFFFFFFFFu, grow)) {
+        const float mn = grow ? fmaxf(mref, mx * sc) : mref;
+        al = grow ? fast_exp2(mref - mn) : 1.f;  // 0 while mref is -inf
+        rescale = j > 0 && __any_sync(0xFFFFFFFFu, grow && mref != -INFINITY);
+        lpart *= al;
+        mref = mn;
+        rthr = (mn + kRescaleLog2) / sc;
+      }
+      // P: register pair (2 r, 2 r + 1) of a half holds tokens (4 r + par, 4 r + par + 2),
+      // which the contraction order places in P column 2 r + par of that half
+      uint32_t pv[32];
+      float ls[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+      if (full) {
+#pragma unroll
+        for (int r2 = 0; r2 < 32; ++r2) {
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * r2]), sc, -mref));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * r2 + 1]), sc, -mref));
+          ls[r2 & 3] += p0;
+          ls[4 + (r2 & 3)] += p1;
+          pv[r2] = pack_f16x2(p0, p1);
+        }
+      } else {
+        // a masked column's exponential may overflow; the select drops it
+#pragma unroll
+        for (int r2 = 0; r2 < 32; ++r2) {
+          const int c0 = 64 * (r2 >> 4) + 4 * (r2 & 15) + par;
+          const float e0 = fast_exp2(fmaf(__uint_as_float(sv[2 * r2]), sc, -mref));
+          const float e1 = fast_exp2(fmaf(__uint_as_float(sv[2 * r2 + 1]), sc, -mref));
+          const float p0 = c0 < nv ? e0 : 0.f, p1 = c0 + 2 < nv ? e1 : 0.f;
+          ls[r2 & 3] += p0;
+          ls[4 + (r2 & 3)] += p1;
+          pv[r2] = pack_f16x2(p0, p1);
+        }
+      }
+      lpart += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      // P and O are free once P.V(j - 1) has completed
+      if (j > 0) {
+        if (!warp_wait(smem_u32(&bs.pvdone[(j - 1) % kWBufs]), ((j - 1) / kWBufs) & 1)) {
+          to = true;
+          break;
+        }
+        tc::fence_after_sync();
+      }
+      if (rescale) {
+        // thread t < 16 rescales O row 16 quad + t
+        const float alo = __shfl_sync(0xFFFFFFFFu, al, src);
+#pragma unroll
+        for (int blk = 0; blk < 4; ++blk) {
+          uint32_t ov[32];
+          tc::tmem_ld32(trow + kWTmemO + 32 * blk, ov);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alo);
+          tc::tmem_st32(trow + kWTmemO + 32 * blk, ov);
+        }
+      }
+      tc::tmem_st16x64b_x16(trow + kWTmemP, *reinterpret_cast<const uint32_t(*)[16]>(&pv[0]));
+      tc::tmem_st16x64b_x16(trow + kWTmemP + 32, *reinterpret_cast<const uint32_t(*)[16]>(&pv[16]));
+      tc::tmem_st_wait();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.pfull));
+    }
+    // ---- epilogue: thread t < 16 writes row 16 quad + t from lane t of O
+    const float lrow = lpart + __shfl_xor_sync(0xFFFFFFFFu, lpart, 2);
+    const float le = __shfl_sync(0xFFFFFFFFu, lrow, src), me = __shfl_sync(0xFFFFFFFFu, mref, src);
+    if (live) {
+      if (!to && ntiles > 0 &&
+          !warp_wait(smem_u32(&bs.pvdone[(ntiles - 1) % kWBufs]), ((ntiles - 1) / kWBufs) & 1))
+        to = true;
+      tc::fence_after_sync();
+      const int re = 16 * quad + (lane & 15);
+      const bool oke = lane < 16 && re < x.rows;
+      const int ie = x.i0 + re / a.G, ge = re % a.G;
+      const int64_t hre = ((int64_t)a.q_start[x.b] + ie) * a.Hq + (int64_t)x.kvh * a.G + ge;
+      float* part = direct ? nullptr : a.partials + ((int64_t)u * kRows + re) * kPartStride;
+      const float inv = le > 0.f ? a.out_scale / le : 0.f;
+#pragma unroll
+      for (int blk = 0; blk < 4; ++blk) {
+        uint32_t ov[32];
+        if (ntiles > 0) {
+          tc::tmem_ld32(trow + kWTmemO + 32 * blk, ov);
+          tc::tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) ov[c] = 0u;
+        }
+        if (!oke || to) continue;
+        if (direct) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            pk[c] = pack_bf16x2(__uint_as_float(ov[2 * c]) * inv, __uint_as_float(ov[2 * c + 1]) * inv);
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + hre * kD + 32 * blk);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+        } else {
+          float4* dst = reinterpret_cast<float4*>(part + 4 + 32 * blk);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            dst[k] = make_float4(__uint_as_float(ov[4 * k]), __uint_as_float(ov[4 * k + 1]),
+                                 __uint_as_float(ov[4 * k + 2]), __uint_as_float(ov[4 * k + 3]));
+        }
+      }
+      if (oke && !to) {
+        if (direct) {
+          if (a.lse) a.lse[hre] = le > 0.f ? (me + __log2f(le)) * kLn2 : -INFINITY;
+        } else {
+          part[0] = me;
+          part[1] = le;
+        }
+      }
+    }
+  }
+
+  if (to) atomicOr(a.status, kErrWaitTimeout);
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == kWMmaWarp) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 // One warp per row of a (request, KV head, row block): folds the chunks'
 // partial states, M = max m_c, out = sum 2^(m_c - M) o_c / sum 2^(m_c - M) l_c.
 constexpr int kMergeWarps = 8;
@@ -1108,6 +1562,13 @@ int pfkv_paged_prefill_attn(void* out, const void* q, const void* k_cache, const
     if (rc != PFKV_OK) return rc;
     const int64_t units2 = (int64_t)batch * num_kv_heads * a.C * ((a.QB + 1) / 2);
     prefill2_kernel<<<(unsigned)units2, k2Threads, k2SmemBytes, s>>>(tmK, tmV, a);
+  } else if ((int64_t)max_q_len * G <= 64) {
+    // every block has at most 64 rows: 128-token tiles, half-height products
+    static std::atomic<uint64_t> smemw_set{0};
+    rc = set_max_dynamic_smem(reinterpret_cast<const void*>(prefillw_kernel), kWSmemBytes, smemw_set,
+                              "paged_prefill set smem attribute");
+    if (rc != PFKV_OK) return rc;
+    prefillw_kernel<<<(unsigned)units, kWThreads, kWSmemBytes, s>>>(tmK, tmV, a);
   } else {
     prefill_kernel<<<(unsigned)units, kThreads, kSmemBytes, s>>>(tmK, tmV, a);
   }
