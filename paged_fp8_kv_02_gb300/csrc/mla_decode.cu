@@ -401,16 +401,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t mask = bs.stage_mask[st];
       const uint8_t* stage = smem + kOffStage + st * kStageBytes;
       uint8_t* cbuf = smem + kOffC + ((j / 2) % kPairs) * kCBufBytes + (j & 1) * kTok * 128;
+      // every load before the first store: the compiler cannot move a load
+      // above a store through another pointer into shared memory
+      uint4 v[kChunksPerThread];
+#pragma unroll
+      for (int m = 0; m < kChunksPerThread; ++m) {
+        v[m] = make_uint4(0, 0, 0, 0);
+        if (crow[m] >= 0 && ((mask >> crow[m]) & 1)) v[m] = lds128(stage + src_off[m]);
+      }
 #pragma unroll
       for (int m = 0; m < kChunksPerThread; ++m) {
         if (crow[m] >= 0) {
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if ((mask >> crow[m]) & 1) v = lds128(stage + src_off[m]);
           uint4 o0, o1;
-          e4m3x4_to_f16x2x2(v.x, o0.x, o0.y);
-          e4m3x4_to_f16x2x2(v.y, o0.z, o0.w);
-          e4m3x4_to_f16x2x2(v.z, o1.x, o1.y);
-          e4m3x4_to_f16x2x2(v.w, o1.z, o1.w);
+          e4m3x4_to_f16x2x2(v[m].x, o0.x, o0.y);
+          e4m3x4_to_f16x2x2(v[m].y, o0.z, o0.w);
+          e4m3x4_to_f16x2x2(v[m].z, o1.x, o1.y);
+          e4m3x4_to_f16x2x2(v[m].w, o1.z, o1.w);
           // units u and u + 1 (u even) differ in bit 0, so their swizzled
           // positions differ by exactly 16 bytes
           *reinterpret_cast<uint4*>(cbuf + dst_off[m]) = o0;

@@ -172,6 +172,36 @@ __device__ __forceinline__ uint32_t atom_off(int r, int u, int atom_bytes) {
   return (uint32_t)((u >> 3) * atom_bytes + r * 128 + 16 * ((u & 7) ^ (r & 7)));
 }
 
+// Widens a 64-token e4m3 stage into a f16 tile, thread ct of the four
+// converter warps taking chunks i = ct + 128 m of the stage (K for i < 512, V
+// after; row (i % 512) / 8, 16-byte chunk c = i % 8) to units 2(c % 4) and
+// 2(c % 4) + 1 of atom c / 4 of the K or V half; rows at or past `valid`
+// become zeros.  All loads are issued before the first store: the compiler
+// cannot move a load above a store through another pointer into shared memory.
+__device__ __forceinline__ void widen_tile64(const uint8_t* stage, uint8_t* kv, int ct, int valid) {
+  uint4 v[8];
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const int i = ct + 128 * m;
+    const int which = i >> 9, row = (i & 511) >> 3, c = i & 7;
+    v[m] = make_uint4(0, 0, 0, 0);
+    if (row < valid) v[m] = lds128(stage + which * (kTokN * kD) + (row >> 4) * kBoxBytes + swz(row & 15, c));
+  }
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const int i = ct + 128 * m;
+    const int which = i >> 9, row = (i & 511) >> 3, c = i & 7;
+    uint4 o0, o1;
+    e4m3x4_to_f16x2x2(v[m].x, o0.x, o0.y);
+    e4m3x4_to_f16x2x2(v[m].y, o0.z, o0.w);
+    e4m3x4_to_f16x2x2(v[m].z, o1.x, o1.y);
+    e4m3x4_to_f16x2x2(v[m].w, o1.z, o1.w);
+    const uint32_t d = which * (2 * kKvAtom) + atom_off(row, 2 * c, kKvAtom);
+    *reinterpret_cast<uint4*>(kv + d) = o0;
+    *reinterpret_cast<uint4*>(kv + (d ^ 16)) = o1;  // unit 2(c%4) + 1: bit 0 of the unit flips
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const PrefillArgs a) {
@@ -310,8 +340,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp < kSoftWarp0) {
     // ---------------------------------------------------------- converters
-    // Chunk i of the stage (K: i < 512, V: i >= 512; row (i % 512) / 8, 16-byte
-    // chunk i % 8) -> e4m3 -> f16 units 2(c % 4), 2(c % 4) + 1 of atom c / 4.
     const int ct = threadIdx.x - kConvWarp0 * 32;
     for (int j = 0; j < ntiles && !to; ++j) {
       const int st = j % kStages, kb = j % kKvBufs;
@@ -325,22 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int valid = min(kTokN, x.t_hi - (x.t_lo + j * kTokN));
       const uint8_t* stage = smem + kOffStage + st * kStageBytes;
       uint8_t* kv = smem + kOffKv + kb * kKvBufBytes;
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const int i = ct + 128 * m;
-        const int which = i >> 9, rem = i & 511;
-        const int row = rem >> 3, c = rem & 7;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (row < valid) v = lds128(stage + which * (kTokN * kD) + (row >> 4) * kBoxBytes + swz(row & 15, c));
-        uint4 o0, o1;
-        e4m3x4_to_f16x2x2(v.x, o0.x, o0.y);
-        e4m3x4_to_f16x2x2(v.y, o0.z, o0.w);
-        e4m3x4_to_f16x2x2(v.z, o1.x, o1.y);
-        e4m3x4_to_f16x2x2(v.w, o1.z, o1.w);
-        const uint32_t d = which * (2 * kKvAtom) + atom_off(row, 2 * c, kKvAtom);
-        *reinterpret_cast<uint4*>(kv + d) = o0;
-        *reinterpret_cast<uint4*>(kv + (d ^ 16)) = o1;  // unit 2(c%4) + 1: bit 0 of the unit flips
-      }
+      widen_tile64(stage, kv, ct, valid);
       fence_proxy_async_smem();  // generic writes -> visible to the tensor core
       __syncwarp();
       if (lane == 0) {
@@ -739,22 +752,7 @@ __global__ void __launch_bounds__(k2Threads, 1)
       const int valid = min(kTokN, t_hi - (xa.t_lo + j * kTokN));
       const uint8_t* stage = smem + k2OffStage + st * kStageBytes;
       uint8_t* kv = smem + k2OffKv + kb * kKvBufBytes;
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const int i = ct + 128 * m;
-        const int which = i >> 9, rem = i & 511;
-        const int row = rem >> 3, c = rem & 7;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (row < valid) v = lds128(stage + which * (kTokN * kD) + (row >> 4) * kBoxBytes + swz(row & 15, c));
-        uint4 o0, o1;
-        e4m3x4_to_f16x2x2(v.x, o0.x, o0.y);
-        e4m3x4_to_f16x2x2(v.y, o0.z, o0.w);
-        e4m3x4_to_f16x2x2(v.z, o1.x, o1.y);
-        e4m3x4_to_f16x2x2(v.w, o1.z, o1.w);
-        const uint32_t d = which * (2 * kKvAtom) + atom_off(row, 2 * c, kKvAtom);
-        *reinterpret_cast<uint4*>(kv + d) = o0;
-        *reinterpret_cast<uint4*>(kv + (d ^ 16)) = o1;
-      }
+      widen_tile64(stage, kv, ct, valid);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
