@@ -96,6 +96,27 @@ def test_group4_many_requests():
     _check_small(_w("many", 16, 4, tuple(lens.tolist()), n_new=8), split=64)
 
 
+@pytest.mark.parametrize("split", [0, 128])
+def test_few_rows_varlen_with_an_empty_request(split):
+    # at most 8 queries x G 8 = 64 rows per block: 128-token tiles with
+    # half-height products; request 1 has no queries, contexts end mid-tile
+    w = _w("wide", 16, 2, (40, 16, 200, 129), n_new=1)
+    _check_small(w, q_lens=np.array([5, 0, 8, 1]), split=split, max_q=8)
+
+
+def test_few_rows_whole_prompt_is_new():
+    w = _w("wide_fresh", 16, 2, (1, 7, 64), n_new=1)
+    _check_small(w, q_lens=np.array([1, 7, 8]), max_q=8)
+
+
+def test_half_height_units_of_the_one_block_kernel():
+    # G 16 x 8 queries = 128 rows per block, but requests 1 and 2 have 48 and
+    # 16 rows: their units take the half-height products of the one-block kernel
+    w = _w("g16_varlen", 16, 1, (100, 50, 300), n_new=1)
+    _check_small(w, q_lens=np.array([8, 3, 1]), max_q=8)
+    _check_small(w, q_lens=np.array([8, 3, 1]), split=64, max_q=8)
+
+
 def test_bad_page_and_clamped_context_set_status():
     p = pf()
     w = _w("bad", 8, 2, (40, 90), n_new=4).set_scales_host()
