@@ -18,7 +18,8 @@
 //    one contiguous run of tiles of equal length (to within one tile), so any
 //    mix of context lengths is balanced without host knowledge of the lengths.
 //    A run that covers a whole (request, KV head) writes the final output; the
-//    others write fp32 (m, ℓ, o) partials that merge_kernel combines.
+//    others write fp32 (m, ℓ, o) partials that a merge kernel combines (one
+//    warp per query head for calls without explicit chunks).
 //  * Each warp is an independent worker with its own ring of kStages shared-
 //    memory stages fed by TMA (cp.async.bulk.tensor, 128-byte swizzle): one
 //    stage = the K and V slabs of one 16-token tile of one KV head.  The
@@ -275,6 +276,7 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 2)
       next_page = __ldg(a.block_tables + (int64_t)pc.b * a.max_pages + (pc.tile * kTile) / a.P);
   };
   load_page();
+  const uint64_t kv_policy = l2_evict_first_policy();  // K/V is read once
   auto issue = [&](int stage) {
     if (lane == 0) {
       const int tok0 = pc.tile * kTile;
@@ -305,13 +307,13 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 2)
         }
       }
       if constexpr (kBf16) {
-        tma_load_3d(dst, &tmK, 0, 0, row, bar);
-        tma_load_3d(dst + 2048, &tmK, 0, 1, row, bar);
-        tma_load_3d(dst + Geo::kKBytes, &tmV, 0, 0, row, bar);
-        tma_load_3d(dst + Geo::kKBytes + 2048, &tmV, 0, 1, row, bar);
+        tma_load_3d_hint(dst, &tmK, 0, 0, row, bar, kv_policy);
+        tma_load_3d_hint(dst + 2048, &tmK, 0, 1, row, bar, kv_policy);
+        tma_load_3d_hint(dst + Geo::kKBytes, &tmV, 0, 0, row, bar, kv_policy);
+        tma_load_3d_hint(dst + Geo::kKBytes + 2048, &tmV, 0, 1, row, bar, kv_policy);
       } else {
-        tma_load_2d(dst, &tmK, 0, row, bar);
-        tma_load_2d(dst + Geo::kKBytes, &tmV, 0, row, bar);
+        tma_load_2d_hint(dst, &tmK, 0, row, bar, kv_policy);
+        tma_load_2d_hint(dst + Geo::kKBytes, &tmV, 0, row, bar, kv_policy);
       }
     }
     cursor_next(pc, a);
@@ -733,13 +735,62 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 2)
 // fold them with an online maximum per head, and warp e then combines the
 // warps' states of head e with the log-sum-exp rule
 //   M = max_k m_k,  out = sum_k 2^{m_k-M} o_k / sum_k 2^{m_k-M} l_k.
+// One head of a unit without explicit chunks: its segments are the
+// consecutive warps first .. last that covered it (one warp per tile when
+// there are fewer tiles than warps).  The calling warp folds them, four
+// segments' loads in flight at a time, and writes the head's output.
+__device__ __forceinline__ void merge_unit_head(const DecodeArgs& a, int64_t ts, int ntiles, int64_t u0, int e,
+                                                int64_t head, int lane) {
+  const int64_t W = a.tile_start[a.B], N = a.nwarps;
+  const int64_t first = owner_of(ts, W, N);
+  const int64_t nseg = W >= N ? owner_of(ts + ntiles - 1, W, N) - first + 1 : ntiles;
+  float M = -INFINITY, den = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t k0 = 0; k0 < nseg; k0 += 4) {
+    float mk[4], lk[4];
+    float4 ok[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int64_t k = k0 + q;
+      mk[q] = -INFINITY;
+      lk[q] = 0.f;
+      ok[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (k < nseg) {
+        const int64_t slot = (W >= N ? first + k : owner_of(ts + k, W, N)) + u0;
+        if (slot < a.capacity) {
+          const float* p = a.partials + (slot * a.G + e) * kPartialStride;
+          mk[q] = p[0];
+          lk[q] = p[1];
+          ok[q] = reinterpret_cast<const float4*>(p + 4)[lane];
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (mk[q] == -INFINITY) continue;
+      const float Mn = fmaxf(M, mk[q]);
+      const float al = fast_exp2(M - Mn), wt = fast_exp2(mk[q] - Mn);
+      den = den * al + wt * lk[q];
+      acc.x = acc.x * al + wt * ok[q].x;
+      acc.y = acc.y * al + wt * ok[q].y;
+      acc.z = acc.z * al + wt * ok[q].z;
+      acc.w = acc.w * al + wt * ok[q].w;
+      M = Mn;
+    }
+  }
+  const float inv = den > 0.f ? a.out_scale / den : 0.f;
+  reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.out) + head * kD)[lane] =
+      make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+  if (a.lse && lane == 0) a.lse[head] = den > 0.f ? (M + __log2f(den)) * kLn2 : -INFINITY;
+}
+
 constexpr int kMergeWarps = 8;
 constexpr int kMergeThreads = kMergeWarps * 32;
 constexpr int kMergeBatch = kMergeThreads;  // chunks enumerated per batch
 
-// kHeads query heads of one (request, KV head) per CTA: 1 for many small CTAs
-// (MHA, or long requests cut into many chunks), 8 to read a segment's heads
-// with one coalesced sweep (GQA without chunking).
+// kMergeHeads query heads of one (request, KV head) per CTA; calls with
+// explicit chunks use 1 (many small CTAs), calls without them use
+// merge_unsplit_kernel below.
 template <int kMergeHeads>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeArgs a) {
   __shared__ float4 red_o[kMergeWarps][kMergeHeads][32];
@@ -770,53 +821,10 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeArgs a
   const int64_t u0 = a.unit_start[b] + (int64_t)kvh * nchunks;
   if (nchunks == 1 && owner_of(ts, W, N) == owner_of(ts + ntiles - 1, W, N)) return;  // direct
   if (nchunks == 1) {
-    // One unit (no explicit split): its segments are the consecutive warps
-    // first .. last (one warp per tile when there are fewer tiles than
-    // warps).  Warp k folds head g_lo + k alone (with one head per CTA, warp
-    // 0 does), four segments' loads in flight at a time, and writes it.
+    // one warp per head (with one head per CTA, warp 0)
     const int e = g_lo + (kMergeHeads == 1 ? 0 : warp);
     if ((kMergeHeads == 1 && warp != 0) || e >= g_hi) return;
-    const int64_t first = owner_of(ts, W, N);
-    const int64_t nseg = W >= N ? owner_of(ts + ntiles - 1, W, N) - first + 1 : ntiles;
-    float M = -INFINITY, den = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int64_t k0 = 0; k0 < nseg; k0 += 4) {
-      float mk[4], lk[4];
-      float4 ok[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int64_t k = k0 + q;
-        mk[q] = -INFINITY;
-        lk[q] = 0.f;
-        ok[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (k < nseg) {
-          const int64_t slot = (W >= N ? first + k : owner_of(ts + k, W, N)) + u0;
-          if (slot < a.capacity) {
-            const float* p = a.partials + (slot * a.G + e) * kPartialStride;
-            mk[q] = p[0];
-            lk[q] = p[1];
-            ok[q] = reinterpret_cast<const float4*>(p + 4)[lane];
-          }
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (mk[q] == -INFINITY) continue;
-        const float Mn = fmaxf(M, mk[q]);
-        const float al = fast_exp2(M - Mn), wt = fast_exp2(mk[q] - Mn);
-        den = den * al + wt * lk[q];
-        acc.x = acc.x * al + wt * ok[q].x;
-        acc.y = acc.y * al + wt * ok[q].y;
-        acc.z = acc.z * al + wt * ok[q].z;
-        acc.w = acc.w * al + wt * ok[q].w;
-        M = Mn;
-      }
-    }
-    const int64_t head = head0 + e;
-    const float inv = den > 0.f ? a.out_scale / den : 0.f;
-    reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.out) + head * kD)[lane] =
-        make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
-    if (a.lse && lane == 0) a.lse[head] = den > 0.f ? (M + __log2f(den)) * kLn2 : -INFINITY;
+    merge_unit_head(a, ts, ntiles, u0, e, head0 + e, lane);
     return;
   }
 
@@ -935,6 +943,28 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeArgs a
   }
 }
 
+// Merge for calls without explicit chunks (one unit per request and KV head):
+// one warp per (request, query head), eight per CTA, so that every unit's
+// heads are folded in a single wave of small CTAs.
+__global__ void __launch_bounds__(kMergeThreads) merge_unsplit_kernel(const DecodeArgs a) {
+  grid_dependency_wait();  // every partial state of the tile kernel is visible
+  const int64_t hw = (int64_t)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);  // b * Hq + query head
+  const int lane = threadIdx.x & 31;
+  if (hw >= (int64_t)a.B * a.Hq) return;
+  const int b = (int)(hw / a.Hq), hq = (int)(hw % a.Hq);
+  const int kvh = hq / a.G, e = hq % a.G;
+  const int ntiles = ntiles_of(a, b);
+  if (ntiles == 0) {
+    reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.out) + hw * kD)[lane] = make_uint2(0, 0);
+    if (a.lse && lane == 0) a.lse[hw] = -INFINITY;
+    return;
+  }
+  const int64_t W = a.tile_start[a.B], N = a.nwarps;
+  const int64_t ts = a.tile_start[b] + (int64_t)kvh * ntiles;
+  if (owner_of(ts, W, N) == owner_of(ts + ntiles - 1, W, N)) return;  // one warp wrote it directly
+  merge_unit_head(a, ts, ntiles, a.unit_start[b] + kvh, e, hw, lane);
+}
+
 // ------------------------------------------------------------------- host
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -998,12 +1028,12 @@ int launch_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const DecodeAr
   cfg.blockDim = dim3(kMergeThreads);
   cfg.dynamicSmemBytes = 0;
   cudaError_t e;
-  if (a.chunk_tiles < (1 << 30) || a.G < 8) {
+  if (a.chunk_tiles < (1 << 30)) {
     cfg.gridDim = dim3(a.B * a.Hq);
     e = cudaLaunchKernelEx(&cfg, merge_kernel<1>, args);
   } else {
-    cfg.gridDim = dim3(a.B * a.Hkv * ((a.G + 7) / 8));
-    e = cudaLaunchKernelEx(&cfg, merge_kernel<8>, args);
+    cfg.gridDim = dim3((unsigned)(((int64_t)a.B * a.Hq + kMergeWarps - 1) / kMergeWarps));
+    e = cudaLaunchKernelEx(&cfg, merge_unsplit_kernel, args);
   }
   if (e != cudaSuccess) return check_cuda("paged_decode merge launch");
   return check_cuda("paged_decode launch");
