@@ -71,7 +71,8 @@ def profiled_traffic():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms while the
+    GPU runs the timed region and the same untimed steps around it."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -86,7 +87,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except OSError:
@@ -96,6 +97,13 @@ class ClockSampler:
     def _read(self):
         for ln in self.proc.stdout:
             self.lines.append(ln.strip())
+
+    def wait_first(self, timeout=10.0):
+        """Block until the sampler has produced a line (nvidia-smi takes a
+        moment to start), so that the load that follows is sampled."""
+        t_end = time.perf_counter() + timeout
+        while self.proc is not None and not self.lines and time.perf_counter() < t_end:
+            time.sleep(0.01)
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -665,7 +673,18 @@ def run_gpu(args, rank, ws, local):
     # ---- timed region: K steps back to back (inputs larger than L2)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    def load_for(seconds):
+        # the same step, untimed: keeps the GPU under the timed region's load
+        # while the clock sampler (50 ms period) records it
+        t_end = time.perf_counter() + seconds
+        while time.perf_counter() < t_end:
+            for _ in range(16):
+                s.step()
+            torch.cuda.synchronize()
+
     with ClockSampler(local) as clk:
+        clk.wait_first()
+        load_for(0.3)
         torch.cuda.synchronize()
         barrier(ws)
         torch.cuda.synchronize()
@@ -679,7 +698,7 @@ def run_gpu(args, rank, ws, local):
         torch.cuda.synchronize()
         barrier(ws)
         torch.cuda.synchronize()
-        time.sleep(0.25)
+        load_for(0.3)
     t_total = start.elapsed_time(end) * 1e-3
     t_total = max_over_ranks(t_total, ws, dev)
     dec = [a.elapsed_time(b) * 1e-3 for a, b in ev]
@@ -715,6 +734,7 @@ def run_gpu(args, rank, ws, local):
             others = other_workloads(pf, peak_gbs, peak_tf)
 
     clocks = clk.summary()
+    clocks["window"] = "50 ms samples over the timed region and 0.3 s of the same step before and after it"
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
