@@ -34,7 +34,7 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 
 METRIC = "decode-attn KV GB/s (% of GB300 HBM peak) and query-tokens/s at 1 GPU"
-HEADLINE = 2
+HEADLINE = "mha_b32_h48_l8192_p16"  # the headline workload: MHA 32 x 48 x 8192, page 16
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "paged_decode_kernel_mha_b32_l8192_traffic.txt")
 DECODE_SRC = os.path.join(ROOT, "paged_fp8_kv_02_gb300", "csrc", "paged_decode.cu")
 
@@ -315,15 +315,15 @@ def other_workloads(pf, peak_gbs, peak_tf, iters=10):
 
     res["prefill"] = prefill_timing(pf, peak_gbs, peak_tf, flush, iters)
     res["scale_granularity_mha_b32_h48_l8192_p16"] = scale_granularity_timing(
-        pf, lambda: synth.config(2), peak_gbs, flush, iters)
+        pf, lambda: synth.workload(synth.MHA_B32), peak_gbs, flush, iters)
     res["scale_granularity_gqa_prefix_b64_h64kv8_p16"] = scale_granularity_timing(
-        pf, lambda: synth.config(3), peak_gbs, flush, iters)
-    paged("gqa_prefix_b64_h64kv8_p16", synth.config(3))
-    res["page_pool_config3_host"] = page_pool_timing(pf, synth.config(3))
-    w5 = synth.config(5)
+        pf, lambda: synth.workload(synth.GQA_PREFIX), peak_gbs, flush, iters)
+    paged("gqa_prefix_b64_h64kv8_p16", synth.workload(synth.GQA_PREFIX))
+    res["page_pool_gqa_prefix_host"] = page_pool_timing(pf, synth.workload(synth.GQA_PREFIX))
+    w5 = synth.workload(synth.LONG_SPLITKV)
     paged("long_splitkv_b8_h64kv8_p64_chunk4096", w5)
-    paged("mha_b32_h48_l8192_p16_bf16_cache", synth.config(2), bf16=True)
-    m = synth.config(4)
+    paged("mha_b32_h48_l8192_p16_bf16_cache", synth.workload(synth.MHA_B32), bf16=True)
+    m = synth.workload(synth.MLA_TOPK)
     s = MlaStep(pf, m)
     for _ in range(3):
         s.append()
@@ -405,7 +405,7 @@ def scale_granularity_timing(pf, w_factory, peak_gbs, flush, iters):
 
 
 def prefill_timing(pf, peak_gbs, peak_tf, flush, iters):
-    """paged_prefill_attn: (a) verification-sized, config 5's 8 appended tokens
+    """paged_prefill_attn: (a) verification-sized, the long split-KV workload's 8 appended tokens
     per request as queries (HBM-bound); (b) a chunked-prefill step, 1024 new
     tokens per request on a 7168-token cached prefix (tensor-bound)."""
     import torch
@@ -424,7 +424,7 @@ def prefill_timing(pf, peak_gbs, peak_tf, flush, iters):
         return 4 * w.D * w.Hq * pos
 
     # (a) verification-sized
-    w = synth.config(5)
+    w = synth.workload(synth.LONG_SPLITKV)
     s, q, qs = setup(w)
     out = torch.empty_like(q)
     st = s.st
@@ -472,7 +472,7 @@ def prefill_timing(pf, peak_gbs, peak_tf, flush, iters):
 
 
 def page_pool_timing(pf, w, repeats=5):
-    """Host time of the page pool + prefix cache building config 3's block
+    """Host time of the page pool + prefix cache building the shared-prefix GQA workload's block
     tables from token streams (requests 0-15 share a 2048-token prefix), and of
     releasing them; every page of the pool ends up used."""
     import numpy as np
@@ -634,7 +634,7 @@ def run_reference(args, rank, ws):
     import synth
     if rank != 0:
         return
-    w = synth.config(HEADLINE)
+    w = synth.workload(HEADLINE)
     n_req = args.oracle_requests
     scales = reference_scales(w, n_req)
     res = oracle_baseline(w, n_req, steps=max(1, args.steps), warmup=min(1, args.warmup))
@@ -643,7 +643,7 @@ def run_reference(args, rank, ws):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(res["seconds_per_step"] * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": synth.CONFIG_NAMES[HEADLINE], "batch": w.B, "q_heads": w.Hq,
+        "config": {"workload": HEADLINE, "batch": w.B, "q_heads": w.Hq,
                    "kv_heads": w.Hkv, "head_dim": w.D, "context": int(w.context_lens[0]), "page_size": w.P,
                    "cache": "e4m3", "sample_requests": n_req, "scales": scales},
         "query_tokens_per_s": round(res["query_tokens_per_s"], 3),
@@ -660,7 +660,7 @@ def run_gpu(args, rank, ws, local):
 
     pf.load()
     peak_gbs, peak_tf, peak_tf_sus, peak_src = load_peaks()
-    w = synth.config(HEADLINE)
+    w = synth.workload(HEADLINE)
     s = PagedStep(pf, w)
     dev = torch.device("cuda", torch.cuda.current_device())
 
@@ -726,7 +726,7 @@ def run_gpu(args, rank, ws, local):
     others = None
     if rank == 0:
         if not args.no_cpu_baseline:
-            cb = oracle_baseline(_with_scales(synth.config(HEADLINE), w), args.oracle_requests)
+            cb = oracle_baseline(_with_scales(synth.workload(HEADLINE), w), args.oracle_requests)
             cpu = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
         if not args.no_others:
             del s
@@ -741,7 +741,7 @@ def run_gpu(args, rank, ws, local):
             "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 cache, f16/bf16 mma, f32 accumulate",
             "data": "synthetic (seeded counter-based N(0,1) approximation)",
-            "config": {"workload": synth.CONFIG_NAMES[HEADLINE], "batch_per_gpu": w.B, "q_heads": w.Hq,
+            "config": {"workload": HEADLINE, "batch_per_gpu": w.B, "q_heads": w.Hq,
                        "kv_heads": w.Hkv, "head_dim": w.D, "context": int(w.context_lens[0]),
                        "page_size": w.P, "new_tokens_per_request": w.n_new, "cache": "e4m3",
                        "parallelism": f"request-dp{ws}",
@@ -881,7 +881,7 @@ def run_profile_case(name):
         s = PagedStep(pf, synth.PagedWorkload("mha_b8", B=8, Hq=48, Hkv=48, D=128, P=16,
                                               context_lens=np.full(8, 8192), n_new=1))
     elif name == "gqa_prefix_b64":
-        s = PagedStep(pf, synth.config(3))
+        s = PagedStep(pf, synth.workload(synth.GQA_PREFIX))
     elif name == "long_b2_l262144":
         s = PagedStep(pf, synth.PagedWorkload("long_b2", B=2, Hq=64, Hkv=8, D=128, P=64,
                                               context_lens=np.full(2, 262144), n_new=8, kv_split_tokens=4096))

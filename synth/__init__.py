@@ -9,6 +9,11 @@ from . import gen  # noqa: F401
 from .workloads import (  # noqa: F401
     MlaWorkload,
     PagedWorkload,
-    config,
-    CONFIG_NAMES,
+    workload,
+    WORKLOADS,
+    TINY_GQA,
+    MHA_B32,
+    GQA_PREFIX,
+    MLA_TOPK,
+    LONG_SPLITKV,
 )

@@ -1,6 +1,6 @@
 """Synthetic workloads of the pages' shapes (seeded, deterministic).
 
-Five named configurations (``config(n)``), plus free construction of smaller
+Five named workloads (``workload(name)``), plus free construction of smaller
 cases for parity tests.  Each workload yields host arrays (block tables, context
 lengths, slot mappings, top-k lists) and a recipe for its bf16 tensors: element
 ``(b, t, h, d)`` of the K, V or latent tensor takes counter index
@@ -23,13 +23,13 @@ from . import gen
 
 TOKEN_SHIFT = 21  # tokens per request < 2^21
 
-CONFIG_NAMES = {
-    1: "tiny_gqa_b4",
-    2: "mha_b32_h48_l8192_p16",
-    3: "gqa_prefix_b64_h64kv8_p16",
-    4: "mla_topk2048_b64_h128_l65536_p64",
-    5: "long_splitkv_b8_h64kv8_p64",
-}
+# the five workloads of the pages' shapes, by name
+TINY_GQA = "tiny_gqa_b4"
+MHA_B32 = "mha_b32_h48_l8192_p16"
+GQA_PREFIX = "gqa_prefix_b64_h64kv8_p16"
+MLA_TOPK = "mla_topk2048_b64_h128_l65536_p64"
+LONG_SPLITKV = "long_splitkv_b8_h64kv8_p64"
+WORKLOADS = (TINY_GQA, MHA_B32, GQA_PREFIX, MLA_TOPK, LONG_SPLITKV)
 
 E4M3_MAX = np.float32(448.0)
 
@@ -361,32 +361,38 @@ class MlaWorkload:
         return 2 * self.H * self.attended_tokens() * (self.Dqk + self.Dv)
 
 
-# --------------------------------------------------------------------- configs
+# ------------------------------------------------------------------ workloads
 def _lognormal_lens(seed: int, B: int, median: float, sigma: float, lo: int, hi: int) -> np.ndarray:
     z = gen.normal_f32(gen.make_key(seed, gen.TENSOR_CTX), np.arange(B, dtype=np.uint64)).astype(np.float64)
     L = np.rint(np.exp(math.log(median) + sigma * z)).astype(np.int64)
     return np.clip(L, lo, hi)
 
 
-def config(n: int, seed: int = 0):
-    """The five workloads of the pages' shapes (see CONFIG_NAMES)."""
-    if n == 1:
+def workload(name: str, seed: int = 0):
+    """One of the five workloads of the pages' shapes (WORKLOADS):
+    tiny GQA (4 requests, 8/2 heads, contexts 16-300, a 128-page pool);
+    MHA (32 requests x 48 heads x 8192 tokens, page 16);
+    GQA with a shared prefix (64 requests, 64/8 heads, lognormal contexts, 16
+    of them sharing 2048 prefix tokens); MLA (64 requests x 128 heads, latent
+    576, top-k 2048 of 65536, page 64); long split-KV (8 requests of 256K-1M
+    tokens, 64/8 heads, page 64, 8 new tokens each, 4096-token chunks)."""
+    if name == TINY_GQA:
         L = gen.uniform_int(gen.make_key(seed, gen.TENSOR_CTX), np.arange(4, dtype=np.uint64), 16, 300)
-        return PagedWorkload(CONFIG_NAMES[1], B=4, Hq=8, Hkv=2, D=128, P=16, context_lens=L, n_new=1,
+        return PagedWorkload(name, B=4, Hq=8, Hkv=2, D=128, P=16, context_lens=L, n_new=1,
                              num_pages=128, seed=seed)
-    if n == 2:
-        return PagedWorkload(CONFIG_NAMES[2], B=32, Hq=48, Hkv=48, D=128, P=16,
+    if name == MHA_B32:
+        return PagedWorkload(name, B=32, Hq=48, Hkv=48, D=128, P=16,
                              context_lens=np.full(32, 8192), n_new=1, seed=seed)
-    if n == 3:
+    if name == GQA_PREFIX:
         L = _lognormal_lens(seed, 64, 4096.0, 0.8, 256, 32768)
         L[:16] = np.maximum(L[:16], 2048 + 16)
-        return PagedWorkload(CONFIG_NAMES[3], B=64, Hq=64, Hkv=8, D=128, P=16, context_lens=L, n_new=1,
+        return PagedWorkload(name, B=64, Hq=64, Hkv=8, D=128, P=16, context_lens=L, n_new=1,
                              shared_requests=16, shared_tokens=2048, seed=seed)
-    if n == 4:
-        return MlaWorkload(CONFIG_NAMES[4], B=64, H=128, context_lens=np.full(64, 65536), topk_n=2048,
+    if name == MLA_TOPK:
+        return MlaWorkload(name, B=64, H=128, context_lens=np.full(64, 65536), topk_n=2048,
                            P=64, n_new=1, seed=seed)
-    if n == 5:
+    if name == LONG_SPLITKV:
         L = np.array([262144, 393216, 524288, 655360, 786432, 917504, 1048576, 1048576])
-        return PagedWorkload(CONFIG_NAMES[5], B=8, Hq=64, Hkv=8, D=128, P=64, context_lens=L, n_new=8,
+        return PagedWorkload(name, B=8, Hq=64, Hkv=8, D=128, P=64, context_lens=L, n_new=8,
                              seed=seed, kv_split_tokens=4096)
-    raise ValueError(f"unknown config {n}")
+    raise ValueError(f"unknown workload {name!r}; choose from {WORKLOADS}")

@@ -45,11 +45,11 @@ def test_every_bf16_pattern_encodes_like_the_oracle(scale):
     assert np.all(np.isin(got[nan_pos], [0x7F, 0xFF]))
 
 
-def test_config1_cache_bytes_bit_exact():
+def test_tiny_gqa_cache_bytes_bit_exact():
     torch = _torch()
     p = pf()
     from synth import device as sdev
-    w = synth.config(1).set_scales_host()
+    w = synth.workload(synth.TINY_GQA).set_scales_host()
     st = sdev.setup_paged(w, append_fp8_fn(p, w))
     p.kv_append_fp8(st.k_new, st.v_new, st.k_cache, st.v_cache, st.step_slots, w.k_scale, w.v_scale)
     torch.cuda.synchronize()

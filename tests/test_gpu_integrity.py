@@ -43,10 +43,10 @@ def test_random_tables_with_planted_faults_match_oracle():
     assert (ref == 0).sum() > 50 and (ref & oracle.REQ_TAG_MISMATCH).sum() > 20 and (ref & oracle.REQ_BAD_INDEX).sum() > 5
 
 
-@pytest.mark.parametrize("n", [2, 5])
-def test_full_size_tables_flag_exactly_the_planted_request(n):
+@pytest.mark.parametrize("name", ["mha_b32_h48_l8192_p16", "long_splitkv_b8_h64kv8_p64"])
+def test_full_size_tables_flag_exactly_the_planted_request(name):
     p = pf()
-    w = synth.config(n)
+    w = synth.workload(name)
     tags = np.arange(w.num_pages, dtype=np.uint32) * np.uint32(2654435761)
     bt = w.block_tables.astype(np.int32)
     tt = np.where(bt >= 0, tags[np.clip(bt, 0, None)], 0).astype(np.uint32)

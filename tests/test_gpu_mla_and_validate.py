@@ -82,9 +82,9 @@ def test_mla_topk_padding_and_out_of_range_indices():
     assert_within_tolerance(out2, ref, "mla bad index skipped")
 
 
-def test_config4_mla_full_size_sampled():
+def test_mla_topk2048_full_size_sampled():
     p = pf()
-    m = synth.config(4)
+    m = synth.workload(synth.MLA_TOPK)
     st = _setup_mla(p, m)
     out, lse, status = _run_mla(p, m, st)
     assert status == 0
@@ -108,7 +108,7 @@ def test_config4_mla_full_size_sampled():
             gots.append(out[b, h])
             refs.append(ref)
             assert abs(lse[b, h] - ref_lse) <= 2e-4 + 2e-5 * abs(ref_lse)
-    assert_within_tolerance(np.stack(gots), np.stack(refs), "mla config 4 sampled")
+    assert_within_tolerance(np.stack(gots), np.stack(refs), "MLA 64 x 128 heads, top-k 2048, sampled")
 
 
 def test_validate_tables_flags_each_error_kind():

@@ -1,4 +1,4 @@
-"""End to end through the host page pool: config 3's block tables and slot
+"""End to end through the host page pool: the shared-prefix GQA workload's block tables and slot
 mappings are produced from token streams by the prefix cache (requests 0-15
 share a 2048-token prompt prefix), the cache is filled through those slots
 (the shared prefix written once), decode runs over the pool's tables, and
@@ -30,10 +30,10 @@ def _streams(w, seed=23):
     return out
 
 
-def test_config3_from_token_streams_through_the_prefix_cache():
+def test_shared_prefix_workload_from_token_streams_through_the_prefix_cache():
     import torch
     p = pf()
-    w = synth.config(3)
+    w = synth.workload(synth.GQA_PREFIX)
     maxp = w.block_tables.shape[1]
     pool = p.PagePool(w.num_pages, w.P)
     rows = np.full((w.B, maxp), -1, np.int32)

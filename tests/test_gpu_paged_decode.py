@@ -62,8 +62,8 @@ def _full_check(p, w, split=0, bf16=False):
     return out
 
 
-def test_config1_tiny_gqa():
-    _full_check(pf(), synth.config(1))
+def test_tiny_gqa_workload():
+    _full_check(pf(), synth.workload(synth.TINY_GQA))
 
 
 @pytest.mark.parametrize("case", [
@@ -165,18 +165,18 @@ def _samples(w, n, seed):
 
 
 @pytest.mark.parametrize("bf16", [False, True])
-def test_config2_mha_full_size_sampled(bf16):
+def test_mha_b32_full_size_sampled(bf16):
     p = pf()
-    w = synth.config(2)
+    w = synth.workload(synth.MHA_B32)
     st = _setup(p, w, bf16=bf16)
     out, lse, status = _run(p, w, st)
     assert status == 0
     _sampled_check(p, w, st, out, lse, _samples(w, 6, 41) + [(0, 0), (31, 47)], bf16=bf16)
 
 
-def test_config3_prefix_full_size_sampled():
+def test_gqa_shared_prefix_full_size_sampled():
     p = pf()
-    w = synth.config(3)
+    w = synth.workload(synth.GQA_PREFIX)
     st = _setup(p, w)
     out, lse, status = _run(p, w, st)
     assert status == 0
@@ -184,9 +184,9 @@ def test_config3_prefix_full_size_sampled():
     _sampled_check(p, w, st, out, lse, samples)
 
 
-def test_config5_long_split_full_size_sampled():
+def test_long_split_kv_full_size_sampled():
     p = pf()
-    w = synth.config(5)
+    w = synth.workload(synth.LONG_SPLITKV)
     st = _setup(p, w)
     out, lse, status = _run(p, w, st, split=w.kv_split_tokens)
     assert status == 0

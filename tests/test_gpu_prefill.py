@@ -4,7 +4,7 @@ on the GPU against the oracle.
 Small cases: caches encoded by the oracle from the host generator are
 uploaded and every output row is compared with the oracle (tolerance
 |err| <= 2e-3 * max|ref| + 1e-3 + half a bf16 ulp; lse to 2e-5 relative).
-Full size: config 5's cache is filled through the product's append from the
+Full size: the long split-KV workload's cache is filled through the product's append from the
 device generator, its 8 appended tokens per request are the queries, and
 sampled (request, query, head) rows are recomputed by the oracle from the
 host generator in a private cache whose bytes are checked against the GPU's."""
@@ -148,11 +148,11 @@ def test_bad_arguments_are_rejected():
     assert e.value.code == -1
 
 
-def test_config5_appended_tokens_full_size_sampled():
+def test_long_splitkv_appended_tokens_full_size_sampled():
     import torch
     from synth import device as sdev
     p = pf()
-    w = synth.config(5)
+    w = synth.workload(synth.LONG_SPLITKV)
     st = sdev.setup_paged(w, append_fp8_fn(p, w))
     p.kv_append_fp8(st.k_new, st.v_new, st.k_cache, st.v_cache, st.step_slots, w.k_scale, w.v_scale)
     qbits = w.q_new_bits()
@@ -183,4 +183,4 @@ def test_config5_appended_tokens_full_size_sampled():
         gots.append(out[row, h])
         refs.append(ref)
         assert abs(lse[row, h] - ref_lse) <= 2e-4 + 2e-5 * abs(ref_lse)
-    assert_within_tolerance(np.stack(gots), np.stack(refs), "config 5 appended tokens sampled")
+    assert_within_tolerance(np.stack(gots), np.stack(refs), "long split-KV appended tokens sampled")

@@ -218,11 +218,11 @@ def test_scaled_decode_rejects_bad_arguments():
 
 
 # ------------------------------------------------------- full size, sampled
-def test_config2_token_scales_full_size_sampled():
+def test_mha_b32_token_scales_full_size_sampled():
     import torch
     from synth import device as sdev
     p = pf()
-    w = synth.config(2)
+    w = synth.workload(synth.MHA_B32)
     shape = (w.num_pages, w.Hkv, w.P)
     ks = torch.zeros(shape, dtype=torch.float32, device="cuda")
     vs = torch.zeros_like(ks)
@@ -256,4 +256,4 @@ def test_config2_token_scales_full_size_sampled():
         gots.append(out[b, h])
         refs.append(ref)
         assert abs(lse[b, h] - ref_lse) <= 2e-4 + 2e-5 * abs(ref_lse)
-    assert_within_tolerance(np.stack(gots), np.stack(refs), "config 2 per-token sampled")
+    assert_within_tolerance(np.stack(gots), np.stack(refs), "MHA 32 x 48 x 8192 per-token sampled")

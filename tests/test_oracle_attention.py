@@ -43,8 +43,8 @@ def test_paged_decode_matches_dense_sdpa(case):
         np.testing.assert_allclose(lse[b], ref_lse, rtol=1e-10, atol=1e-12)
 
 
-def test_config1_matches_dense_sdpa():
-    w = synth.config(1).set_scales_host()
+def test_tiny_gqa_workload_matches_dense_sdpa():
+    w = synth.workload(synth.TINY_GQA).set_scales_host()
     kc, vc = oracle_fill_paged(w)
     out, lse = oracle.paged_decode(w.q_bits(), kc, vc, w.block_tables, w.context_lens, w.P,
                                    w.k_scale, w.v_scale, w.softmax_scale, w.Hkv)

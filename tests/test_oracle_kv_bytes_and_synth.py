@@ -35,9 +35,9 @@ def test_fp8_halves_bytes_and_doubles_capacity():
     assert abs(g["fp8_tokens_approx"] / g["bf16_tokens_approx"] - 2.0) < 0.01
 
 
-def test_allocated_cache_bytes_equal_formula_for_every_paged_config():
-    for n in (1, 2, 3, 5):
-        w = synth.config(n)
+def test_allocated_cache_bytes_equal_formula_for_every_paged_workload():
+    for name in (synth.TINY_GQA, synth.MHA_B32, synth.GQA_PREFIX, synth.LONG_SPLITKV):
+        w = synth.workload(name)
         # a cache holding exactly the workload's pages, one layer
         pages_needed = int(w.pages_per_req.sum()) - max(w.shared_requests - 1, 0) * (w.shared_tokens // w.P)
         alloc = 2 * pages_needed * w.Hkv * w.P * w.D  # K + V, e4m3
@@ -45,10 +45,10 @@ def test_allocated_cache_bytes_equal_formula_for_every_paged_config():
         assert alloc == oracle.kv_bytes(1, w.Hkv, w.D, padded_tokens, 1)
         if all(int(L) % w.P == 0 for L in w.context_lens) and w.shared_requests == 0:
             assert alloc == w.kv_bytes(1)
-    w2 = synth.config(2)
+    w2 = synth.workload(synth.MHA_B32)
     assert w2.kv_bytes(1) == 3_221_225_472
     assert w2.kv_bytes(2) == 2 * w2.kv_bytes(1)
-    assert synth.config(5).kv_bytes(1) == 11_542_724_608
+    assert synth.workload(synth.LONG_SPLITKV).kv_bytes(1) == 11_542_724_608
 
 
 def test_generator_is_deterministic_and_roughly_standard_normal():
@@ -71,8 +71,8 @@ def test_bf16_rounding_matches_torch_cast():
 
 
 def test_workload_tables_are_valid():
-    for n in (1, 2, 3, 5):
-        w = synth.config(n)
+    for name in (synth.TINY_GQA, synth.MHA_B32, synth.GQA_PREFIX, synth.LONG_SPLITKV):
+        w = synth.workload(name)
         used = []
         for b in range(w.B):
             npg = int(w.pages_per_req[b])
@@ -83,17 +83,17 @@ def test_workload_tables_are_valid():
         u = np.concatenate(used)
         shared_dups = max(w.shared_requests - 1, 0) * (w.shared_tokens // w.P)
         assert len(np.unique(u)) == len(u) - shared_dups
-    w3 = synth.config(3)
+    w3 = synth.workload(synth.GQA_PREFIX)
     assert np.all(w3.context_lens >= 256) and np.all(w3.context_lens <= 32768)
     assert np.all(w3.context_lens[:16] >= 2048 + 16)
     assert np.all(w3.block_tables[1:16, :128] == w3.block_tables[0, :128])
     assert 2000 < np.median(w3.context_lens) < 8000
-    w1 = synth.config(1)
+    w1 = synth.workload(synth.TINY_GQA)
     assert np.all((w1.context_lens >= 16) & (w1.context_lens <= 300)) and w1.num_pages == 128
 
 
 def test_mla_topk_lists_are_unique_sorted_in_range():
-    m = synth.config(4)
+    m = synth.workload(synth.MLA_TOPK)
     assert m.topk.shape == (64, 2048)
     assert np.all(np.diff(m.topk, axis=1) > 0)
     assert m.topk.min() >= 0 and m.topk.max() < 65536
@@ -102,7 +102,7 @@ def test_mla_topk_lists_are_unique_sorted_in_range():
 
 
 def test_slots_follow_block_tables_and_shared_tokens_map_to_request_0():
-    w = synth.config(3)
+    w = synth.workload(synth.GQA_PREFIX)
     sl = w.slots(5, 100, 140)
     t = np.arange(100, 140)
     assert np.array_equal(sl, w.block_tables[5, t // 16].astype(np.int64) * 16 + t % 16)
@@ -125,7 +125,7 @@ def test_host_c_generator_twin_matches_numpy_definition():
 
 
 def test_workload_rows_follow_the_documented_counter_layout():
-    w = synth.config(3)
+    w = synth.workload(synth.GQA_PREFIX)
     b, t0, t1 = 20, 100, 131
     idx = (((np.int64(b) << 21) + np.arange(t0, t1))[:, None] * (w.Hkv * w.D)
            + np.arange(w.Hkv * w.D)[None, :]).astype(np.uint64)
