@@ -109,6 +109,14 @@ def test_few_rows_whole_prompt_is_new():
     _check_small(w, q_lens=np.array([1, 7, 8]), max_q=8)
 
 
+@pytest.mark.parametrize("Hq,Hkv,n_new", [(4, 4, 64), (8, 4, 32), (32, 2, 4), (64, 1, 1)])
+def test_few_rows_across_group_sizes(Hq, Hkv, n_new):
+    # G x n_new = 64 rows per block for G = 1, 2, 16, 64; contexts end mid-tile
+    w = _w(f"wide_g{Hq // Hkv}", Hq, Hkv, (70, 129, 300), n_new=n_new)
+    _check_small(w)
+    _check_small(w, split=128)
+
+
 def test_half_height_units_of_the_one_block_kernel():
     # G 16 x 8 queries = 128 rows per block, but requests 1 and 2 have 48 and
     # 16 rows: their units take the half-height products of the one-block kernel
