@@ -37,6 +37,7 @@
 // so that each widened tile feeds both and two softmax groups overlap.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "pfkv_internal.h"
 #include "pfkv_ptx.cuh"
@@ -964,39 +965,45 @@ __global__ void __launch_bounds__(k2Threads, 1)
 // thread can pack its own P pairs, the contraction order of P.V swaps the
 // middle two tokens of every group of four: P column pair (4r + 2e, 4r + 2e + 1)
 // holds tokens (4r + e, 4r + e + 2), and row 4r + i of the widened V tile holds
-// token 4r + (i with its two low bits swapped).  Only two tiles fit in shared
-// memory, so each resource is released as soon as its last reader is done:
+// token 4r + (i with its two low bits swapped).  The score products read the
+// e4m3 K rows straight from the TMA stage (kind::f8f6f4): each Q row is
+// scaled by a power of two and split exactly into three e4m3 parts, so
+// S = sum over the parts of part . K, accumulated in fp32, and only V is
+// widened to f16.  Each resource is released as soon as its last reader is done:
 //   * P has tensor-memory columns of its own: a score buffer is free once the
 //     softmax warps have read it, not once P.V has run;
-//   * the K and V halves of a widened tile are filled and freed separately
-//     (K after its score product, V after its P.V product).
-// tensor memory: two 128-column score buffers, O (128), Q (64), P (64).
-// shared memory: three 32 KB e4m3 stages, two 64 KB widened K/V tiles.
+//   * a stage is free once its K has been read by the score products and its
+//     V widened; a widened V tile once its P.V product has run.
+// tensor memory: two 128-column score buffers, O (128), P (64).
+// shared memory: four 32 KB e4m3 stages, two 32 KB widened V tiles, Q's parts (24 KB).
 constexpr int kWTok = 128;                      // tokens per tile
 constexpr int kWBoxes = kWTok / kBoxTok;        // 8 TMA boxes per tensor
-constexpr int kWStages = 3;
+constexpr int kWStages = 4;
 constexpr int kWStageBytes = 2 * kWTok * kD;    // K + V e4m3: 32 KB
 constexpr int kWAtom = kWTok * 128;             // [128 tokens][64 f16]: 16 KB
-constexpr int kWBufBytes = 4 * kWAtom;          // K (2 atoms) + V (2 atoms): 64 KB
+constexpr int kWVBytes = 2 * kWAtom;            // widened V (2 atoms): 32 KB
+constexpr int kWQPart = 64 * 128;               // one e4m3 part of Q: [64 rows][128 bytes], 8 KB
 constexpr int kWBufs = 2;
-constexpr int kWOffKv = 0;
-constexpr int kWOffStage = kWOffKv + kWBufs * kWBufBytes;
-constexpr int kWOffBars = kWOffStage + kWStages * kWStageBytes;
+constexpr int kWOffV = 0;
+constexpr int kWOffStage = kWOffV + kWBufs * kWVBytes;
+constexpr int kWOffQ = kWOffStage + kWStages * kWStageBytes;  // three parts
+constexpr int kWOffQs = kWOffQ + 3 * kWQPart;                 // float[64]: each row's 1 / (Q scale)
+constexpr int kWOffBars = kWOffQs + 64 * 4;
 constexpr int kWSmemBytes = kWOffBars + 512 + 1024;
 static_assert(kWSmemBytes <= 232448, "shared memory over the per-CTA limit");
-constexpr uint32_t kWTmemS = 0, kWTmemO = kWBufs * kWTok, kWTmemQ = kWTmemO + kD, kWTmemP = kWTmemQ + kD / 2;
+constexpr uint32_t kWTmemS = 0, kWTmemO = kWBufs * kWTok, kWTmemP = kWTmemO + kD;
 static_assert(kWTmemP + kWTok / 2 <= kTmemCols, "tensor memory columns");
-constexpr uint32_t kIdescQKW = tc::idesc_f16(64, kWTok, false);
+constexpr uint32_t kIdescQKW = tc::idesc_f16(64, kWTok, false);  // with kind::f8f6f4: e4m3 x e4m3
 constexpr uint32_t kIdescPVW = tc::idesc_f16(64, kD, true);
 constexpr int kWConvWarps = 4;
 constexpr int kWProdWarp = 0, kWMmaWarp = 1, kWConvWarp0 = 2, kWSoftWarp0 = kWConvWarp0 + kWConvWarps,
               kWPvWarp = kWSoftWarp0 + 4;
 constexpr int kWThreads = (kWPvWarp + 1) * 32;
-constexpr int kWChunks = kWTok * kD / 16 / (32 * kWConvWarps);  // 16-byte chunks of K (or V) per converter thread
+constexpr int kWChunks = kWTok * kD / 16 / (32 * kWConvWarps);  // 16-byte chunks of V per converter thread
 
 struct BarsW {
   uint64_t stage_full[kWStages], stage_empty[kWStages];
-  uint64_t kfull[kWBufs], vfull[kWBufs];  // K / V half of a widened tile written
+  uint64_t vfull[kWBufs];                 // widened V of a tile written
   uint64_t sfull[kWBufs];                 // scores of a tile complete
   uint64_t sread[kWBufs];                 // the softmax warps have read a score buffer
   uint64_t pvdone[kWBufs];                // P.V of a tile complete (index: tile % 2)
@@ -1006,19 +1013,18 @@ struct BarsW {
 };
 static_assert(sizeof(BarsW) <= 512, "barrier block");
 
-// Widens 16-byte chunk rows of K (which = 0) or V (which = 1) of a stage into
-// the tile's f16 atoms (V rows in the P.V contraction order); rows at or past
-// `valid` become zeros.  All loads are
+// Widens the V rows of a stage into f16 atoms at dst, rows in the P.V
+// contraction order; rows at or past `valid` become zeros.  All loads are
 // issued before the first store: the compiler cannot move a load above a
 // store through another pointer into shared memory.
-__device__ __forceinline__ void widen_half(const uint8_t* stage, uint8_t* kv, int which, int ct, int valid) {
+__device__ __forceinline__ void widen_v(const uint8_t* vstage, uint8_t* dst, int ct, int valid) {
   uint4 v[kWChunks];
 #pragma unroll
   for (int m = 0; m < kWChunks; ++m) {
-    const int i = ct + 32 * kWConvWarps * m;  // chunk of this half: row i / 8, 16-byte chunk i % 8
+    const int i = ct + 32 * kWConvWarps * m;  // row i / 8, 16-byte chunk i % 8
     const int row = i >> 3, c = i & 7;
     v[m] = make_uint4(0, 0, 0, 0);
-    if (row < valid) v[m] = lds128(stage + which * (kWTok * kD) + (row >> 4) * kBoxBytes + swz(row & 15, c));
+    if (row < valid) v[m] = lds128(vstage + (row >> 4) * kBoxBytes + swz(row & 15, c));
   }
 #pragma unroll
   for (int m = 0; m < kWChunks; ++m) {
@@ -1029,11 +1035,19 @@ __device__ __forceinline__ void widen_half(const uint8_t* stage, uint8_t* kv, in
     e4m3x4_to_f16x2x2(v[m].y, o0.z, o0.w);
     e4m3x4_to_f16x2x2(v[m].z, o1.x, o1.y);
     e4m3x4_to_f16x2x2(v[m].w, o1.z, o1.w);
-    const int drow = which ? (row & ~3) | ((row & 1) << 1) | ((row >> 1) & 1) : row;
-    const uint32_t d = which * (2 * kWAtom) + atom_off(drow, 2 * c, kWAtom);
-    *reinterpret_cast<uint4*>(kv + d) = o0;
-    *reinterpret_cast<uint4*>(kv + (d ^ 16)) = o1;
+    const int drow = (row & ~3) | ((row & 1) << 1) | ((row >> 1) & 1);
+    const uint32_t d = atom_off(drow, 2 * c, kWAtom);
+    *reinterpret_cast<uint4*>(dst + d) = o0;
+    *reinterpret_cast<uint4*>(dst + (d ^ 16)) = o1;
   }
+}
+
+// e4m3 code pair (byte 0 -> lo) -> two floats (exact).
+__device__ __forceinline__ void e4m3x2_to_f32x2(uint16_t code, float& lo, float& hi) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(code));
+  lo = __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
+  hi = __half2float(__ushort_as_half((unsigned short)(h >> 16)));
 }
 
 __global__ void __launch_bounds__(kWThreads, 1)
@@ -1054,11 +1068,10 @@ __global__ void __launch_bounds__(kWThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kWStages; ++s) {
       mbar_init(smem_u32(&bs.stage_full[s]), 1);
-      mbar_init(smem_u32(&bs.stage_empty[s]), kWConvWarps);
+      mbar_init(smem_u32(&bs.stage_empty[s]), kWConvWarps + 1);  // V widened + the score products done
     }
     const int live_warps = min(4, (x.rows + 15) / 16);
     for (int k = 0; k < kWBufs; ++k) {
-      mbar_init(smem_u32(&bs.kfull[k]), kWConvWarps);
       mbar_init(smem_u32(&bs.vfull[k]), kWConvWarps);
       mbar_init(smem_u32(&bs.sfull[k]), 1);
       mbar_init(smem_u32(&bs.sread[k]), live_warps);
@@ -1124,30 +1137,35 @@ __global__ void __launch_bounds__(kWThreads, 1)
       if (!mbar_wait(smem_u32(&bs.stage_full[j % kWStages]), (j / kWStages) & 1)) to = true;
   } else if (warp == kWMmaWarp) {
     // ------------------------------------------------- score MMA issuer
-    // S(j) = Q . K(j)^T (N = 128) into buffer j % 2, once K(j) is widened and
-    // the softmax warps have read S(j - 2) from that buffer.
+    // S(j) = Q . K(j)^T (N = 128) into buffer j % 2, straight from the e4m3 K
+    // rows of the stage (kind::f8f6f4: Q in three exact e4m3 parts, four
+    // K = 32 steps each), once the stage has landed and the softmax warps have
+    // read S(j - 2) from that buffer.  A second commit releases the stage's K.
     if (lane == 0 && ntiles > 0) {
       if (!mbar_wait(smem_u32(&bs.qready), 0)) to = true;
-      const uint32_t kv0 = smem_u32(smem + kWOffKv);
+      const uint64_t qdesc = tc::desc_sw128(smem_u32(smem + kWOffQ), 16, 1024);
       for (int qn = 0; qn < ntiles && !to; ++qn) {
-        const int kb = qn % kWBufs;
-        if (!mbar_wait(smem_u32(&bs.kfull[kb]), (qn / kWBufs) & 1)) to = true;
+        const int kb = qn % kWBufs, st = qn % kWStages;
+        if (!mbar_wait(smem_u32(&bs.stage_full[st]), (qn / kWStages) & 1)) to = true;
         if (qn >= kWBufs && !to && !mbar_wait(smem_u32(&bs.sread[kb]), ((qn - kWBufs) / kWBufs) & 1)) to = true;
         if (to) break;
         tc::fence_after_sync();
-        const uint64_t kdesc = tc::desc_sw128(kv0 + kb * kWBufBytes, 16, 1024);
+        const uint64_t kdesc = tc::desc_sw128(smem_u32(smem + kWOffStage + st * kWStageBytes), 16, 1024);
 #pragma unroll
-        for (int k = 0; k < kD / 16; ++k)
-          tc::mma_ts(tmem + kWTmemS + kWTok * kb, tmem + kWTmemQ + 8 * k,
-                     kdesc + (uint64_t)(((k >> 2) * kWAtom + 32 * (k & 3)) >> 4), kIdescQKW, k > 0 ? 1u : 0u);
+        for (int p = 0; p < 3; ++p)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            tc::mma_ss_e4m3(tmem + kWTmemS + kWTok * kb, qdesc + (uint64_t)((p * kWQPart + 32 * k) >> 4),
+                            kdesc + (uint64_t)((32 * k) >> 4), kIdescQKW, (p > 0 || k > 0) ? 1u : 0u);
         tc::mma_commit(smem_u32(&bs.sfull[kb]));
+        tc::mma_commit(smem_u32(&bs.stage_empty[st]));
       }
     }
     __syncwarp();
   } else if (warp == kWPvWarp) {
     // ---------------------------------------------------- P.V MMA issuer
     if (lane == 0 && ntiles > 0) {
-      const uint32_t kv0 = smem_u32(smem + kWOffKv);
+      const uint32_t v0 = smem_u32(smem + kWOffV);
       int pn = 0;
       for (; pn < ntiles && !to; ++pn) {
         const int kb = pn % kWBufs;
@@ -1156,7 +1174,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
           break;
         }
         tc::fence_after_sync();
-        const uint64_t vdesc = tc::desc_sw128(kv0 + kb * kWBufBytes + 2 * kWAtom, kWAtom, 1024);
+        const uint64_t vdesc = tc::desc_sw128(v0 + kb * kWVBytes, kWAtom, 1024);
 #pragma unroll
         for (int k = 0; k < kWTok / 16; ++k)
           tc::mma_ts(tmem + kWTmemO, tmem + kWTmemP + 8 * k, vdesc + (uint64_t)((2048 * k) >> 4), kIdescPVW,
@@ -1168,25 +1186,15 @@ __global__ void __launch_bounds__(kWThreads, 1)
     __syncwarp();
   } else if (warp < kWSoftWarp0) {
     // ---------------------------------------------------------- converters
-    // K(j) once S(j - 2) has completed, V(j) once P.V(j - 2) has.
+    // V(j) once the stage has landed and P.V(j - 2) has completed (its buffer).
     const int ct = threadIdx.x - kWConvWarp0 * 32;
     for (int j = 0; j < ntiles && !to; ++j) {
       const int st = j % kWStages, kb = j % kWBufs;
       if (!warp_wait(smem_u32(&bs.stage_full[st]), (j / kWStages) & 1)) to = true;
-      if (j >= kWBufs && !to && !warp_wait(smem_u32(&bs.sfull[kb]), ((j - kWBufs) / kWBufs) & 1)) to = true;
+      if (j >= kWBufs && !to && !warp_wait(smem_u32(&bs.pvdone[kb]), ((j - kWBufs) / kWBufs) & 1)) to = true;
       if (to) break;
       const int valid = min(kWTok, x.t_hi - (x.t_lo + j * kWTok));
-      const uint8_t* stage = smem + kWOffStage + st * kWStageBytes;
-      uint8_t* kv = smem + kWOffKv + kb * kWBufBytes;
-      widen_half(stage, kv, 0, ct, valid);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.kfull[kb]));
-      if (j >= kWBufs && !warp_wait(smem_u32(&bs.pvdone[kb]), ((j - kWBufs) / kWBufs) & 1)) {
-        to = true;
-        break;
-      }
-      widen_half(stage, kv, 1, ct, valid);
+      widen_v(smem + kWOffStage + st * kWStageBytes + kWTok * kD, smem + kWOffV + kb * kWVBytes, ct, valid);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -1198,29 +1206,62 @@ __global__ void __launch_bounds__(kWThreads, 1)
     // -------------------------------------------------- softmax + epilogue
     const int quad = warp & 3;
     const uint32_t trow = tmem + ((uint32_t)(32 * quad) << 16);
-    // Q: thread t < 16 writes row 16 quad + t into its own lane (the lanes
-    // half-height products read), zeros elsewhere
+    // Q: thread t < 16 splits row 16 quad + t exactly into three e4m3 parts
+    // (x = q s with s a power of two taking max |q| into (224, 448]; part 1 =
+    // e4m3(x), part 2 = e4m3(x - part 1), part 3 = e4m3 of what is left),
+    // written as the A operands of the score products, and records 1 / s
+    float* const qinv = reinterpret_cast<float*>(smem + kWOffQs);
     {
       const int rq = 16 * quad + (lane & 15);
       const bool okq = lane < 16 && rq < x.rows;
       const int64_t hq = ((int64_t)a.q_start[x.b] + x.i0 + rq / a.G) * a.Hq + (int64_t)x.kvh * a.G + rq % a.G;
       const uint4* qp = reinterpret_cast<const uint4*>(a.q + hq * kD);
+      float amax = 0.f;
+      if (okq) {
+#pragma unroll 4
+        for (int uu = 0; uu < 16; ++uu) {
+          const uint4 w = __ldg(qp + uu);
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t f[32];
-#pragma unroll
-        for (int uu = 0; uu < 8; ++uu) {
-          uint4 w = make_uint4(0, 0, 0, 0);
-          if (okq) w = __ldg(qp + 8 * half + uu);
-          f[4 * uu] = pack_f16x2(bf16_lo(w.x), bf16_hi(w.x));
-          f[4 * uu + 1] = pack_f16x2(bf16_lo(w.y), bf16_hi(w.y));
-          f[4 * uu + 2] = pack_f16x2(bf16_lo(w.z), bf16_hi(w.z));
-          f[4 * uu + 3] = pack_f16x2(bf16_lo(w.w), bf16_hi(w.w));
+          for (int k = 0; k < 4; ++k) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(ww[k])), fabsf(bf16_hi(ww[k]))));
         }
-        tc::tmem_st32(trow + kWTmemQ + 32 * half, f);
       }
-      tc::tmem_st_wait();
-      tc::fence_before_sync();
+      // s = 2^floor(log2(448 / amax)), at least 2^-126 (1 for a zero row)
+      const float s =
+          amax > 0.f ? fmaxf(__uint_as_float(__float_as_uint(448.f / amax) & 0x7F800000u), 1.17549435e-38f) : 1.f;
+      if (lane < 16) {
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {  // 16 elements per 16-byte chunk
+          uint32_t p1[4] = {0u, 0u, 0u, 0u}, p2[4] = {0u, 0u, 0u, 0u}, p3[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint4 w = make_uint4(0, 0, 0, 0);
+            if (okq) w = __ldg(qp + 2 * c + h);
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {  // elements 8 h + 2 k and 8 h + 2 k + 1 of the chunk
+              const float x0 = bf16_lo(ww[k]) * s, x1 = bf16_hi(ww[k]) * s;
+              const uint16_t c1 = f32x2_to_e4m3x2(x0, x1);
+              float d0, d1;
+              e4m3x2_to_f32x2(c1, d0, d1);
+              const float r0 = x0 - d0, r1 = x1 - d1;  // exact
+              const uint16_t c2 = f32x2_to_e4m3x2(r0, r1);
+              e4m3x2_to_f32x2(c2, d0, d1);
+              const uint16_t c3 = f32x2_to_e4m3x2(r0 - d0, r1 - d1);
+              const int word = 2 * h + (k >> 1), sh = 16 * (k & 1);
+              p1[word] |= (uint32_t)c1 << sh;
+              p2[word] |= (uint32_t)c2 << sh;
+              p3[word] |= (uint32_t)c3 << sh;
+            }
+          }
+          const uint32_t off = rq * 128 + 16 * (c ^ (rq & 7));  // 128-byte swizzle
+          *reinterpret_cast<uint4*>(smem + kWOffQ + off) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
+          *reinterpret_cast<uint4*>(smem + kWOffQ + kWQPart + off) = make_uint4(p2[0], p2[1], p2[2], p2[3]);
+          *reinterpret_cast<uint4*>(smem + kWOffQ + 2 * kWQPart + off) = make_uint4(p3[0], p3[1], p3[2], p3[3]);
+        }
+        qinv[rq] = okq ? 1.f / s : 0.f;  // exact: s is a power of two
+      }
+      fence_proxy_async_smem();  // generic writes -> visible to the tensor core
       __syncwarp();
       if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.qready));
     }
@@ -1232,7 +1273,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
     const bool okm = rm < x.rows;
     const int im = x.i0 + rm / a.G;
     const int limm = okm ? min(x.L - x.n + im + 1, x.t_end_chunk) : x.t_lo;
-    const float sc = a.score_scale;
+    const float sc = a.score_scale * qinv[rm];  // the scores carry the row's Q scale s
     float mref = -INFINITY, rthr = -INFINITY, lpart = 0.f;  // lpart: this thread's share of the row sum
     // O row 16 quad + t (t < 16) sits in lane t of the quadrant; its statistics
     // are held by thread 4 (t % 8) + t / 8
