@@ -967,15 +967,20 @@ __global__ void __launch_bounds__(k2Threads, 1)
 // holds tokens (4r + e, 4r + e + 2), and row 4r + i of the widened V tile holds
 // token 4r + (i with its two low bits swapped).  The score products read the
 // e4m3 K rows straight from the TMA stage (kind::f8f6f4): each Q row is
-// scaled by a power of two and split exactly into three e4m3 parts, so
-// S = sum over the parts of part . K, accumulated in fp32, and only V is
+// scaled by a power of two (its largest element into (224, 448]) and split
+// into two e4m3 parts: a bf16 value has 8 significant bits and each part holds
+// 4 (the remainder after rounding to the first is at most half its last unit),
+// so the split is exact for every scaled element above 0.25 (checked over all
+// bf16 values); smaller ones, below 1/896 of the row's largest, are off by at
+// most half e4m3's subnormal step, 2^-10, under 2^-17 of the largest; so
+// S = part 1 . K + part 2 . K, accumulated in fp32, and only V is
 // widened to f16.  Each resource is released as soon as its last reader is done:
 //   * P has tensor-memory columns of its own: a score buffer is free once the
 //     softmax warps have read it, not once P.V has run;
 //   * a stage is free once its K has been read by the score products and its
 //     V widened; a widened V tile once its P.V product has run.
 // tensor memory: two 128-column score buffers, O (128), P (64).
-// shared memory: four 32 KB e4m3 stages, two 32 KB widened V tiles, Q's parts (24 KB).
+// shared memory: four 32 KB e4m3 stages, two 32 KB widened V tiles, Q's parts (16 KB).
 constexpr int kWTok = 128;                      // tokens per tile
 constexpr int kWBoxes = kWTok / kBoxTok;        // 8 TMA boxes per tensor
 constexpr int kWStages = 4;
@@ -986,8 +991,8 @@ constexpr int kWQPart = 64 * 128;               // one e4m3 part of Q: [64 rows]
 constexpr int kWBufs = 2;
 constexpr int kWOffV = 0;
 constexpr int kWOffStage = kWOffV + kWBufs * kWVBytes;
-constexpr int kWOffQ = kWOffStage + kWStages * kWStageBytes;  // three parts
-constexpr int kWOffQs = kWOffQ + 3 * kWQPart;                 // float[64]: each row's 1 / (Q scale)
+constexpr int kWOffQ = kWOffStage + kWStages * kWStageBytes;  // two parts
+constexpr int kWOffQs = kWOffQ + 2 * kWQPart;                 // float[64]: each row's 1 / (Q scale)
 constexpr int kWOffBars = kWOffQs + 64 * 4;
 constexpr int kWSmemBytes = kWOffBars + 512 + 1024;
 static_assert(kWSmemBytes <= 232448, "shared memory over the per-CTA limit");
@@ -1138,7 +1143,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
   } else if (warp == kWMmaWarp) {
     // ------------------------------------------------- score MMA issuer
     // S(j) = Q . K(j)^T (N = 128) into buffer j % 2, straight from the e4m3 K
-    // rows of the stage (kind::f8f6f4: Q in three exact e4m3 parts, four
+    // rows of the stage (kind::f8f6f4: Q in two exact e4m3 parts, four
     // K = 32 steps each), once the stage has landed and the softmax warps have
     // read S(j - 2) from that buffer.  A second commit releases the stage's K.
     if (lane == 0 && ntiles > 0) {
@@ -1152,7 +1157,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
         tc::fence_after_sync();
         const uint64_t kdesc = tc::desc_sw128(smem_u32(smem + kWOffStage + st * kWStageBytes), 16, 1024);
 #pragma unroll
-        for (int p = 0; p < 3; ++p)
+        for (int p = 0; p < 2; ++p)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             tc::mma_ss_e4m3(tmem + kWTmemS + kWTok * kb, qdesc + (uint64_t)((p * kWQPart + 32 * k) >> 4),
@@ -1206,9 +1211,9 @@ __global__ void __launch_bounds__(kWThreads, 1)
     // -------------------------------------------------- softmax + epilogue
     const int quad = warp & 3;
     const uint32_t trow = tmem + ((uint32_t)(32 * quad) << 16);
-    // Q: thread t < 16 splits row 16 quad + t exactly into three e4m3 parts
-    // (x = q s with s a power of two taking max |q| into (224, 448]; part 1 =
-    // e4m3(x), part 2 = e4m3(x - part 1), part 3 = e4m3 of what is left),
+    // Q: thread t < 16 splits row 16 quad + t into two e4m3 parts (x = q s
+    // with s a power of two taking max |q| into (224, 448]; part 1 = e4m3(x),
+    // part 2 = e4m3(x - part 1) = x - part 1),
     // written as the A operands of the score products, and records 1 / s
     float* const qinv = reinterpret_cast<float*>(smem + kWOffQs);
     {
@@ -1232,7 +1237,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
       if (lane < 16) {
 #pragma unroll 1
         for (int c = 0; c < 8; ++c) {  // 16 elements per 16-byte chunk
-          uint32_t p1[4] = {0u, 0u, 0u, 0u}, p2[4] = {0u, 0u, 0u, 0u}, p3[4] = {0u, 0u, 0u, 0u};
+          uint32_t p1[4] = {0u, 0u, 0u, 0u}, p2[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             uint4 w = make_uint4(0, 0, 0, 0);
@@ -1244,20 +1249,15 @@ __global__ void __launch_bounds__(kWThreads, 1)
               const uint16_t c1 = f32x2_to_e4m3x2(x0, x1);
               float d0, d1;
               e4m3x2_to_f32x2(c1, d0, d1);
-              const float r0 = x0 - d0, r1 = x1 - d1;  // exact
-              const uint16_t c2 = f32x2_to_e4m3x2(r0, r1);
-              e4m3x2_to_f32x2(c2, d0, d1);
-              const uint16_t c3 = f32x2_to_e4m3x2(r0 - d0, r1 - d1);
+              const uint16_t c2 = f32x2_to_e4m3x2(x0 - d0, x1 - d1);  // the difference is exact
               const int word = 2 * h + (k >> 1), sh = 16 * (k & 1);
               p1[word] |= (uint32_t)c1 << sh;
               p2[word] |= (uint32_t)c2 << sh;
-              p3[word] |= (uint32_t)c3 << sh;
             }
           }
           const uint32_t off = rq * 128 + 16 * (c ^ (rq & 7));  // 128-byte swizzle
           *reinterpret_cast<uint4*>(smem + kWOffQ + off) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
           *reinterpret_cast<uint4*>(smem + kWOffQ + kWQPart + off) = make_uint4(p2[0], p2[1], p2[2], p2[3]);
-          *reinterpret_cast<uint4*>(smem + kWOffQ + 2 * kWQPart + off) = make_uint4(p3[0], p3[1], p3[2], p3[3]);
         }
         qinv[rq] = okq ? 1.f / s : 0.f;  // exact: s is a power of two
       }
