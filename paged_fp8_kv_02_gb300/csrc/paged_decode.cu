@@ -335,6 +335,7 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 2)
   int chunk_left = 0;  // tiles left in the current unit, including the current one
   int64_t seg_begin = f_begin;
   float sc = a.score_scale;  // unit mode: set per unit from the device K scale
+  float qinv = 1.f;          // e4m3 cache: 1 / (the unit's power-of-two Q scale)
   float unit_vs = 1.f;       // unit mode: the unit's V scale
   float vref = 0.f, vinv = 0.f;  // token mode: largest V scale of the unit so far, 1 / it
 
@@ -462,13 +463,55 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 2)
       const uint32_t wd[16] = {r[0].x, r[0].y, r[0].z, r[0].w, r[1].x, r[1].y, r[1].z, r[1].w,
                                r[2].x, r[2].y, r[2].z, r[2].w, r[3].x, r[3].y, r[3].z, r[3].w};
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        if constexpr (kBf16) {
-          qf[j][ks][0] = wd[2 * ks];
-          qf[j][ks][1] = wd[2 * ks + 1];
-        } else {
-          qf[j][ks][0] = pack_f16x2(bf16_lo(wd[2 * ks]), bf16_hi(wd[2 * ks]));
-          qf[j][ks][1] = pack_f16x2(bf16_lo(wd[2 * ks + 1]), bf16_hi(wd[2 * ks + 1]));
+      for (int i = 0; i < 16; ++i) qf[j][i >> 1][i & 1] = wd[i];  // bf16 pairs (the e4m3 cache splits them below)
+    }
+    if constexpr (!kBf16) {
+      // Q as two exact e4m3 parts for the e4m3 products on the raw K bytes:
+      // x = q s, s = 2^floor(log2(448 / max |q|)) over the unit's heads;
+      // part 1 = e4m3(x), part 2 = e4m3(x - part 1) (a bf16 value has 8
+      // significant bits, each part 4).  Register pair (2 kk + p) holds part p
+      // of head_dim values 32t + 8kk .. 32t + 8kk + 7, the K elements that
+      // the e4m3 product's k 4t.. and 16 + 4t.. pick in step kk.
+      float amax = 0.f;
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(qf[j][i >> 1][i & 1])), fabsf(bf16_hi(qf[j][i >> 1][i & 1]))));
+#pragma unroll
+      for (int o2 = 16; o2 >= 1; o2 >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o2));
+      const float s = amax > 0.f ? fmaxf(__uint_as_float(__float_as_uint(448.f / amax) & 0x7F800000u),
+                                         1.17549435e-38f)
+                                 : 1.f;
+      qinv = 1.f / s;  // exact: s is a power of two
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        uint32_t wq[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) wq[i] = qf[j][i >> 1][i & 1];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          uint32_t p1[2], p2[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {  // bf16 pairs wq[4kk + 2h], wq[4kk + 2h + 1]: four values
+            uint32_t c1w = 0u, c2w = 0u;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const uint32_t w = wq[4 * kk + 2 * h + e];
+              const float x0 = bf16_lo(w) * s, x1 = bf16_hi(w) * s;
+              const uint16_t c1 = f32x2_to_e4m3x2(x0, x1);
+              const uint32_t hf = e4m3x2_to_f16x2(c1);
+              const uint16_t c2 = f32x2_to_e4m3x2(x0 - f16_lo(hf), x1 - f16_hi(hf));  // exact difference
+              c1w |= (uint32_t)c1 << (16 * e);
+              c2w |= (uint32_t)c2 << (16 * e);
+            }
+            p1[h] = c1w;
+            p2[h] = c2w;
+          }
+          qf[j][2 * kk][0] = p1[0];
+          qf[j][2 * kk][1] = p1[1];
+          qf[j][2 * kk + 1][0] = p2[0];
+          qf[j][2 * kk + 1][1] = p2[1];
         }
       }
     }
@@ -521,13 +564,23 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 2)
       const uint4 y0 = lds128(kb + swz(g + 8, 2 * t)), y1 = lds128(kb + swz(g + 8, 2 * t + 1));
       const uint32_t xr[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
       const uint32_t yr[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+      // the K bytes feed the e4m3 products as they are: step kk takes head_dim
+      // 32t + 8kk .. 32t + 8kk + 7 of rows g and g + 8, against Q's two parts
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        uint32_t a0, a1, a2, a3;
-        e4m3x4_to_f16x2x2(xr[ks], a0, a2);
-        e4m3x4_to_f16x2x2(yr[ks], a1, a3);
+      for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
-        for (int j = 0; j < NT; ++j) mma_f16(s[j], a0, a1, a2, a3, qf[j][ks][0], qf[j][ks][1]);
+        for (int j = 0; j < NT; ++j) {
+          mma_e4m3(s[j], xr[2 * kk], yr[2 * kk], xr[2 * kk + 1], yr[2 * kk + 1], qf[j][2 * kk][0], qf[j][2 * kk][1]);
+          mma_e4m3(s[j], xr[2 * kk], yr[2 * kk], xr[2 * kk + 1], yr[2 * kk + 1], qf[j][2 * kk + 1][0],
+                   qf[j][2 * kk + 1][1]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {  // undo the Q scale (a power of two: exact)
+        s[j][0] *= qinv;
+        s[j][1] *= qinv;
+        s[j][2] *= qinv;
+        s[j][3] *= qinv;
       }
     }
 
