@@ -555,21 +555,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------ two row blocks per CTA
 // For several row blocks per (request, KV head) -- a chunked-prefill step --
 // a CTA takes two neighbouring blocks A and B over the same KV chunk: every
-// widened K/V tile feeds the products of both blocks, and two groups of four
-// softmax warps (each with its own rows, O accumulator and score buffers) run
-// side by side, so the softmax of one block overlaps the other's.
+// K/V tile feeds the products of both blocks, and two groups of four softmax
+// warps (each with its own rows, O accumulator and score buffers) run side by
+// side, so the softmax of one block overlaps the other's.  The score products
+// are e4m3 (kind::f8f6f4) on the K rows of the TMA stage, against each Q row
+// split exactly into two e4m3 parts (as in prefillw_kernel below); only V is
+// widened to f16.
 //   tensor memory: block X in columns 256 X .. 256 X + 255: two 64-column
-//   score / P buffers, then O (128 columns); Q of both blocks in shared memory
-//   (the A operand of the score products).
+//   score / P buffers, then O (128 columns); Q's parts of both blocks in
+//   shared memory (the A operands of the score products).
 //   warps: 0 producer, 1 score MMAs, 2-5 widening, 6-9 softmax of block A,
 //   10-13 softmax of block B, 14 P.V MMAs.
-constexpr int k2KvBufs = 3;
-constexpr int k2Stages = 3;
+constexpr int k2KvBufs = 3;            // widened V tiles
+constexpr int k2Stages = 6;
 constexpr int k2SBufs = 2;
-constexpr int k2QAtom = kRows * 128;  // [128 rows][64 f16] swizzled atom: 16 KB
-constexpr int k2OffQ = 0;             // block X: 2 atoms at 2 X k2QAtom
+constexpr int k2QAtom = kRows * 128;  // [128 rows][128 bytes] swizzled atom: 16 KB
+constexpr int k2OffQ = 0;             // block X: its two e4m3 parts of Q at (2 X + p) k2QAtom
+constexpr int k2VBufBytes = 2 * kKvAtom;  // widened V of a tile (2 atoms): 16 KB
 constexpr int k2OffKv = k2OffQ + 4 * k2QAtom;
-constexpr int k2OffStage = k2OffKv + k2KvBufs * kKvBufBytes;
+constexpr int k2OffStage = k2OffKv + k2KvBufs * k2VBufBytes;
 constexpr int k2OffBars = k2OffStage + k2Stages * kStageBytes;
 constexpr int k2SmemBytes = k2OffBars + 512 + 1024;
 constexpr int k2ProdWarp = 0, k2MmaWarp = 1, k2ConvWarp0 = 2, k2SoftWarp0 = 6, k2PvWarp = 14;
@@ -584,6 +588,34 @@ struct Bars2 {
   uint32_t tmem_base;
 };
 static_assert(sizeof(Bars2) <= 512, "barrier block");
+
+// Widens the V rows of a 64-token stage (thread ct of the four converter
+// warps takes 16-byte chunks i = ct + 128 m: row i / 8, chunk c = i % 8) into
+// units 2(c % 4), 2(c % 4) + 1 of atom c / 4 at dst; rows at or past `valid`
+// become zeros.  Loads first, then stores (see widen_tile64).
+__device__ __forceinline__ void widen_v64(const uint8_t* vstage, uint8_t* dst, int ct, int valid) {
+  uint4 v[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const int i = ct + 128 * m;
+    const int row = i >> 3, c = i & 7;
+    v[m] = make_uint4(0, 0, 0, 0);
+    if (row < valid) v[m] = lds128(vstage + (row >> 4) * kBoxBytes + swz(row & 15, c));
+  }
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const int i = ct + 128 * m;
+    const int row = i >> 3, c = i & 7;
+    uint4 o0, o1;
+    e4m3x4_to_f16x2x2(v[m].x, o0.x, o0.y);
+    e4m3x4_to_f16x2x2(v[m].y, o0.z, o0.w);
+    e4m3x4_to_f16x2x2(v[m].z, o1.x, o1.y);
+    e4m3x4_to_f16x2x2(v[m].w, o1.z, o1.w);
+    const uint32_t d = atom_off(row, 2 * c, kKvAtom);
+    *reinterpret_cast<uint4*>(dst + d) = o0;
+    *reinterpret_cast<uint4*>(dst + (d ^ 16)) = o1;
+  }
+}
 
 __global__ void __launch_bounds__(k2Threads, 1)
     prefill2_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -614,10 +646,10 @@ __global__ void __launch_bounds__(k2Threads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < k2Stages; ++s) {
       mbar_init(smem_u32(&bs.stage_full[s]), 1);
-      mbar_init(smem_u32(&bs.stage_empty[s]), 4);
+      mbar_init(smem_u32(&bs.stage_empty[s]), 5);  // V widened + both blocks' score products done
     }
     for (int k = 0; k < k2KvBufs; ++k) {
-      mbar_init(smem_u32(&bs.kvfull[k]), 4);
+      mbar_init(smem_u32(&bs.kvfull[k]), 4);  // V widened
       mbar_init(smem_u32(&bs.kvfree[k]), 1);
     }
     for (int X = 0; X < 2; ++X) {
@@ -686,17 +718,19 @@ __global__ void __launch_bounds__(k2Threads, 1)
       if (!mbar_wait(smem_u32(&bs.stage_full[j % k2Stages]), (j / k2Stages) & 1)) to = true;
   } else if (warp == k2MmaWarp) {
     // ------------------------------------------------- score MMA issuer
-    // S_X(j) = Q_X . K(j)^T for both blocks once the tile is widened and the
-    // block's score buffer is free (P.V_X(j - 2) has completed).
+    // S_X(j) = Q_X . K(j)^T for both blocks, e4m3 products (kind::f8f6f4) on
+    // the K rows of the stage against Q_X's two e4m3 parts, once the stage has
+    // landed and the block's score buffer is free (P.V_X(j - 2) has
+    // completed); a commit after both blocks releases the stage's K.
     if (lane == 0 && ntiles > 0) {
       if (!mbar_wait(smem_u32(&bs.qready), 0)) to = true;
-      const uint32_t kv0 = smem_u32(smem + k2OffKv);
       for (int j = 0; j < ntiles && !to; ++j) {
-        if (!mbar_wait(smem_u32(&bs.kvfull[j % k2KvBufs]), (j / k2KvBufs) & 1)) {
+        const int st = j % k2Stages;
+        if (!mbar_wait(smem_u32(&bs.stage_full[st]), (j / k2Stages) & 1)) {
           to = true;
           break;
         }
-        const uint64_t kdesc = tc::desc_sw128(kv0 + (j % k2KvBufs) * kKvBufBytes, 16, 1024);
+        const uint64_t kdesc = tc::desc_sw128(smem_u32(smem + k2OffStage + st * kStageBytes), 16, 1024);
         for (int X = 0; X < nblk && !to; ++X) {
           if (j >= k2SBufs &&
               !mbar_wait(smem_u32(&bs.pvdone[X][(j - k2SBufs) % k2SBufs]), ((j - k2SBufs) / k2SBufs) & 1)) {
@@ -706,11 +740,14 @@ __global__ void __launch_bounds__(k2Threads, 1)
           tc::fence_after_sync();
           const uint64_t qdesc = tc::desc_sw128(smem_u32(smem + k2OffQ + 2 * X * k2QAtom), 16, 1024);
 #pragma unroll
-          for (int k = 0; k < kD / 16; ++k)
-            tc::mma_ss(tmem + 256 * X + 64 * (j % k2SBufs), qdesc + (uint64_t)(((k >> 2) * k2QAtom + 32 * (k & 3)) >> 4),
-                       kdesc + (uint64_t)(((k >> 2) * kKvAtom + 32 * (k & 3)) >> 4), kIdescQK, k > 0 ? 1u : 0u);
+          for (int p = 0; p < 2; ++p)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              tc::mma_ss_e4m3(tmem + 256 * X + 64 * (j % k2SBufs), qdesc + (uint64_t)((p * k2QAtom + 32 * k) >> 4),
+                              kdesc + (uint64_t)((32 * k) >> 4), kIdescQK, (p > 0 || k > 0) ? 1u : 0u);
           tc::mma_commit(smem_u32(&bs.sfull[X][j % k2SBufs]));
         }
+        if (!to) tc::mma_commit(smem_u32(&bs.stage_empty[st]));
       }
     }
     __syncwarp();
@@ -720,7 +757,11 @@ __global__ void __launch_bounds__(k2Threads, 1)
       const uint32_t kv0 = smem_u32(smem + k2OffKv);
       int j = 0;
       for (; j < ntiles && !to; ++j) {
-        const uint64_t vdesc = tc::desc_sw128(kv0 + (j % k2KvBufs) * kKvBufBytes + 2 * kKvAtom, kKvAtom, 1024);
+        if (!mbar_wait(smem_u32(&bs.kvfull[j % k2KvBufs]), (j / k2KvBufs) & 1)) {  // V(j) widened
+          to = true;
+          break;
+        }
+        const uint64_t vdesc = tc::desc_sw128(kv0 + (j % k2KvBufs) * k2VBufBytes, kKvAtom, 1024);
         for (int X = 0; X < nblk && !to; ++X) {
           if (!mbar_wait(smem_u32(&bs.pfull[X][j % k2SBufs]), (j / k2SBufs) & 1)) {
             to = true;
@@ -733,7 +774,7 @@ __global__ void __launch_bounds__(k2Threads, 1)
                        vdesc + (uint64_t)((2048 * k) >> 4), kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
           tc::mma_commit(smem_u32(&bs.pvdone[X][j % k2SBufs]));
         }
-        // both products of the tile issued: the widened tile frees once they (and its score products) complete
+        // both products of the tile issued: the widened V frees once they complete
         if (!to) tc::mma_commit(smem_u32(&bs.kvfree[j % k2KvBufs]));
       }
       // no MMA may still be running when the tensor memory is freed
@@ -751,9 +792,7 @@ __global__ void __launch_bounds__(k2Threads, 1)
       if (j >= k2KvBufs && !to && !warp_wait(smem_u32(&bs.kvfree[kb]), ((j - k2KvBufs) / k2KvBufs) & 1)) to = true;
       if (to) break;
       const int valid = min(kTokN, t_hi - (xa.t_lo + j * kTokN));
-      const uint8_t* stage = smem + k2OffStage + st * kStageBytes;
-      uint8_t* kv = smem + k2OffKv + kb * kKvBufBytes;
-      widen_tile64(stage, kv, ct, valid);
+      widen_v64(smem + k2OffStage + st * kStageBytes + kTokN * kD, smem + k2OffKv + kb * k2VBufBytes, ct, valid);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -773,26 +812,53 @@ __global__ void __launch_bounds__(k2Threads, 1)
     const bool row_ok = r < xrows;
     const int i = x.i0 + r / a.G, g = r % a.G;
     const int64_t head_row = ((int64_t)a.q_start[x.b] + i) * a.Hq + (int64_t)x.kvh * a.G + g;
-    // Q row -> f16 -> the swizzled K-major A operand of this block (zeros for padding rows)
+    // Q row -> two exact e4m3 parts (x = q s, s = 2^floor(log2(448 / max |q|));
+    // part 1 = e4m3(x), part 2 = e4m3(x - part 1)) -> the swizzled K-major A
+    // operands of this block (zeros for padding rows); 1 / s joins the score scale
+    float qinv = 0.f;
     {
       const uint4* qp4 = reinterpret_cast<const uint4*>(a.q + head_row * kD);
+      float amax = 0.f;
+      if (row_ok) {
+#pragma unroll 4
+        for (int uu = 0; uu < 16; ++uu) {
+          const uint4 w = __ldg(qp4 + uu);
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-      for (int uu = 0; uu < 16; ++uu) {
-        uint4 w = make_uint4(0, 0, 0, 0);
-        if (row_ok) w = __ldg(qp4 + uu);
-        uint4 f;
-        f.x = pack_f16x2(bf16_lo(w.x), bf16_hi(w.x));
-        f.y = pack_f16x2(bf16_lo(w.y), bf16_hi(w.y));
-        f.z = pack_f16x2(bf16_lo(w.z), bf16_hi(w.z));
-        f.w = pack_f16x2(bf16_lo(w.w), bf16_hi(w.w));
-        *reinterpret_cast<uint4*>(smem + k2OffQ + 2 * X * k2QAtom + atom_off(r, uu, k2QAtom)) = f;
+          for (int k = 0; k < 4; ++k) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(ww[k])), fabsf(bf16_hi(ww[k]))));
+        }
+      }
+      const float qs =
+          amax > 0.f ? fmaxf(__uint_as_float(__float_as_uint(448.f / amax) & 0x7F800000u), 1.17549435e-38f) : 1.f;
+      qinv = row_ok ? 1.f / qs : 0.f;  // exact: qs is a power of two
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {  // 16 elements per 16-byte chunk
+        uint32_t p1[4] = {0u, 0u, 0u, 0u}, p2[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint4 w = make_uint4(0, 0, 0, 0);
+          if (row_ok) w = __ldg(qp4 + 2 * c + h);
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float x0 = bf16_lo(ww[k]) * qs, x1 = bf16_hi(ww[k]) * qs;
+            const uint16_t c1 = f32x2_to_e4m3x2(x0, x1);
+            const uint32_t hf = e4m3x2_to_f16x2(c1);
+            const uint16_t c2 = f32x2_to_e4m3x2(x0 - f16_lo(hf), x1 - f16_hi(hf));  // exact difference
+            p1[2 * h + (k >> 1)] |= (uint32_t)c1 << (16 * (k & 1));
+            p2[2 * h + (k >> 1)] |= (uint32_t)c2 << (16 * (k & 1));
+          }
+        }
+        const uint32_t off = r * 128 + 16 * (c ^ (r & 7));  // 128-byte swizzle
+        *reinterpret_cast<uint4*>(smem + k2OffQ + 2 * X * k2QAtom + off) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
+        *reinterpret_cast<uint4*>(smem + k2OffQ + (2 * X + 1) * k2QAtom + off) = make_uint4(p2[0], p2[1], p2[2], p2[3]);
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.qready));
     }
     const int lim = row_ok ? min(x.L - x.n + i + 1, x.t_end_chunk) : xa.t_lo;
-    const float sc = a.score_scale;
+    const float sc = a.score_scale * qinv;  // the scores carry the row's Q scale
     float mref = -INFINITY, rthr = -INFINITY, l = 0.f;
     const bool warp_live = 32 * quad < xrows;
     for (int j = 0; j < ntiles && !to && warp_live; ++j) {
