@@ -463,9 +463,14 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 2)
       const uint32_t wd[16] = {r[0].x, r[0].y, r[0].z, r[0].w, r[1].x, r[1].y, r[1].z, r[1].w,
                                r[2].x, r[2].y, r[2].z, r[2].w, r[3].x, r[3].y, r[3].z, r[3].w};
 #pragma unroll
-      for (int i = 0; i < 16; ++i) qf[j][i >> 1][i & 1] = wd[i];  // bf16 pairs (the e4m3 cache splits them below)
+      for (int i = 0; i < 16; ++i) {
+        if constexpr (!kBf16 && kScl == kSclToken)  // f16 pairs for the widened-K products
+          qf[j][i >> 1][i & 1] = pack_f16x2(bf16_lo(wd[i]), bf16_hi(wd[i]));
+        else
+          qf[j][i >> 1][i & 1] = wd[i];  // bf16 pairs (the e4m3 products split them below)
+      }
     }
-    if constexpr (!kBf16) {
+    if constexpr (!kBf16 && kScl != kSclToken) {
       // Q as two exact e4m3 parts for the e4m3 products on the raw K bytes:
       // x = q s, s = 2^floor(log2(448 / max |q|)) over the unit's heads;
       // part 1 = e4m3(x), part 2 = e4m3(x - part 1) (a bf16 value has 8
@@ -558,6 +563,21 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 2)
             mma_bf16(s[j], xr[2 * jj], yr[2 * jj], xr[2 * jj + 1], yr[2 * jj + 1], qf[j][ks][0],
                      qf[j][ks][1]);
         }
+      }
+    } else if constexpr (kScl == kSclToken) {
+      // per-token scales: K widened to f16 (this variant is at its register
+      // limit, where the e4m3 products' Q parts cost more than they save)
+      const uint4 x0 = lds128(kb + swz(g, 2 * t)), x1 = lds128(kb + swz(g, 2 * t + 1));
+      const uint4 y0 = lds128(kb + swz(g + 8, 2 * t)), y1 = lds128(kb + swz(g + 8, 2 * t + 1));
+      const uint32_t xr[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      const uint32_t yr[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        e4m3x4_to_f16x2x2(xr[ks], a0, a2);
+        e4m3x4_to_f16x2x2(yr[ks], a1, a3);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) mma_f16(s[j], a0, a1, a2, a3, qf[j][ks][0], qf[j][ks][1]);
       }
     } else {
       const uint4 x0 = lds128(kb + swz(g, 2 * t)), x1 = lds128(kb + swz(g, 2 * t + 1));
