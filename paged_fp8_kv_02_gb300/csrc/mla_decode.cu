@@ -129,6 +129,7 @@ struct __align__(8) Bars {
   uint64_t cfull[kBufs], sfull[kBufs], pfull[kBufs], pvdone[kBufs];
   uint64_t sent[kBufs];      // the sender warps have read the scores of a tile
   uint64_t qready;
+  float qinv[kRows];         // 1 / the power-of-two Q scale of each head row (this CTA's columns)
   uint64_t xfull[kXDepth];   // the peer's partial scores of a tile have landed
   uint64_t xack[kXDepth];    // the peer has read a tile this CTA sent
   uint64_t rdone[kXDepth];   // this CTA's softmax warps have read a received tile
@@ -151,7 +152,10 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) { return pack_f16x2(bf16_lo(v), bf16_hi(v)); }
+// bf16 pair times a power of two -> f16 pair
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v, float s) {
+  return pack_f16x2(bf16_lo(v) * s, bf16_hi(v) * s);
+}
 
 // Remote stores into a peer CTA's shared memory whose bytes are counted on
 // the peer's mbarrier when they land (no separate arrival needed).
@@ -483,8 +487,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // stored straight into the peer's receive buffer j % 3.
     const int t = threadIdx.x - kSendWarp0 * 32;  // head row = TMEM lane
     const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-    const float sc = a.score_scale;
     const uint32_t peer_recv0 = tc::mapa(smem_u32(smem + kOffRecv), peer);
+    if (!to) to = !mbar_wait(smem_u32(&bs.qready), 0);  // the rows' Q scales are written
+    const float sc = a.score_scale * bs.qinv[t];
     for (int j = 0; j < ntiles; ++j) {
       const int sb = j % kBufs, xb = j % kXDepth;
       if (!to) to = !mbar_wait(smem_u32(&bs.sfull[sb]), (j / kBufs) & 1);
@@ -528,32 +533,57 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------- softmax warps
     const int t = threadIdx.x - kSoftWarp0 * 32;  // head row = TMEM lane
     const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-    {  // Q: this CTA's latent columns into tensor memory, the rope into shared memory
+    // Q: this CTA's latent columns into tensor memory, the rope into shared
+    // memory, as f16.  A row whose largest |q| (over these columns) lies in
+    // [2^-4, 2^15] converts as it is: it fits f16 and every value at least
+    // 2^-10 of the largest is an exact f16 normal.  Any other row is
+    // converted again after a power-of-two scale qs taking its largest |q|
+    // into (2^14, 2^15]; 1 / qs joins this CTA's score scale (here and in
+    // the sender warps).
+    float qinv_row = 1.f;
+    {
       const bool have = t < a.H;
       const __nv_bfloat16* qrow = a.q + ((int64_t)b * a.H + (have ? t : 0)) * kDqk;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          uint4 x = make_uint4(0, 0, 0, 0);
-          if (have) x = ldg_nc(qrow + kLatCols * rank + 64 * c + 8 * u);
-          v[4 * u + 0] = bf16x2_to_f16x2(x.x);
-          v[4 * u + 1] = bf16x2_to_f16x2(x.y);
-          v[4 * u + 2] = bf16x2_to_f16x2(x.z);
-          v[4 * u + 3] = bf16x2_to_f16x2(x.w);
-        }
-        tc::tmem_st32(tl + kTmemQ + 32 * c, v);
-      }
       uint8_t* qr = smem + kOffQRope + t * 128;
+      float amax = 0.f;
+      auto convert = [&](float qs) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
 #pragma unroll
-      for (int u = 0; u < 8 * (int)rank; ++u) {
-        uint4 x = make_uint4(0, 0, 0, 0);
-        if (have) x = ldg_nc(qrow + kDv + 8 * u);
-        const uint4 y = make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z),
-                                   bf16x2_to_f16x2(x.w));
-        *reinterpret_cast<uint4*>(qr + 16 * (u ^ (t & 7))) = y;
+          for (int u = 0; u < 8; ++u) {
+            uint4 x = make_uint4(0, 0, 0, 0);
+            if (have) x = ldg_nc(qrow + kLatCols * rank + 64 * c + 8 * u);
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[k])), fabsf(bf16_hi(w[k]))));
+              v[4 * u + k] = bf16x2_to_f16x2(w[k], qs);
+            }
+          }
+          tc::tmem_st32(tl + kTmemQ + 32 * c, v);
+        }
+#pragma unroll
+        for (int u = 0; u < 8 * (int)rank; ++u) {
+          uint4 x = make_uint4(0, 0, 0, 0);
+          if (have) x = ldg_nc(qrow + kDv + 8 * u);
+          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[k])), fabsf(bf16_hi(w[k]))));
+          const uint4 y = make_uint4(bf16x2_to_f16x2(x.x, qs), bf16x2_to_f16x2(x.y, qs),
+                                     bf16x2_to_f16x2(x.z, qs), bf16x2_to_f16x2(x.w, qs));
+          *reinterpret_cast<uint4*>(qr + 16 * (u ^ (t & 7))) = y;
+        }
+      };
+      convert(1.f);
+      const bool rescale = amax > 32768.f || (amax > 0.f && amax < 0.0625f);
+      if (__any_sync(0xFFFFFFFFu, rescale)) {  // the whole warp: tensor-memory stores are warp-wide
+        const float qs = rescale ? pow2_scale(32768.f, amax) : 1.f;
+        qinv_row = 1.f / qs;  // exact: qs is a power of two
+        tc::tmem_st_wait();   // the first conversion's stores complete before they are overwritten
+        convert(qs);
       }
+      bs.qinv[t] = qinv_row;
       tc::tmem_st_wait();
       fence_proxy_async_smem();
       tc::fence_before_sync();
@@ -561,7 +591,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.qready));
     }
 
-    const float sc = a.score_scale;
+    const float sc = a.score_scale * qinv_row;
     const uint32_t recv0 = smem_u32(smem + kOffRecv);
     float mref = -INFINITY, l = 0.f;
     // Receive buffer xb expects the peer's tile j only once its tile j - 3 has

@@ -335,7 +335,11 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 2)
   int chunk_left = 0;  // tiles left in the current unit, including the current one
   int64_t seg_begin = f_begin;
   float sc = a.score_scale;  // unit mode: set per unit from the device K scale
-  float qinv = 1.f;          // e4m3 cache: 1 / (the unit's power-of-two Q scale)
+  // e4m3 cache: 1 / the power-of-two Q scale, per head of the score columns
+  // 2t and 2t + 1 of each head tile (per unit for per-token scales)
+  float qinv[NT][2];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) qinv[j][0] = qinv[j][1] = 1.f;
   float unit_vs = 1.f;       // unit mode: the unit's V scale
   float vref = 0.f, vinv = 0.f;  // token mode: largest V scale of the unit so far, 1 / it
 
@@ -463,20 +467,13 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 2)
       const uint32_t wd[16] = {r[0].x, r[0].y, r[0].z, r[0].w, r[1].x, r[1].y, r[1].z, r[1].w,
                                r[2].x, r[2].y, r[2].z, r[2].w, r[3].x, r[3].y, r[3].z, r[3].w};
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        if constexpr (!kBf16 && kScl == kSclToken)  // f16 pairs for the widened-K products
-          qf[j][i >> 1][i & 1] = pack_f16x2(bf16_lo(wd[i]), bf16_hi(wd[i]));
-        else
-          qf[j][i >> 1][i & 1] = wd[i];  // bf16 pairs (the e4m3 products split them below)
-      }
+      for (int i = 0; i < 16; ++i) qf[j][i >> 1][i & 1] = wd[i];  // bf16 pairs
     }
-    if constexpr (!kBf16 && kScl != kSclToken) {
-      // Q as two exact e4m3 parts for the e4m3 products on the raw K bytes:
-      // x = q s, s = 2^floor(log2(448 / max |q|)) over the unit's heads;
-      // part 1 = e4m3(x), part 2 = e4m3(x - part 1) (a bf16 value has 8
-      // significant bits, each part 4).  Register pair (2 kk + p) holds part p
-      // of head_dim values 32t + 8kk .. 32t + 8kk + 7, the K elements that
-      // the e4m3 product's k 4t.. and 16 + 4t.. pick in step kk.
+    if constexpr (!kBf16 && kScl == kSclToken) {
+      // Q in f16 for the widened-K products, times a power of two s over the
+      // unit's heads taking max |q s| into (2^14, 2^15]: every finite bf16
+      // query fits and each value at least 2^-29 of the largest is an exact
+      // f16 normal; the raw scores are multiplied by 1 / s
       float amax = 0.f;
 #pragma unroll
       for (int j = 0; j < NT; ++j)
@@ -485,12 +482,38 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 2)
           amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(qf[j][i >> 1][i & 1])), fabsf(bf16_hi(qf[j][i >> 1][i & 1]))));
 #pragma unroll
       for (int o2 = 16; o2 >= 1; o2 >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o2));
-      const float s = amax > 0.f ? fmaxf(__uint_as_float(__float_as_uint(448.f / amax) & 0x7F800000u),
-                                         1.17549435e-38f)
-                                 : 1.f;
-      qinv = 1.f / s;  // exact: s is a power of two
+      const float s = pow2_scale(32768.f, amax);
+      qinv[0][0] = 1.f / s;  // exact: s is a power of two
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t w = qf[j][i >> 1][i & 1];
+          qf[j][i >> 1][i & 1] = pack_f16x2(bf16_lo(w) * s, bf16_hi(w) * s);
+        }
+    } else if constexpr (!kBf16) {
+      // Q as two exact e4m3 parts for the e4m3 products on the raw K bytes:
+      // x = q s with s a power of two per head, s = 2^floor(log2(448 /
+      // max |q|)) over the head's 128 values (the four lanes of group g hold
+      // them); part 1 = e4m3(x), part 2 = e4m3(x - part 1): a bf16 value
+      // has 8 significant bits, each part 4, so every scaled value above 1/4
+      // (at least 1/896 of the head's largest) is split exactly, and smaller
+      // ones within 2^-10.  Register pair (2 kk + p)
+      // holds part p of head_dim values 32t + 8kk .. 32t + 8kk + 7, the K
+      // elements that the e4m3 product's k 4t.. and 16 + 4t.. pick in step kk.
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(qf[j][i >> 1][i & 1])), fabsf(bf16_hi(qf[j][i >> 1][i & 1]))));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+        const float s = pow2_scale(448.f, amax);
+        const float hinv = 1.f / s;  // head 8j + g; exact: s is a power of two
+        // the score columns of this thread are heads 8j + 2t and 8j + 2t + 1
+        qinv[j][0] = __shfl_sync(0xFFFFFFFFu, hinv, 8 * t);
+        qinv[j][1] = __shfl_sync(0xFFFFFFFFu, hinv, 8 * t + 4);
         uint32_t wq[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) wq[i] = qf[j][i >> 1][i & 1];
@@ -597,10 +620,10 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 2)
       }
 #pragma unroll
       for (int j = 0; j < NT; ++j) {  // undo the Q scale (a power of two: exact)
-        s[j][0] *= qinv;
-        s[j][1] *= qinv;
-        s[j][2] *= qinv;
-        s[j][3] *= qinv;
+        s[j][0] *= qinv[j][0];
+        s[j][1] *= qinv[j][1];
+        s[j][2] *= qinv[j][0];
+        s[j][3] *= qinv[j][1];
       }
     }
 
@@ -608,8 +631,8 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 2)
     float ks0 = 1.f, ks8 = 1.f, vs0 = 0.f, vs8 = 0.f;
     if constexpr (kScl == kSclToken) {
       const float* sp = sptr + stage * (kScaleStageBytes / 4);
-      ks0 = sp[g];
-      ks8 = sp[g + 8];
+      ks0 = sp[g] * qinv[0][0];  // the token's K scale and the Q scale's inverse
+      ks8 = sp[g + 8] * qinv[0][0];
       vs0 = sp[16 + g];
       vs8 = sp[24 + g];
 #pragma unroll

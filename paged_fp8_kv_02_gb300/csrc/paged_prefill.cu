@@ -372,9 +372,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool row_ok = (!m64 || lane < 16) && r < x.rows;
     const int i = x.i0 + r / a.G, g = r % a.G;
     const int64_t head_row = ((int64_t)a.q_start[x.b] + i) * a.Hq + (int64_t)x.kvh * a.G + g;  // row of q / out
-    // Q row -> f16 pairs -> the A operand in tensor memory (zeros for padding rows)
+    // Q row -> f16 pairs -> the A operand in tensor memory (zeros for padding
+    // rows).  The row is scaled by a power of two qs taking its largest |q|
+    // into (2^14, 2^15], so every finite bf16 row fits f16 and each value at
+    // least 2^-29 of the largest converts exactly; 1 / qs joins the score scale.
+    float qinv = 1.f;
     {
       const uint4* qp = reinterpret_cast<const uint4*>(a.q + head_row * kD);
+      float amax = 0.f;
+      if (row_ok) {
+#pragma unroll 4
+        for (int uu = 0; uu < 16; ++uu) {
+          const uint4 w = __ldg(qp + uu);
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(ww[k])), fabsf(bf16_hi(ww[k]))));
+        }
+      }
+      const float qs = pow2_scale(32768.f, amax);
+      qinv = 1.f / qs;  // exact: qs is a power of two
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t f[32];
@@ -382,10 +398,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int uu = 0; uu < 8; ++uu) {
           uint4 w = make_uint4(0, 0, 0, 0);
           if (row_ok) w = __ldg(qp + 8 * half + uu);
-          f[4 * uu] = pack_f16x2(bf16_lo(w.x), bf16_hi(w.x));
-          f[4 * uu + 1] = pack_f16x2(bf16_lo(w.y), bf16_hi(w.y));
-          f[4 * uu + 2] = pack_f16x2(bf16_lo(w.z), bf16_hi(w.z));
-          f[4 * uu + 3] = pack_f16x2(bf16_lo(w.w), bf16_hi(w.w));
+          f[4 * uu] = pack_f16x2(bf16_lo(w.x) * qs, bf16_hi(w.x) * qs);
+          f[4 * uu + 1] = pack_f16x2(bf16_lo(w.y) * qs, bf16_hi(w.y) * qs);
+          f[4 * uu + 2] = pack_f16x2(bf16_lo(w.z) * qs, bf16_hi(w.z) * qs);
+          f[4 * uu + 3] = pack_f16x2(bf16_lo(w.w) * qs, bf16_hi(w.w) * qs);
         }
         tc::tmem_st32(trow + kTmemQ + 32 * half, f);
       }
@@ -396,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // keys t < lim are attended by this row
     const int lim = row_ok ? min(x.L - x.n + i + 1, x.t_end_chunk) : x.t_lo;
-    const float sc = a.score_scale;
+    const float sc = a.score_scale * qinv;
     float mref = -INFINITY, rthr = -INFINITY, l = 0.f;
     // a warp whose 32 rows are all padding has nothing to do after writing its
     // zero Q rows (their scores are 0, which read as f16 pairs are P = 0)
@@ -828,8 +844,7 @@ __global__ void __launch_bounds__(k2Threads, 1)
           for (int k = 0; k < 4; ++k) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(ww[k])), fabsf(bf16_hi(ww[k]))));
         }
       }
-      const float qs =
-          amax > 0.f ? fmaxf(__uint_as_float(__float_as_uint(448.f / amax) & 0x7F800000u), 1.17549435e-38f) : 1.f;
+      const float qs = pow2_scale(448.f, amax);
       qinv = row_ok ? 1.f / qs : 0.f;  // exact: qs is a power of two
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {  // 16 elements per 16-byte chunk
@@ -1297,9 +1312,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
           for (int k = 0; k < 4; ++k) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(ww[k])), fabsf(bf16_hi(ww[k]))));
         }
       }
-      // s = 2^floor(log2(448 / amax)), at least 2^-126 (1 for a zero row)
-      const float s =
-          amax > 0.f ? fmaxf(__uint_as_float(__float_as_uint(448.f / amax) & 0x7F800000u), 1.17549435e-38f) : 1.f;
+      // s = 2^floor(log2(448 / amax)) within [2^-126, 2^126] (1 for a zero row)
+      const float s = pow2_scale(448.f, amax);
       if (lane < 16) {
 #pragma unroll 1
         for (int c = 0; c < 8; ++c) {  // 16 elements per 16-byte chunk

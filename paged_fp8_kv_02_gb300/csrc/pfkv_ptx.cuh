@@ -186,6 +186,17 @@ __device__ __forceinline__ float f16_hi(uint32_t v) {
   return f;
 }
 
+// A power of two s with s * amax <= top, the largest such (s * amax in
+// (top / 2, top]) as long as that lies in [2^-126, 2^126]; clamped there
+// otherwise (top / amax overflows for subnormal amax), 1 for amax == 0.  Query
+// rows are multiplied by s before a narrow-format conversion and the scores by
+// 1 / s after the product; both are exact.
+__device__ __forceinline__ float pow2_scale(float top, float amax) {
+  if (!(amax > 0.f)) return 1.f;
+  const float r = __uint_as_float(__float_as_uint(top / amax) & 0x7F800000u);
+  return fminf(fmaxf(r, 1.17549435e-38f), 8.50705917e37f);
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
