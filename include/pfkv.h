@@ -179,6 +179,13 @@ PFKV_API int pfkv_kv_append_fp8_scaled(const void *k_new, const void *v_new, voi
  *                  bytes, 256-byte aligned; contents on entry are ignored.
  * L_b == 0 gives out = 0 and lse = -inf.  For a bf16 cache the scales still
  * multiply (pass 1.0).
+ * Numerics: fp32 accumulation throughout.  e4m3 cache: scores are e4m3
+ * products on the cached K bytes against q split into two e4m3 parts after a
+ * power-of-two scale per query head (largest |q| into (224, 448]; exact for
+ * every value at least 1/896 of the head's largest, within 2^-10 of the scaled
+ * value below that; any finite bf16 q is accepted, 1 / scale multiplies the raw
+ * scores); P.V takes f16 products (V widens exactly, P <= 2^8).  bf16 cache:
+ * bf16 products for both.
  * Supported: head_dim 128; page_size a multiple of 16; num_q_heads /
  * num_kv_heads in 1..16; num_pages * num_kv_heads * page_size < 2^31.
  * Device errors (status word): PFKV_DEVERR_BAD_PAGE (rows outside the pool
@@ -239,6 +246,10 @@ PFKV_API int pfkv_paged_decode_attn_noalloc(void *out, const void *q, const void
  * the largest V scale seen so far in the work unit, multiplies its token's
  * probability before the f16 P.V product (the accumulator is rescaled when
  * that largest scale grows, as for the running maximum of the softmax).
+ * Numerics: per tensor and per head as pfkv_paged_decode_attn; per token, the
+ * score products are f16 on K widened in registers, against q times one
+ * power of two per work unit that takes its largest |q| into (2^14, 2^15]
+ * (any finite bf16 q; exact for every value at least 2^-29 of that largest).
  * Scales: finite and >= 0 (TENSOR, HEAD: > 0); not checked (device arrays).
  * The scale of a token past L_b is never used.  Workspace: as
  * pfkv_paged_decode_attn (pfkv_paged_decode_workspace_size).  Other arguments
@@ -276,9 +287,15 @@ PFKV_API int pfkv_paged_decode_attn_scaled(void *out, const void *q, const void 
  *         t = 0 .. L_b - n_b + i
  *   out = sum_t e^{s_t - m} V(t) * v_scale / sum_t e^{s_t - m}
  *   lse = m + ln sum_t e^{s_t - m}
- * Products on the tensor cores in f16 (e4m3 widens exactly; q is rounded from
- * bf16 to f16, exact for 2^-14 <= |q| <= 65504; P is f16 <= 2^8) with fp32
- * accumulation.
+ * Products on the tensor cores with fp32 accumulation.  Scores: when every row
+ * block holds more than 64 rows and there is one block per request, f16
+ * products on the widened K (e4m3 widens exactly) with each q row scaled by a
+ * power of two into f16's range; otherwise e4m3 products on the K bytes with
+ * each q row, scaled by a power of two (largest |q| into (224, 448]), split
+ * into two e4m3 parts (exact for every value at least 1/896 of the row's
+ * largest, within 2^-10 of the scaled value below that).  Either way any
+ * finite bf16 q is accepted and 1 / scale multiplies the raw scores.  P.V: f16
+ * (P <= 2^8, V widened exactly).
  *   out, q        bf16 [q_start[batch]][num_q_heads][head_dim]
  *   q_start       int32 [batch + 1] (device), non-decreasing, q_start[0] = 0
  *   max_q_len     host bound on every n_b; max_context_len host bound on
@@ -328,8 +345,11 @@ PFKV_API int pfkv_paged_prefill_attn(void *out, const void *q, const void *k_cac
  * Supported: d_latent 512, d_rope 64, num_heads 128 or fewer and a multiple of
  * 16, page_size a multiple of 16, num_pages * page_size < 2^31.  Listed
  * indices >= L_b are skipped and set PFKV_DEVERR_BAD_TOPK.
- * Numerics: f16 operands (the latent exactly; q rounded from bf16, exact for
- * 2^-14 <= |q| <= 65504) with f32 accumulation.  Each request runs on a pair
+ * Numerics: f16 operands with f32 accumulation: the latent widens exactly; a q
+ * row converts as it is when its largest |q| over the columns one SM contracts
+ * lies in [2^-4, 2^15] (then every value at least 2^-10 of that largest is
+ * exact), otherwise after a power-of-two scale into (2^14, 2^15] that the
+ * SM's partial scores undo; any finite bf16 q is accepted.  Each request runs on a pair
  * of SMs that each contract part of the 576 columns; a score is one SM's
  * exact f32 partial plus the other's partial carried as 16-bit fixed point
  * over its range within a 32-token tile (at most range / 65535 added error,
@@ -377,7 +397,8 @@ PFKV_API int pfkv_validate_tables(const int32_t *block_tables, int max_pages_per
  * Entries past a request's context are not read and not checked.  Asynchronous
  * on `stream`; the caller reads request_status after the stream reaches this
  * point and leaves flagged requests out of the decode call.  Returns PFKV_OK,
- * PFKV_ERR_INVALID_ARG or PFKV_ERR_CUDA. */
+ * PFKV_ERR_INVALID_ARG (bad sizes, a NULL or not 4-byte aligned pointer) or
+ * PFKV_ERR_CUDA. */
 #define PFKV_REQ_TAG_MISMATCH 0x1
 #define PFKV_REQ_BAD_INDEX 0x2
 PFKV_API int pfkv_verify_page_tags(const int32_t *block_tables, const uint32_t *table_tags,

@@ -162,6 +162,9 @@ extern "C" int pfkv_verify_page_tags(const int32_t* block_tables, const uint32_t
   if (batch == 0) return PFKV_OK;
   if (!block_tables || !table_tags || !context_lens || !page_tags || !request_status)
     return fail(PFKV_ERR_INVALID_ARG, "verify_page_tags: null pointer");
+  if (!aligned(block_tables, 4) || !aligned(table_tags, 4) || !aligned(context_lens, 4) ||
+      !aligned(page_tags, 4) || !aligned(request_status, 4))
+    return fail(PFKV_ERR_INVALID_ARG, "verify_page_tags: misaligned pointer");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   TagArgs a{block_tables, table_tags, context_lens, page_tags, request_status, max_pages_per_seq, page_size, num_pages};
   verify_tags_kernel<<<batch, kTagThreads, 0, s>>>(a);

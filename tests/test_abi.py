@@ -86,3 +86,89 @@ def test_host_validation_rejects_bad_arguments_without_cuda(lib):
     rc = lib.pfkv_validate_tables(None, 4, None, 1, 16, i64(4), None, 0, None, 0, None, None)
     assert rc == -1
     assert lib.pfkv_version().decode().startswith("pfkv")
+
+
+def _fake(addr=0x10000):
+    """A device-looking address that the host checks never dereference."""
+    return ctypes.c_void_p(addr)
+
+
+def _err(lib):
+    return lib.pfkv_last_error().decode()
+
+
+def test_prefill_host_validation_without_cuda(lib):
+    i64 = ctypes.c_int64
+    ptrs = [_fake()] * 5  # out, q, k_cache, v_cache, block_tables
+
+    def call(*, B=2, Hq=16, Hkv=2, D=128, P=16, pages=64, maxp=8, mq=4, mctx=100, ks=1.0, vs=1.0,
+             sm=0.088, split=0, ctx=_fake(), qs=_fake(), ws=_fake(), wsb=1 << 20, out=None, lse=None):
+        p = list(ptrs)
+        if out is not None:
+            p[0] = out
+        return lib.pfkv_paged_prefill_attn(*p, maxp, ctx, qs, B, Hq, Hkv, D, P, i64(pages), mq, mctx, ks,
+                                           vs, sm, split, ws, wsb, lse, None)
+
+    assert call(B=-1) == -1 and "bad sizes" in _err(lib)
+    assert call(Hkv=3) == -1                      # 16 % 3 != 0
+    assert call(Hq=96, Hkv=1) == -2               # G = 96 does not divide 128
+    assert call(D=64) == -2
+    assert call(P=8) == -2
+    assert call(split=32) == -1                   # not a multiple of 64
+    assert call(sm=0.0) == -1 and call(ks=float("inf")) == -1
+    assert call(pages=1 << 28) == -2              # 2^31 token rows or more
+    assert call(B=0) == 0                         # nothing to do
+    assert call(ctx=None) == -1 and "null pointer" in _err(lib)
+    assert call(out=_fake(0x10008)) == -1 and "misaligned" in _err(lib)
+    assert call(ws=_fake(0x10080)) == -1           # workspace not 256-byte aligned
+    need = lib.pfkv_paged_prefill_workspace_size(2, 16, 2, 128, 4, 100, 64)
+    assert need > 256
+    assert call(split=64, wsb=need - 1) == -5 and "too small" in _err(lib)
+    assert lib.pfkv_paged_prefill_workspace_size(2, 16, 2, 128, 4, 100, 0) == 256  # status word only
+    assert lib.pfkv_paged_prefill_workspace_size(2, 16, 3, 128, 4, 100, 0) == 0
+
+
+def test_scaled_decode_host_validation_without_cuda(lib):
+    i64 = ctypes.c_int64
+
+    def call(gran=0, kscl=_fake(), vscl=_fake(), B=2, Hq=16, Hkv=2, D=128, P=16, split=0, ws=_fake(), wsb=1 << 24):
+        return lib.pfkv_paged_decode_attn_scaled(_fake(), _fake(), _fake(), _fake(), gran, kscl, vscl, _fake(), 8,
+                                                 _fake(), B, Hq, Hkv, D, P, i64(64), 0.088, split, ws, wsb, None,
+                                                 None)
+
+    assert call(gran=7) == -1 and "granularity" in _err(lib)
+    assert call(kscl=None) == -1 and "null scale" in _err(lib)
+    assert call(vscl=_fake(0x10004)) == -1 and "16-byte" in _err(lib)
+    assert call(Hq=64, Hkv=2) == -2               # group size 32
+    assert call(split=8) == -1
+    assert call(B=0) == 0
+    assert call(wsb=64) == -5
+
+
+def test_scaled_append_host_validation_without_cuda(lib):
+    i64 = ctypes.c_int64
+
+    def call(gran=2, T=4, H=2, D=128, kscl=_fake(), vscl=_fake(), v=True, slots=_fake()):
+        vn, vc = (_fake(), _fake()) if v else (None, None)
+        return lib.pfkv_kv_append_fp8_scaled(_fake(), vn, _fake(), vc, slots, T, H, D, 16, i64(8), gran, kscl,
+                                             vscl if v else None, None)
+
+    assert call(gran=3) == -1 and "granularity" in _err(lib)
+    assert call(kscl=None) == -1 and "null scale" in _err(lib)
+    assert call(vscl=_fake(0x10002)) == -1 and "4-byte" in _err(lib)
+    assert call(D=576) == -2                      # per-token scales need head_dim <= 512
+    assert call(D=24) == -2                       # not a multiple of 16
+    assert call(T=0) == 0
+    assert call(slots=_fake(0x10004)) == -1       # slot mapping must be 8-byte aligned
+
+
+def test_page_tag_check_host_validation_without_cuda(lib):
+    i64 = ctypes.c_int64
+
+    def call(B=3, maxp=4, P=16, pages=64, bt=_fake(), tt=_fake(), ctx=_fake(), pt=_fake(), st=_fake()):
+        return lib.pfkv_verify_page_tags(bt, tt, maxp, ctx, B, P, pt, i64(pages), st, None)
+
+    assert call(B=-1) == -1 and call(P=0) == -1 and call(pages=0) == -1
+    assert call(B=0) == 0
+    assert call(pt=None) == -1 and "null pointer" in _err(lib)
+    assert call(st=_fake(0x10002)) == -1 and "misaligned" in _err(lib)
