@@ -17,6 +17,10 @@
  *  - bf16 = IEEE bfloat16 bit patterns (uint16); e4m3 = OCP 8-bit E4M3 codes
  *    (uint8: bias 7, subnormals, 0x7F/0xFF NaN, no infinity, max 448).
  *  - Layouts are row-major (C order) with the shapes written in brackets.
+ *  - Alignment: bf16 and e4m3 tensors start on 16 bytes, workspaces on 256,
+ *    int32 / uint32 / fp32 arrays on 4 and int64 slot mappings on 8 (device
+ *    scale arrays as their call says); a pointer that is not is rejected with
+ *    PFKV_ERR_INVALID_ARG before anything is enqueued.
  *  - Paged caches: K and V are separate tensors [num_pages][Hkv][P][D]; the
  *    token at logical position t of request b lives in page
  *    block_tables[b][t / P], row t % P ("slot" = page * P + t % P).  The MLA

@@ -752,7 +752,9 @@ int pfkv_mla_decode_attn(void* out, const void* q, const void* ckv_cache, const 
   if (!out || !q || !ckv_cache || !block_tables || !context_lens || !workspace)
     return fail(PFKV_ERR_INVALID_ARG, "mla_decode: null pointer");
   if (workspace_bytes < 256) return fail(PFKV_ERR_WORKSPACE, "mla_decode: workspace too small");
-  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(ckv_cache, 16) || !aligned(workspace, 256))
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(ckv_cache, 16) || !aligned(workspace, 256) ||
+      !aligned(block_tables, 4) || !aligned(context_lens, 4) || (topk_idx && !aligned(topk_idx, 4)) ||
+      (lse_out && !aligned(lse_out, 4)))
     return fail(PFKV_ERR_INVALID_ARG, "mla_decode: misaligned pointer");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   MlaArgs a;

@@ -125,6 +125,10 @@ extern "C" int pfkv_validate_tables(const int32_t* block_tables, int max_pages_p
     return fail(PFKV_ERR_INVALID_ARG, "validate_tables: null table pointer");
   if (num_slots > 0 && !slot_mapping)
     return fail(PFKV_ERR_INVALID_ARG, "validate_tables: null slot mapping");
+  if (!aligned(d_err_word, 4) || (block_tables && !aligned(block_tables, 4)) ||
+      (context_lens && !aligned(context_lens, 4)) || (topk_idx && !aligned(topk_idx, 4)) ||
+      (num_slots > 0 && !aligned(slot_mapping, 8)))
+    return fail(PFKV_ERR_INVALID_ARG, "validate_tables: misaligned pointer");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(d_err_word, 0, sizeof(int32_t), s) != cudaSuccess)
     return check_cuda("validate_tables reset");

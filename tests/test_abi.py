@@ -172,3 +172,24 @@ def test_page_tag_check_host_validation_without_cuda(lib):
     assert call(B=0) == 0
     assert call(pt=None) == -1 and "null pointer" in _err(lib)
     assert call(st=_fake(0x10002)) == -1 and "misaligned" in _err(lib)
+
+
+def test_mla_and_table_validation_reject_misaligned_arrays_without_cuda(lib):
+    i64 = ctypes.c_int64
+
+    def mla(bt=_fake(), ctx=_fake(), topk=None, k=0, lse=None):
+        return lib.pfkv_mla_decode_attn(_fake(), _fake(), _fake(), bt, 4, ctx, topk, k, 2, 128, 512, 64, 64,
+                                        i64(16), 0.05, 0.07, _fake(), 256, lse, None)
+
+    assert mla(bt=_fake(0x10002)) == -1 and "misaligned" in _err(lib)
+    assert mla(ctx=_fake(0x10001)) == -1
+    assert mla(topk=_fake(0x10006), k=8) == -1
+    assert mla(lse=_fake(0x10003)) == -1
+
+    def val(err=_fake(), bt=_fake(), slots=None, n=0):
+        return lib.pfkv_validate_tables(bt, 4, _fake(), 2, 16, i64(8), None, 0, slots, n, err, None)
+
+    assert val(err=_fake(0x10002)) == -1 and "misaligned" in _err(lib)
+    assert val(bt=_fake(0x10001)) == -1
+    assert val(slots=_fake(0x10004), n=3) == -1   # int64 slots need 8 bytes
+    assert val(slots=None, n=3) == -1 and "null slot" in _err(lib)
