@@ -24,13 +24,16 @@
 //    memory stages fed by TMA (cp.async.bulk.tensor, 128-byte swizzle): one
 //    stage = the K and V slabs of one 16-token tile of one KV head.  The
 //    swizzle makes the fragment loads below bank-conflict free.
-//  * Scores and P.V run on warp-level tensor-core MMA (m16n8k16, f32 accumulate):
+//  * Scores and P.V run on warp-level tensor-core MMA with f32 accumulation:
 //    S^T[16 tokens x 8 heads] = K_tile . Q^T, then O^T[128 x 8] += V_tile^T . P^T.
-//    The e4m3 -> f16 conversion is exact and fused into the fragment build; the
-//    K fragment takes 32 contiguous bytes per thread (the head_dim sum is
-//    permuted consistently in Q), the V fragment is built with byte permutes.
-//    This keeps the CUDA-core work per KV byte small enough for G = 8 heads
-//    per KV head at full HBM bandwidth.
+//    e4m3 cache: the scores are m16n8k32 e4m3 products straight on the K bytes
+//    in shared memory (each thread's K fragment is 32 contiguous bytes of a
+//    row; the head_dim sum is permuted the same way in Q) against Q split per
+//    head into two exact e4m3 parts after a power-of-two scale; the per-token-
+//    scale variant widens K to f16 instead (m16n8k16).  V widens to f16
+//    (exact) inside the fragment build, with byte permutes.  bf16 cache: bf16
+//    products for both.  This keeps the CUDA-core work per KV byte small
+//    enough for G = 8 heads per KV head at full HBM bandwidth.
 //  * Online softmax in the exp2 domain on warp shuffles; P goes to the second
 //    MMA through movmatrix (transpose of the accumulator fragment).
 #include <cuda_bf16.h>
