@@ -13,7 +13,9 @@
 // the pair splits the score contraction instead of repeating it: CTA 0
 // contracts latent columns 0 .. 255, CTA 1 latent columns 256 .. 511 and the
 // 64 rope columns (Q's latent part held in tensor memory as the A operand,
-// the rope part in shared memory), so each CTA reads one contiguous span of
+// the rope part in shared memory, both f16; a row whose largest |q| over the
+// CTA's columns lies outside [2^-4, 2^15] is first scaled by a power of two,
+// undone on that CTA's partial scores), so each CTA reads one contiguous span of
 // every row (256 or 320 bytes).  The partial score tiles cross between the
 // pair through distributed shared memory (asynchronous remote stores that
 // count their bytes on the receiver's mbarrier) as 16-bit fixed point

@@ -34,7 +34,15 @@
 // partial states (m, l, o) and a merge kernel combines them by the log-sum-exp
 // rule (kLLM article, §5.2.2).  When a (request, KV head) has several row
 // blocks (a chunked-prefill step), prefill2_kernel takes two blocks per CTA
-// so that each widened tile feeds both and two softmax groups overlap.
+// so that each tile feeds both and two softmax groups overlap; when every
+// block holds at most 64 rows (a verification pass), prefillw_kernel runs
+// 128-token tiles with half-height products.  These two take the scores as
+// e4m3 products (tcgen05 kind::f8f6f4) straight on the K tile of the TMA
+// stage, against each Q row scaled by a power of two (largest |q| into
+// (224, 448]) and split into two exact e4m3 parts; only V is widened.  The
+// one-block kernel described above widens K as well and takes Q as f16, each
+// row scaled by a power of two into f16's range.  In every kernel the row's
+// 1 / scale joins its score scale, so any finite bf16 query is accepted.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
