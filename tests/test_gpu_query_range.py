@@ -81,11 +81,8 @@ DECODE_CASES = [
 
 
 @pytest.mark.parametrize("regime", REGIMES)
-@pytest.mark.parametrize("case", range(len(DECODE_CASES)))
-@pytest.mark.parametrize("bf16", [False, True])
+@pytest.mark.parametrize("case,bf16", [(i, False) for i in range(len(DECODE_CASES))] + [(0, True)])
 def test_decode_query_range(regime, case, bf16):
-    if bf16 and case != 0:
-        pytest.skip("the bf16 cache is covered by the first case")
     p = pf()
     c = dict(DECODE_CASES[case])
     lens = c.pop("lens")
