@@ -739,7 +739,7 @@ def run_gpu(args, rank, ws, local):
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 cache, f16/bf16 mma, f32 accumulate",
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 cache; e4m3 score and f16 P.V mma, f32 accumulate",
             "data": "synthetic (seeded counter-based N(0,1) approximation)",
             "config": {"workload": HEADLINE, "batch_per_gpu": w.B, "q_heads": w.Hq,
                        "kv_heads": w.Hkv, "head_dim": w.D, "context": int(w.context_lens[0]),
