@@ -449,9 +449,10 @@ PFKV_API int pfkv_pool_page_tags(const pfkv_page_pool *pool, uint32_t *tags_out)
 PFKV_API int pfkv_pool_map_request(pfkv_page_pool *pool, const int32_t *tokens, int n_tokens,
                                    int32_t *block_table_row, uint32_t *table_tags, int max_pages,
                                    int *cached_tokens);
-/* Release a request's first n_pages pages (one holder each); pages with no
- * holder left return to the free list.  PFKV_ERR_INVALID_ARG (nothing
- * changed) if an entry is not a held page. */
+/* Release a request's first n_pages pages (one holder per entry: a page
+ * listed k times drops k holders); pages with no holder left return to the
+ * free list.  PFKV_ERR_INVALID_ARG (nothing changed) if an entry is not a held
+ * page, or lists a page more times than it has holders. */
 PFKV_API int pfkv_pool_release(pfkv_page_pool *pool, const int32_t *block_table_row, int n_pages);
 /* The FNV-1a chain hash of one block (n tokens) given its parent's hash. */
 PFKV_API uint64_t pfkv_block_hash(uint64_t parent, const int32_t *tokens, int n);

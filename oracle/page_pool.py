@@ -86,8 +86,12 @@ class PagePool:
         return row, tags, hits * P
 
     def release(self, row, n_pages: int):
+        # each listed entry is one reference: a page listed k times needs k
+        listed = {}
         for page in row[:n_pages]:
-            if page < 0 or page >= len(self.ref) or self.ref[page] <= 0:
+            listed[page] = listed.get(page, 0) + 1
+        for page, k in listed.items():
+            if page < 0 or page >= len(self.ref) or self.ref[page] < k:
                 raise ValueError("not a held page")
         for page in row[:n_pages]:
             self.ref[page] -= 1

@@ -391,6 +391,8 @@ class PagePool:
     def release(self, row, n_pages: int):
         import numpy as np
         r, rp = _host(row, np.int32)
+        if not 0 <= n_pages <= r.shape[0]:
+            raise ValueError(f"n_pages {n_pages} outside the row's {r.shape[0]} entries")
         _check("pool_release", load().pfkv_pool_release(self._h, rp, n_pages))
 
 

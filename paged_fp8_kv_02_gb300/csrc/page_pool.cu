@@ -193,12 +193,19 @@ int pfkv_pool_release(pfkv_page_pool* pool, const int32_t* block_table_row, int 
   pfkv::clear_error();
   if (pool == nullptr || (n_pages > 0 && block_table_row == nullptr))
     return pfkv::fail(PFKV_ERR_INVALID_ARG, "pool_release: null pointer");
-  for (int i = 0; i < n_pages; ++i) {
+  // Each entry drops one reference, so a page listed k times must hold k:
+  // take the references tentatively, put them back, and fail on the first
+  // entry that finds none left (the pool is then unchanged).
+  int i = 0;
+  for (; i < n_pages; ++i) {
     const int32_t page = block_table_row[i];
-    if (page < 0 || page >= pool->num_pages || pool->refcount[page] <= 0)
-      return pfkv::fail(PFKV_ERR_INVALID_ARG, "pool_release: page %d (entry %d) is not held", page, i);
+    if (page < 0 || page >= pool->num_pages || pool->refcount[page] <= 0) break;
+    --pool->refcount[page];
   }
-  for (int i = 0; i < n_pages; ++i) drop_ref(pool, block_table_row[i]);
+  for (int j = 0; j < i; ++j) ++pool->refcount[block_table_row[j]];
+  if (i < n_pages)
+    return pfkv::fail(PFKV_ERR_INVALID_ARG, "pool_release: page %d (entry %d) is not held", block_table_row[i], i);
+  for (int k = 0; k < n_pages; ++k) drop_ref(pool, block_table_row[k]);
   return PFKV_OK;
 }
 

@@ -72,3 +72,35 @@ def test_slots_follow_the_table(pf):
     assert np.array_equal(sl, row[t // 16].astype(np.int64) * 16 + t % 16)
     with pytest.raises(pf.PfkvError):
         pf.slots_from_table(row, 16, 40, 10)  # tokens 48.. fall in the unmapped 4th entry
+
+
+def test_a_page_listed_twice_needs_two_holders(pf):
+    """Each entry of a released row drops one holder.  A page held once but
+    listed twice is an error that changes nothing (it would otherwise return
+    to the free list while still counted); a shared page held by two requests
+    may be listed twice and is then freed once."""
+    from oracle.page_pool import PagePool as OraclePool
+    P = 4
+    lib, ref = pf.PagePool(16, P), OraclePool(16, P)
+    toks = np.arange(8, dtype=np.int32)              # two full blocks
+    row, _, _ = lib.map_request(toks, 4)
+    rrow, _, _ = ref.map_request(toks, 4)
+    assert list(row[:2]) == list(rrow[:2])
+    dup = np.array([row[0], row[0]], np.int32)
+    with pytest.raises(pf.PfkvError):
+        lib.release(dup, 2)
+    with pytest.raises(ValueError):
+        ref.release(list(dup), 2)
+    assert lib.refcount(int(row[0])) == 1 and lib.num_free() == 14
+    assert ref.ref[int(row[0])] == 1 and len(ref.free) == 14
+    # a second request shares both blocks: each page now has two holders
+    row2, _, cached = lib.map_request(toks, 4)
+    rrow2, _, rcached = ref.map_request(toks, 4)
+    assert cached == rcached == 8 and list(row2[:2]) == list(row[:2]) == list(rrow2[:2])
+    lib.release(dup, 2)
+    ref.release(list(dup), 2)
+    assert lib.refcount(int(row[0])) == 0 and ref.ref[int(row[0])] == 0
+    assert lib.num_free() == len(ref.free) == 15
+    assert lib.refcount(int(row[1])) == 2
+    with pytest.raises(ValueError):
+        lib.release(row, 5)                           # more entries than the row holds
