@@ -193,3 +193,18 @@ def test_mla_and_table_validation_reject_misaligned_arrays_without_cuda(lib):
     assert val(bt=_fake(0x10001)) == -1
     assert val(slots=_fake(0x10004), n=3) == -1   # int64 slots need 8 bytes
     assert val(slots=None, n=3) == -1 and "null slot" in _err(lib)
+
+
+def test_noalloc_decode_rejects_on_the_host_without_cuda(lib):
+    i64 = ctypes.c_int64
+
+    def call(B=8, Hq=64, Hkv=8, split=0, chunks=0):
+        return lib.pfkv_paged_decode_attn_noalloc(_fake(), _fake(), _fake(), _fake(), 0, _fake(), 64, _fake(), B, Hq,
+                                                  Hkv, 128, 16, i64(4096), 1.0, 1.0, 0.088, split, i64(chunks),
+                                                  None, None, None)
+
+    assert call(Hkv=3) == -1 and "head counts" in _err(lib)
+    # 8 requests x 1M tokens cut into 4096-token chunks: 2048 chunks x 8 KV heads of partial states
+    need = lib.pfkv_paged_decode_workspace_size(8, 64, 8, 128, 4096, 2048)
+    assert need > 64 << 20
+    assert call(split=4096, chunks=2048) == -5 and "64 MiB" in _err(lib)
