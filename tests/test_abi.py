@@ -208,3 +208,17 @@ def test_noalloc_decode_rejects_on_the_host_without_cuda(lib):
     need = lib.pfkv_paged_decode_workspace_size(8, 64, 8, 128, 4096, 2048)
     assert need > 64 << 20
     assert call(split=4096, chunks=2048) == -5 and "64 MiB" in _err(lib)
+
+
+@pytest.mark.parametrize("compiler,std,lang", [("gcc", "-std=c99", "c"), ("g++", "-std=c++11", "c++")])
+def test_header_compiles_as_plain_c_and_cpp(tmp_path, compiler, std, lang):
+    """The boundary header needs no CUDA or torch headers and no extensions."""
+    import shutil
+    import subprocess
+    if shutil.which(compiler) is None:
+        pytest.skip(f"{compiler} not installed")
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "pfkv.h"\nint main(void) { return pfkv_version() == 0; }\n')
+    r = subprocess.run([compiler, std, "-Wall", "-Wextra", "-Werror", "-pedantic", "-fsyntax-only", "-x", lang,
+                        "-I", os.path.join(ROOT, "include"), str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
