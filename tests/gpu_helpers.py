@@ -78,7 +78,7 @@ def gpu_pages_of(cache_dev, bt_row, kvh, L, P):
     import torch
     npg = (L + P - 1) // P
     pages = torch.as_tensor(bt_row[:npg].astype(np.int64), device=cache_dev.device)
-    rows = cache_dev.index_select(0, pages)[:, kvh]  # [npg][P][D]
+    rows = cache_dev[:, kvh].index_select(0, pages)  # [npg][P][D], this head only
     if rows.dtype == torch.bfloat16:
         rows = rows.view(torch.int16)
     return rows.reshape(npg * P, -1)[:L].cpu().numpy()

@@ -136,26 +136,63 @@ def test_workspace_too_small_is_rejected_on_host():
 
 
 # ------------------------------------------------------------ full-size, sampled
-def _sampled_check(p, w, st, out, lse, samples, bf16=False):
-    q = w.q_bits()
-    bt = w.block_tables
-    gots, refs = [], []
-    for (b, h) in samples:
-        kvh = h // w.G
-        L = int(w.context_lens[b])
-        kc, vc, bt_row = oracle_one_head(w, b, kvh, bf16=bf16)
-        got_k = gpu_pages_of(st.k_cache, bt[b], kvh, L, w.P)
-        got_v = gpu_pages_of(st.v_cache, bt[b], kvh, L, w.P)
-        if bf16:
-            got_k, got_v = got_k.view(np.uint16), got_v.view(np.uint16)
-        assert np.array_equal(got_k, kc.reshape(-1, w.D)[:L]), (b, kvh)
-        assert np.array_equal(got_v, vc.reshape(-1, w.D)[:L]), (b, kvh)
-        ks, vs = (1.0, 1.0) if bf16 else (w.k_scale, w.v_scale)
+def _check_group(w, st, q, out, lse, b, kvh, heads, bf16):
+    """One (request, KV head): the GPU's K/V rows of that head bit for bit
+    against the oracle's encoding of the host generator's rows, then every
+    listed query head of the group against the oracle's decode."""
+    L = int(w.context_lens[b])
+    kc, vc, bt_row = oracle_one_head(w, b, kvh, bf16=bf16)
+    got_k = gpu_pages_of(st.k_cache, w.block_tables[b], kvh, L, w.P)
+    got_v = gpu_pages_of(st.v_cache, w.block_tables[b], kvh, L, w.P)
+    if bf16:
+        got_k, got_v = got_k.view(np.uint16), got_v.view(np.uint16)
+    assert np.array_equal(got_k, kc.reshape(-1, w.D)[:L]), ("K rows", b, kvh)
+    assert np.array_equal(got_v, vc.reshape(-1, w.D)[:L]), ("V rows", b, kvh)
+    ks, vs = (1.0, 1.0) if bf16 else (w.k_scale, w.v_scale)
+    res = []
+    for h in heads:
         ref, ref_lse = oracle.paged_decode_one(q[b, h], kc, vc, bt_row, L, 0, w.P, ks, vs, w.softmax_scale)
-        gots.append(out[b, h])
-        refs.append(ref)
-        assert abs(lse[b, h] - ref_lse) <= 2e-4 + 2e-5 * abs(ref_lse)
-    assert_within_tolerance(np.stack(gots), np.stack(refs), f"{w.name} sampled {samples}")
+        assert abs(lse[b, h] - ref_lse) <= 2e-4 + 2e-5 * abs(ref_lse), ("lse", b, h, lse[b, h], ref_lse)
+        res.append((out[b, h], ref))
+    return res
+
+
+def _sampled_check(p, w, st, out, lse, samples, bf16=False, threads=8):
+    """Every sampled (request, query head) against the oracle; the samples are
+    grouped by (request, KV head) so each group's rows are encoded once, and
+    the groups run on host threads (the oracle's ctypes calls release the GIL)."""
+    from concurrent.futures import ThreadPoolExecutor
+    q = w.q_bits()
+    groups = {}
+    for (b, h) in samples:
+        groups.setdefault((int(b), int(h) // w.G), set()).add(int(h))
+    # longest contexts first, so the pool's tail is short
+    keys = sorted(groups, key=lambda k: -int(w.context_lens[k[0]]))
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        futs = [ex.submit(_check_group, w, st, q, out, lse, b, kvh, sorted(groups[(b, kvh)]), bf16)
+                for (b, kvh) in keys]
+        pairs = [r for f in futs for r in f.result()]
+    gots = np.stack([g for g, _ in pairs])
+    refs = np.stack([r for _, r in pairs])
+    assert_within_tolerance(gots, refs, f"{w.name} sampled {len(pairs)} (request, head) rows")
+
+
+def _appended_rows_check(w, st):
+    """The step's appended rows (every request, every KV head) bit for bit:
+    read back through the slot mapping and compared with the oracle's encoding
+    of the same bf16 rows."""
+    import torch
+    slots = w.step_slots()
+    if slots.size == 0:
+        return
+    T = slots.size
+    sl = torch.as_tensor(slots, device=st.k_cache.device)
+    for which, cache, scale in (("k", st.k_cache, w.k_scale), ("v", st.v_cache, w.v_scale)):
+        rows = cache.permute(0, 2, 1, 3).reshape(-1, w.Hkv, w.D)  # [page*P + off][Hkv][D]
+        got = rows.index_select(0, sl).cpu().numpy()
+        mini = np.zeros((T, w.Hkv, 1, w.D), np.uint8)
+        oracle.kv_append(w.step_kv_bits(which), mini, np.arange(T, dtype=np.int64), 1, scale)
+        assert np.array_equal(got, mini[:, :, 0, :]), f"appended {which} rows differ"
 
 
 def _samples(w, n, seed):
@@ -166,28 +203,53 @@ def _samples(w, n, seed):
 
 @pytest.mark.parametrize("bf16", [False, True])
 def test_mha_b32_full_size_sampled(bf16):
+    """MHA B 32 x 48 heads x 8192: every head of request 7 and of the last
+    request, plus seeded samples."""
     p = pf()
     w = synth.workload(synth.MHA_B32)
     st = _setup(p, w, bf16=bf16)
     out, lse, status = _run(p, w, st)
     assert status == 0
-    _sampled_check(p, w, st, out, lse, _samples(w, 6, 41) + [(0, 0), (31, 47)], bf16=bf16)
+    whole = [(7, h) for h in range(w.Hq)] + [(w.B - 1, h) for h in range(w.Hq)]
+    _sampled_check(p, w, st, out, lse, _samples(w, 6, 41) + [(0, 0)] + whole, bf16=bf16)
+    if not bf16:
+        _appended_rows_check(w, st)
 
 
 def test_gqa_shared_prefix_full_size_sampled():
+    """GQA 64/8 with a 2048-token prefix shared by requests 0-15: two query
+    heads (on different KV heads) of every sharer and of 16 private requests,
+    including the last."""
     p = pf()
     w = synth.workload(synth.GQA_PREFIX)
     st = _setup(p, w)
     out, lse, status = _run(p, w, st)
     assert status == 0
-    samples = _samples(w, 6, 43) + [(0, 0), (5, 63), (15, 8), (16, 9)]
+    privs = list(range(w.shared_requests, w.B, 3))[:15] + [w.B - 1]
+    samples = []
+    for i, b in enumerate(list(range(w.shared_requests)) + privs):
+        samples += [(b, (5 * i) % w.Hq), (b, (5 * i + 4 * w.G + 3) % w.Hq)]
+    samples += [(0, 0), (5, 63)]
     _sampled_check(p, w, st, out, lse, samples)
+    _appended_rows_check(w, st)
 
 
 def test_long_split_kv_full_size_sampled():
+    """Long split-KV B 8, contexts 256K-1M, 4096-token chunks: two query heads
+    on different KV heads of every request (both 1,048,576-token requests
+    included, the last KV head among them), and every request's eight appended
+    rows on every KV head."""
     p = pf()
     w = synth.workload(synth.LONG_SPLITKV)
     st = _setup(p, w)
     out, lse, status = _run(p, w, st, split=w.kv_split_tokens)
     assert status == 0
-    _sampled_check(p, w, st, out, lse, [(0, 0), (0, 1), (0, 63)])
+    samples = []
+    for b in range(w.B):
+        kv_a, kv_b = b % w.Hkv, (b + 4) % w.Hkv
+        samples += [(b, kv_a * w.G + (3 * b) % w.G), (b, kv_b * w.G + (5 * b + 1) % w.G)]
+    samples += [(0, 0), (w.B - 1, w.Hq - 1)]
+    assert {b for b, _ in samples} == set(range(w.B))
+    assert (w.Hq - 1) // w.G == w.Hkv - 1
+    _sampled_check(p, w, st, out, lse, samples)
+    _appended_rows_check(w, st)
