@@ -45,6 +45,52 @@ def test_every_bf16_pattern_encodes_like_the_oracle(scale):
     assert np.all(np.isin(got[nan_pos], [0x7F, 0xFF]))
 
 
+def _wide_scales(n):
+    """n seeded positive fp32 scales: exponent fields uniform over every
+    normal binade (1 .. 254) with random mantissas, so x / s spans subnormal,
+    normal and saturating e4m3 results for every bf16 input, plus the
+    smallest subnormal and the largest finite scale."""
+    key = gen.make_key(17, gen.TENSOR_PERM)
+    idx = np.arange(n, dtype=np.uint64)
+    e = gen.uniform_int(key, idx, 1, 254).astype(np.uint32)
+    m = (gen.uniform_u64(key ^ 0x9E3779B97F4A7C15, idx) & np.uint64(0x7FFFFF)).astype(np.uint32)
+    bits = (e << np.uint32(23)) | m
+    bits[0] = 0x00000001  # 2^-149
+    bits[1] = 0x7F7FFFFF  # largest finite fp32
+    return bits.view(np.float32)
+
+
+def test_every_bf16_pattern_over_512_scales_encodes_like_the_oracle():
+    """All 65536 bf16 patterns against 512 seeded scales (256 calls, K and V
+    each with its own scale) through the host-scalar append path: bit-exact
+    codes, NaN inputs excepted (any NaN code)."""
+    torch = _torch()
+    p = pf()
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    T, H, D, P = 4096, 1, 16, 16
+    x = bits.reshape(T, H, D)
+    slots = np.arange(T, dtype=np.int64)
+    pages = T // P
+    scales = _wide_scales(512)
+    xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+    sl = torch.from_numpy(slots).cuda()
+    nan_in = np.isnan(gen.bf16_bits_to_f32(bits)).reshape(pages, H, P, D)
+    kcs = torch.empty((256, pages, H, P, D), dtype=torch.uint8, device="cuda")
+    vcs = torch.empty_like(kcs)
+    for i in range(256):
+        p.kv_append_fp8(xd, xd, kcs[i], vcs[i], sl, float(scales[2 * i]), float(scales[2 * i + 1]))
+    got_k, got_v = kcs.cpu().numpy(), vcs.cpu().numpy()
+    bad = 0
+    for i in range(512):
+        ref = np.zeros((pages, H, P, D), np.uint8)
+        oracle.kv_append(x, ref, slots, P, float(scales[i]))
+        got = (got_k if i % 2 == 0 else got_v)[i // 2]
+        same = got == ref
+        bad += int((~same & ~nan_in).sum())
+        assert np.all(np.isin(got[nan_in], [0x7F, 0xFF]))
+    assert bad == 0, f"{bad} codes differ"
+
+
 def test_tiny_gqa_cache_bytes_bit_exact():
     torch = _torch()
     p = pf()
