@@ -224,7 +224,12 @@ PFKV_API int pfkv_paged_decode_attn(void *out, const void *q, const void *k_cach
  *  - All calls share the one array.  Two calls whose work overlaps on the GPU
  *    (different streams without ordering between them) race on it; order them.
  *  - status_out: optional device int32 that receives the device status word
- *    (PFKV_DEVERR_* bits) of this call, copied after the decode on `stream`.
+ *    (PFKV_DEVERR_* bits) of this call, copied after the decode on `stream`;
+ *    for batch == 0 it is set to 0 on `stream`.
+ *  - The array's device address is looked up once per device and kept for
+ *    the life of the process: resetting a device (cudaDeviceReset) while the
+ *    library is loaded is not supported, since later calls would use the
+ *    address the reset invalidated.
  *  - Other arguments, layouts and errors as pfkv_paged_decode_attn. */
 PFKV_API int pfkv_paged_decode_attn_noalloc(void *out, const void *q, const void *k_cache,
                                             const void *v_cache, pfkv_cache_dtype cache_dtype,

@@ -1398,7 +1398,12 @@ extern "C" int pfkv_paged_decode_attn_noalloc(
                               context_lens, batch, num_q_heads, num_kv_heads, head_dim, page_size,
                               num_pages, k_scale, v_scale, softmax_scale, kv_split_tokens, ws,
                               kNoAllocScratchBytes, lse_out, stream);
-  if (rc != PFKV_OK || status_out == nullptr || batch == 0) return rc;
+  if (rc != PFKV_OK || status_out == nullptr) return rc;
+  if (batch == 0) {  // nothing was enqueued: the status of an empty call is 0
+    if (cudaMemsetAsync(status_out, 0, sizeof(int32_t), reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return check_cuda("paged_decode_attn_noalloc: status clear");
+    return PFKV_OK;
+  }
   if (cudaMemcpyAsync(status_out, ws, sizeof(int32_t), cudaMemcpyDeviceToDevice,
                       reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return check_cuda("paged_decode_attn_noalloc: status copy");
