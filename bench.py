@@ -2,12 +2,15 @@
 
 A step is one pass of the whole hot path over one batch: kv_append_fp8 of the
 step's new K/V rows into the paged cache, then paged_decode_attn over every
-request (plan, tile kernel, merge).  The headline workload is the MHA layer of
-the pages' 60-layer / 48-KV-head / head_dim-128 example: batch 32, contexts of
-8192 tokens, page size 16, e4m3 cache (3.22 GB of KV, far larger than L2, so
-back-to-back steps stream from HBM).  Other workloads (GQA with a shared
-prefix, MLA top-k, long-context split-KV, the bf16 cache) are measured after
-the timed region and reported under "other_workloads".
+request (plan, tile kernel, merge).  The headline workload is the largest one
+that fits one GPU: long-context GQA split-KV decode, 8 requests of 256K to 1M
+tokens (5,636,096 in all), 64 query / 8 KV heads, head_dim 128, page size 64,
+e4m3 cache (11.54 GB of KV, far larger than L2, so back-to-back steps stream
+from HBM), 8 new tokens appended per request, 4096-token chunks merged by
+log-sum-exp.  Other workloads (MHA 32 x 48 x 8192 with e4m3 and bf16 caches,
+GQA with a shared prefix, MLA top-k, multi-query attention, scale
+granularities) are measured after the timed region and reported under
+"other_workloads".
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 Under torchrun each rank runs its own batch (request-level data parallelism,
@@ -34,8 +37,8 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 
 METRIC = "decode-attn KV GB/s (% of GB300 HBM peak) and query-tokens/s at 1 GPU"
-HEADLINE = "mha_b32_h48_l8192_p16"  # the headline workload: MHA 32 x 48 x 8192, page 16
-PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "paged_decode_kernel_mha_b32_l8192_traffic.txt")
+HEADLINE = "long_splitkv_b8_h64kv8_p64"  # the headline: 8 requests, 256K-1M tokens, 64/8 heads, page 64
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "paged_decode_kernel_long_b8_traffic.txt")
 DECODE_SRC = os.path.join(ROOT, "paged_fp8_kv_02_gb300", "csrc", "paged_decode.cu")
 
 
@@ -274,14 +277,14 @@ def time_events(fn, iters, flush=None):
     return statistics.median(a.elapsed_time(b) * 1e-3 for a, b in evs)
 
 
-def other_workloads(pf, peak_gbs, peak_tf, iters=10):
+def other_workloads(pf, peak_gbs, peak_tf, headline_step=None, iters=10):
     import torch
     import synth
     res = {}
     flush = torch.ones(128 << 20, dtype=torch.float32, device="cuda")  # 512 MB > L2 (129 MB)
 
-    def paged(name, w, bf16=False):
-        s = PagedStep(pf, w, bf16_cache=bf16)
+    def paged(name, w, bf16=False, step=None):
+        s = step if step is not None else PagedStep(pf, w, bf16_cache=bf16)
         for _ in range(3):
             s.step()
         torch.cuda.synchronize()
@@ -310,8 +313,9 @@ def other_workloads(pf, peak_gbs, peak_tf, iters=10):
                      "decode_with_page_tag_check_us": round(t_both * 1e6, 2),
                      "page_tag_check_added_pct": round(100 * (t_both - t_dec) / t_dec, 3),
                      "page_tag_check_flagged": int((req_status != 0).sum().item())}
-        del s
-        torch.cuda.empty_cache()
+        if step is None:
+            del s
+            torch.cuda.empty_cache()
 
     res["prefill"] = prefill_timing(pf, peak_gbs, peak_tf, flush, iters)
     res["scale_granularity_mha_b32_h48_l8192_p16"] = scale_granularity_timing(
@@ -320,8 +324,9 @@ def other_workloads(pf, peak_gbs, peak_tf, iters=10):
         pf, lambda: synth.workload(synth.GQA_PREFIX), peak_gbs, flush, iters)
     paged("gqa_prefix_b64_h64kv8_p16", synth.workload(synth.GQA_PREFIX))
     res["page_pool_gqa_prefix_host"] = page_pool_timing(pf, synth.workload(synth.GQA_PREFIX))
-    w5 = synth.workload(synth.LONG_SPLITKV)
-    paged("long_splitkv_b8_h64kv8_p64_chunk4096", w5)
+    if headline_step is not None:  # the headline's decode call alone, with the page-tag check
+        paged("long_splitkv_b8_h64kv8_p64_chunk4096", headline_step.w, step=headline_step)
+    paged("mha_b32_h48_l8192_p16", synth.workload(synth.MHA_B32))
     paged("mha_b32_h48_l8192_p16_bf16_cache", synth.workload(synth.MHA_B32), bf16=True)
     m = synth.workload(synth.MLA_TOPK)
     s = MlaStep(pf, m)
@@ -643,9 +648,7 @@ def run_reference(args, rank, ws):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(res["seconds_per_step"] * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": HEADLINE, "batch": w.B, "q_heads": w.Hq,
-                   "kv_heads": w.Hkv, "head_dim": w.D, "context": int(w.context_lens[0]), "page_size": w.P,
-                   "cache": "e4m3", "sample_requests": n_req, "scales": scales},
+        "config": dict(headline_config(w, 1), sample_requests=n_req, scales=scales),
         "query_tokens_per_s": round(res["query_tokens_per_s"], 3),
         "cpu_baseline": {k: res[k] for k in ("value", "unit", "cores", "kind", "sample")},
         "e2e": {"value": round(res["value"], 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -719,6 +722,7 @@ def run_gpu(args, rank, ws, local):
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak_gbs, "unit": "GB/s",
                 "frac": round(achieved / peak_gbs, 4), "traffic": traffic,
                 "kernel": "paged_decode_attn (plan + paged_decode_kernel + merge, one call)",
+                "traffic_of": "paged_decode_kernel, one launch (ncu on 2 x 262144 tokens, scaled by tokens x10.75)",
                 "algorithmic_bytes_per_launch": s.decode_bytes(), "launch_us": round(t_dec * 1e6, 2),
                 "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_src})"}
 
@@ -729,9 +733,7 @@ def run_gpu(args, rank, ws, local):
             cb = oracle_baseline(_with_scales(synth.workload(HEADLINE), w), args.oracle_requests)
             cpu = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
         if not args.no_others:
-            del s
-            torch.cuda.empty_cache()
-            others = other_workloads(pf, peak_gbs, peak_tf)
+            others = other_workloads(pf, peak_gbs, peak_tf, headline_step=s)
 
     clocks = clk.summary()
     clocks["window"] = "50 ms samples over the timed region and 0.3 s of the same step before and after it"
@@ -741,11 +743,7 @@ def run_gpu(args, rank, ws, local):
             "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 cache; e4m3 score and f16 P.V mma, f32 accumulate",
             "data": "synthetic (seeded counter-based N(0,1) approximation)",
-            "config": {"workload": HEADLINE, "batch_per_gpu": w.B, "q_heads": w.Hq,
-                       "kv_heads": w.Hkv, "head_dim": w.D, "context": int(w.context_lens[0]),
-                       "page_size": w.P, "new_tokens_per_request": w.n_new, "cache": "e4m3",
-                       "parallelism": f"request-dp{ws}",
-                       "l2": "inputs larger than L2 (3.22 GB KV per step); no flush between steps"},
+            "config": headline_config(w, ws),
             "pct_of_hbm_peak": round(100 * value / (ws * peak_gbs), 2),
             "query_tokens_per_s": round(qps, 1),
             "step_bytes": step_bytes,
@@ -757,6 +755,13 @@ def run_gpu(args, rank, ws, local):
             "other_workloads": others,
         }
         print(json.dumps(line), flush=True)
+
+
+def headline_config(w, ws):
+    return {"workload": HEADLINE, "batch_per_gpu": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D,
+            "contexts": [int(x) for x in w.context_lens], "page_size": w.P, "new_tokens_per_request": w.n_new,
+            "kv_split_tokens": w.kv_split_tokens, "cache": "e4m3", "parallelism": f"request-dp{ws}",
+            "l2": f"inputs larger than L2 ({w.kv_bytes() / 1e9:.2f} GB of KV per step); no flush between steps"}
 
 
 def s_launches(steps):
@@ -911,7 +916,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--oracle-requests", type=int, default=8)
+    ap.add_argument("--oracle-requests", type=int, default=1,
+                    help="requests of the headline workload in the CPU oracle's sample (request 0 first)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-others", action="store_true")
     args = ap.parse_args()

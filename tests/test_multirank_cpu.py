@@ -63,4 +63,4 @@ def test_reference_arm_under_torchrun_prints_once_from_rank0():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
-    assert d["config"]["workload"] == "mha_b32_h48_l8192_p16"
+    assert d["config"]["workload"] == "long_splitkv_b8_h64kv8_p64"
