@@ -328,22 +328,24 @@ def other_workloads(pf, peak_gbs, peak_tf, headline_step=None, iters=10):
         paged("long_splitkv_b8_h64kv8_p64_chunk4096", headline_step.w, step=headline_step)
     paged("mha_b32_h48_l8192_p16", synth.workload(synth.MHA_B32))
     paged("mha_b32_h48_l8192_p16_bf16_cache", synth.workload(synth.MHA_B32), bf16=True)
-    m = synth.workload(synth.MLA_TOPK)
-    s = MlaStep(pf, m)
-    for _ in range(3):
-        s.append()
-        s.decode()
-    torch.cuda.synchronize()
-    t_dec = time_events(s.decode, iters, flush)
-    gbs = s.decode_bytes() / t_dec / 1e9
-    res["mla_topk2048_b64_h128_l65536_p64"] = {
-        "decode_us": round(t_dec * 1e6, 2), "decode_GBs": round(gbs, 1),
-        "frac_of_hbm_peak": round(gbs / peak_gbs, 4),
-        "tflops": round(m.flops() / t_dec / 1e12, 2),
-        "frac_of_bf16_peak": round(m.flops() / t_dec / 1e12 / peak_tf, 4),
-        "query_tokens_per_s": round(m.B / t_dec, 1)}
-    del s
-    torch.cuda.empty_cache()
+    for name, m in (("mla_topk2048_b64_h128_l65536_p64", synth.workload(synth.MLA_TOPK)),
+                    ("mla_topk2048_b16_h128_l65536_p64",
+                     synth.MlaWorkload("mla_b16", B=16, H=128, context_lens=np.full(16, 65536), topk_n=2048, P=64))):
+        s = MlaStep(pf, m)
+        for _ in range(3):
+            s.append()
+            s.decode()
+        torch.cuda.synchronize()
+        t_dec = time_events(s.decode, iters, flush)
+        gbs = s.decode_bytes() / t_dec / 1e9
+        res[name] = {
+            "decode_us": round(t_dec * 1e6, 2), "decode_GBs": round(gbs, 1),
+            "frac_of_hbm_peak": round(gbs / peak_gbs, 4),
+            "tflops": round(m.flops() / t_dec / 1e12, 2),
+            "frac_of_bf16_peak": round(m.flops() / t_dec / 1e12 / peak_tf, 4),
+            "query_tokens_per_s": round(m.B / t_dec, 1)}
+        del s
+        torch.cuda.empty_cache()
     return res
 
 

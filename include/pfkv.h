@@ -362,7 +362,16 @@ PFKV_API int pfkv_paged_prefill_attn(void *out, const void *q, const void *k_cac
  * of SMs that each contract part of the 576 columns; a score is one SM's
  * exact f32 partial plus the other's partial carried as 16-bit fixed point
  * over its range within a 32-token tile (at most range / 65535 added error,
- * in log2 units).  The workspace holds only the status word. */
+ * in log2 units).
+ * Small batches: when 2 * batch SMs leave pairs of SMs idle, each request's
+ * list is split into runs of at least 256 positions handled by separate
+ * pairs, whose (reference, sum, unnormalised output) states are folded by
+ * log-sum-exp in a second kernel (kLLM article §5.2.2: blockwise states
+ * combine to full attention).  pfkv_mla_decode_workspace_size returns the
+ * status word plus room for those states (batch * splits * num_heads * 2064
+ * bytes, splits chosen from the current device's SM count); with a smaller
+ * workspace (at least 256 bytes) the call uses as many splits as fit, down
+ * to one.  The split changes only the order of the softmax sums. */
 PFKV_API size_t pfkv_mla_decode_workspace_size(int batch, int num_heads, int d_latent, int topk);
 PFKV_API int pfkv_mla_decode_attn(void *out, const void *q, const void *ckv_cache,
                          const int32_t *block_tables, int max_pages_per_seq,

@@ -119,6 +119,10 @@ struct MlaArgs {
   const int32_t* topk;
   float* lse;
   int32_t* status;
+  float* part_o;      // split calls: raw O of every (request, split) [B * nsplit][H][512] fp32
+  float2* part_ml;    // split calls: (reference, running sum) [B * nsplit][2 halves][H]
+  int nsplit;         // clusters per request (list positions split into nsplit runs)
+  int chunk_pos;      // list positions per split (a multiple of 32)
   int topk_n, B, H, P, max_pages;
   int p_shift;        // log2(P) when P is a power of two, else -1
   int64_t num_pages;
@@ -230,13 +234,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   const uint32_t rank = tc::cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
-  const int b = blockIdx.x >> 1;
+  const int cid = blockIdx.x >> 1;           // cluster: (request, split of its list)
+  const int b = cid / a.nsplit, split = cid - b * a.nsplit;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   int L = a.context_lens[b];
   if (L < 0) L = 0;
   if (L > a.max_pages * a.P) L = a.max_pages * a.P;
-  const int n = a.topk ? a.topk_n : L;
+  // this cluster's run of list positions: p0 .. p0 + n - 1
+  const int p0 = split * a.chunk_pos;
+  const int n_all = a.topk ? a.topk_n : L;
+  const int n = max(0, min(n_all - p0, a.chunk_pos));
   const int ntiles = (n + kTok - 1) / kTok;
 
   if (threadIdx.x == 0) {
@@ -458,7 +466,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int m = 0; m < 8; ++m) {
         const int p = c * kChunkPos + lane + 32 * m;
-        tok[m] = p < n ? (a.topk ? a.topk[tbase + p] : p) : -1;
+        tok[m] = p < n ? (a.topk ? a.topk[tbase + p0 + p] : p0 + p) : -1;
       }
 #pragma unroll
       for (int m = 0; m < 8; ++m) {
@@ -687,6 +695,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (ntiles > 0 && !to)
       to = !mbar_wait(smem_u32(&bs.pvdone[(ntiles - 1) % kBufs]), ((ntiles - 1) / kBufs) & 1);
     tc::fence_after_sync();
+    if (a.nsplit > 1) {
+      // a split of the list: the raw accumulator, reference and sum go to the
+      // workspace; mla_merge_kernel folds the splits by log-sum-exp
+      const int64_t u = (int64_t)b * a.nsplit + split;
+      float* dstf = a.part_o + (u * a.H + t) * kDv + kLatCols * rank;
+#pragma unroll 1
+      for (int c = 0; c < kLatCols / 32; ++c) {
+        uint32_t v[32];
+        if (ntiles > 0) {
+          tc::tmem_ld32(tl + kTmemO + 32 * c, v);
+          tc::tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0u;
+        }
+        if (t < a.H) {
+          uint4* d4 = reinterpret_cast<uint4*>(dstf + 32 * c);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) d4[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        }
+      }
+      if (t < a.H) a.part_ml[(u * 2 + rank) * a.H + t] = make_float2(l > 0.f ? mref : -INFINITY, l);
+    } else {
     const float inv = l > 0.f ? a.out_scale / l : 0.f;
     uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) + ((int64_t)b * a.H + t) * kDv + kLatCols * rank;
 #pragma unroll 1
@@ -708,6 +739,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     if (rank == 0 && a.lse && t < a.H)
       a.lse[(int64_t)b * a.H + t] = l > 0.f ? (mref + __log2f(l)) * kLn2 : -INFINITY;
+    }
   }
 
   if (to) atomicOr(a.status, kErrWaitTimeout);
@@ -717,17 +749,81 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
+// Folds the splits of each (request, head) row: with m_s the reference (log2
+// units) and l_s the running sum of split s for this half of the columns,
+// M = max_s m_s, out = ckv_scale * sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s
+// (kLLM article §5.2.2: blockwise (m, l, O) states combine to full attention).
+// One warp per row; lane i takes columns 4i .. 4i + 3 of each 128-column block.
+constexpr int kMergeWarps = 8;
+__global__ void __launch_bounds__(kMergeWarps * 32) mla_merge_kernel(const MlaArgs a) {
+  const int row = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= a.B * a.H) return;
+  const int b = row / a.H, hh = row - b * a.H;
+  float lse_val = -INFINITY;
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    float M = -INFINITY;
+    for (int s = 0; s < a.nsplit; ++s)
+      M = fmaxf(M, a.part_ml[(((int64_t)b * a.nsplit + s) * 2 + half) * a.H + hh].x);
+    float Lsum = 0.f;
+    float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+    for (int s = 0; s < a.nsplit; ++s) {
+      const int64_t u = (int64_t)b * a.nsplit + s;
+      const float2 ml = a.part_ml[(u * 2 + half) * a.H + hh];
+      if (!(ml.y > 0.f)) continue;
+      const float w = exp2f(ml.x - M);
+      Lsum += w * ml.y;
+      const float* src = a.part_o + (u * a.H + hh) * kDv + kLatCols * half;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float4 o = *reinterpret_cast<const float4*>(src + 128 * k + 4 * lane);
+        acc[k].x += w * o.x;
+        acc[k].y += w * o.y;
+        acc[k].z += w * o.z;
+        acc[k].w += w * o.w;
+      }
+    }
+    const float inv = Lsum > 0.f ? a.out_scale / Lsum : 0.f;
+    uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) + (int64_t)row * kDv + kLatCols * half;
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+      *reinterpret_cast<uint2*>(dst + 128 * k + 4 * lane) =
+          make_uint2(pack_bf16x2(acc[k].x * inv, acc[k].y * inv), pack_bf16x2(acc[k].z * inv, acc[k].w * inv));
+    if (half == 0) lse_val = Lsum > 0.f ? (M + __log2f(Lsum)) * kLn2 : -INFINITY;
+  }
+  if (a.lse && lane == 0) a.lse[row] = lse_val;
+}
+
+// Clusters per request: enough to fill the GPU's SM pairs (one cluster of two
+// CTAs per pair) when the batch alone does not, each split taking at least
+// kMinSplitTiles tiles of the list.
+constexpr int kMinSplitTiles = 8;
+constexpr size_t kWsHead = 256;  // status word
+size_t split_bytes(int num_heads) { return (size_t)num_heads * (kDv * sizeof(float) + 2 * sizeof(float2)); }
+int max_splits(int batch, int64_t list_len) {
+  if (batch <= 0) return 1;
+  const int pairs = device_sm_count() / 2;
+  int ns = pairs / batch;
+  const int64_t tiles = (list_len + kTok - 1) / kTok;
+  const int64_t by_len = tiles / kMinSplitTiles;
+  if (ns > by_len) ns = (int)by_len;
+  return ns < 1 ? 1 : ns;
+}
+
 }  // namespace
 }  // namespace pfkv
 
 extern "C" {
 
 size_t pfkv_mla_decode_workspace_size(int batch, int num_heads, int d_latent, int topk) {
-  (void)batch;
-  (void)num_heads;
   (void)d_latent;
-  (void)topk;
-  return 256;  // status word
+  using namespace pfkv;
+  if (batch <= 0 || num_heads <= 0) return kWsHead;
+  // topk <= 0 (every token attended): the split count is bounded by the SM pairs alone
+  const int ns = max_splits(batch, topk > 0 ? topk : ((int64_t)1 << 30));
+  if (ns <= 1) return kWsHead;
+  return kWsHead + (size_t)batch * ns * split_bytes(num_heads);
 }
 
 int pfkv_mla_decode_attn(void* out, const void* q, const void* ckv_cache, const int32_t* block_tables,
@@ -777,6 +873,17 @@ int pfkv_mla_decode_attn(void* out, const void* q, const void* ckv_cache, const 
   a.num_pages = num_pages;
   a.score_scale = ckv_scale * softmax_scale * kLog2e;
   a.out_scale = ckv_scale;
+  // split each request's list over several clusters when the batch leaves SM
+  // pairs idle, as far as the workspace holds the partial states
+  const int64_t list_len = topk_idx ? (int64_t)topk : (int64_t)max_pages_per_seq * page_size;
+  int nsplit = max_splits(batch, list_len);
+  while (nsplit > 1 && kWsHead + (size_t)batch * nsplit * split_bytes(num_heads) > workspace_bytes) --nsplit;
+  const int64_t tiles = (list_len + kTok - 1) / kTok;
+  a.nsplit = nsplit;
+  a.chunk_pos = (int)(((tiles + nsplit - 1) / nsplit) * kTok);
+  a.part_o = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kWsHead);
+  a.part_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + kWsHead +
+                                        (size_t)batch * nsplit * num_heads * kDv * sizeof(float));
   static std::atomic<uint64_t> smem_set{0};
   const int smem_rc = set_max_dynamic_smem(reinterpret_cast<const void*>(mla_decode_kernel), (int)kSmemBytes, smem_set,
                                        "mla_decode set smem attribute");
@@ -794,7 +901,9 @@ int pfkv_mla_decode_attn(void* out, const void* q, const void* ckv_cache, const 
     rc = encode_tensor_map(&tm1, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(ckv_cache), dims, strides,
                            box1, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (rc != PFKV_OK) return rc;
-  mla_decode_kernel<<<dim3(2 * batch), kThreads, kSmemBytes, s>>>(tm0, tm1, a);
+  mla_decode_kernel<<<dim3(2 * batch * nsplit), kThreads, kSmemBytes, s>>>(tm0, tm1, a);
+  if (nsplit > 1)
+    mla_merge_kernel<<<dim3((batch * num_heads + kMergeWarps - 1) / kMergeWarps), kMergeWarps * 32, 0, s>>>(a);
   return check_cuda("mla_decode launch");
 }
 

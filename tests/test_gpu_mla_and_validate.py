@@ -60,6 +60,53 @@ def test_mla_small_cases_match_oracle(case):
     np.testing.assert_allclose(lse, ref_lse, rtol=2e-5, atol=2e-4)
 
 
+def _mla_check(p, m, st, topk=None, ws=None, what="mla"):
+    import torch
+    out = torch.empty((m.B, m.H, m.Dv), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((m.B, m.H), dtype=torch.float32, device="cuda")
+    tk = st.topk if topk is None else torch.from_numpy(topk).cuda()
+    ws = p.mla_decode_attn(out, st.q, st.ckv_cache, st.block_tables, st.context_lens,
+                           tk if (m.topk is not None or topk is not None) else None, m.ckv_scale, m.softmax_scale,
+                           lse_out=lse, workspace=ws)
+    torch.cuda.synchronize()
+    assert p.workspace_status(ws) == 0
+    c = _oracle_cache(m)
+    ref, ref_lse = oracle.mla_decode(m.q_bits(), c, m.block_tables, m.context_lens,
+                                     m.topk if topk is None else topk, m.P, m.Dv, m.ckv_scale, m.softmax_scale)
+    assert_within_tolerance(to_np_bf16(out), ref, what)
+    fin = np.isfinite(ref_lse)
+    np.testing.assert_allclose(lse.cpu().numpy()[fin], ref_lse[fin], rtol=2e-5, atol=2e-4)
+    assert np.all(np.isneginf(lse.cpu().numpy()[~fin]))
+    return to_np_bf16(out)
+
+
+def test_mla_small_batch_splits_lists_across_sm_pairs():
+    """Three requests leave most SM pairs idle, so each list (every token here)
+    is split into runs on separate pairs and folded by log-sum-exp; the short
+    request's later runs are empty."""
+    p = pf()
+    m = synth.MlaWorkload("mla_split", B=3, H=128, context_lens=np.array([4000, 2500, 70]), topk_n=0, P=64, seed=12)
+    assert p.mla_decode_workspace_size(3, 128, 512, 0) > 256  # room for the split states
+    st = _setup_mla(p, m)
+    full = _mla_check(p, m, st, what="mla split across pairs")
+    import torch
+    one = torch.empty(256, dtype=torch.uint8, device="cuda")  # room for no split: one pair per request
+    single = _mla_check(p, m, st, ws=one, what="mla unsplit")
+    assert np.abs(full - single).max() < 0.05
+
+
+def test_mla_split_with_padded_and_partial_lists():
+    """Top-k lists split across pairs where one request's second half is all
+    padding (a run with no token at all)."""
+    p = pf()
+    m = synth.MlaWorkload("mla_split_pad", B=2, H=64, context_lens=np.array([3000, 2000]), topk_n=600, P=64,
+                          seed=14)
+    st = _setup_mla(p, m)
+    tk = m.topk.copy()
+    tk[1, 300:] = -1
+    _mla_check(p, m, st, topk=tk, what="mla split, padded list")
+
+
 def test_mla_topk_padding_and_out_of_range_indices():
     import torch
     p = pf()
