@@ -304,6 +304,22 @@ def other_workloads(pf, peak_gbs, peak_tf, headline_step=None, iters=10):
             check()
             s.decode()
         t_both = time_events(checked_decode, iters, flush)
+        # the check does not feed the decode (it flags requests for the caller to
+        # drop), so it can also run beside it: on a side stream forked from and
+        # joined back into the decode's stream
+        side = torch.cuda.Stream()
+        fork, join = torch.cuda.Event(), torch.cuda.Event()
+
+        def concurrent_checked_decode():
+            main = torch.cuda.current_stream()
+            fork.record(main)
+            side.wait_event(fork)
+            with torch.cuda.stream(side):
+                check()
+                join.record(side)
+            s.decode()
+            main.wait_event(join)
+        t_conc = time_events(concurrent_checked_decode, iters, flush)
         res[name] = {"decode_us": round(t_dec * 1e6, 2), "append_us": round(t_app * 1e6, 2),
                      "kv_bytes": s.bytes()["kv"], "decode_GBs": round(gbs, 1),
                      "frac_of_hbm_peak": round(gbs / peak_gbs, 4),
@@ -312,6 +328,8 @@ def other_workloads(pf, peak_gbs, peak_tf, headline_step=None, iters=10):
                      "page_tag_check_pct_of_decode": round(100 * t_chk / t_dec, 3),
                      "decode_with_page_tag_check_us": round(t_both * 1e6, 2),
                      "page_tag_check_added_pct": round(100 * (t_both - t_dec) / t_dec, 3),
+                     "decode_with_concurrent_page_tag_check_us": round(t_conc * 1e6, 2),
+                     "page_tag_check_concurrent_added_pct": round(100 * (t_conc - t_dec) / t_dec, 3),
                      "page_tag_check_flagged": int((req_status != 0).sum().item())}
         if step is None:
             del s
