@@ -161,6 +161,37 @@ def test_mla_topk2048_full_size_sampled():
     assert_within_tolerance(np.stack(gots), np.stack(refs), "MLA 64 x 128 heads, top-k 2048, 4 whole requests")
 
 
+def test_mla_topk2048_batch16_split_full_size_sampled():
+    """16 requests x 128 heads, top-k 2048 of 65536: the lists are split over
+    idle SM pairs and folded; every head of requests 0 and 15 against the
+    oracle, with their selected latent rows bit for bit."""
+    import torch
+    p = pf()
+    m = synth.MlaWorkload("mla_b16", B=16, H=128, context_lens=np.full(16, 65536), topk_n=2048, P=64)
+    assert p.mla_decode_workspace_size(16, 128, 512, 2048) > 256  # the split states fit
+    st = _setup_mla(p, m)
+    out, lse, status = _run_mla(p, m, st)
+    assert status == 0
+    q = m.q_bits()
+    gots, refs = [], []
+    for b in (0, m.B - 1):
+        tok = m.topk[b]
+        rows = m.ckv_rows_bits(b, tok)
+        mini = np.zeros((len(tok), 1, 1, m.Dqk), np.uint8)
+        oracle.kv_append(rows[:, None, :], mini, np.arange(len(tok), dtype=np.int64), 1, m.ckv_scale)
+        mini = mini.reshape(len(tok), 1, m.Dqk)
+        pages = torch.as_tensor(m.block_tables[b, tok // m.P].astype(np.int64), device="cuda")
+        offs = torch.as_tensor((tok % m.P).astype(np.int64), device="cuda")
+        assert np.array_equal(st.ckv_cache[pages, offs].cpu().numpy(), mini[:, 0, :]), b
+        for h in range(m.H):
+            ref, ref_lse = oracle.mla_decode_one(q[b, h], mini, np.arange(len(tok), dtype=np.int32),
+                                                 len(tok), None, 1, m.Dv, m.ckv_scale, m.softmax_scale)
+            gots.append(out[b, h])
+            refs.append(ref)
+            assert abs(lse[b, h] - ref_lse) <= 2e-4 + 2e-5 * abs(ref_lse), (b, h)
+    assert_within_tolerance(np.stack(gots), np.stack(refs), "MLA 16 x 128 heads, top-k 2048, split")
+
+
 def test_validate_tables_flags_each_error_kind():
     import torch
     p = pf()
