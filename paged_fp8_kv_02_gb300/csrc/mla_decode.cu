@@ -247,6 +247,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int n = max(0, min(n_all - p0, a.chunk_pos));
   const int ntiles = (n + kTok - 1) / kTok;
 
+  // This CTA's span of the request's query rows (128-byte lines 4 rank ..
+  // 4 rank + 3 of each 1152-byte row, plus line 8, the rope, for rank 1) into
+  // L2 now, so that the conversion below reads them from L2 while the
+  // barriers, tensor memory and the first gathers are set up.
+  {
+    const int lines = rank ? 5 : 4;
+    const char* q0 = reinterpret_cast<const char*>(a.q + (int64_t)b * a.H * kDqk) + 512 * rank;
+    for (int i = threadIdx.x; i < a.H * lines; i += kThreads) {
+      const int row = i / lines, ln = i - row * lines;
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(q0 + (int64_t)row * (2 * kDqk) + 128 * ln));
+    }
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&bs.stage_full[s]), 1);
@@ -557,21 +569,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint8_t* qr = smem + kOffQRope + t * 128;
       float amax = 0.f;
       auto convert = [&](float qs) {
+        // two chunks of 64 columns per round: sixteen 16-byte loads in flight
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
+        for (int c0 = 0; c0 < 4; c0 += 2) {
+          uint4 xs[16];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            uint4 x = make_uint4(0, 0, 0, 0);
-            if (have) x = ldg_nc(qrow + kLatCols * rank + 64 * c + 8 * u);
-            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[k])), fabsf(bf16_hi(w[k]))));
-              v[4 * u + k] = bf16x2_to_f16x2(w[k], qs);
-            }
+          for (int u = 0; u < 16; ++u) {
+            xs[u] = make_uint4(0, 0, 0, 0);
+            if (have) xs[u] = ldg_nc(qrow + kLatCols * rank + 64 * c0 + 8 * u);
           }
-          tc::tmem_st32(tl + kTmemQ + 32 * c, v);
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t v[32];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const uint4 x = xs[8 * cc + u];
+              const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[k])), fabsf(bf16_hi(w[k]))));
+                v[4 * u + k] = bf16x2_to_f16x2(w[k], qs);
+              }
+            }
+            tc::tmem_st32(tl + kTmemQ + 32 * (c0 + cc), v);
+          }
         }
 #pragma unroll
         for (int u = 0; u < 8 * (int)rank; ++u) {
