@@ -290,6 +290,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc::fence_before_sync();
   tc::cluster_sync();  // both CTAs' barriers initialised before any remote arrival
   tc::fence_after_sync();
+  grid_launch_dependents();  // the merge of a split call may be scheduled as CTAs retire
   const uint32_t tmem = bs.tmem_base;
   bool to = false;  // this thread gave up a wait
 
@@ -777,6 +778,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // One warp per row; lane i takes columns 4i .. 4i + 3 of each 128-column block.
 constexpr int kMergeWarps = 8;
 __global__ void __launch_bounds__(kMergeWarps * 32) mla_merge_kernel(const MlaArgs a) {
+  grid_dependency_wait();  // every run's state is written and visible
   const int row = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= a.B * a.H) return;
@@ -923,8 +925,21 @@ int pfkv_mla_decode_attn(void* out, const void* q, const void* ckv_cache, const 
                            box1, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (rc != PFKV_OK) return rc;
   mla_decode_kernel<<<dim3(2 * batch * nsplit), kThreads, kSmemBytes, s>>>(tm0, tm1, a);
-  if (nsplit > 1)
-    mla_merge_kernel<<<dim3((batch * num_heads + kMergeWarps - 1) / kMergeWarps), kMergeWarps * 32, 0, s>>>(a);
+  if (nsplit > 1) {
+    // a programmatic dependent: its launch overlaps the tail of the decode
+    // kernel; it waits (griddepcontrol.wait) before reading the run states
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3((batch * num_heads + kMergeWarps - 1) / kMergeWarps);
+    cfg.blockDim = dim3(kMergeWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    if (cudaLaunchKernelEx(&cfg, mla_merge_kernel, a) != cudaSuccess) return check_cuda("mla_decode merge launch");
+  }
   return check_cuda("mla_decode launch");
 }
 
