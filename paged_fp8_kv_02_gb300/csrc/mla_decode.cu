@@ -718,10 +718,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       to = !mbar_wait(smem_u32(&bs.pvdone[(ntiles - 1) % kBufs]), ((ntiles - 1) / kBufs) & 1);
     tc::fence_after_sync();
     if (a.nsplit > 1) {
-      // a split of the list: the raw accumulator, reference and sum go to the
-      // workspace; mla_merge_kernel folds the splits by log-sum-exp
+      // A run of a split list: the raw accumulator, reference and sum go to
+      // the workspace; mla_merge_kernel folds the runs by log-sum-exp.  Each
+      // 32-column chunk of this warp's 32 rows goes through shared memory (the
+      // widened-tile buffers, idle once the last output product is done) so
+      // that every store instruction writes whole 128-byte runs of 4 rows.
+      float* stg = reinterpret_cast<float*>(smem + kOffC) + (warp - kSoftWarp0) * (32 * 33);
       const int64_t u = (int64_t)b * a.nsplit + split;
-      float* dstf = a.part_o + (u * a.H + t) * kDv + kLatCols * rank;
 #pragma unroll 1
       for (int c = 0; c < kLatCols / 32; ++c) {
         uint32_t v[32];
@@ -732,35 +735,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0u;
         }
-        if (t < a.H) {
-          uint4* d4 = reinterpret_cast<uint4*>(dstf + 32 * c);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) d4[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        for (int i = 0; i < 32; ++i) stg[lane * 33 + i] = __uint_as_float(v[i]);
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int r = 4 * k + (lane >> 3), c4 = 4 * (lane & 7);
+          const int row = 32 * (warp - kSoftWarp0) + r;  // head
+          const float* sp = stg + r * 33 + c4;
+          if (row < a.H)
+            *reinterpret_cast<float4*>(a.part_o + (u * a.H + row) * kDv + kLatCols * rank + 32 * c + c4) =
+                make_float4(sp[0], sp[1], sp[2], sp[3]);
         }
+        __syncwarp();  // the staging rows are rewritten by the next chunk
       }
       if (t < a.H) a.part_ml[(u * 2 + rank) * a.H + t] = make_float2(l > 0.f ? mref : -INFINITY, l);
     } else {
-    const float inv = l > 0.f ? a.out_scale / l : 0.f;
-    uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) + ((int64_t)b * a.H + t) * kDv + kLatCols * rank;
+      const float inv = l > 0.f ? a.out_scale / l : 0.f;
+      uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) + ((int64_t)b * a.H + t) * kDv + kLatCols * rank;
 #pragma unroll 1
-    for (int c = 0; c < kLatCols / 32; ++c) {
-      uint32_t v[32];
-      if (ntiles > 0) {
-        tc::tmem_ld32(tl + kTmemO + 32 * c, v);
-        tc::tmem_ld_wait();
-      }
-      if (t < a.H) {
-        uint32_t pk[16];
+      for (int c = 0; c < kLatCols / 32; ++c) {
+        uint32_t v[32];
+        if (ntiles > 0) {
+          tc::tmem_ld32(tl + kTmemO + 32 * c, v);
+          tc::tmem_ld_wait();
+        }
+        if (t < a.H) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = l > 0.f ? pack_bf16x2(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv) : 0u;
-        uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+          for (int i = 0; i < 16; ++i)
+            pk[i] = l > 0.f ? pack_bf16x2(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv) : 0u;
+          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
       }
-    }
-    if (rank == 0 && a.lse && t < a.H)
-      a.lse[(int64_t)b * a.H + t] = l > 0.f ? (mref + __log2f(l)) * kLn2 : -INFINITY;
+      if (rank == 0 && a.lse && t < a.H)
+        a.lse[(int64_t)b * a.H + t] = l > 0.f ? (mref + __log2f(l)) * kLn2 : -INFINITY;
     }
   }
 
