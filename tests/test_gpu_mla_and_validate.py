@@ -129,67 +129,66 @@ def test_mla_topk_padding_and_out_of_range_indices():
     assert_within_tolerance(out2, ref, "mla bad index skipped")
 
 
-def test_mla_topk2048_full_size_sampled():
-    """MLA B 64 x 128 heads, top-k 2048 of 65536: every head of requests 0,
-    21, 42 and 63 (the first and last clusters of the grid among them), each
-    request's selected latent rows checked bit for bit first."""
+def _mla_request_check(m, st, q, out, lse, b, heads):
+    """One request: its selected latent rows on the GPU bit for bit against
+    the oracle's encoding of the host generator's rows, then each listed head
+    against the oracle's decode over those rows."""
     import torch
+    tok = m.topk[b]
+    rows = m.ckv_rows_bits(b, tok)  # [k][576] bf16 bits of the selected tokens
+    mini = np.zeros((len(tok), 1, 1, m.Dqk), np.uint8)
+    oracle.kv_append(rows[:, None, :], mini, np.arange(len(tok), dtype=np.int64), 1, m.ckv_scale)
+    mini = mini.reshape(len(tok), 1, m.Dqk)
+    pages = torch.as_tensor(m.block_tables[b, tok // m.P].astype(np.int64), device="cuda")
+    offs = torch.as_tensor((tok % m.P).astype(np.int64), device="cuda")
+    assert np.array_equal(st.ckv_cache[pages, offs].cpu().numpy(), mini[:, 0, :]), ("latent rows", b)
+    res = []
+    for h in heads:
+        ref, ref_lse = oracle.mla_decode_one(q[b, h], mini, np.arange(len(tok), dtype=np.int32),
+                                             len(tok), None, 1, m.Dv, m.ckv_scale, m.softmax_scale)
+        assert abs(lse[b, h] - ref_lse) <= 2e-4 + 2e-5 * abs(ref_lse), ("lse", b, h)
+        res.append((out[b, h], ref))
+    return res
+
+
+def _mla_sampled(m, st, out, lse, whole, what):
+    """Every request's latent rows bit for bit; every head of the requests in
+    `whole`, and 8 heads (a different stride phase per request) of the rest."""
+    from concurrent.futures import ThreadPoolExecutor
+    q = m.q_bits()
+    plan = [(b, list(range(m.H)) if b in whole else list(range(b % 16, m.H, 16))) for b in range(m.B)]
+    with ThreadPoolExecutor(max_workers=8) as ex:
+        futs = [ex.submit(_mla_request_check, m, st, q, out, lse, b, hs) for b, hs in plan]
+        pairs = [r for f in futs for r in f.result()]
+    assert_within_tolerance(np.stack([g for g, _ in pairs]), np.stack([r for _, r in pairs]),
+                            f"{what}, {len(pairs)} sampled rows")
+
+
+def test_mla_topk2048_full_size_sampled():
+    """MLA B 64 x 128 heads, top-k 2048 of 65536: every request's selected
+    latent rows bit for bit; every head of requests 0, 21, 42 and 63 (the
+    first and last clusters of the grid among them) and 8 heads of each
+    other request against the oracle."""
     p = pf()
     m = synth.workload(synth.MLA_TOPK)
     st = _setup_mla(p, m)
     out, lse, status = _run_mla(p, m, st)
     assert status == 0
-    q = m.q_bits()
-    cache = st.ckv_cache
-    gots, refs = [], []
-    for b in (0, 21, 42, m.B - 1):
-        tok = m.topk[b]
-        rows = m.ckv_rows_bits(b, tok)  # [k][576] bf16 bits of the selected tokens
-        mini = np.zeros((len(tok), 1, 1, m.Dqk), np.uint8)
-        oracle.kv_append(rows[:, None, :], mini, np.arange(len(tok), dtype=np.int64), 1, m.ckv_scale)
-        mini = mini.reshape(len(tok), 1, m.Dqk)
-        pages = torch.as_tensor(m.block_tables[b, tok // m.P].astype(np.int64), device="cuda")
-        offs = torch.as_tensor((tok % m.P).astype(np.int64), device="cuda")
-        got_rows = cache[pages, offs].cpu().numpy()
-        assert np.array_equal(got_rows, mini[:, 0, :]), b
-        for h in range(m.H):
-            ref, ref_lse = oracle.mla_decode_one(q[b, h], mini, np.arange(len(tok), dtype=np.int32),
-                                                 len(tok), None, 1, m.Dv, m.ckv_scale, m.softmax_scale)
-            gots.append(out[b, h])
-            refs.append(ref)
-            assert abs(lse[b, h] - ref_lse) <= 2e-4 + 2e-5 * abs(ref_lse), (b, h)
-    assert_within_tolerance(np.stack(gots), np.stack(refs), "MLA 64 x 128 heads, top-k 2048, 4 whole requests")
+    _mla_sampled(m, st, out, lse, (0, 21, 42, m.B - 1), "MLA 64 x 128 heads, top-k 2048")
 
 
 def test_mla_topk2048_batch16_split_full_size_sampled():
     """16 requests x 128 heads, top-k 2048 of 65536: the lists are split over
-    idle SM pairs and folded; every head of requests 0 and 15 against the
-    oracle, with their selected latent rows bit for bit."""
-    import torch
+    idle SM pairs and folded; every request's selected latent rows bit for
+    bit, every head of requests 0 and 15 and 8 heads of each other request
+    against the oracle."""
     p = pf()
     m = synth.MlaWorkload("mla_b16", B=16, H=128, context_lens=np.full(16, 65536), topk_n=2048, P=64)
     assert p.mla_decode_workspace_size(16, 128, 512, 2048) > 256  # the split states fit
     st = _setup_mla(p, m)
     out, lse, status = _run_mla(p, m, st)
     assert status == 0
-    q = m.q_bits()
-    gots, refs = [], []
-    for b in (0, m.B - 1):
-        tok = m.topk[b]
-        rows = m.ckv_rows_bits(b, tok)
-        mini = np.zeros((len(tok), 1, 1, m.Dqk), np.uint8)
-        oracle.kv_append(rows[:, None, :], mini, np.arange(len(tok), dtype=np.int64), 1, m.ckv_scale)
-        mini = mini.reshape(len(tok), 1, m.Dqk)
-        pages = torch.as_tensor(m.block_tables[b, tok // m.P].astype(np.int64), device="cuda")
-        offs = torch.as_tensor((tok % m.P).astype(np.int64), device="cuda")
-        assert np.array_equal(st.ckv_cache[pages, offs].cpu().numpy(), mini[:, 0, :]), b
-        for h in range(m.H):
-            ref, ref_lse = oracle.mla_decode_one(q[b, h], mini, np.arange(len(tok), dtype=np.int32),
-                                                 len(tok), None, 1, m.Dv, m.ckv_scale, m.softmax_scale)
-            gots.append(out[b, h])
-            refs.append(ref)
-            assert abs(lse[b, h] - ref_lse) <= 2e-4 + 2e-5 * abs(ref_lse), (b, h)
-    assert_within_tolerance(np.stack(gots), np.stack(refs), "MLA 16 x 128 heads, top-k 2048, split")
+    _mla_sampled(m, st, out, lse, (0, m.B - 1), "MLA 16 x 128 heads, top-k 2048, split")
 
 
 def test_validate_tables_flags_each_error_kind():

@@ -156,8 +156,32 @@ def test_bad_arguments_are_rejected():
     assert e.value.code == -1
 
 
+def _prefill_group(w, st, qbits, out, lse, b, kvh, rows):
+    """One (request, KV head): the GPU's K/V rows of that head bit for bit
+    against the oracle's encoding, then each listed (query token, head)
+    against the oracle's decode over the context up to and including that token."""
+    L = int(w.context_lens[b])
+    kc, vc, bt_row = oracle_one_head(w, b, kvh)
+    assert np.array_equal(gpu_pages_of(st.k_cache, w.block_tables[b], kvh, L, w.P), kc.reshape(-1, w.D)[:L])
+    assert np.array_equal(gpu_pages_of(st.v_cache, w.block_tables[b], kvh, L, w.P), vc.reshape(-1, w.D)[:L])
+    qs = w.q_start()
+    res = []
+    for i, h in rows:
+        row = qs[b] + i
+        ref, ref_lse = oracle.paged_decode_one(qbits[row, h], kc, vc, bt_row, L - w.n_new + i + 1, 0, w.P,
+                                               w.k_scale, w.v_scale, w.softmax_scale)
+        assert abs(lse[row, h] - ref_lse) <= 2e-4 + 2e-5 * abs(ref_lse), ("lse", b, i, h)
+        res.append((out[row, h], ref))
+    return res
+
+
 def test_long_splitkv_appended_tokens_full_size_sampled():
+    """Long split-KV B 8 (256K-1M tokens), the 8 appended tokens of each
+    request as causal queries: for every request, two KV heads (the last KV
+    head among them), on each the first, a middle and the last appended token
+    with two query heads each."""
     import torch
+    from concurrent.futures import ThreadPoolExecutor
     from synth import device as sdev
     p = pf()
     w = synth.workload(synth.LONG_SPLITKV)
@@ -173,22 +197,17 @@ def test_long_splitkv_appended_tokens_full_size_sampled():
     torch.cuda.synchronize()
     assert p.workspace_status(ws) == 0
     out, lse = to_np_bf16(out), lse.cpu().numpy()
-    qs = w.q_start()
-    gots, refs = [], []
-    heads = {}
-    for b, i, h in [(0, 0, 0), (0, 7, 5), (3, 2, 17), (3, 6, 23)]:
-        kvh = h // w.G
-        L = int(w.context_lens[b])
-        if (b, kvh) not in heads:  # a 1M-token head takes seconds to regenerate
-            heads[(b, kvh)] = oracle_one_head(w, b, kvh)
-        kc, vc, bt_row = heads[(b, kvh)]
-        if i in (0, 2):
-            assert np.array_equal(gpu_pages_of(st.k_cache, w.block_tables[b], kvh, L, w.P), kc.reshape(-1, w.D)[:L])
-            assert np.array_equal(gpu_pages_of(st.v_cache, w.block_tables[b], kvh, L, w.P), vc.reshape(-1, w.D)[:L])
-        row = qs[b] + i
-        ref, ref_lse = oracle.paged_decode_one(qbits[row, h], kc, vc, bt_row, L - w.n_new + i + 1, 0, w.P,
-                                               w.k_scale, w.v_scale, w.softmax_scale)
-        gots.append(out[row, h])
-        refs.append(ref)
-        assert abs(lse[row, h] - ref_lse) <= 2e-4 + 2e-5 * abs(ref_lse)
-    assert_within_tolerance(np.stack(gots), np.stack(refs), "long split-KV appended tokens sampled")
+    groups = {}
+    for b in range(w.B):
+        for j, kvh in enumerate((b % w.Hkv, (b + 4) % w.Hkv)):
+            rows = []
+            for i in (0, (b + j) % w.n_new, w.n_new - 1):
+                rows += [(i, kvh * w.G + (3 * b + i) % w.G), (i, kvh * w.G + (5 * b + 2 * i + 1) % w.G)]
+            groups[(b, kvh)] = sorted(set(rows))
+    assert {kvh for _, kvh in groups} == set(range(w.Hkv))
+    keys = sorted(groups, key=lambda k: -int(w.context_lens[k[0]]))
+    with ThreadPoolExecutor(max_workers=8) as ex:
+        futs = [ex.submit(_prefill_group, w, st, qbits, out, lse, b, kvh, groups[(b, kvh)]) for b, kvh in keys]
+        pairs = [r for f in futs for r in f.result()]
+    assert_within_tolerance(np.stack([g for g, _ in pairs]), np.stack([r for _, r in pairs]),
+                            f"long split-KV appended tokens, {len(pairs)} sampled rows")
