@@ -233,6 +233,36 @@ class PagedStep:
         return b["kv"] + b["q"] + b["o"] + b["tables"]
 
 
+class TokenScaleStep:
+    """Resident cache of a workload with per-token K/V scales, filled by the
+    per-token append; its step appends and decodes with those scales."""
+
+    def __init__(self, pf, w):
+        import torch
+        from synth import device as sdev
+        self.pf, self.w = pf, w
+        self.ks = torch.zeros((w.num_pages, w.Hkv, w.P), dtype=torch.float32, device="cuda")
+        self.vs = torch.zeros_like(self.ks)
+        w.k_scale = w.v_scale = 1.0  # replaced by the per-token scales
+        self.st = sdev.setup_paged(w, self._append)
+        self.out = torch.empty_like(self.st.q)
+        n = pf.paged_decode_workspace_size(w.B, w.Hq, w.Hkv, w.D)
+        self.ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+
+    def _append(self, k, v, kc, vc, slots):
+        self.pf.kv_append_fp8_scaled(k, v, kc, vc, slots, self.pf.SCALE_TOKEN, self.ks, self.vs)
+
+    def append(self):
+        st = self.st
+        self._append(st.k_new, st.v_new, st.k_cache, st.v_cache, st.step_slots)
+
+    def decode(self):
+        st, w = self.st, self.w
+        self.pf.paged_decode_attn_scaled(self.out, st.q, st.k_cache, st.v_cache, self.pf.SCALE_TOKEN, self.ks,
+                                         self.vs, st.block_tables, st.context_lens, w.softmax_scale,
+                                         workspace=self.ws)
+
+
 class MlaStep:
     def __init__(self, pf, m):
         import torch
@@ -860,6 +890,7 @@ def measure_e2e(pf, s, iters):
 PROFILE_CASES = {
     # name: (description, factory)
     "mha_b8_l8192": "MHA, 8 requests x 48 heads x 8192 tokens, page 16 (a quarter of the headline batch)",
+    "mha_b8_l8192_token": "MHA, 8 requests x 48 heads x 8192 tokens, page 16, per-token K/V scales",
     "gqa_prefix_b64": "GQA 64/8 heads, 64 requests, lognormal contexts, 16 share a 2048-token prefix",
     "long_b2_l262144": "GQA 64/8 heads, 2 requests x 262144 tokens, page 64, 4096-token chunks",
     "mla_b16_topk2048": "MLA 128 heads x 576, 16 requests x 65536 tokens, top-k 2048, page 64",
@@ -905,6 +936,9 @@ def run_profile_case(name):
     if name == "mha_b8_l8192":
         s = PagedStep(pf, synth.PagedWorkload("mha_b8", B=8, Hq=48, Hkv=48, D=128, P=16,
                                               context_lens=np.full(8, 8192), n_new=1))
+    elif name == "mha_b8_l8192_token":
+        s = TokenScaleStep(pf, synth.PagedWorkload("mha_b8", B=8, Hq=48, Hkv=48, D=128, P=16,
+                                                   context_lens=np.full(8, 8192), n_new=1))
     elif name == "gqa_prefix_b64":
         s = PagedStep(pf, synth.workload(synth.GQA_PREFIX))
     elif name == "long_b2_l262144":
