@@ -109,6 +109,7 @@ struct PrefillArgs {
   int64_t num_pages;
   float score_scale;  // k_scale * softmax_scale * log2(e)
   float out_scale;    // v_scale
+  int box_tok;        // prefillw_kernel: tokens per TMA box (16, 32 or 64, dividing the page)
 };
 
 struct Bars {
@@ -1066,9 +1067,12 @@ __global__ void __launch_bounds__(k2Threads, 1)
 // widened to f16.  Each resource is released as soon as its last reader is done:
 //   * P has tensor-memory columns of its own: a score buffer is free once the
 //     softmax warps have read it, not once P.V has run;
+//   * P is double-buffered: the softmax writes P(j) once P.V(j - 2) has read
+//     that buffer, so P.V(j - 1) and the softmax of tile j overlap (O is
+//     waited for only on the rare tiles whose reference moves);
 //   * a stage is free once its K has been read by the score products and its
 //     V widened; a widened V tile once its P.V product has run.
-// tensor memory: two 128-column score buffers, O (128), P (64).
+// tensor memory: two 128-column score buffers, O (128), two P buffers (64 each).
 // shared memory: four 32 KB e4m3 stages, two 32 KB widened V tiles, Q's parts (16 KB).
 constexpr int kWTok = 128;                      // tokens per tile
 constexpr int kWBoxes = kWTok / kBoxTok;        // 8 TMA boxes per tensor
@@ -1086,7 +1090,7 @@ constexpr int kWOffBars = kWOffQs + 64 * 4;
 constexpr int kWSmemBytes = kWOffBars + 512 + 1024;
 static_assert(kWSmemBytes <= 232448, "shared memory over the per-CTA limit");
 constexpr uint32_t kWTmemS = 0, kWTmemO = kWBufs * kWTok, kWTmemP = kWTmemO + kD;
-static_assert(kWTmemP + kWTok / 2 <= kTmemCols, "tensor memory columns");
+static_assert(kWTmemP + kWBufs * (kWTok / 2) <= kTmemCols, "tensor memory columns");
 constexpr uint32_t kIdescQKW = tc::idesc_f16(64, kWTok, false);  // with kind::f8f6f4: e4m3 x e4m3
 constexpr uint32_t kIdescPVW = tc::idesc_f16(64, kD, true);
 constexpr int kWConvWarps = 4;
@@ -1101,18 +1105,17 @@ struct BarsW {
   uint64_t sfull[kWBufs];                 // scores of a tile complete
   uint64_t sread[kWBufs];                 // the softmax warps have read a score buffer
   uint64_t pvdone[kWBufs];                // P.V of a tile complete (index: tile % 2)
-  uint64_t pfull;                         // P of the next tile written (one phase per tile)
+  uint64_t pfull[kWBufs];                 // P of a tile written (index: tile % 2)
   uint64_t qready;
   uint32_t tmem_base;
 };
 static_assert(sizeof(BarsW) <= 512, "barrier block");
 
-// Widens the V rows of a stage into f16 atoms at dst, rows in the P.V
-// contraction order; rows at or past `valid` become zeros.  All loads are
-// issued before the first store: the compiler cannot move a load above a
-// store through another pointer into shared memory.
-__device__ __forceinline__ void widen_v(const uint8_t* vstage, uint8_t* dst, int ct, int valid) {
-  uint4 v[kWChunks];
+// Widening of a stage's V rows into f16 atoms, rows in the P.V contraction
+// order, in two steps: load_v reads this thread's e4m3 chunks (rows at or past
+// `valid` as zeros), so the stage can be released before the destination
+// buffer is free; store_v converts and writes them.
+__device__ __forceinline__ void load_v(const uint8_t* vstage, int ct, int valid, uint4 (&v)[kWChunks]) {
 #pragma unroll
   for (int m = 0; m < kWChunks; ++m) {
     const int i = ct + 32 * kWConvWarps * m;  // row i / 8, 16-byte chunk i % 8
@@ -1120,6 +1123,8 @@ __device__ __forceinline__ void widen_v(const uint8_t* vstage, uint8_t* dst, int
     v[m] = make_uint4(0, 0, 0, 0);
     if (row < valid) v[m] = lds128(vstage + (row >> 4) * kBoxBytes + swz(row & 15, c));
   }
+}
+__device__ __forceinline__ void store_v(const uint4 (&v)[kWChunks], uint8_t* dst, int ct) {
 #pragma unroll
   for (int m = 0; m < kWChunks; ++m) {
     const int i = ct + 32 * kWConvWarps * m;
@@ -1170,8 +1175,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
       mbar_init(smem_u32(&bs.sfull[k]), 1);
       mbar_init(smem_u32(&bs.sread[k]), live_warps);
       mbar_init(smem_u32(&bs.pvdone[k]), 1);
+      mbar_init(smem_u32(&bs.pfull[k]), live_warps);
     }
-    mbar_init(smem_u32(&bs.pfull), live_warps);
     mbar_init(smem_u32(&bs.qready), 4);
     fence_mbar_init();
     prefetch_tensormap(&tmK);
@@ -1189,20 +1194,25 @@ __global__ void __launch_bounds__(kWThreads, 1)
 
   if (warp == kWProdWarp) {
     // ------------------------------------------------------------ producer
-    // Lane l holds the block-table entry of box l % 8 of tile (batch + l / 8),
-    // four tiles per load, the next batch loaded while this one is issued.
-    constexpr int kBatch = 32 / kWBoxes;
+    // A tile is nb = 128 / box_tok boxes per tensor, each inside one page
+    // (tiles start at multiples of 64 tokens): with 64-token pages two 8 KB
+    // boxes instead of eight 2 KB ones, since the copy engine takes a roughly
+    // fixed time per box.  A 64-row box lands in shared memory exactly as four
+    // 16-row boxes would (the 128-byte swizzle repeats every 8 rows).
+    // Lane l holds the block-table entry of box l % nb of tile (batch + l / nb),
+    // 32 / nb tiles per load, the next batch loaded while this one is issued.
+    const int btok = a.box_tok, nb = kWTok / btok, tpb = 32 / nb;
     const int32_t* bt = a.block_tables + (int64_t)x.b * a.max_pages;
     auto load_batch = [&](int j0) {
-      const int j = j0 + lane / kWBoxes;
-      const int tb = x.t_lo + j * kWTok + (lane % kWBoxes) * kBoxTok;
+      const int j = j0 + lane / nb;
+      const int tb = x.t_lo + j * kWTok + (lane % nb) * btok;
       return (j < ntiles && tb < x.t_hi) ? __ldg(bt + tb / a.P) : 0;
     };
-    int cur = load_batch(0), nxt = load_batch(kBatch);
+    int cur = load_batch(0), nxt = load_batch(tpb);
     for (int j = 0; j < ntiles && !to; ++j) {
-      if (j > 0 && j % kBatch == 0) {
+      if (j > 0 && j % tpb == 0) {
         cur = nxt;
-        nxt = load_batch(j + kBatch);
+        nxt = load_batch(j + tpb);
       }
       const int st = j % kWStages;
       if (j >= kWStages && !warp_wait(smem_u32(&bs.stage_empty[st]), ((j / kWStages) - 1) & 1)) {
@@ -1210,19 +1220,19 @@ __global__ void __launch_bounds__(kWThreads, 1)
         break;
       }
       const int tok0 = x.t_lo + j * kWTok;
-      const int nbox = min(kWBoxes, (x.t_hi - tok0 + kBoxTok - 1) / kBoxTok);
+      const int nbox = min(nb, (x.t_hi - tok0 + btok - 1) / btok);
       const uint32_t bar = smem_u32(&bs.stage_full[st]);
-      if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(2 * nbox * kBoxBytes));
+      if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(2 * nbox * btok * kD));
       __syncwarp();
-      int page = __shfl_sync(0xFFFFFFFFu, cur, (j % kBatch) * kWBoxes + (lane % kWBoxes));
+      int page = __shfl_sync(0xFFFFFFFFu, cur, (j % tpb) * nb + (lane % nb));
       if (lane < nbox) {
-        const int tb = tok0 + lane * kBoxTok;
+        const int tb = tok0 + lane * btok;
         if (page < 0 || (int64_t)page >= a.num_pages) {
           atomicOr(a.status, kErrBadPage);
           page = -1;  // the box lands outside the tensor and reads zeros
         }
         const int row = (page * a.Hkv + x.kvh) * a.P + tb % a.P;
-        const uint32_t dst = smem_u32(smem + kWOffStage + st * kWStageBytes) + lane * kBoxBytes;
+        const uint32_t dst = smem_u32(smem + kWOffStage + st * kWStageBytes) + lane * btok * kD;
         tma_load_2d(dst, &tmK, 0, row, bar);
         tma_load_2d(dst + kWTok * kD, &tmV, 0, row, bar);
       }
@@ -1263,7 +1273,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
       int pn = 0;
       for (; pn < ntiles && !to; ++pn) {
         const int kb = pn % kWBufs;
-        if (!mbar_wait(smem_u32(&bs.pfull), pn & 1) || !mbar_wait(smem_u32(&bs.vfull[kb]), (pn / kWBufs) & 1)) {
+        if (!mbar_wait(smem_u32(&bs.pfull[kb]), (pn / kWBufs) & 1) ||
+            !mbar_wait(smem_u32(&bs.vfull[kb]), (pn / kWBufs) & 1)) {
           to = true;
           break;
         }
@@ -1271,7 +1282,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
         const uint64_t vdesc = tc::desc_sw128(v0 + kb * kWVBytes, kWAtom, 1024);
 #pragma unroll
         for (int k = 0; k < kWTok / 16; ++k)
-          tc::mma_ts(tmem + kWTmemO, tmem + kWTmemP + 8 * k, vdesc + (uint64_t)((2048 * k) >> 4), kIdescPVW,
+          tc::mma_ts(tmem + kWTmemO, tmem + kWTmemP + (kWTok / 2) * kb + 8 * k, vdesc + (uint64_t)((2048 * k) >> 4),
+                     kIdescPVW,
                      (pn > 0 || k > 0) ? 1u : 0u);
         tc::mma_commit(smem_u32(&bs.pvdone[kb]));
       }
@@ -1280,21 +1292,28 @@ __global__ void __launch_bounds__(kWThreads, 1)
     __syncwarp();
   } else if (warp < kWSoftWarp0) {
     // ---------------------------------------------------------- converters
-    // V(j) once the stage has landed and P.V(j - 2) has completed (its buffer).
+    // V(j): read once the stage has landed, which releases the stage's V at
+    // once; written once P.V(j - 2) has completed (its buffer).
     const int ct = threadIdx.x - kWConvWarp0 * 32;
     for (int j = 0; j < ntiles && !to; ++j) {
       const int st = j % kWStages, kb = j % kWBufs;
-      if (!warp_wait(smem_u32(&bs.stage_full[st]), (j / kWStages) & 1)) to = true;
-      if (j >= kWBufs && !to && !warp_wait(smem_u32(&bs.pvdone[kb]), ((j - kWBufs) / kWBufs) & 1)) to = true;
-      if (to) break;
+      if (!warp_wait(smem_u32(&bs.stage_full[st]), (j / kWStages) & 1)) {
+        to = true;
+        break;
+      }
       const int valid = min(kWTok, x.t_hi - (x.t_lo + j * kWTok));
-      widen_v(smem + kWOffStage + st * kWStageBytes + kWTok * kD, smem + kWOffV + kb * kWVBytes, ct, valid);
+      uint4 v[kWChunks];
+      load_v(smem + kWOffStage + st * kWStageBytes + kWTok * kD, ct, valid, v);
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.stage_empty[st]));  // release: the reads are done
+      if (j >= kWBufs && !warp_wait(smem_u32(&bs.pvdone[kb]), ((j - kWBufs) / kWBufs) & 1)) {
+        to = true;
+        break;
+      }
+      store_v(v, smem + kWOffV + kb * kWVBytes, ct);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        tc::mbar_arrive_local(smem_u32(&bs.vfull[kb]));
-        tc::mbar_arrive_local(smem_u32(&bs.stage_empty[st]));
-      }
+      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.vfull[kb]));
     }
   } else {
     // -------------------------------------------------- softmax + epilogue
@@ -1447,9 +1466,11 @@ __global__ void __launch_bounds__(kWThreads, 1)
         }
       }
       lpart += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-      // P and O are free once P.V(j - 1) has completed
-      if (j > 0) {
-        if (!warp_wait(smem_u32(&bs.pvdone[(j - 1) % kWBufs]), ((j - 1) / kWBufs) & 1)) {
+      // P buffer j % 2 is free once P.V(j - 2) has completed; O, for a
+      // rescale, once P.V(j - 1) has (every earlier product is then applied)
+      if (j >= kWBufs || (rescale && j > 0)) {
+        const int jw = rescale ? j - 1 : j - kWBufs;
+        if (!warp_wait(smem_u32(&bs.pvdone[jw % kWBufs]), (jw / kWBufs) & 1)) {
           to = true;
           break;
         }
@@ -1468,12 +1489,13 @@ __global__ void __launch_bounds__(kWThreads, 1)
           tc::tmem_st32(trow + kWTmemO + 32 * blk, ov);
         }
       }
-      tc::tmem_st16x64b_x16(trow + kWTmemP, *reinterpret_cast<const uint32_t(*)[16]>(&pv[0]));
-      tc::tmem_st16x64b_x16(trow + kWTmemP + 32, *reinterpret_cast<const uint32_t(*)[16]>(&pv[16]));
+      const uint32_t pbuf = trow + kWTmemP + (kWTok / 2) * kb;
+      tc::tmem_st16x64b_x16(pbuf, *reinterpret_cast<const uint32_t(*)[16]>(&pv[0]));
+      tc::tmem_st16x64b_x16(pbuf + 32, *reinterpret_cast<const uint32_t(*)[16]>(&pv[16]));
       tc::tmem_st_wait();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.pfull));
+      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.pfull[kb]));
     }
     // ---- epilogue: thread t < 16 writes row 16 quad + t from lane t of O
     const float lrow = lpart + __shfl_xor_sync(0xFFFFFFFFu, lpart, 2);
@@ -1661,6 +1683,7 @@ int pfkv_paged_prefill_attn(void* out, const void* q, const void* k_cache, const
   a.num_pages = num_pages;
   a.score_scale = k_scale * softmax_scale * kLog2e;
   a.out_scale = v_scale;
+  a.box_tok = kBoxTok;
   const int64_t units = units_of(batch, num_kv_heads, a.QB, a.C);
   if (units > 0x7FFFFFFF) return fail(PFKV_ERR_UNSUPPORTED, "paged_prefill: too many work units");
 
@@ -1695,6 +1718,17 @@ int pfkv_paged_prefill_attn(void* out, const void* q, const void* k_cache, const
     rc = set_max_dynamic_smem(reinterpret_cast<const void*>(prefillw_kernel), kWSmemBytes, smemw_set,
                               "paged_prefill set smem attribute");
     if (rc != PFKV_OK) return rc;
+    // boxes as tall as the page allows (up to 64 rows): fewer copies per tile
+    a.box_tok = page_size % 64 == 0 ? 64 : (page_size % 32 == 0 ? 32 : kBoxTok);
+    if (a.box_tok != kBoxTok) {
+      const cuuint32_t boxw[2] = {128, (cuuint32_t)a.box_tok};
+      rc = encode_tensor_map(&tmK, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(k_cache), dims, strides,
+                             boxw, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (rc == PFKV_OK)
+        rc = encode_tensor_map(&tmV, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(v_cache), dims,
+                               strides, boxw, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (rc != PFKV_OK) return rc;
+    }
     prefillw_kernel<<<(unsigned)units, kWThreads, kWSmemBytes, s>>>(tmK, tmV, a);
   } else {
     prefill_kernel<<<(unsigned)units, kThreads, kSmemBytes, s>>>(tmK, tmV, a);
