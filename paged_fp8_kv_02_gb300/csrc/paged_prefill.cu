@@ -110,6 +110,7 @@ struct PrefillArgs {
   float score_scale;  // k_scale * softmax_scale * log2(e)
   float out_scale;    // v_scale
   int box_tok;        // prefillw_kernel: tokens per TMA box (16, 32 or 64, dividing the page)
+  uint32_t* work;     // prefillw_kernel: next work unit to hand out (zeroed per call)
 };
 
 struct Bars {
@@ -1075,7 +1076,6 @@ __global__ void __launch_bounds__(k2Threads, 1)
 // tensor memory: two 128-column score buffers, O (128), two P buffers (64 each).
 // shared memory: four 32 KB e4m3 stages, two 32 KB widened V tiles, Q's parts (16 KB).
 constexpr int kWTok = 128;                      // tokens per tile
-constexpr int kWBoxes = kWTok / kBoxTok;        // 8 TMA boxes per tensor
 constexpr int kWStages = 4;
 constexpr int kWStageBytes = 2 * kWTok * kD;    // K + V e4m3: 32 KB
 constexpr int kWAtom = kWTok * 128;             // [128 tokens][64 f16]: 16 KB
@@ -1106,10 +1106,16 @@ struct BarsW {
   uint64_t sread[kWBufs];                 // the softmax warps have read a score buffer
   uint64_t pvdone[kWBufs];                // P.V of a tile complete (index: tile % 2)
   uint64_t pfull[kWBufs];                 // P of a tile written (index: tile % 2)
-  uint64_t qready;
+  uint64_t ufull[2], uempty[2];           // the unit queue's two slots
+  uint64_t qready;                        // Q of the current unit written
+  uint64_t qfree;                         // the previous unit's score products are done with Q
+  uint64_t oread;                         // a unit's epilogue has read O
+  int64_t uq[2];                          // unit ids (-1: no more work)
   uint32_t tmem_base;
 };
 static_assert(sizeof(BarsW) <= 512, "barrier block");
+// warps that read each unit id from the queue: score issuer, converters, softmax, P.V issuer
+constexpr int kWUnitReaders = 1 + kWConvWarps + 4 + 1;
 
 // Widening of a stage's V rows into f16 atoms, rows in the P.V contraction
 // order, in two steps: load_v reads this thread's e4m3 chunks (rows at or past
@@ -1149,35 +1155,44 @@ __device__ __forceinline__ void e4m3x2_to_f32x2(uint16_t code, float& lo, float&
   hi = __half2float(__ushort_as_half((unsigned short)(h >> 16)));
 }
 
+// Persistent: one CTA per SM takes work units, in index order, from a counter
+// in the workspace until none is left; the
+// producer streams the next unit's tiles while the current one drains, so a
+// unit's fixed costs (first copies in flight, last products) overlap its
+// neighbours and no wave of CTAs waits for the slowest.  Every ring's phase
+// follows the CTA's running tile count g, not the tile index inside a unit.
+// Per unit: the producer publishes the unit id in a two-slot queue (ufull /
+// uempty); the softmax warps write Q once the previous unit's score products
+// are done (qfree) and signal qready; P.V of a unit's first tile overwrites O
+// once the epilogue of the previous unit with tiles has read it (oread, one
+// phase per unit that has tiles, so that no phase can run two ahead).
 __global__ void __launch_bounds__(kWThreads, 1)
     prefillw_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                    const PrefillArgs a) {
+                    const PrefillArgs a, const int64_t units) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* const smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   BarsW& bs = *reinterpret_cast<BarsW*>(smem + kWOffBars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  const int64_t u = blockIdx.x;
-  const Unit x = unit_of(a, u, threadIdx.x == 0 && (u % ((int64_t)a.QB * a.C * a.Hkv)) == 0);
-  if (!x.active) return;  // uniform over the CTA
-  const int ntiles = x.ntiles == 0 ? 0 : (x.t_hi - x.t_lo + kWTok - 1) / kWTok;
   const bool direct = a.C == 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kWStages; ++s) {
       mbar_init(smem_u32(&bs.stage_full[s]), 1);
-      mbar_init(smem_u32(&bs.stage_empty[s]), kWConvWarps + 1);  // V widened + the score products done
+      mbar_init(smem_u32(&bs.stage_empty[s]), kWConvWarps + 1);  // V read + the score products done
     }
-    const int live_warps = min(4, (x.rows + 15) / 16);
     for (int k = 0; k < kWBufs; ++k) {
       mbar_init(smem_u32(&bs.vfull[k]), kWConvWarps);
       mbar_init(smem_u32(&bs.sfull[k]), 1);
-      mbar_init(smem_u32(&bs.sread[k]), live_warps);
+      mbar_init(smem_u32(&bs.sread[k]), 4);
       mbar_init(smem_u32(&bs.pvdone[k]), 1);
-      mbar_init(smem_u32(&bs.pfull[k]), live_warps);
+      mbar_init(smem_u32(&bs.pfull[k]), 4);
+      mbar_init(smem_u32(&bs.ufull[k]), 1);
+      mbar_init(smem_u32(&bs.uempty[k]), kWUnitReaders);
     }
     mbar_init(smem_u32(&bs.qready), 4);
+    mbar_init(smem_u32(&bs.qfree), 1);
+    mbar_init(smem_u32(&bs.oread), 4);
     fence_mbar_init();
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
@@ -1192,172 +1207,280 @@ __global__ void __launch_bounds__(kWThreads, 1)
   const uint32_t tmem = bs.tmem_base;
   bool to = false;  // a bounded wait gave up
 
+  // Unit k of this CTA from the queue (every reader warp, all lanes): -1 when
+  // the work is done or a wait gave up.  Lane 0 frees the slot once all lanes
+  // hold the id.
+  auto next_unit = [&](int k, bool whole_warp) -> int64_t {
+    const uint32_t full = smem_u32(&bs.ufull[k % 2]);
+    const bool ok = whole_warp ? warp_wait(full, (k / 2) & 1) : mbar_wait(full, (k / 2) & 1);
+    if (!ok) {
+      to = true;
+      return -1;
+    }
+    const int64_t uu = bs.uq[k % 2];
+    if (whole_warp) __syncwarp();
+    if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.uempty[k % 2]));
+    return uu;
+  };
+  auto ntiles_of = [&](const Unit& x) { return x.ntiles == 0 ? 0 : (x.t_hi - x.t_lo + kWTok - 1) / kWTok; };
+
   if (warp == kWProdWarp) {
     // ------------------------------------------------------------ producer
     // A tile is nb = 128 / box_tok boxes per tensor, each inside one page
     // (tiles start at multiples of 64 tokens): with 64-token pages two 8 KB
-    // boxes instead of eight 2 KB ones, since the copy engine takes a roughly
-    // fixed time per box.  A 64-row box lands in shared memory exactly as four
-    // 16-row boxes would (the 128-byte swizzle repeats every 8 rows).
-    // Lane l holds the block-table entry of box l % nb of tile (batch + l / nb),
-    // 32 / nb tiles per load, the next batch loaded while this one is issued.
+    // copies instead of eight 2 KB ones, which measured faster.  A 64-row box
+    // lands in shared memory exactly as four 16-row boxes would (the 128-byte
+    // swizzle repeats every 8 rows).  Lane l holds the block-table entry of box
+    // l % nb of tile (batch + l / nb), 32 / nb tiles per load, the next batch
+    // loaded while this one is issued.
     const int btok = a.box_tok, nb = kWTok / btok, tpb = 32 / nb;
-    const int32_t* bt = a.block_tables + (int64_t)x.b * a.max_pages;
-    auto load_batch = [&](int j0) {
-      const int j = j0 + lane / nb;
-      const int tb = x.t_lo + j * kWTok + (lane % nb) * btok;
-      return (j < ntiles && tb < x.t_hi) ? __ldg(bt + tb / a.P) : 0;
-    };
-    int cur = load_batch(0), nxt = load_batch(tpb);
-    for (int j = 0; j < ntiles && !to; ++j) {
-      if (j > 0 && j % tpb == 0) {
-        cur = nxt;
-        nxt = load_batch(j + tpb);
+    int64_t g = 0;  // tiles issued by this CTA so far
+    for (int k = 0; !to; ++k) {
+      // the next unit with work: every index is taken by exactly one CTA
+      int64_t u = -1;
+      if (lane == 0) {
+        while (true) {
+          const int64_t c = (int64_t)atomicAdd(a.work, 1u);
+          if (c >= units) break;
+          const Unit xc = unit_of(a, c, (c % ((int64_t)a.QB * a.C * a.Hkv)) == 0);
+          if (xc.active) {
+            u = c;
+            break;
+          }
+        }
       }
-      const int st = j % kWStages;
-      if (j >= kWStages && !warp_wait(smem_u32(&bs.stage_empty[st]), ((j / kWStages) - 1) & 1)) {
+      u = __shfl_sync(0xFFFFFFFFu, u, 0);
+      if (k >= 2 && !warp_wait(smem_u32(&bs.uempty[k % 2]), ((k / 2) - 1) & 1)) {
         to = true;
         break;
       }
-      const int tok0 = x.t_lo + j * kWTok;
-      const int nbox = min(nb, (x.t_hi - tok0 + btok - 1) / btok);
-      const uint32_t bar = smem_u32(&bs.stage_full[st]);
-      if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(2 * nbox * btok * kD));
-      __syncwarp();
-      int page = __shfl_sync(0xFFFFFFFFu, cur, (j % tpb) * nb + (lane % nb));
-      if (lane < nbox) {
-        const int tb = tok0 + lane * btok;
-        if (page < 0 || (int64_t)page >= a.num_pages) {
-          atomicOr(a.status, kErrBadPage);
-          page = -1;  // the box lands outside the tensor and reads zeros
-        }
-        const int row = (page * a.Hkv + x.kvh) * a.P + tb % a.P;
-        const uint32_t dst = smem_u32(smem + kWOffStage + st * kWStageBytes) + lane * btok * kD;
-        tma_load_2d(dst, &tmK, 0, row, bar);
-        tma_load_2d(dst + kWTok * kD, &tmV, 0, row, bar);
+      if (lane == 0) {
+        bs.uq[k % 2] = u;
+        tc::mbar_arrive_local(smem_u32(&bs.ufull[k % 2]));  // release: the id is visible to the readers
       }
+      if (u < 0) break;
+      const Unit x = unit_of(a, u, false);
+      const int ntiles = ntiles_of(x);
+      const int32_t* bt = a.block_tables + (int64_t)x.b * a.max_pages;
+      auto load_batch = [&](int j0) {
+        const int j = j0 + lane / nb;
+        const int tb = x.t_lo + j * kWTok + (lane % nb) * btok;
+        return (j < ntiles && tb < x.t_hi) ? __ldg(bt + tb / a.P) : 0;
+      };
+      int cur = load_batch(0), nxt = load_batch(tpb);
+      for (int j = 0; j < ntiles; ++j) {
+        if (j > 0 && j % tpb == 0) {
+          cur = nxt;
+          nxt = load_batch(j + tpb);
+        }
+        const int64_t gg = g + j;
+        const int st = (int)(gg % kWStages);
+        if (gg >= kWStages && !warp_wait(smem_u32(&bs.stage_empty[st]), ((gg / kWStages) - 1) & 1)) {
+          to = true;
+          break;
+        }
+        const int tok0 = x.t_lo + j * kWTok;
+        const int nbox = min(nb, (x.t_hi - tok0 + btok - 1) / btok);
+        const uint32_t bar = smem_u32(&bs.stage_full[st]);
+        if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(2 * nbox * btok * kD));
+        __syncwarp();
+        int page = __shfl_sync(0xFFFFFFFFu, cur, (j % tpb) * nb + (lane % nb));
+        if (lane < nbox) {
+          const int tb = tok0 + lane * btok;
+          if (page < 0 || (int64_t)page >= a.num_pages) {
+            atomicOr(a.status, kErrBadPage);
+            page = -1;  // the box lands outside the tensor and reads zeros
+          }
+          const int row = (page * a.Hkv + x.kvh) * a.P + tb % a.P;
+          const uint32_t dst = smem_u32(smem + kWOffStage + st * kWStageBytes) + lane * btok * kD;
+          tma_load_2d(dst, &tmK, 0, row, bar);
+          tma_load_2d(dst + kWTok * kD, &tmV, 0, row, bar);
+        }
+      }
+      g += ntiles;
     }
-    for (int j = ntiles > kWStages ? ntiles - kWStages : 0; j < ntiles; ++j)
-      if (!mbar_wait(smem_u32(&bs.stage_full[j % kWStages]), (j / kWStages) & 1)) to = true;
+    // no copy may still be landing when the CTA retires
+    for (int64_t gg = g > kWStages ? g - kWStages : 0; gg < g; ++gg)
+      if (!mbar_wait(smem_u32(&bs.stage_full[gg % kWStages]), (gg / kWStages) & 1)) to = true;
   } else if (warp == kWMmaWarp) {
     // ------------------------------------------------- score MMA issuer
-    // S(j) = Q . K(j)^T (N = 128) into buffer j % 2, straight from the e4m3 K
+    // S(g) = Q . K(g)^T (N = 128) into buffer g % 2, straight from the e4m3 K
     // rows of the stage (kind::f8f6f4: Q in two exact e4m3 parts, four
     // K = 32 steps each), once the stage has landed and the softmax warps have
-    // read S(j - 2) from that buffer.  A second commit releases the stage's K.
-    if (lane == 0 && ntiles > 0) {
-      if (!mbar_wait(smem_u32(&bs.qready), 0)) to = true;
+    // read S(g - 2) from that buffer.  A second commit releases the stage's K;
+    // after a unit's last tile a third releases Q.
+    if (lane == 0) {
       const uint64_t qdesc = tc::desc_sw128(smem_u32(smem + kWOffQ), 16, 1024);
-      for (int qn = 0; qn < ntiles && !to; ++qn) {
-        const int kb = qn % kWBufs, st = qn % kWStages;
-        if (!mbar_wait(smem_u32(&bs.stage_full[st]), (qn / kWStages) & 1)) to = true;
-        if (qn >= kWBufs && !to && !mbar_wait(smem_u32(&bs.sread[kb]), ((qn - kWBufs) / kWBufs) & 1)) to = true;
-        if (to) break;
-        tc::fence_after_sync();
-        const uint64_t kdesc = tc::desc_sw128(smem_u32(smem + kWOffStage + st * kWStageBytes), 16, 1024);
+      int64_t g = 0;
+      for (int k = 0; !to; ++k) {
+        const int64_t u = next_unit(k, false);
+        if (u < 0) break;
+        const int ntiles = ntiles_of(unit_of(a, u, false));
+        if (!mbar_wait(smem_u32(&bs.qready), k & 1)) {
+          to = true;
+          break;
+        }
+        for (int j = 0; j < ntiles && !to; ++j) {
+          const int64_t gg = g + j;
+          const int kb = (int)(gg % kWBufs), st = (int)(gg % kWStages);
+          if (!mbar_wait(smem_u32(&bs.stage_full[st]), (gg / kWStages) & 1)) to = true;
+          if (gg >= kWBufs && !to && !mbar_wait(smem_u32(&bs.sread[kb]), ((gg - kWBufs) / kWBufs) & 1)) to = true;
+          if (to) break;
+          tc::fence_after_sync();
+          const uint64_t kdesc = tc::desc_sw128(smem_u32(smem + kWOffStage + st * kWStageBytes), 16, 1024);
 #pragma unroll
-        for (int p = 0; p < 2; ++p)
+          for (int p = 0; p < 2; ++p)
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            tc::mma_ss_e4m3(tmem + kWTmemS + kWTok * kb, qdesc + (uint64_t)((p * kWQPart + 32 * k) >> 4),
-                            kdesc + (uint64_t)((32 * k) >> 4), kIdescQKW, (p > 0 || k > 0) ? 1u : 0u);
-        tc::mma_commit(smem_u32(&bs.sfull[kb]));
-        tc::mma_commit(smem_u32(&bs.stage_empty[st]));
+            for (int kk = 0; kk < 4; ++kk)
+              tc::mma_ss_e4m3(tmem + kWTmemS + kWTok * kb, qdesc + (uint64_t)((p * kWQPart + 32 * kk) >> 4),
+                              kdesc + (uint64_t)((32 * kk) >> 4), kIdescQKW, (p > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_commit(smem_u32(&bs.sfull[kb]));
+          tc::mma_commit(smem_u32(&bs.stage_empty[st]));
+        }
+        tc::mma_commit(smem_u32(&bs.qfree));  // Q is free once these products complete
+        g += ntiles;
       }
     }
     __syncwarp();
   } else if (warp == kWPvWarp) {
     // ---------------------------------------------------- P.V MMA issuer
-    if (lane == 0 && ntiles > 0) {
+    // O += P(g) . V(g) once P and the widened V of tile g are written; a
+    // unit's first product overwrites O once the previous unit's epilogue has
+    // read it.
+    if (lane == 0) {
       const uint32_t v0 = smem_u32(smem + kWOffV);
-      int pn = 0;
-      for (; pn < ntiles && !to; ++pn) {
-        const int kb = pn % kWBufs;
-        if (!mbar_wait(smem_u32(&bs.pfull[kb]), (pn / kWBufs) & 1) ||
-            !mbar_wait(smem_u32(&bs.vfull[kb]), (pn / kWBufs) & 1)) {
-          to = true;
-          break;
+      int64_t g = 0;
+      int m = 0;  // units with tiles so far
+      for (int k = 0; !to; ++k) {
+        const int64_t u = next_unit(k, false);
+        if (u < 0) break;
+        const int ntiles = ntiles_of(unit_of(a, u, false));
+        if (ntiles > 0) {
+          if (m > 0 && !mbar_wait(smem_u32(&bs.oread), (m - 1) & 1)) {
+            to = true;
+            break;
+          }
+          ++m;
         }
-        tc::fence_after_sync();
-        const uint64_t vdesc = tc::desc_sw128(v0 + kb * kWVBytes, kWAtom, 1024);
+        for (int j = 0; j < ntiles && !to; ++j) {
+          const int64_t gg = g + j;
+          const int kb = (int)(gg % kWBufs);
+          if (!mbar_wait(smem_u32(&bs.pfull[kb]), (gg / kWBufs) & 1) ||
+              !mbar_wait(smem_u32(&bs.vfull[kb]), (gg / kWBufs) & 1)) {
+            to = true;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint64_t vdesc = tc::desc_sw128(v0 + kb * kWVBytes, kWAtom, 1024);
 #pragma unroll
-        for (int k = 0; k < kWTok / 16; ++k)
-          tc::mma_ts(tmem + kWTmemO, tmem + kWTmemP + (kWTok / 2) * kb + 8 * k, vdesc + (uint64_t)((2048 * k) >> 4),
-                     kIdescPVW,
-                     (pn > 0 || k > 0) ? 1u : 0u);
-        tc::mma_commit(smem_u32(&bs.pvdone[kb]));
+          for (int kk = 0; kk < kWTok / 16; ++kk)
+            tc::mma_ts(tmem + kWTmemO, tmem + kWTmemP + (kWTok / 2) * kb + 8 * kk,
+                       vdesc + (uint64_t)((2048 * kk) >> 4), kIdescPVW, (j > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_commit(smem_u32(&bs.pvdone[kb]));
+        }
+        g += ntiles;
       }
-      if (pn > 0 && !mbar_wait(smem_u32(&bs.pvdone[(pn - 1) % kWBufs]), ((pn - 1) / kWBufs) & 1)) to = true;
+      // every product complete before tensor memory is freed
+      if (g > 0 && !mbar_wait(smem_u32(&bs.pvdone[(g - 1) % kWBufs]), ((g - 1) / kWBufs) & 1)) to = true;
     }
     __syncwarp();
   } else if (warp < kWSoftWarp0) {
-    // ---------------------------------------------------------- converters
-    // V(j): read once the stage has landed, which releases the stage's V at
-    // once; written once P.V(j - 2) has completed (its buffer).
+    // ------------------------------------------------------------ converters
+    // V(g): read once the stage has landed, which releases the stage's V at
+    // once; written once P.V(g - 2) has completed (its buffer).
     const int ct = threadIdx.x - kWConvWarp0 * 32;
-    for (int j = 0; j < ntiles && !to; ++j) {
-      const int st = j % kWStages, kb = j % kWBufs;
-      if (!warp_wait(smem_u32(&bs.stage_full[st]), (j / kWStages) & 1)) {
-        to = true;
-        break;
+    int64_t g = 0;
+    for (int k = 0; !to; ++k) {
+      const int64_t u = next_unit(k, true);
+      if (u < 0) break;
+      const Unit x = unit_of(a, u, false);
+      const int ntiles = ntiles_of(x);
+      for (int j = 0; j < ntiles; ++j) {
+        const int64_t gg = g + j;
+        const int st = (int)(gg % kWStages), kb = (int)(gg % kWBufs);
+        if (!warp_wait(smem_u32(&bs.stage_full[st]), (gg / kWStages) & 1)) {
+          to = true;
+          break;
+        }
+        const int valid = min(kWTok, x.t_hi - (x.t_lo + j * kWTok));
+        uint4 v[kWChunks];
+        load_v(smem + kWOffStage + st * kWStageBytes + kWTok * kD, ct, valid, v);
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.stage_empty[st]));  // release: the reads are done
+        if (gg >= kWBufs && !warp_wait(smem_u32(&bs.pvdone[kb]), ((gg - kWBufs) / kWBufs) & 1)) {
+          to = true;
+          break;
+        }
+        store_v(v, smem + kWOffV + kb * kWVBytes, ct);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.vfull[kb]));
       }
-      const int valid = min(kWTok, x.t_hi - (x.t_lo + j * kWTok));
-      uint4 v[kWChunks];
-      load_v(smem + kWOffStage + st * kWStageBytes + kWTok * kD, ct, valid, v);
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.stage_empty[st]));  // release: the reads are done
-      if (j >= kWBufs && !warp_wait(smem_u32(&bs.pvdone[kb]), ((j - kWBufs) / kWBufs) & 1)) {
-        to = true;
-        break;
-      }
-      store_v(v, smem + kWOffV + kb * kWVBytes, ct);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.vfull[kb]));
+      g += ntiles;
     }
   } else {
     // -------------------------------------------------- softmax + epilogue
     const int quad = warp & 3;
     const uint32_t trow = tmem + ((uint32_t)(32 * quad) << 16);
-    // Q: thread t < 16 splits row 16 quad + t into two e4m3 parts (x = q s
-    // with s a power of two taking max |q| into (224, 448]; part 1 = e4m3(x),
-    // part 2 = e4m3(x - part 1) = x - part 1),
-    // written as the A operands of the score products, and records 1 / s
     float* const qinv = reinterpret_cast<float*>(smem + kWOffQs);
-    {
-      const int rq = 16 * quad + (lane & 15);
-      const bool okq = lane < 16 && rq < x.rows;
-      const int64_t hq = ((int64_t)a.q_start[x.b] + x.i0 + rq / a.G) * a.Hq + (int64_t)x.kvh * a.G + rq % a.G;
-      const uint4* qp = reinterpret_cast<const uint4*>(a.q + hq * kD);
-      float amax = 0.f;
-      if (okq) {
-#pragma unroll 4
-        for (int uu = 0; uu < 16; ++uu) {
-          const uint4 w = __ldg(qp + uu);
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(ww[k])), fabsf(bf16_hi(ww[k]))));
-        }
+    // the 16-lane shape: thread t holds row 16 quad + Lm, Lm = (t >> 2) + 8 (t & 1),
+    // and the columns of parity par = (t >> 1) & 1 (register k of a 64-column
+    // read is column 2 k + par)
+    const int Lm = (lane >> 2) + 8 * (lane & 1), par = (lane >> 1) & 1;
+    const int rm = 16 * quad + Lm;
+    // O row 16 quad + t (t < 16) sits in lane t of the quadrant; its statistics
+    // are held by thread 4 (t % 8) + t / 8
+    const int src = 4 * (lane & 7) + ((lane >> 3) & 1);
+    int64_t g = 0;
+    for (int k = 0; !to; ++k) {
+      const int64_t u = next_unit(k, true);
+      if (u < 0) break;
+      const Unit x = unit_of(a, u, false);
+      const int ntiles = ntiles_of(x);
+      // Q: threads t and t + 16 split row 16 quad + t (t < 16), each its half
+      // (64 elements), into two e4m3 parts (x = q s with s a power of two
+      // taking max |q| of the row into (224, 448]; part 1 = e4m3(x), part 2 =
+      // e4m3(x - part 1) = x - part 1), written as the A operands of the score
+      // products once the previous unit's products are done; thread t records
+      // 1 / s
+      if (k > 0 && !warp_wait(smem_u32(&bs.qfree), (k - 1) & 1)) {
+        to = true;
+        break;
       }
-      // s = 2^floor(log2(448 / amax)) within [2^-126, 2^126] (1 for a zero row)
-      const float s = pow2_scale(448.f, amax);
-      if (lane < 16) {
-#pragma unroll 1
-        for (int c = 0; c < 8; ++c) {  // 16 elements per 16-byte chunk
+      {
+        const int rq = 16 * quad + (lane & 15), hh = lane >> 4;
+        const bool okq = rq < x.rows;
+        const int64_t hq = ((int64_t)a.q_start[x.b] + x.i0 + rq / a.G) * a.Hq + (int64_t)x.kvh * a.G + rq % a.G;
+        const uint4* qp = reinterpret_cast<const uint4*>(a.q + hq * kD) + 8 * hh;
+        uint4 qw[8];  // loaded together: one memory latency per unit
+#pragma unroll
+        for (int uu = 0; uu < 8; ++uu) qw[uu] = okq ? __ldg(qp + uu) : make_uint4(0, 0, 0, 0);
+        float amax = 0.f;
+#pragma unroll
+        for (int uu = 0; uu < 8; ++uu) {
+          const uint32_t ww[4] = {qw[uu].x, qw[uu].y, qw[uu].z, qw[uu].w};
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(ww[kk])), fabsf(bf16_hi(ww[kk]))));
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 16));  // the row's other half
+        // s = 2^floor(log2(448 / amax)) within [2^-126, 2^126] (1 for a zero row)
+        const float s = pow2_scale(448.f, amax);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {  // chunk c = 4 hh + cc: 16 elements
+          const int c = 4 * hh + cc;
           uint32_t p1[4] = {0u, 0u, 0u, 0u}, p2[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            uint4 w = make_uint4(0, 0, 0, 0);
-            if (okq) w = __ldg(qp + 2 * c + h);
+            const uint4 w = qw[2 * cc + h];
             const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {  // elements 8 h + 2 k and 8 h + 2 k + 1 of the chunk
-              const float x0 = bf16_lo(ww[k]) * s, x1 = bf16_hi(ww[k]) * s;
+            for (int kk = 0; kk < 4; ++kk) {  // elements 8 h + 2 kk and 8 h + 2 kk + 1 of the chunk
+              const float x0 = bf16_lo(ww[kk]) * s, x1 = bf16_hi(ww[kk]) * s;
               const uint16_t c1 = f32x2_to_e4m3x2(x0, x1);
               float d0, d1;
               e4m3x2_to_f32x2(c1, d0, d1);
               const uint16_t c2 = f32x2_to_e4m3x2(x0 - d0, x1 - d1);  // the difference is exact
-              const int word = 2 * h + (k >> 1), sh = 16 * (k & 1);
+              const int word = 2 * h + (kk >> 1), sh = 16 * (kk & 1);
               p1[word] |= (uint32_t)c1 << sh;
               p2[word] |= (uint32_t)c2 << sh;
             }
@@ -1366,144 +1489,138 @@ __global__ void __launch_bounds__(kWThreads, 1)
           *reinterpret_cast<uint4*>(smem + kWOffQ + off) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
           *reinterpret_cast<uint4*>(smem + kWOffQ + kWQPart + off) = make_uint4(p2[0], p2[1], p2[2], p2[3]);
         }
-        qinv[rq] = okq ? 1.f / s : 0.f;  // exact: s is a power of two
+        if (lane < 16) qinv[rq] = okq ? 1.f / s : 0.f;  // exact: s is a power of two
+        fence_proxy_async_smem();  // generic writes -> visible to the tensor core
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.qready));
       }
-      fence_proxy_async_smem();  // generic writes -> visible to the tensor core
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.qready));
-    }
-    // the 16-lane shape: thread t holds row 16 quad + Lm, Lm = (t >> 2) + 8 (t & 1),
-    // and the columns of parity par = (t >> 1) & 1 (register k of a 64-column
-    // read is column 2 k + par)
-    const int Lm = (lane >> 2) + 8 * (lane & 1), par = (lane >> 1) & 1;
-    const int rm = 16 * quad + Lm;
-    const bool okm = rm < x.rows;
-    const int im = x.i0 + rm / a.G;
-    const int limm = okm ? min(x.L - x.n + im + 1, x.t_end_chunk) : x.t_lo;
-    const float sc = a.score_scale * qinv[rm];  // the scores carry the row's Q scale s
-    float mref = -INFINITY, rthr = -INFINITY, lpart = 0.f;  // lpart: this thread's share of the row sum
-    // O row 16 quad + t (t < 16) sits in lane t of the quadrant; its statistics
-    // are held by thread 4 (t % 8) + t / 8
-    const int src = 4 * (lane & 7) + ((lane >> 3) & 1);
-    const bool live = 16 * quad < x.rows;
-    for (int j = 0; j < ntiles && !to && live; ++j) {
-      const int kb = j % kWBufs;
-      if (!warp_wait(smem_u32(&bs.sfull[kb]), (j / kWBufs) & 1)) {
-        to = true;
-        break;
-      }
-      tc::fence_after_sync();
-      // all 128 scores of the row half in registers: sv[32 h + k] is column
-      // 64 h + 2 k + par; the buffer is then free for S(j + 2)
-      uint32_t sv[64];
-      {
-        uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
-        uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
-        tc::tmem_ld16x64b_x32(trow + kWTmemS + kWTok * kb, s0);
-        tc::tmem_ld16x64b_x32(trow + kWTmemS + kWTok * kb + 64, s1);
-        tc::tmem_ld_wait();
-      }
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.sread[kb]));
-      // columns c < nv are attended (none for a padding row); every branch on
-      // `full` is warp-uniform and the masks are selects, so no lane diverges
-      const int nv = okm ? limm - (x.t_lo + j * kWTok) : 0;
-      const bool full = __all_sync(0xFFFFFFFFu, nv >= kWTok);
-      float mx;
-      {
-        float m8[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
-        if (full) {
-#pragma unroll
-          for (int k = 0; k < 64; ++k) m8[k & 7] = fmaxf(m8[k & 7], __uint_as_float(sv[k]));
-        } else {
-#pragma unroll
-          for (int k = 0; k < 64; ++k)
-            m8[k & 7] = fmaxf(m8[k & 7], 64 * (k >> 5) + 2 * (k & 31) + par < nv ? __uint_as_float(sv[k]) : -INFINITY);
-        }
-        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-      }
-      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));  // the row's other half
-      const bool grow = mx > rthr;
-      float al = 1.f;
-      bool rescale = false;
-      if (__any_sync(0xFFFFFFFFu, grow)) {
-        const float mn = grow ? fmaxf(mref, mx * sc) : mref;
-        al = grow ? fast_exp2(mref - mn) : 1.f;  // 0 while mref is -inf
-        rescale = j > 0 && __any_sync(0xFFFFFFFFu, grow && mref != -INFINITY);
-        lpart *= al;
-        mref = mn;
-        rthr = (mn + kRescaleLog2) / sc;
-      }
-      // P: register pair (2 r, 2 r + 1) of a half holds tokens (4 r + par, 4 r + par + 2),
-      // which the contraction order places in P column 2 r + par of that half
-      uint32_t pv[32];
-      float ls[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) ls[k] = 0.f;
-      if (full) {
-#pragma unroll
-        for (int r2 = 0; r2 < 32; ++r2) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * r2]), sc, -mref));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * r2 + 1]), sc, -mref));
-          ls[r2 & 3] += p0;
-          ls[4 + (r2 & 3)] += p1;
-          pv[r2] = pack_f16x2(p0, p1);
-        }
-      } else {
-        // a masked column's exponential may overflow; the select drops it
-#pragma unroll
-        for (int r2 = 0; r2 < 32; ++r2) {
-          const int c0 = 64 * (r2 >> 4) + 4 * (r2 & 15) + par;
-          const float e0 = fast_exp2(fmaf(__uint_as_float(sv[2 * r2]), sc, -mref));
-          const float e1 = fast_exp2(fmaf(__uint_as_float(sv[2 * r2 + 1]), sc, -mref));
-          const float p0 = c0 < nv ? e0 : 0.f, p1 = c0 + 2 < nv ? e1 : 0.f;
-          ls[r2 & 3] += p0;
-          ls[4 + (r2 & 3)] += p1;
-          pv[r2] = pack_f16x2(p0, p1);
-        }
-      }
-      lpart += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-      // P buffer j % 2 is free once P.V(j - 2) has completed; O, for a
-      // rescale, once P.V(j - 1) has (every earlier product is then applied)
-      if (j >= kWBufs || (rescale && j > 0)) {
-        const int jw = rescale ? j - 1 : j - kWBufs;
-        if (!warp_wait(smem_u32(&bs.pvdone[jw % kWBufs]), (jw / kWBufs) & 1)) {
+      const bool okm = rm < x.rows;
+      const int im = x.i0 + rm / a.G;
+      const int limm = okm ? min(x.L - x.n + im + 1, x.t_end_chunk) : x.t_lo;
+      const float sc = a.score_scale * qinv[rm];  // the scores carry the row's Q scale s
+      float mref = -INFINITY, rthr = -INFINITY, lpart = 0.f;  // lpart: this thread's share of the row sum
+      for (int j = 0; j < ntiles; ++j) {
+        const int64_t gg = g + j;
+        const int kb = (int)(gg % kWBufs);
+        if (!warp_wait(smem_u32(&bs.sfull[kb]), (gg / kWBufs) & 1)) {
           to = true;
           break;
         }
         tc::fence_after_sync();
-      }
-      if (rescale) {
-        // thread t < 16 rescales O row 16 quad + t
-        const float alo = __shfl_sync(0xFFFFFFFFu, al, src);
-#pragma unroll
-        for (int blk = 0; blk < 4; ++blk) {
-          uint32_t ov[32];
-          tc::tmem_ld32(trow + kWTmemO + 32 * blk, ov);
+        // all 128 scores of the row half in registers: sv[32 h + kk] is column
+        // 64 h + 2 kk + par; the buffer is then free for S(g + 2)
+        uint32_t sv[64];
+        {
+          uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
+          uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
+          tc::tmem_ld16x64b_x32(trow + kWTmemS + kWTok * kb, s0);
+          tc::tmem_ld16x64b_x32(trow + kWTmemS + kWTok * kb + 64, s1);
           tc::tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alo);
-          tc::tmem_st32(trow + kWTmemO + 32 * blk, ov);
         }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.sread[kb]));
+        // columns c < nv are attended (none for a padding row); every branch on
+        // `full` is warp-uniform and the masks are selects, so no lane diverges
+        const int nv = okm ? limm - (x.t_lo + j * kWTok) : 0;
+        const bool full = __all_sync(0xFFFFFFFFu, nv >= kWTok);
+        float mx;
+        {
+          float m8[8];
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) m8[kk] = -INFINITY;
+          if (full) {
+#pragma unroll
+            for (int kk = 0; kk < 64; ++kk) m8[kk & 7] = fmaxf(m8[kk & 7], __uint_as_float(sv[kk]));
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 64; ++kk)
+              m8[kk & 7] = fmaxf(m8[kk & 7],
+                                 64 * (kk >> 5) + 2 * (kk & 31) + par < nv ? __uint_as_float(sv[kk]) : -INFINITY);
+          }
+          mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));  // the row's other half
+        const bool grow = mx > rthr;
+        float al = 1.f;
+        bool rescale = false;
+        if (__any_sync(0xFFFFFFFFu, grow)) {
+          const float mn = grow ? fmaxf(mref, mx * sc) : mref;
+          al = grow ? fast_exp2(mref - mn) : 1.f;  // 0 while mref is -inf
+          rescale = j > 0 && __any_sync(0xFFFFFFFFu, grow && mref != -INFINITY);
+          lpart *= al;
+          mref = mn;
+          rthr = (mn + kRescaleLog2) / sc;
+        }
+        // P: register pair (2 r, 2 r + 1) of a half holds tokens (4 r + par, 4 r + par + 2),
+        // which the contraction order places in P column 2 r + par of that half
+        uint32_t pv[32];
+        float ls[8];
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) ls[kk] = 0.f;
+        if (full) {
+#pragma unroll
+          for (int r2 = 0; r2 < 32; ++r2) {
+            const float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * r2]), sc, -mref));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * r2 + 1]), sc, -mref));
+            ls[r2 & 3] += p0;
+            ls[4 + (r2 & 3)] += p1;
+            pv[r2] = pack_f16x2(p0, p1);
+          }
+        } else {
+          // a masked column's exponential may overflow; the select drops it
+#pragma unroll
+          for (int r2 = 0; r2 < 32; ++r2) {
+            const int c0 = 64 * (r2 >> 4) + 4 * (r2 & 15) + par;
+            const float e0 = fast_exp2(fmaf(__uint_as_float(sv[2 * r2]), sc, -mref));
+            const float e1 = fast_exp2(fmaf(__uint_as_float(sv[2 * r2 + 1]), sc, -mref));
+            const float p0 = c0 < nv ? e0 : 0.f, p1 = c0 + 2 < nv ? e1 : 0.f;
+            ls[r2 & 3] += p0;
+            ls[4 + (r2 & 3)] += p1;
+            pv[r2] = pack_f16x2(p0, p1);
+          }
+        }
+        lpart += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+        // P buffer g % 2 is free once P.V(g - 2) has completed; O, for a
+        // rescale, once P.V(g - 1) has (every earlier product is then applied)
+        if (gg >= kWBufs || rescale) {
+          const int64_t gw = rescale ? gg - 1 : gg - kWBufs;
+          if (!warp_wait(smem_u32(&bs.pvdone[gw % kWBufs]), (gw / kWBufs) & 1)) {
+            to = true;
+            break;
+          }
+          tc::fence_after_sync();
+        }
+        if (rescale) {
+          // thread t < 16 rescales O row 16 quad + t
+          const float alo = __shfl_sync(0xFFFFFFFFu, al, src);
+#pragma unroll
+          for (int blk = 0; blk < 4; ++blk) {
+            uint32_t ov[32];
+            tc::tmem_ld32(trow + kWTmemO + 32 * blk, ov);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alo);
+            tc::tmem_st32(trow + kWTmemO + 32 * blk, ov);
+          }
+        }
+        const uint32_t pbuf = trow + kWTmemP + (kWTok / 2) * kb;
+        tc::tmem_st16x64b_x16(pbuf, *reinterpret_cast<const uint32_t(*)[16]>(&pv[0]));
+        tc::tmem_st16x64b_x16(pbuf + 32, *reinterpret_cast<const uint32_t(*)[16]>(&pv[16]));
+        tc::tmem_st_wait();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.pfull[kb]));
       }
-      const uint32_t pbuf = trow + kWTmemP + (kWTok / 2) * kb;
-      tc::tmem_st16x64b_x16(pbuf, *reinterpret_cast<const uint32_t(*)[16]>(&pv[0]));
-      tc::tmem_st16x64b_x16(pbuf + 32, *reinterpret_cast<const uint32_t(*)[16]>(&pv[16]));
-      tc::tmem_st_wait();
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.pfull[kb]));
-    }
-    // ---- epilogue: thread t < 16 writes row 16 quad + t from lane t of O
-    const float lrow = lpart + __shfl_xor_sync(0xFFFFFFFFu, lpart, 2);
-    const float le = __shfl_sync(0xFFFFFFFFu, lrow, src), me = __shfl_sync(0xFFFFFFFFu, mref, src);
-    if (live) {
-      if (!to && ntiles > 0 &&
-          !warp_wait(smem_u32(&bs.pvdone[(ntiles - 1) % kWBufs]), ((ntiles - 1) / kWBufs) & 1))
+      if (to) break;
+      // ---- epilogue: thread t < 16 writes row 16 quad + t from lane t of O
+      const float lrow = lpart + __shfl_xor_sync(0xFFFFFFFFu, lpart, 2);
+      const float le = __shfl_sync(0xFFFFFFFFu, lrow, src), me = __shfl_sync(0xFFFFFFFFu, mref, src);
+      if (ntiles > 0 && !warp_wait(smem_u32(&bs.pvdone[(g + ntiles - 1) % kWBufs]),
+                                   ((g + ntiles - 1) / kWBufs) & 1)) {
         to = true;
+        break;
+      }
       tc::fence_after_sync();
       const int re = 16 * quad + (lane & 15);
       const bool oke = lane < 16 && re < x.rows;
@@ -1521,7 +1638,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
 #pragma unroll
           for (int c = 0; c < 32; ++c) ov[c] = 0u;
         }
-        if (!oke || to) continue;
+        if (!oke) continue;
         if (direct) {
           uint32_t pk[16];
 #pragma unroll
@@ -1529,16 +1646,17 @@ __global__ void __launch_bounds__(kWThreads, 1)
             pk[c] = pack_bf16x2(__uint_as_float(ov[2 * c]) * inv, __uint_as_float(ov[2 * c + 1]) * inv);
           uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + hre * kD + 32 * blk);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+          for (int kk = 0; kk < 4; ++kk)
+            dst[kk] = make_uint4(pk[4 * kk], pk[4 * kk + 1], pk[4 * kk + 2], pk[4 * kk + 3]);
         } else {
           float4* dst = reinterpret_cast<float4*>(part + 4 + 32 * blk);
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            dst[k] = make_float4(__uint_as_float(ov[4 * k]), __uint_as_float(ov[4 * k + 1]),
-                                 __uint_as_float(ov[4 * k + 2]), __uint_as_float(ov[4 * k + 3]));
+          for (int kk = 0; kk < 8; ++kk)
+            dst[kk] = make_float4(__uint_as_float(ov[4 * kk]), __uint_as_float(ov[4 * kk + 1]),
+                                  __uint_as_float(ov[4 * kk + 2]), __uint_as_float(ov[4 * kk + 3]));
         }
       }
-      if (oke && !to) {
+      if (oke) {
         if (direct) {
           if (a.lse) a.lse[hre] = le > 0.f ? (me + __log2f(le)) * kLn2 : -INFINITY;
         } else {
@@ -1546,6 +1664,13 @@ __global__ void __launch_bounds__(kWThreads, 1)
           part[1] = le;
         }
       }
+      // O has been read: the next unit's first P.V may overwrite it
+      if (ntiles > 0) {
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.oread));
+      }
+      g += ntiles;
     }
   }
 
@@ -1668,6 +1793,7 @@ int pfkv_paged_prefill_attn(void* out, const void* q, const void* k_cache, const
   a.q_start = q_start;
   a.lse = lse_out;
   a.status = reinterpret_cast<int32_t*>(ws);
+  a.work = reinterpret_cast<uint32_t*>(ws + sizeof(int32_t));
   a.partials = reinterpret_cast<float*>(ws + kStatusBytes);
   a.B = batch;
   a.Hq = num_q_heads;
@@ -1703,7 +1829,8 @@ int pfkv_paged_prefill_attn(void* out, const void* q, const void* k_cache, const
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(prefill_kernel), kSmemBytes, smem_set,
                             "paged_prefill set smem attribute");
   if (rc != PFKV_OK) return rc;
-  if (cudaMemsetAsync(a.status, 0, sizeof(int32_t), s) != cudaSuccess) return check_cuda("paged_prefill status");
+  // the status word and the persistent kernel's work counter
+  if (cudaMemsetAsync(a.status, 0, 2 * sizeof(int32_t), s) != cudaSuccess) return check_cuda("paged_prefill status");
   if (a.QB >= 2) {
     // several row blocks per (request, KV head): two blocks per CTA
     static std::atomic<uint64_t> smem2_set{0};
@@ -1729,7 +1856,8 @@ int pfkv_paged_prefill_attn(void* out, const void* q, const void* k_cache, const
                                strides, boxw, CU_TENSOR_MAP_SWIZZLE_128B);
       if (rc != PFKV_OK) return rc;
     }
-    prefillw_kernel<<<(unsigned)units, kWThreads, kWSmemBytes, s>>>(tmK, tmV, a);
+    const int64_t grid = units < device_sm_count() ? units : device_sm_count();  // one CTA per SM
+    prefillw_kernel<<<(unsigned)grid, kWThreads, kWSmemBytes, s>>>(tmK, tmV, a, units);
   } else {
     prefill_kernel<<<(unsigned)units, kThreads, kSmemBytes, s>>>(tmK, tmV, a);
   }
