@@ -110,7 +110,8 @@ struct PrefillArgs {
   float score_scale;  // k_scale * softmax_scale * log2(e)
   float out_scale;    // v_scale
   int box_tok;        // prefillw_kernel: tokens per TMA box (16, 32 or 64, dividing the page)
-  uint32_t* work;     // prefillw_kernel: next work unit to hand out (zeroed per call)
+  int64_t* tile_start;  // prefillw_kernel: [B + 1] flattened start of each request's (KV head, tile) range
+  int ncta;             // prefillw_kernel: CTAs sharing the flattened range
 };
 
 struct Bars {
@@ -1106,16 +1107,13 @@ struct BarsW {
   uint64_t sread[kWBufs];                 // the softmax warps have read a score buffer
   uint64_t pvdone[kWBufs];                // P.V of a tile complete (index: tile % 2)
   uint64_t pfull[kWBufs];                 // P of a tile written (index: tile % 2)
-  uint64_t ufull[2], uempty[2];           // the unit queue's two slots
-  uint64_t qready;                        // Q of the current unit written
-  uint64_t qfree;                         // the previous unit's score products are done with Q
-  uint64_t oread;                         // a unit's epilogue has read O
-  int64_t uq[2];                          // unit ids (-1: no more work)
+  uint64_t qready;                        // Q of the current segment written
+  uint64_t qfree;                         // the previous segment's score products are done with Q
+  uint64_t oread;                         // a segment's epilogue has read O
   uint32_t tmem_base;
 };
 static_assert(sizeof(BarsW) <= 512, "barrier block");
-// warps that read each unit id from the queue: score issuer, converters, softmax, P.V issuer
-constexpr int kWUnitReaders = 1 + kWConvWarps + 4 + 1;
+constexpr int kWRows = 64;  // rows of a block on this path (every block holds at most 64)
 
 // Widening of a stage's V rows into f16 atoms, rows in the P.V contraction
 // order, in two steps: load_v reads this thread's e4m3 chunks (rows at or past
@@ -1155,26 +1153,130 @@ __device__ __forceinline__ void e4m3x2_to_f32x2(uint16_t code, float& lo, float&
   hi = __half2float(__ushort_as_half((unsigned short)(h >> 16)));
 }
 
-// Persistent: one CTA per SM takes work units, in index order, from a counter
-// in the workspace until none is left; the
-// producer streams the next unit's tiles while the current one drains, so a
-// unit's fixed costs (first copies in flight, last products) overlap its
-// neighbours and no wave of CTAs waits for the slowest.  Every ring's phase
-// follows the CTA's running tile count g, not the tile index inside a unit.
-// Per unit: the producer publishes the unit id in a two-slot queue (ufull /
-// uempty); the softmax warps write Q once the previous unit's score products
-// are done (qfree) and signal qready; P.V of a unit's first tile overwrites O
-// once the epilogue of the previous unit with tiles has read it (oread, one
-// phase per unit that has tiles, so that no phase can run two ahead).
+// Clamped context length and query count of request b, as unit_of takes them.
+__device__ __forceinline__ void clamped_ln(const PrefillArgs& a, int b, int& L, int& n, bool report) {
+  const int L_raw = a.context_lens[b];
+  const int n_raw = a.q_start[b + 1] - a.q_start[b];
+  int cap = a.max_pages * a.P;
+  if (a.max_ctx < cap) cap = a.max_ctx;
+  L = L_raw < 0 ? 0 : (L_raw > cap ? cap : L_raw);
+  const int ncap = L < a.max_q_len ? L : a.max_q_len;
+  n = n_raw < 0 ? 0 : (n_raw > ncap ? ncap : n_raw);
+  if (report && (L != L_raw || n != n_raw)) atomicOr(a.status, kErrBadContext);
+}
+
+// One CTA: tile_start[b] = sum over earlier requests of Hkv x their 128-token
+// tiles (a request without queries has none); tile_start[B] = W.
+__global__ void __launch_bounds__(1024) prefillw_plan_kernel(const PrefillArgs a) {
+  __shared__ int64_t warp_sum[32];
+  __shared__ int64_t carry;
+  grid_launch_dependents();  // the tile kernel may start its prologue now
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  for (int base = 0; base < a.B; base += 1024) {
+    const int b = base + threadIdx.x;
+    int64_t t = 0;
+    if (b < a.B) {
+      int L, n;
+      clamped_ln(a, b, L, n, true);
+      t = n > 0 ? (int64_t)((L + kWTok - 1) / kWTok) * a.Hkv : 0;
+    }
+    int64_t sc = t;  // inclusive warp scan
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xFFFFFFFFu, sc, o);
+      if (lane >= o) sc += y;
+    }
+    if (lane == 31) warp_sum[wid] = sc;
+    __syncthreads();
+    if (wid == 0) {
+      int64_t w = warp_sum[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(0xFFFFFFFFu, w, o);
+        if (lane >= o) w += y;
+      }
+      warp_sum[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    const int64_t before = carry + (wid > 0 ? warp_sum[wid - 1] : 0) + sc - t;
+    if (b < a.B) a.tile_start[b] = before;
+    __syncthreads();
+    if (threadIdx.x == 0) carry += warp_sum[31];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) a.tile_start[a.B] = carry;
+}
+
+// A CTA's run of tiles inside one (request, KV head): tiles [ta, tb) of its
+// ceil(L / 128), as a unit (tokens [t_lo, t_hi), causal mask as usual).
+struct Seg {
+  Unit x;
+  bool whole;    // the run is the pair's whole range: the output rows are written directly
+  int64_t slot;  // otherwise its partial state's slot: CTA + b Hkv + kvh
+};
+__device__ __forceinline__ Seg seg_at(const PrefillArgs& a, int64_t f, int64_t f1) {
+  // the last request whose range starts at or before f (it has tiles: f < W)
+  int lo = 0, hi = a.B;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (a.tile_start[mid] <= f) lo = mid;
+    else hi = mid;
+  }
+  const int b = lo;
+  const int64_t s0 = a.tile_start[b];
+  const int per = (int)((a.tile_start[b + 1] - s0) / a.Hkv);  // tiles per KV head
+  const int64_t off = f - s0;
+  const int kvh = (int)(off / per), ta = (int)(off % per);
+  const int64_t room = (int64_t)per - ta;
+  const int tb = ta + (int)(f1 - f < room ? f1 - f : room);
+  Seg sg;
+  Unit& x = sg.x;
+  int L, n;
+  clamped_ln(a, b, L, n, false);
+  x.b = b;
+  x.kvh = kvh;
+  x.qb = 0;
+  x.c = 0;
+  x.L = L;
+  x.n = n;
+  x.i0 = 0;
+  x.i1 = n;
+  x.rows = n * a.G;
+  x.t_lo = ta * kWTok;
+  x.t_hi = min(tb * kWTok, L);
+  x.t_end_chunk = x.t_hi;
+  x.ntiles = tb - ta;
+  x.active = true;
+  sg.whole = ta == 0 && tb == per;
+  sg.slot = (int64_t)blockIdx.x + (int64_t)b * a.Hkv + kvh;
+  return sg;
+}
+
+// Flattened and persistent: the (request, KV head, 128-token tile) space is
+// laid out request by request (prefillw_plan_kernel writes where each
+// request's range starts) and CTA i of N takes tiles [i W / N, (i + 1) W / N):
+// every SM gets the same number of tiles whatever the mix of lengths.  A
+// CTA's range is a few segments, one per (request, KV head) it touches; each
+// warp role walks the same segments (a deterministic walk, no queue), and the
+// producer streams the next segment's tiles while the current one drains.
+// Every ring's phase follows the CTA's running tile count g.  A segment that
+// covers its whole (request, KV head) writes the output rows; any other writes
+// a partial state (m, l, o) to slot i + (b Hkv + kvh), distinct for every
+// (CTA, pair) since a CTA's pairs are consecutive, and prefillw_merge_kernel
+// folds them (kLLM article, §5.2.2).
+// Per segment: the softmax warps write Q once the previous segment's score
+// products are done (qfree) and signal qready; P.V of a segment's first tile
+// overwrites O once the previous segment's epilogue has read it (oread).
 __global__ void __launch_bounds__(kWThreads, 1)
     prefillw_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                    const PrefillArgs a, const int64_t units) {
+                    const PrefillArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* const smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   BarsW& bs = *reinterpret_cast<BarsW*>(smem + kWOffBars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const bool direct = a.C == 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kWStages; ++s) {
@@ -1187,8 +1289,6 @@ __global__ void __launch_bounds__(kWThreads, 1)
       mbar_init(smem_u32(&bs.sread[k]), 4);
       mbar_init(smem_u32(&bs.pvdone[k]), 1);
       mbar_init(smem_u32(&bs.pfull[k]), 4);
-      mbar_init(smem_u32(&bs.ufull[k]), 1);
-      mbar_init(smem_u32(&bs.uempty[k]), kWUnitReaders);
     }
     mbar_init(smem_u32(&bs.qready), 4);
     mbar_init(smem_u32(&bs.qfree), 1);
@@ -1207,22 +1307,10 @@ __global__ void __launch_bounds__(kWThreads, 1)
   const uint32_t tmem = bs.tmem_base;
   bool to = false;  // a bounded wait gave up
 
-  // Unit k of this CTA from the queue (every reader warp, all lanes): -1 when
-  // the work is done or a wait gave up.  Lane 0 frees the slot once all lanes
-  // hold the id.
-  auto next_unit = [&](int k, bool whole_warp) -> int64_t {
-    const uint32_t full = smem_u32(&bs.ufull[k % 2]);
-    const bool ok = whole_warp ? warp_wait(full, (k / 2) & 1) : mbar_wait(full, (k / 2) & 1);
-    if (!ok) {
-      to = true;
-      return -1;
-    }
-    const int64_t uu = bs.uq[k % 2];
-    if (whole_warp) __syncwarp();
-    if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.uempty[k % 2]));
-    return uu;
-  };
-  auto ntiles_of = [&](const Unit& x) { return x.ntiles == 0 ? 0 : (x.t_hi - x.t_lo + kWTok - 1) / kWTok; };
+  grid_launch_dependents();  // the merge kernel may be scheduled as CTAs retire
+  grid_dependency_wait();    // the plan's tile offsets are complete and visible
+  const int64_t W = a.tile_start[a.B];
+  const int64_t f0 = (int64_t)blockIdx.x * W / gridDim.x, f1 = ((int64_t)blockIdx.x + 1) * W / gridDim.x;
 
   if (warp == kWProdWarp) {
     // ------------------------------------------------------------ producer
@@ -1235,32 +1323,10 @@ __global__ void __launch_bounds__(kWThreads, 1)
     // loaded while this one is issued.
     const int btok = a.box_tok, nb = kWTok / btok, tpb = 32 / nb;
     int64_t g = 0;  // tiles issued by this CTA so far
-    for (int k = 0; !to; ++k) {
-      // the next unit with work: every index is taken by exactly one CTA
-      int64_t u = -1;
-      if (lane == 0) {
-        while (true) {
-          const int64_t c = (int64_t)atomicAdd(a.work, 1u);
-          if (c >= units) break;
-          const Unit xc = unit_of(a, c, (c % ((int64_t)a.QB * a.C * a.Hkv)) == 0);
-          if (xc.active) {
-            u = c;
-            break;
-          }
-        }
-      }
-      u = __shfl_sync(0xFFFFFFFFu, u, 0);
-      if (k >= 2 && !warp_wait(smem_u32(&bs.uempty[k % 2]), ((k / 2) - 1) & 1)) {
-        to = true;
-        break;
-      }
-      if (lane == 0) {
-        bs.uq[k % 2] = u;
-        tc::mbar_arrive_local(smem_u32(&bs.ufull[k % 2]));  // release: the id is visible to the readers
-      }
-      if (u < 0) break;
-      const Unit x = unit_of(a, u, false);
-      const int ntiles = ntiles_of(x);
+    for (int64_t f = f0; f < f1 && !to;) {
+      const Seg sg = seg_at(a, f, f1);
+      const Unit& x = sg.x;
+      const int ntiles = x.ntiles;
       const int32_t* bt = a.block_tables + (int64_t)x.b * a.max_pages;
       auto load_batch = [&](int j0) {
         const int j = j0 + lane / nb;
@@ -1298,6 +1364,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
         }
       }
       g += ntiles;
+      f += ntiles;
     }
     // no copy may still be landing when the CTA retires
     for (int64_t gg = g > kWStages ? g - kWStages : 0; gg < g; ++gg)
@@ -1312,10 +1379,10 @@ __global__ void __launch_bounds__(kWThreads, 1)
     if (lane == 0) {
       const uint64_t qdesc = tc::desc_sw128(smem_u32(smem + kWOffQ), 16, 1024);
       int64_t g = 0;
-      for (int k = 0; !to; ++k) {
-        const int64_t u = next_unit(k, false);
-        if (u < 0) break;
-        const int ntiles = ntiles_of(unit_of(a, u, false));
+      int k = 0;
+      for (int64_t f = f0; f < f1 && !to; ++k) {
+        const int ntiles = seg_at(a, f, f1).x.ntiles;
+        f += ntiles;
         if (!mbar_wait(smem_u32(&bs.qready), k & 1)) {
           to = true;
           break;
@@ -1350,17 +1417,13 @@ __global__ void __launch_bounds__(kWThreads, 1)
     if (lane == 0) {
       const uint32_t v0 = smem_u32(smem + kWOffV);
       int64_t g = 0;
-      int m = 0;  // units with tiles so far
-      for (int k = 0; !to; ++k) {
-        const int64_t u = next_unit(k, false);
-        if (u < 0) break;
-        const int ntiles = ntiles_of(unit_of(a, u, false));
-        if (ntiles > 0) {
-          if (m > 0 && !mbar_wait(smem_u32(&bs.oread), (m - 1) & 1)) {
-            to = true;
-            break;
-          }
-          ++m;
+      int k = 0;  // every segment has tiles
+      for (int64_t f = f0; f < f1 && !to; ++k) {
+        const int ntiles = seg_at(a, f, f1).x.ntiles;
+        f += ntiles;
+        if (k > 0 && !mbar_wait(smem_u32(&bs.oread), (k - 1) & 1)) {
+          to = true;
+          break;
         }
         for (int j = 0; j < ntiles && !to; ++j) {
           const int64_t gg = g + j;
@@ -1390,11 +1453,11 @@ __global__ void __launch_bounds__(kWThreads, 1)
     // once; written once P.V(g - 2) has completed (its buffer).
     const int ct = threadIdx.x - kWConvWarp0 * 32;
     int64_t g = 0;
-    for (int k = 0; !to; ++k) {
-      const int64_t u = next_unit(k, true);
-      if (u < 0) break;
-      const Unit x = unit_of(a, u, false);
-      const int ntiles = ntiles_of(x);
+    for (int64_t f = f0; f < f1 && !to;) {
+      const Seg sg = seg_at(a, f, f1);
+      const Unit& x = sg.x;
+      const int ntiles = x.ntiles;
+      f += ntiles;
       for (int j = 0; j < ntiles; ++j) {
         const int64_t gg = g + j;
         const int st = (int)(gg % kWStages), kb = (int)(gg % kWBufs);
@@ -1432,11 +1495,12 @@ __global__ void __launch_bounds__(kWThreads, 1)
     // are held by thread 4 (t % 8) + t / 8
     const int src = 4 * (lane & 7) + ((lane >> 3) & 1);
     int64_t g = 0;
-    for (int k = 0; !to; ++k) {
-      const int64_t u = next_unit(k, true);
-      if (u < 0) break;
-      const Unit x = unit_of(a, u, false);
-      const int ntiles = ntiles_of(x);
+    int k = 0;
+    for (int64_t f = f0; f < f1 && !to; ++k) {
+      const Seg sg = seg_at(a, f, f1);
+      const Unit& x = sg.x;
+      const int ntiles = x.ntiles;
+      f += ntiles;
       // Q: threads t and t + 16 split row 16 quad + t (t < 16), each its half
       // (64 elements), into two e4m3 parts (x = q s with s a power of two
       // taking max |q| of the row into (224, 448]; part 1 = e4m3(x), part 2 =
@@ -1626,7 +1690,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
       const bool oke = lane < 16 && re < x.rows;
       const int ie = x.i0 + re / a.G, ge = re % a.G;
       const int64_t hre = ((int64_t)a.q_start[x.b] + ie) * a.Hq + (int64_t)x.kvh * a.G + ge;
-      float* part = direct ? nullptr : a.partials + ((int64_t)u * kRows + re) * kPartStride;
+      const bool direct = sg.whole;
+      float* part = direct ? nullptr : a.partials + ((sg.slot * kWRows) + re) * kPartStride;
       const float inv = le > 0.f ? a.out_scale / le : 0.f;
 #pragma unroll
       for (int blk = 0; blk < 4; ++blk) {
@@ -1664,12 +1729,10 @@ __global__ void __launch_bounds__(kWThreads, 1)
           part[1] = le;
         }
       }
-      // O has been read: the next unit's first P.V may overwrite it
-      if (ntiles > 0) {
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.oread));
-      }
+      // O has been read: the next segment's first P.V may overwrite it
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.oread));
       g += ntiles;
     }
   }
@@ -1720,9 +1783,62 @@ __global__ void __launch_bounds__(kMergeWarps * 32) prefill_merge_kernel(const P
   if (a.lse && lane == 0) a.lse[head_row] = den > 0.f ? (M + __log2f(den)) * kLn2 : -INFINITY;
 }
 
+// One warp per row of a (request, KV head) on the flattened path: folds the
+// partial states of the CTAs whose tile ranges cut the pair's range (slot
+// CTA + pair), in CTA order, skipping CTAs whose range is empty; a pair
+// inside one CTA's range was written by it.
+__global__ void __launch_bounds__(kMergeWarps * 32) prefillw_merge_kernel(const PrefillArgs a) {
+  grid_dependency_wait();  // every partial state of the tile kernel is visible
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t u = blockIdx.x / (kWRows / kMergeWarps);
+  const int r = (int)(blockIdx.x % (kWRows / kMergeWarps)) * kMergeWarps + warp;
+  const int b = (int)(u / a.Hkv), kvh = (int)(u % a.Hkv);
+  const int64_t s0 = a.tile_start[b];
+  const int64_t per = (a.tile_start[b + 1] - s0) / a.Hkv;
+  if (per == 0) return;
+  int L, n;
+  clamped_ln(a, b, L, n, false);
+  if (r >= n * a.G) return;
+  const int64_t W = a.tile_start[a.B], N = a.ncta;
+  const int64_t T0 = s0 + kvh * per, T1 = T0 + per;
+  const int64_t i0 = ((T0 + 1) * N - 1) / W, i1 = (T1 * N - 1) / W;  // owners of tiles T0 and T1 - 1
+  if (i0 == i1) return;
+  float M = -INFINITY, den = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t i = i0; i <= i1; ++i) {
+    if (i * W / N == (i + 1) * W / N) continue;  // an empty range (fewer tiles than CTAs) wrote nothing
+    const float* p = a.partials + ((i + u) * kWRows + r) * kPartStride;
+    const float mk = p[0], lk = p[1];
+    if (lk == 0.f) continue;  // a run this row does not reach
+    const float4 ok = reinterpret_cast<const float4*>(p + 4)[lane];
+    const float Mn = fmaxf(M, mk);
+    const float al = fast_exp2(M - Mn), wt = fast_exp2(mk - Mn);
+    den = den * al + wt * lk;
+    acc.x = acc.x * al + wt * ok.x;
+    acc.y = acc.y * al + wt * ok.y;
+    acc.z = acc.z * al + wt * ok.z;
+    acc.w = acc.w * al + wt * ok.w;
+    M = Mn;
+  }
+  const int64_t head_row = ((int64_t)a.q_start[b] + r / a.G) * a.Hq + (int64_t)kvh * a.G + r % a.G;
+  const float inv = den > 0.f ? a.out_scale / den : 0.f;
+  reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.out) + head_row * kD)[lane] =
+      make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+  if (a.lse && lane == 0) a.lse[head_row] = den > 0.f ? (M + __log2f(den)) * kLn2 : -INFINITY;
+}
+
 constexpr size_t kStatusBytes = 256;
 
 int64_t units_of(int B, int Hkv, int QB, int C) { return (int64_t)B * Hkv * QB * C; }
+
+// The flattened path (every block at most 64 rows): the request offsets, then
+// one 64-row partial state per (CTA, pair) slot, CTAs + B Hkv slots.
+size_t wide_offsets_bytes(int B) { return ((size_t)(B + 1) * sizeof(int64_t) + 255) / 256 * 256; }
+size_t wide_workspace_bytes(int B, int Hkv) {
+  const int ncta = device_sm_count() > 0 ? device_sm_count() : 1;
+  return kStatusBytes + wide_offsets_bytes(B) +
+         ((size_t)ncta + (size_t)B * Hkv) * kWRows * kPartStride * sizeof(float);
+}
 
 }  // namespace
 }  // namespace pfkv
@@ -1739,6 +1855,7 @@ size_t pfkv_paged_prefill_workspace_size(int batch, int num_q_heads, int num_kv_
   const int G = num_q_heads / num_kv_heads;
   if (G > kRows) return 0;
   const int QB = (int)(((int64_t)max_q_len * G + kRows - 1) / kRows);
+  if ((int64_t)max_q_len * G <= kWRows) return wide_workspace_bytes(batch, num_kv_heads);
   const int C = kv_split_tokens > 0 ? (max_context_len + kv_split_tokens - 1) / kv_split_tokens : 1;
   if (C <= 1) return kStatusBytes;
   return kStatusBytes + (size_t)units_of(batch, num_kv_heads, QB, C) * kRows * kPartStride * sizeof(float);
@@ -1793,7 +1910,6 @@ int pfkv_paged_prefill_attn(void* out, const void* q, const void* k_cache, const
   a.q_start = q_start;
   a.lse = lse_out;
   a.status = reinterpret_cast<int32_t*>(ws);
-  a.work = reinterpret_cast<uint32_t*>(ws + sizeof(int32_t));
   a.partials = reinterpret_cast<float*>(ws + kStatusBytes);
   a.B = batch;
   a.Hq = num_q_heads;
@@ -1829,8 +1945,7 @@ int pfkv_paged_prefill_attn(void* out, const void* q, const void* k_cache, const
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(prefill_kernel), kSmemBytes, smem_set,
                             "paged_prefill set smem attribute");
   if (rc != PFKV_OK) return rc;
-  // the status word and the persistent kernel's work counter
-  if (cudaMemsetAsync(a.status, 0, 2 * sizeof(int32_t), s) != cudaSuccess) return check_cuda("paged_prefill status");
+  if (cudaMemsetAsync(a.status, 0, sizeof(int32_t), s) != cudaSuccess) return check_cuda("paged_prefill status");
   if (a.QB >= 2) {
     // several row blocks per (request, KV head): two blocks per CTA
     static std::atomic<uint64_t> smem2_set{0};
@@ -1856,8 +1971,29 @@ int pfkv_paged_prefill_attn(void* out, const void* q, const void* k_cache, const
                                strides, boxw, CU_TENSOR_MAP_SWIZZLE_128B);
       if (rc != PFKV_OK) return rc;
     }
-    const int64_t grid = units < device_sm_count() ? units : device_sm_count();  // one CTA per SM
-    prefillw_kernel<<<(unsigned)grid, kWThreads, kWSmemBytes, s>>>(tmK, tmV, a, units);
+    // the KV range of all (request, KV head) pairs split evenly over one CTA
+    // per SM (kv_split_tokens is not needed here); plan, tile kernel and merge,
+    // the last two as programmatic dependents of the kernel before them
+    a.ncta = device_sm_count() > 0 ? device_sm_count() : 1;
+    a.tile_start = reinterpret_cast<int64_t*>(ws + kStatusBytes);
+    a.partials = reinterpret_cast<float*>(ws + kStatusBytes + wide_offsets_bytes(batch));
+    prefillw_plan_kernel<<<1, 1024, 0, s>>>(a);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3((unsigned)a.ncta);
+    cfg.blockDim = dim3(kWThreads);
+    cfg.dynamicSmemBytes = kWSmemBytes;
+    if (cudaLaunchKernelEx(&cfg, prefillw_kernel, tmK, tmV, a) != cudaSuccess) return check_cuda("paged_prefill launch");
+    cfg.gridDim = dim3((unsigned)((int64_t)batch * num_kv_heads * (kWRows / kMergeWarps)));
+    cfg.blockDim = dim3(kMergeWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    if (cudaLaunchKernelEx(&cfg, prefillw_merge_kernel, a) != cudaSuccess) return check_cuda("paged_prefill merge");
+    return check_cuda("paged_prefill launch");
   } else {
     prefill_kernel<<<(unsigned)units, kThreads, kSmemBytes, s>>>(tmK, tmV, a);
   }
