@@ -313,7 +313,13 @@ PFKV_API int pfkv_paged_decode_attn_scaled(void *out, const void *q, const void 
  *   kv_split_tokens  0: one pass over each request's context; > 0 (a
  *                 multiple of 64): chunks of that many tokens run in parallel
  *                 and are merged (workspace grows with batch * num_kv_heads *
- *                 ceil(max_q_len * G / 128) * ceil(max_context_len / split))
+ *                 ceil(max_q_len * G / 128) * ceil(max_context_len / split)).
+ *                 Not used when max_q_len * G <= 64 (verification-sized
+ *                 calls): the contexts of all (request, KV head) pairs are
+ *                 then split evenly over one CTA per SM and the pieces merged
+ *                 (workspace: (SMs + batch * num_kv_heads) 64-row partial
+ *                 states plus batch + 1 offsets), whatever the value (it is
+ *                 still checked)
  *   workspace     >= pfkv_paged_prefill_workspace_size(...) bytes, 256-byte
  *                 aligned; lse_out optional fp32 [q_start[batch]][num_q_heads]
  * Other layouts as pfkv_paged_decode_attn.
