@@ -483,24 +483,19 @@ def prefill_timing(pf, peak_gbs, peak_tf, flush, iters):
     s, q, qs = setup(w)
     out = torch.empty_like(q)
     st = s.st
-    best = None
-    sweep = {}
-    for split in (4096, 16384, 65536):
-        ws = torch.empty(pf.paged_prefill_workspace_size(w.B, w.Hq, w.Hkv, w.n_new, int(w.context_lens.max()), split),
-                         dtype=torch.uint8, device="cuda")
-        fn = lambda: pf.paged_prefill_attn(out, q, st.k_cache, st.v_cache, st.block_tables, st.context_lens, qs,
-                                           w.n_new, int(w.context_lens.max()), w.k_scale, w.v_scale, w.softmax_scale,
-                                           kv_split_tokens=split, workspace=ws)
-        fn()
-        t = time_events(fn, iters, flush)
-        sweep[str(split)] = round(t * 1e6, 1)
-        if best is None or t < best[0]:
-            best = (t, split)
-        del ws
-    t, split = best
+    # 8 queries x G 8 = 64 rows per (request, KV head): the tile space of all
+    # pairs is split evenly over the SMs, so no kv_split_tokens is chosen
+    ws = torch.empty(pf.paged_prefill_workspace_size(w.B, w.Hq, w.Hkv, w.n_new, int(w.context_lens.max()), 0),
+                     dtype=torch.uint8, device="cuda")
+    fn = lambda: pf.paged_prefill_attn(out, q, st.k_cache, st.v_cache, st.block_tables, st.context_lens, qs,
+                                       w.n_new, int(w.context_lens.max()), w.k_scale, w.v_scale, w.softmax_scale,
+                                       workspace=ws)
+    fn()
+    t = time_events(fn, iters, flush)
+    del ws
     nbytes = s.bytes()["kv"] + 2 * q.numel() * 2 + s.bytes()["tables"]
     res["verify_long_b8_h64kv8_q8"] = {
-        "prefill_us": round(t * 1e6, 2), "kv_split_tokens": split, "split_sweep_us": sweep,
+        "prefill_us": round(t * 1e6, 2), "partition": "tile space split evenly over one CTA per SM",
         "GBs": round(nbytes / t / 1e9, 1), "frac_of_hbm_peak": round(nbytes / t / 1e9 / peak_gbs, 4),
         "tflops": round(causal_flops(w) / t / 1e12, 2)}
     del s, q, out, st
@@ -896,7 +891,7 @@ PROFILE_CASES = {
     "mla_b16_topk2048": "MLA 128 heads x 576, 16 requests x 65536 tokens, top-k 2048, page 64",
     "prefill_chunk_b1_n1024_l8192": "multi-query: 1 request, 1024 new tokens on a 7168-token prefix, GQA 64/8",
     "prefill_verify_b2_l262144_q8": "multi-query: 2 requests x 262144 tokens, 8 new tokens each, GQA 64/8, "
-                                    "page 64, 16384-token chunks",
+                                    "page 64, the tile space split evenly over the SMs",
 }
 
 
@@ -949,7 +944,7 @@ def run_profile_case(name):
                                                 context_lens=np.full(1, 8192), n_new=1024, seed=7))
     elif name == "prefill_verify_b2_l262144_q8":
         s = PrefillStep(pf, synth.PagedWorkload("verify_b2", B=2, Hq=64, Hkv=8, D=128, P=64,
-                                                context_lens=np.full(2, 262144), n_new=8), split=16384)
+                                                context_lens=np.full(2, 262144), n_new=8))
     elif name == "mla_b16_topk2048":
         s = MlaStep(pf, synth.MlaWorkload("mla_b16", B=16, H=128, context_lens=np.full(16, 65536), topk_n=2048,
                                           P=64))

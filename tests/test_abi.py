@@ -121,10 +121,15 @@ def test_prefill_host_validation_without_cuda(lib):
     assert call(ctx=None) == -1 and "null pointer" in _err(lib)
     assert call(out=_fake(0x10008)) == -1 and "misaligned" in _err(lib)
     assert call(ws=_fake(0x10080)) == -1           # workspace not 256-byte aligned
+    # 4 queries x G 8 = 32 rows: the tile space is split evenly over the SMs,
+    # so the workspace holds request offsets and partial states whatever the split
     need = lib.pfkv_paged_prefill_workspace_size(2, 16, 2, 128, 4, 100, 64)
-    assert need > 256
+    assert need > 256 and need == lib.pfkv_paged_prefill_workspace_size(2, 16, 2, 128, 4, 100, 0)
     assert call(split=64, wsb=need - 1) == -5 and "too small" in _err(lib)
-    assert lib.pfkv_paged_prefill_workspace_size(2, 16, 2, 128, 4, 100, 0) == 256  # status word only
+    assert call(wsb=need - 1) == -5
+    # 16 queries x G 8 = 128 rows, one pass: the status word only; chunks add partial states
+    assert lib.pfkv_paged_prefill_workspace_size(2, 16, 2, 128, 16, 100, 0) == 256
+    assert lib.pfkv_paged_prefill_workspace_size(2, 16, 2, 128, 16, 100, 64) > 256
     assert lib.pfkv_paged_prefill_workspace_size(2, 16, 3, 128, 4, 100, 0) == 0
 
 
