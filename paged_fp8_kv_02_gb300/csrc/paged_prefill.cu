@@ -1827,6 +1827,463 @@ __global__ void __launch_bounds__(kMergeWarps * 32) prefillw_merge_kernel(const 
   if (a.lse && lane == 0) a.lse[head_row] = den > 0.f ? (M + __log2f(den)) * kLn2 : -INFINITY;
 }
 
+// ------------------------------------- one 128-row block per CTA, Q in TMEM
+// For row blocks of more than 64 rows (chunked prefill), prefillm_kernel
+// takes one block of 128 rows per CTA over 128-token tiles, with Q's two
+// exact e4m3 parts in tensor memory as the A operand of the score products
+// (kind::f8f6f4, M = 128, N = 128), so those products read only the K rows
+// from shared memory; the shared-memory operand traffic of the two-block
+// kernel, whose score products read Q there, bounded it.  Eight softmax
+// warps, two per lane quadrant, each take 64 of a row's 128 scores: the two
+// halves of a row swap their maxima (and, once per unit, Q's largest
+// magnitude and at the end the row sums) through shared memory, handing over
+// with an mbarrier per quadrant and bounded waits, so the reference and the
+// rescale are the same in both.  P (f16) has 64 tensor-memory columns of its
+// own; V rows are widened in token order (a thread packs the columns of its
+// row two by two).
+//   tensor memory: S 2 x 128, O 128, Q 2 x 32 (part p at 384 + 32 p), P 64.
+//   shared memory: three 32 KB e4m3 stages, three 32 KB widened V tiles (a
+//   stage is released once its V is read, so three cover the copy latency;
+//   the third V tile lets the widening of tile j + 2 run while P.V(j) waits
+//   for its P).
+//   warps: 0 K producer, 1 score MMAs, 2-5 widening, 6-13 softmax (warp w:
+//   lane quadrant w % 4, half (w - 6) / 4), 14 P.V MMAs, 15 V producer (one
+//   warp issuing every copy of a tile measured slower, most of all with
+//   16-token pages: 16 copies per tile).
+// Units in order of decreasing row block, so the longest (causal) ones start first.
+constexpr int kMTmemO = 256, kMTmemQ = 384, kMTmemP = 448;
+static_assert(kMTmemP + kWTok / 2 <= kTmemCols, "tensor memory columns");
+constexpr int kMStages = 3, kMVBufs = 3;
+constexpr int kMOffV = 0;
+constexpr int kMOffStage = kMOffV + kMVBufs * kWVBytes;
+constexpr int kMOffX = kMOffStage + kMStages * kWStageBytes;  // float [2 parity][2 halves][128 rows]
+constexpr int kMOffBars = kMOffX + 2 * 2 * kRows * 4;
+constexpr int kMSmemBytes = kMOffBars + 512 + 1024;
+static_assert(kMSmemBytes <= 232448, "shared memory over the per-CTA limit");
+constexpr uint32_t kIdescQKM = tc::idesc_f16(kRows, kWTok, false);  // with kind::f8f6f4: e4m3 x e4m3
+constexpr uint32_t kIdescPVM = tc::idesc_f16(kRows, kD, true);
+constexpr int kMProdWarp = 0, kMMmaWarp = 1, kMConvWarp0 = 2, kMSoftWarp0 = 6, kMPvWarp = 14, kMProdWarpV = 15;
+constexpr int kMThreads = 16 * 32;
+
+struct BarsM {
+  uint64_t stage_full[kMStages], stage_empty[kMStages];
+  uint64_t vfull[kMVBufs], vfree[kMVBufs];  // widened V written / read by its P.V
+  uint64_t sfull[kWBufs], sread[kWBufs], pvdone[kWBufs];
+  uint64_t pfull, qready;
+  uint64_t xch[4];  // the two softmax warps of a lane quadrant hand over shared values
+  uint32_t tmem_base;
+};
+static_assert(sizeof(BarsM) <= 512, "barrier block");
+
+// As store_v, rows in token order.
+__device__ __forceinline__ void store_v_tokens(const uint4 (&v)[kWChunks], uint8_t* dst, int ct) {
+#pragma unroll
+  for (int m = 0; m < kWChunks; ++m) {
+    const int i = ct + 32 * kWConvWarps * m;
+    const int row = i >> 3, c = i & 7;
+    uint4 o0, o1;
+    e4m3x4_to_f16x2x2(v[m].x, o0.x, o0.y);
+    e4m3x4_to_f16x2x2(v[m].y, o0.z, o0.w);
+    e4m3x4_to_f16x2x2(v[m].z, o1.x, o1.y);
+    e4m3x4_to_f16x2x2(v[m].w, o1.z, o1.w);
+    const uint32_t d = atom_off(row, 2 * c, kWAtom);
+    *reinterpret_cast<uint4*>(dst + d) = o0;
+    *reinterpret_cast<uint4*>(dst + (d ^ 16)) = o1;
+  }
+}
+
+__global__ void __launch_bounds__(kMThreads, 1)
+    prefillm_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const PrefillArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* const smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  BarsM& bs = *reinterpret_cast<BarsM*>(smem + kMOffBars);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // CTA -> unit: row blocks from the last (longest under the causal mask) down
+  const int64_t per_qb = (int64_t)a.B * a.Hkv * a.C;
+  const int qb = a.QB - 1 - (int)(blockIdx.x / per_qb);
+  const int64_t u = (blockIdx.x % per_qb) * a.QB + qb;
+  const Unit x = unit_of(a, u, threadIdx.x == 0 && qb == 0 && (u / a.QB) % ((int64_t)a.C * a.Hkv) == 0);
+  if (!x.active) return;  // uniform over the CTA
+  const int ntiles = x.ntiles == 0 ? 0 : (x.t_hi - x.t_lo + kWTok - 1) / kWTok;
+  const bool direct = a.C == 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kMStages; ++s) {
+      mbar_init(smem_u32(&bs.stage_full[s]), 2);  // the K and the V producer
+      mbar_init(smem_u32(&bs.stage_empty[s]), kWConvWarps + 1);  // V read + the score products done
+    }
+    for (int k = 0; k < kMVBufs; ++k) {
+      mbar_init(smem_u32(&bs.vfull[k]), kWConvWarps);
+      mbar_init(smem_u32(&bs.vfree[k]), 1);
+    }
+    for (int k = 0; k < kWBufs; ++k) {
+      mbar_init(smem_u32(&bs.sfull[k]), 1);
+      mbar_init(smem_u32(&bs.sread[k]), 8);
+      mbar_init(smem_u32(&bs.pvdone[k]), 1);
+    }
+    mbar_init(smem_u32(&bs.pfull), 8);
+    mbar_init(smem_u32(&bs.qready), 8);
+    for (int q = 0; q < 4; ++q) mbar_init(smem_u32(&bs.xch[q]), 2);
+    fence_mbar_init();
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  if (warp == kMMmaWarp) {
+    tc::tmem_alloc(smem_u32(&bs.tmem_base), kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = bs.tmem_base;
+  bool to = false;  // a bounded wait gave up
+
+  if (warp == kMProdWarp || warp == kMProdWarpV) {
+    // ------------------------------------------------------------ producers
+    // as in prefillw_kernel: nb boxes of box_tok rows per tensor and tile;
+    // warp kMProdWarp copies K, warp kMProdWarpV copies V, each arriving on
+    // the stage with its own byte count
+    const bool isv = warp == kMProdWarpV;
+    const int btok = a.box_tok, nb = kWTok / btok, tpb = 32 / nb;
+    const int32_t* bt = a.block_tables + (int64_t)x.b * a.max_pages;
+    auto load_batch = [&](int j0) {
+      const int j = j0 + lane / nb;
+      const int tb = x.t_lo + j * kWTok + (lane % nb) * btok;
+      return (j < ntiles && tb < x.t_hi) ? __ldg(bt + tb / a.P) : 0;
+    };
+    int cur = load_batch(0), nxt = load_batch(tpb);
+    for (int j = 0; j < ntiles && !to; ++j) {
+      if (j > 0 && j % tpb == 0) {
+        cur = nxt;
+        nxt = load_batch(j + tpb);
+      }
+      const int st = j % kMStages;
+      if (j >= kMStages && !warp_wait(smem_u32(&bs.stage_empty[st]), ((j / kMStages) - 1) & 1)) {
+        to = true;
+        break;
+      }
+      const int tok0 = x.t_lo + j * kWTok;
+      const int nbox = min(nb, (x.t_hi - tok0 + btok - 1) / btok);
+      const uint32_t bar = smem_u32(&bs.stage_full[st]);
+      if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(nbox * btok * kD));
+      __syncwarp();
+      int page = __shfl_sync(0xFFFFFFFFu, cur, (j % tpb) * nb + (lane % nb));
+      if (lane < nbox) {
+        const int tb = tok0 + lane * btok;
+        if (page < 0 || (int64_t)page >= a.num_pages) {
+          if (!isv) atomicOr(a.status, kErrBadPage);
+          page = -1;  // the box lands outside the tensor and reads zeros
+        }
+        const int row = (page * a.Hkv + x.kvh) * a.P + tb % a.P;
+        const uint32_t dst = smem_u32(smem + kMOffStage + st * kWStageBytes) + lane * btok * kD;
+        if (isv) tma_load_2d(dst + kWTok * kD, &tmV, 0, row, bar);
+        else tma_load_2d(dst, &tmK, 0, row, bar);
+      }
+    }
+    for (int j = ntiles > kMStages ? ntiles - kMStages : 0; j < ntiles; ++j)
+      if (!mbar_wait(smem_u32(&bs.stage_full[j % kMStages]), (j / kMStages) & 1)) to = true;
+  } else if (warp == kMMmaWarp) {
+    // ------------------------------------------------- score MMA issuer
+    // S(j) = Q . K(j)^T (M = N = 128) into buffer j % 2, Q's two e4m3 parts
+    // from tensor memory (four K = 32 steps each), once the stage has landed
+    // and the softmax warps have read S(j - 2); a second commit releases K.
+    if (lane == 0 && ntiles > 0) {
+      if (!mbar_wait(smem_u32(&bs.qready), 0)) to = true;
+      for (int j = 0; j < ntiles && !to; ++j) {
+        const int kb = j % kWBufs, st = j % kMStages;
+        if (!mbar_wait(smem_u32(&bs.stage_full[st]), (j / kMStages) & 1)) to = true;
+        if (j >= kWBufs && !to && !mbar_wait(smem_u32(&bs.sread[kb]), ((j - kWBufs) / kWBufs) & 1)) to = true;
+        if (to) break;
+        tc::fence_after_sync();
+        const uint64_t kdesc = tc::desc_sw128(smem_u32(smem + kMOffStage + st * kWStageBytes), 16, 1024);
+#pragma unroll
+        for (int p = 0; p < 2; ++p)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc::mma_ts_e4m3(tmem + kWTok * kb, tmem + kMTmemQ + 32 * p + 8 * kk, kdesc + (uint64_t)((32 * kk) >> 4),
+                            kIdescQKM, (p > 0 || kk > 0) ? 1u : 0u);
+        tc::mma_commit(smem_u32(&bs.sfull[kb]));
+        tc::mma_commit(smem_u32(&bs.stage_empty[st]));
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMPvWarp) {
+    // ---------------------------------------------------- P.V MMA issuer
+    if (lane == 0 && ntiles > 0) {
+      const uint32_t v0 = smem_u32(smem + kMOffV);
+      int pn = 0;
+      for (; pn < ntiles && !to; ++pn) {
+        const int kb = pn % kWBufs, vb = pn % kMVBufs;
+        if (!mbar_wait(smem_u32(&bs.pfull), pn & 1) || !mbar_wait(smem_u32(&bs.vfull[vb]), (pn / kMVBufs) & 1)) {
+          to = true;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint64_t vdesc = tc::desc_sw128(v0 + vb * kWVBytes, kWAtom, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kWTok / 16; ++kk)
+          tc::mma_ts(tmem + kMTmemO, tmem + kMTmemP + 8 * kk, vdesc + (uint64_t)((2048 * kk) >> 4), kIdescPVM,
+                     (pn > 0 || kk > 0) ? 1u : 0u);
+        tc::mma_commit(smem_u32(&bs.pvdone[kb]));
+        tc::mma_commit(smem_u32(&bs.vfree[vb]));
+      }
+      if (pn > 0 && !mbar_wait(smem_u32(&bs.pvdone[(pn - 1) % kWBufs]), ((pn - 1) / kWBufs) & 1)) to = true;
+    }
+    __syncwarp();
+  } else if (warp < kMSoftWarp0) {
+    // ------------------------------------------------------------ converters
+    const int ct = threadIdx.x - kMConvWarp0 * 32;
+    for (int j = 0; j < ntiles && !to; ++j) {
+      const int st = j % kMStages, vb = j % kMVBufs;
+      if (!warp_wait(smem_u32(&bs.stage_full[st]), (j / kMStages) & 1)) {
+        to = true;
+        break;
+      }
+      const int valid = min(kWTok, x.t_hi - (x.t_lo + j * kWTok));
+      uint4 v[kWChunks];
+      load_v(smem + kMOffStage + st * kWStageBytes + kWTok * kD, ct, valid, v);
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.stage_empty[st]));  // release: the reads are done
+      if (j >= kMVBufs && !warp_wait(smem_u32(&bs.vfree[vb]), ((j - kMVBufs) / kMVBufs) & 1)) {
+        to = true;
+        break;
+      }
+      store_v_tokens(v, smem + kMOffV + vb * kWVBytes, ct);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.vfull[vb]));
+    }
+  } else {
+    // -------------------------------------------------- softmax + epilogue
+    const int quad = warp & 3, half = (warp - kMSoftWarp0) >> 2;
+    const int r = 32 * quad + lane;  // this thread's row; columns 64 half .. 64 half + 63
+    const uint32_t trow = tmem + ((uint32_t)(32 * quad) << 16);
+    const bool row_ok = r < x.rows;
+    const int i = x.i0 + r / a.G, g = r % a.G;
+    const int64_t head_row = ((int64_t)a.q_start[x.b] + i) * a.Hq + (int64_t)x.kvh * a.G + g;
+    float* const xv = reinterpret_cast<float*>(smem + kMOffX);  // [parity][half][row]
+    const uint32_t xbar = smem_u32(&bs.xch[quad]);
+    int ex = 0;  // exchanges so far (the barrier's phase)
+    // hand this half's value for row r to the other half and return the other's
+    auto swap = [&](float val) -> float {
+      xv[((ex & 1) * 2 + half) * kRows + r] = val;
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_local(xbar);
+      if (!warp_wait(xbar, ex & 1)) to = true;
+      const float other = xv[((ex & 1) * 2 + (half ^ 1)) * kRows + r];
+      ++ex;
+      return other;
+    };
+    // Q: this half's 64 elements of row r as two exact e4m3 parts (x = q s, s
+    // = 2^floor(log2(448 / max |q|)) over the whole row; part 1 = e4m3(x),
+    // part 2 = e4m3(x - part 1)) into tensor memory, K order, four per column
+    float qinv;
+    {
+      const uint4* qp = reinterpret_cast<const uint4*>(a.q + head_row * kD) + 8 * half;
+      uint4 qw[8];
+#pragma unroll
+      for (int uu = 0; uu < 8; ++uu) qw[uu] = row_ok ? __ldg(qp + uu) : make_uint4(0, 0, 0, 0);
+      float amax = 0.f;
+#pragma unroll
+      for (int uu = 0; uu < 8; ++uu) {
+        const uint32_t ww[4] = {qw[uu].x, qw[uu].y, qw[uu].z, qw[uu].w};
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(ww[kk])), fabsf(bf16_hi(ww[kk]))));
+      }
+      amax = fmaxf(amax, swap(amax));
+      const float s = pow2_scale(448.f, amax);
+      qinv = row_ok ? 1.f / s : 0.f;  // exact: s is a power of two
+      uint32_t p1[16], p2[16];
+#pragma unroll
+      for (int uu = 0; uu < 8; ++uu) {
+        const uint32_t ww[4] = {qw[uu].x, qw[uu].y, qw[uu].z, qw[uu].w};
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {  // elements 8 uu + 4 h2 .. + 3: one column
+          uint32_t c1w = 0u, c2w = 0u;
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const uint32_t w = ww[2 * h2 + e];
+            const float x0 = bf16_lo(w) * s, x1 = bf16_hi(w) * s;
+            const uint16_t c1 = f32x2_to_e4m3x2(x0, x1);
+            float d0, d1;
+            e4m3x2_to_f32x2(c1, d0, d1);
+            const uint16_t c2 = f32x2_to_e4m3x2(x0 - d0, x1 - d1);  // the difference is exact
+            c1w |= (uint32_t)c1 << (16 * e);
+            c2w |= (uint32_t)c2 << (16 * e);
+          }
+          p1[2 * uu + h2] = c1w;
+          p2[2 * uu + h2] = c2w;
+        }
+      }
+      tc::tmem_st16(trow + kMTmemQ + 16 * half, p1);
+      tc::tmem_st16(trow + kMTmemQ + 32 + 16 * half, p2);
+      tc::tmem_st_wait();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.qready));
+    }
+    const int lim = row_ok ? min(x.L - x.n + i + 1, x.t_end_chunk) : x.t_lo;
+    const float sc = a.score_scale * qinv;  // the scores carry the row's Q scale
+    float mref = -INFINITY, rthr = -INFINITY, lpart = 0.f;
+    for (int j = 0; j < ntiles && !to; ++j) {
+      const int kb = j % kWBufs;
+      if (!warp_wait(smem_u32(&bs.sfull[kb]), (j / kWBufs) & 1)) {
+        to = true;
+        break;
+      }
+      tc::fence_after_sync();
+      const uint32_t sbase = trow + kWTok * kb + 64 * half;
+      const int nv = lim - (x.t_lo + j * kWTok + 64 * half);  // this half's columns c < nv are attended
+      const bool full = __all_sync(0xFFFFFFFFu, nv >= 64);
+      // this half's 64 scores in registers at once; the buffer is then free for S(j + 2)
+      uint32_t sv[64];
+      {
+        uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
+        uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
+        tc::tmem_ld32(sbase, s0);
+        tc::tmem_ld32(sbase + 32, s1);
+        tc::tmem_ld_wait();
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.sread[kb]));
+      float mx;
+      {
+        float m8[8];
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) m8[kk] = -INFINITY;
+        if (full) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sv[c]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], c < nv ? __uint_as_float(sv[c]) : -INFINITY);
+        }
+        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      }
+      mx = fmaxf(mx, swap(mx));  // the row's maximum, the same in both halves
+      if (to) break;
+      const bool grow = mx > rthr;
+      float al = 1.f;
+      bool rescale = false;
+      if (__any_sync(0xFFFFFFFFu, grow)) {
+        const float mn = grow ? fmaxf(mref, mx * sc) : mref;
+        al = grow ? fast_exp2(mref - mn) : 1.f;  // 0 while mref is -inf
+        rescale = j > 0 && __any_sync(0xFFFFFFFFu, grow && mref != -INFINITY);
+        lpart *= al;
+        mref = mn;
+        rthr = (mn + kRescaleLog2) / sc;
+      }
+      // P for this half (column pair c -> word c / 2 of 32)
+      uint32_t pv[32];
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      if (full) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float x1 = fmaf(__uint_as_float(sv[2 * c + 1]), sc, -mref);
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * c]), sc, -mref));
+          const float p1 = fast_exp2(x1);
+          ls[c & 3] += p0 + p1;
+          pv[c] = pack_f16x2(p0, p1);
+        }
+      } else {
+        // a masked column's exponential may overflow; the select drops it
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float x1 = fmaf(__uint_as_float(sv[2 * c + 1]), sc, -mref);
+          const float e0 = fast_exp2(fmaf(__uint_as_float(sv[2 * c]), sc, -mref));
+          const float e1 = fast_exp2(x1);
+          const float p0 = 2 * c < nv ? e0 : 0.f, p1 = 2 * c + 1 < nv ? e1 : 0.f;
+          ls[c & 3] += p0 + p1;
+          pv[c] = pack_f16x2(p0, p1);
+        }
+      }
+      lpart += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      // P and O are free once P.V(j - 1) has completed
+      if (j > 0) {
+        if (!warp_wait(smem_u32(&bs.pvdone[(j - 1) % kWBufs]), ((j - 1) / kWBufs) & 1)) {
+          to = true;
+          break;
+        }
+        tc::fence_after_sync();
+      }
+      if (rescale) {  // this half's 64 columns of O for the warp's rows
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+          uint32_t ov[32];
+          tc::tmem_ld32(trow + kMTmemO + 64 * half + 32 * blk, ov);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * al);
+          tc::tmem_st32(trow + kMTmemO + 64 * half + 32 * blk, ov);
+        }
+      }
+      tc::tmem_st32(trow + kMTmemP + 32 * half, pv);
+      tc::tmem_st_wait();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.pfull));
+    }
+    // ---- epilogue: this half's 64 columns of row r
+    if (!to) {
+      const float l = lpart + swap(lpart);
+      if (!to && ntiles > 0 &&
+          !warp_wait(smem_u32(&bs.pvdone[(ntiles - 1) % kWBufs]), ((ntiles - 1) / kWBufs) & 1))
+        to = true;
+      tc::fence_after_sync();
+      float* part = direct ? nullptr : a.partials + (u * kRows + r) * kPartStride;
+      const float inv = l > 0.f ? a.out_scale / l : 0.f;
+#pragma unroll
+      for (int blk = 0; blk < 2; ++blk) {
+        uint32_t ov[32];
+        if (ntiles > 0) {
+          tc::tmem_ld32(trow + kMTmemO + 64 * half + 32 * blk, ov);
+          tc::tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) ov[c] = 0u;
+        }
+        if (!row_ok || to) continue;
+        const int d0 = 64 * half + 32 * blk;  // head_dim columns d0 .. d0 + 31
+        if (direct) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            pk[c] = pack_bf16x2(__uint_as_float(ov[2 * c]) * inv, __uint_as_float(ov[2 * c + 1]) * inv);
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + head_row * kD + d0);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) dst[kk] = make_uint4(pk[4 * kk], pk[4 * kk + 1], pk[4 * kk + 2], pk[4 * kk + 3]);
+        } else {
+          float4* dst = reinterpret_cast<float4*>(part + 4 + d0);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            dst[kk] = make_float4(__uint_as_float(ov[4 * kk]), __uint_as_float(ov[4 * kk + 1]),
+                                  __uint_as_float(ov[4 * kk + 2]), __uint_as_float(ov[4 * kk + 3]));
+        }
+      }
+      if (row_ok && !to && half == 0) {
+        if (direct) {
+          if (a.lse) a.lse[head_row] = l > 0.f ? (mref + __log2f(l)) * kLn2 : -INFINITY;
+        } else {
+          part[0] = mref;
+          part[1] = l;
+        }
+      }
+    }
+  }
+
+  if (to) atomicOr(a.status, kErrWaitTimeout);
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == kMMmaWarp) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 constexpr size_t kStatusBytes = 256;
 
 int64_t units_of(int B, int Hkv, int QB, int C) { return (int64_t)B * Hkv * QB * C; }
@@ -1941,36 +2398,25 @@ int pfkv_paged_prefill_attn(void* out, const void* q, const void* k_cache, const
                            box, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != PFKV_OK) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  static std::atomic<uint64_t> smem_set{0};
-  rc = set_max_dynamic_smem(reinterpret_cast<const void*>(prefill_kernel), kSmemBytes, smem_set,
-                            "paged_prefill set smem attribute");
-  if (rc != PFKV_OK) return rc;
   if (cudaMemsetAsync(a.status, 0, sizeof(int32_t), s) != cudaSuccess) return check_cuda("paged_prefill status");
-  if (a.QB >= 2) {
-    // several row blocks per (request, KV head): two blocks per CTA
-    static std::atomic<uint64_t> smem2_set{0};
-    rc = set_max_dynamic_smem(reinterpret_cast<const void*>(prefill2_kernel), k2SmemBytes, smem2_set,
-                              "paged_prefill set smem attribute");
+  // both kernels take 128-token tiles as boxes as tall as the page allows
+  // (up to 64 rows): fewer copies per tile
+  a.box_tok = page_size % 64 == 0 ? 64 : (page_size % 32 == 0 ? 32 : kBoxTok);
+  if (a.box_tok != kBoxTok) {
+    const cuuint32_t boxw[2] = {128, (cuuint32_t)a.box_tok};
+    rc = encode_tensor_map(&tmK, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(k_cache), dims, strides,
+                           boxw, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc == PFKV_OK)
+      rc = encode_tensor_map(&tmV, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(v_cache), dims, strides,
+                             boxw, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc != PFKV_OK) return rc;
-    const int64_t units2 = (int64_t)batch * num_kv_heads * a.C * ((a.QB + 1) / 2);
-    prefill2_kernel<<<(unsigned)units2, k2Threads, k2SmemBytes, s>>>(tmK, tmV, a);
-  } else if ((int64_t)max_q_len * G <= 64) {
+  }
+  if ((int64_t)max_q_len * G <= 64) {
     // every block has at most 64 rows: 128-token tiles, half-height products
     static std::atomic<uint64_t> smemw_set{0};
     rc = set_max_dynamic_smem(reinterpret_cast<const void*>(prefillw_kernel), kWSmemBytes, smemw_set,
                               "paged_prefill set smem attribute");
     if (rc != PFKV_OK) return rc;
-    // boxes as tall as the page allows (up to 64 rows): fewer copies per tile
-    a.box_tok = page_size % 64 == 0 ? 64 : (page_size % 32 == 0 ? 32 : kBoxTok);
-    if (a.box_tok != kBoxTok) {
-      const cuuint32_t boxw[2] = {128, (cuuint32_t)a.box_tok};
-      rc = encode_tensor_map(&tmK, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(k_cache), dims, strides,
-                             boxw, CU_TENSOR_MAP_SWIZZLE_128B);
-      if (rc == PFKV_OK)
-        rc = encode_tensor_map(&tmV, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(v_cache), dims,
-                               strides, boxw, CU_TENSOR_MAP_SWIZZLE_128B);
-      if (rc != PFKV_OK) return rc;
-    }
     // the KV range of all (request, KV head) pairs split evenly over one CTA
     // per SM (kv_split_tokens is not needed here); plan, tile kernel and merge,
     // the last two as programmatic dependents of the kernel before them
@@ -1994,9 +2440,13 @@ int pfkv_paged_prefill_attn(void* out, const void* q, const void* k_cache, const
     cfg.dynamicSmemBytes = 0;
     if (cudaLaunchKernelEx(&cfg, prefillw_merge_kernel, a) != cudaSuccess) return check_cuda("paged_prefill merge");
     return check_cuda("paged_prefill launch");
-  } else {
-    prefill_kernel<<<(unsigned)units, kThreads, kSmemBytes, s>>>(tmK, tmV, a);
   }
+  // blocks of up to 128 rows: one per CTA, Q in tensor memory, longest first
+  static std::atomic<uint64_t> smemm_set{0};
+  rc = set_max_dynamic_smem(reinterpret_cast<const void*>(prefillm_kernel), kMSmemBytes, smemm_set,
+                            "paged_prefill set smem attribute");
+  if (rc != PFKV_OK) return rc;
+  prefillm_kernel<<<(unsigned)units, kMThreads, kMSmemBytes, s>>>(tmK, tmV, a);
   if (a.C > 1) {
     const int64_t mblocks = (int64_t)batch * num_kv_heads * a.QB * (kRows / kMergeWarps);
     prefill_merge_kernel<<<(unsigned)mblocks, kMergeWarps * 32, 0, s>>>(a);
