@@ -296,15 +296,12 @@ PFKV_API int pfkv_paged_decode_attn_scaled(void *out, const void *q, const void 
  *         t = 0 .. L_b - n_b + i
  *   out = sum_t e^{s_t - m} V(t) * v_scale / sum_t e^{s_t - m}
  *   lse = m + ln sum_t e^{s_t - m}
- * Products on the tensor cores with fp32 accumulation.  Scores: when every row
- * block holds more than 64 rows and there is one block per request, f16
- * products on the widened K (e4m3 widens exactly) with each q row scaled by a
- * power of two into f16's range; otherwise e4m3 products on the K bytes with
- * each q row, scaled by a power of two (largest |q| into (224, 448]), split
- * into two e4m3 parts (exact for every value at least 1/896 of the row's
- * largest, within 2^-10 of the scaled value below that).  Either way any
- * finite bf16 q is accepted and 1 / scale multiplies the raw scores.  P.V: f16
- * (P <= 2^8, V widened exactly).
+ * Products on the tensor cores with fp32 accumulation.  Scores: e4m3
+ * products on the K bytes with each q row, scaled by a power of two (largest
+ * |q| into (224, 448]), split into two e4m3 parts (exact for every value at
+ * least 1/896 of the row's largest, within 2^-10 of the scaled value below
+ * that); any finite bf16 q is accepted and 1 / scale multiplies the raw
+ * scores.  P.V: f16 (P <= 2^8, V widened exactly).
  *   out, q        bf16 [q_start[batch]][num_q_heads][head_dim]
  *   q_start       int32 [batch + 1] (device), non-decreasing, q_start[0] = 0
  *   max_q_len     host bound on every n_b; max_context_len host bound on

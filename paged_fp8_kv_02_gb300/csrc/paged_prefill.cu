@@ -11,38 +11,28 @@
 // keys 0 .. L_b - n_b + i.
 //
 // With several queries per KV head the step becomes a dense contraction, so
-// the products run on tcgen05 (kind::f16, fp32 accumulation in tensor memory):
-//   * a work unit is (request, KV head, block of 128 rows, KV chunk), a row
-//     being one (query token, query head) pair of that KV head: 128 / G query
-//     tokens per block;
-//   * the producer warp gathers 64-token K and V tiles of e4m3 with TMA (four
-//     16-token boxes each, one block-table entry per box, loaded eight tiles
-//     ahead);
-//   * four converter warps widen them to f16 in 128-byte-swizzled atoms (the
-//     K tile is the K-major B operand of S = Q.K^T, the V tile the MN-major B
-//     operand of O = P.V), four tiles in flight;
-//   * one thread issues S for a tile into one of four 64-column
-//     tensor-memory buffers, with Q (f16) as the A operand in tensor memory,
-//     and a thread of another warp issues O += P.V with P read from tensor
-//     memory; blocks of at most 64 rows use half-height (M = 64) products;
-//   * four softmax warps own one row each per lane: mask (causal and context
-//     end), lazy-reference exp2 online softmax (the reference moves only when a
-//     score exceeds it by more than 2^8; the accumulator in tensor memory is
-//     then rescaled), P as f16 pairs written over the row's scores, and the
-//     epilogue.
-// Long contexts are cut into chunks of kv_split_tokens; chunks write fp32
-// partial states (m, l, o) and a merge kernel combines them by the log-sum-exp
-// rule (kLLM article, §5.2.2).  When a (request, KV head) has several row
-// blocks (a chunked-prefill step), prefill2_kernel takes two blocks per CTA
-// so that each tile feeds both and two softmax groups overlap; when every
-// block holds at most 64 rows (a verification pass), prefillw_kernel runs
-// 128-token tiles with half-height products.  These two take the scores as
-// e4m3 products (tcgen05 kind::f8f6f4) straight on the K tile of the TMA
-// stage, against each Q row scaled by a power of two (largest |q| into
-// (224, 448]) and split into two exact e4m3 parts; only V is widened.  The
-// one-block kernel described above widens K as well and takes Q as f16, each
-// row scaled by a power of two into f16's range.  In every kernel the row's
-// 1 / scale joins its score scale, so any finite bf16 query is accepted.
+// the products run on tcgen05 with fp32 accumulation in tensor memory.  A row
+// is one (query token, query head) pair of a KV head; a request's rows form
+// blocks of 128 (128 / G query tokens per block).  Two kernels:
+//   * prefillm_kernel, blocks of more than 64 rows (chunked prefill): one
+//     128-row block per CTA over 128-token tiles; Q's two exact e4m3 parts in
+//     tensor memory as the A operand of the score products (kind::f8f6f4,
+//     straight on the K rows of the TMA stage); V widened to f16 for P.V
+//     (kind::f16, P read from tensor memory); eight softmax warps, two per
+//     lane quadrant, each taking half of a row's scores;
+//   * prefillw_kernel, blocks of at most 64 rows (a few queries per request:
+//     speculative verification): 128-token tiles with half-height (M = 64)
+//     products, Q's parts in shared memory, the (request, KV head, tile) space
+//     split evenly over one persistent CTA per SM.
+// Both: K/V tiles gathered by TMA through the block table, boxes as tall as
+// the page allows; lazy-reference exp2 online softmax (the reference moves
+// only when a score exceeds it by more than 2^8; O in tensor memory is then
+// rescaled); each Q row scaled by a power of two (largest |q| into
+// (224, 448]) before the split, its 1 / scale joined to the score scale, so
+// any finite bf16 query is accepted.  Pieces of one row's context computed
+// apart (chunks of kv_split_tokens, or the even split's CTA boundaries) write
+// fp32 partial states (m, l, o) that a merge kernel folds by the log-sum-exp
+// rule (kLLM article, §5.2.2).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -55,42 +45,15 @@ namespace pfkv {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kRows = 128;                    // MMA M: rows of a work unit
-constexpr int kTokN = 64;                     // KV tokens per tile
-constexpr int kBoxTok = 16;                   // tokens per TMA box
-constexpr int kBoxes = kTokN / kBoxTok;       // 4
-constexpr int kStages = 5;                    // e4m3 stage ring
-constexpr int kKvBufs = 4;                    // widened f16 K/V tiles in flight
-constexpr int kSBufs = 4;                     // score / P buffers in tensor memory
+constexpr int kRows = 128;                    // rows of a work unit's block (one per MMA row)
+constexpr int kTokN = 64;                     // granularity of kv_split_tokens and of unit tile counts
+constexpr int kBoxTok = 16;                   // tokens per TMA box unless the page allows taller ones
 constexpr int kBoxBytes = kBoxTok * kD;       // 2 KB
-constexpr int kStageBytes = 2 * kTokN * kD;   // K + V e4m3: 16 KB
-constexpr int kKvAtom = kTokN * 128;          // [64 tokens][64 f16] swizzled atom: 8 KB
-constexpr int kKvBufBytes = 4 * kKvAtom;      // K (2 atoms) + V (2 atoms): 32 KB
 constexpr int kPartStride = 132;              // floats per row of a partial state: m, l, -, -, o[128]
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.f;
-constexpr int kPageBatch = 8;                 // tiles whose block-table entries one load covers
-
-constexpr int kOffKv = 0;
-constexpr int kOffStage = kOffKv + kKvBufs * kKvBufBytes;
-constexpr int kOffBars = kOffStage + kStages * kStageBytes;
-constexpr int kSmemBytes = kOffBars + 256 + 1024;  // + 1024-byte alignment slack
-
-constexpr int kProdWarp = 0, kMmaWarp = 1, kConvWarp0 = 2, kSoftWarp0 = 6, kPvWarp = 10;
-constexpr int kThreads = 352;
-
-// tensor memory: S/P buffers at columns 0, 64, 128, 192; O at 256..383; Q (the
-// A operand of the scores, f16 pairs) at 384..447
-constexpr uint32_t kTmemS = 0, kTmemO = 64 * kSBufs, kTmemQ = kTmemO + kD, kTmemCols = 512;
-static_assert(kTmemQ + kD / 2 <= kTmemCols, "tensor memory columns");
-constexpr uint32_t kIdescQK = tc::idesc_f16(kRows, kTokN, false);
-constexpr uint32_t kIdescPV = tc::idesc_f16(kRows, kD, true);
-// Units with at most 64 rows use M = 64 products: row m of the accumulator
-// (and of an A operand in tensor memory) then sits in lane (m % 16) + 32 (m / 16),
-// i.e. the first 16 lanes of each warp's quarter (checked on the device).
-constexpr uint32_t kIdescQK64 = tc::idesc_f16(64, kTokN, false);
-constexpr uint32_t kIdescPV64 = tc::idesc_f16(64, kD, true);
+constexpr uint32_t kTmemCols = 512;
 
 struct PrefillArgs {
   __nv_bfloat16* out;
@@ -113,14 +76,6 @@ struct PrefillArgs {
   int64_t* tile_start;  // prefillw_kernel: [B + 1] flattened start of each request's (KV head, tile) range
   int ncta;             // prefillw_kernel: CTAs sharing the flattened range
 };
-
-struct Bars {
-  uint64_t stage_full[kStages], stage_empty[kStages];
-  uint64_t kvfull[kKvBufs], sfull[kSBufs], pfull[kSBufs], pvdone[kSBufs];
-  uint64_t qready;
-  uint32_t tmem_base;
-};
-static_assert(sizeof(Bars) <= 256, "barrier block");
 
 // Geometry of one (request, KV head, row block, chunk) unit, the same in both
 // kernels.  Lengths are clamped to what the launch covers; the tile kernel
@@ -182,868 +137,6 @@ __device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 12
 // 128-byte-swizzled K-major atoms [rows][64] (atom size atom_bytes).
 __device__ __forceinline__ uint32_t atom_off(int r, int u, int atom_bytes) {
   return (uint32_t)((u >> 3) * atom_bytes + r * 128 + 16 * ((u & 7) ^ (r & 7)));
-}
-
-// Widens a 64-token e4m3 stage into a f16 tile, thread ct of the four
-// converter warps taking chunks i = ct + 128 m of the stage (K for i < 512, V
-// after; row (i % 512) / 8, 16-byte chunk c = i % 8) to units 2(c % 4) and
-// 2(c % 4) + 1 of atom c / 4 of the K or V half; rows at or past `valid`
-// become zeros.  All loads are issued before the first store: the compiler
-// cannot move a load above a store through another pointer into shared memory.
-__device__ __forceinline__ void widen_tile64(const uint8_t* stage, uint8_t* kv, int ct, int valid) {
-  uint4 v[8];
-#pragma unroll
-  for (int m = 0; m < 8; ++m) {
-    const int i = ct + 128 * m;
-    const int which = i >> 9, row = (i & 511) >> 3, c = i & 7;
-    v[m] = make_uint4(0, 0, 0, 0);
-    if (row < valid) v[m] = lds128(stage + which * (kTokN * kD) + (row >> 4) * kBoxBytes + swz(row & 15, c));
-  }
-#pragma unroll
-  for (int m = 0; m < 8; ++m) {
-    const int i = ct + 128 * m;
-    const int which = i >> 9, row = (i & 511) >> 3, c = i & 7;
-    uint4 o0, o1;
-    e4m3x4_to_f16x2x2(v[m].x, o0.x, o0.y);
-    e4m3x4_to_f16x2x2(v[m].y, o0.z, o0.w);
-    e4m3x4_to_f16x2x2(v[m].z, o1.x, o1.y);
-    e4m3x4_to_f16x2x2(v[m].w, o1.z, o1.w);
-    const uint32_t d = which * (2 * kKvAtom) + atom_off(row, 2 * c, kKvAtom);
-    *reinterpret_cast<uint4*>(kv + d) = o0;
-    *reinterpret_cast<uint4*>(kv + (d ^ 16)) = o1;  // unit 2(c%4) + 1: bit 0 of the unit flips
-  }
-}
-
-__global__ void __launch_bounds__(kThreads, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                   const PrefillArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_addr = smem_u32(smem_raw);
-  uint8_t* const smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-  Bars& bs = *reinterpret_cast<Bars*>(smem + kOffBars);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  const int64_t u = blockIdx.x;
-  const Unit x = unit_of(a, u, threadIdx.x == 0 && (u % ((int64_t)a.QB * a.C * a.Hkv)) == 0);
-  if (!x.active) return;  // uniform over the CTA: nothing to compute or write
-  const int ntiles = x.ntiles;
-  const bool direct = a.C == 1;
-  const bool m64 = x.rows <= 64;  // half-height products
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&bs.stage_full[s]), 1);
-      mbar_init(smem_u32(&bs.stage_empty[s]), 4);
-    }
-    for (int k = 0; k < kKvBufs; ++k) mbar_init(smem_u32(&bs.kvfull[k]), 4);
-    // softmax warps with at least one real row (16 rows per warp in half-height mode)
-    const int live_warps = m64 ? min(4, (x.rows + 15) / 16) : min(4, (x.rows + 31) / 32);
-    for (int k = 0; k < kSBufs; ++k) {
-      mbar_init(smem_u32(&bs.sfull[k]), 1);
-      mbar_init(smem_u32(&bs.pfull[k]), live_warps);
-      mbar_init(smem_u32(&bs.pvdone[k]), 1);
-    }
-    mbar_init(smem_u32(&bs.qready), 4);
-    fence_mbar_init();
-    prefetch_tensormap(&tmK);
-    prefetch_tensormap(&tmV);
-  }
-  if (warp == kMmaWarp) {
-    tc::tmem_alloc(smem_u32(&bs.tmem_base), kTmemCols);
-    tc::tmem_relinquish();
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = bs.tmem_base;
-  bool to = false;  // a bounded wait gave up
-
-  if (warp == kProdWarp) {
-    // ------------------------------------------------------------ producer
-    // Lane l holds the block-table entry of box l % 4 of tile (batch + l / 4);
-    // the next batch is loaded while the current one is issued.
-    const int32_t* bt = a.block_tables + (int64_t)x.b * a.max_pages;
-    auto load_batch = [&](int j0) {
-      const int j = j0 + lane / kBoxes;
-      const int tb = x.t_lo + j * kTokN + (lane % kBoxes) * kBoxTok;
-      return (j < ntiles && tb < x.t_hi) ? __ldg(bt + tb / a.P) : 0;
-    };
-    int cur = load_batch(0), nxt = load_batch(kPageBatch);
-    for (int j = 0; j < ntiles && !to; ++j) {
-      if (j > 0 && j % kPageBatch == 0) {
-        cur = nxt;
-        nxt = load_batch(j + kPageBatch);
-      }
-      const int st = j % kStages;
-      if (j >= kStages && !warp_wait(smem_u32(&bs.stage_empty[st]), ((j / kStages) - 1) & 1)) {
-        to = true;
-        break;
-      }
-      const int tok0 = x.t_lo + j * kTokN;
-      const int nbox = min(kBoxes, (x.t_hi - tok0 + kBoxTok - 1) / kBoxTok);
-      const uint32_t bar = smem_u32(&bs.stage_full[st]);
-      if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(2 * nbox * kBoxBytes));
-      __syncwarp();
-      int page = __shfl_sync(0xFFFFFFFFu, cur, (j % kPageBatch) * kBoxes + (lane & 3));
-      if (lane < nbox) {
-        const int tb = tok0 + lane * kBoxTok;
-        if (page < 0 || (int64_t)page >= a.num_pages) {
-          atomicOr(a.status, kErrBadPage);
-          page = -1;  // the box lands outside the tensor and reads zeros
-        }
-        const int row = (page * a.Hkv + x.kvh) * a.P + tb % a.P;
-        const uint32_t dst = smem_u32(smem + kOffStage + st * kStageBytes) + lane * kBoxBytes;
-        tma_load_2d(dst, &tmK, 0, row, bar);
-        tma_load_2d(dst + kTokN * kD, &tmV, 0, row, bar);
-      }
-    }
-    // no copy may still be landing when the CTA retires
-    for (int j = ntiles > kStages ? ntiles - kStages : 0; j < ntiles; ++j)
-      if (!mbar_wait(smem_u32(&bs.stage_full[j % kStages]), (j / kStages) & 1)) to = true;
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------- score MMA issuer
-    // One thread issues S = Q.K^T per tile; the products O += P.V come from
-    // another warp, so that the two streams of (slow to issue) small MMAs
-    // overlap.  S(qn) reuses the buffer of P(qn - kSBufs): it waits until
-    // that product has completed.
-    if (lane == 0 && ntiles > 0) {
-      if (!mbar_wait(smem_u32(&bs.qready), 0)) to = true;
-      const uint32_t kv0 = smem_u32(smem + kOffKv);
-      const uint32_t idesc_qk = m64 ? kIdescQK64 : kIdescQK;
-      for (int qn = 0; qn < ntiles && !to; ++qn) {
-        if (!mbar_wait(smem_u32(&bs.kvfull[qn % kKvBufs]), (qn / kKvBufs) & 1)) to = true;
-        if (qn >= kSBufs && !to) {
-          const int jp = qn - kSBufs;
-          if (!mbar_wait(smem_u32(&bs.pvdone[jp % kSBufs]), (jp / kSBufs) & 1)) to = true;
-        }
-        if (to) break;
-        tc::fence_after_sync();
-        const uint64_t kdesc = tc::desc_sw128(kv0 + (qn % kKvBufs) * kKvBufBytes, 16, 1024);
-#pragma unroll
-        for (int k = 0; k < kD / 16; ++k)
-          tc::mma_ts(tmem + kTmemS + 64 * (qn % kSBufs), tmem + kTmemQ + 8 * k,
-                     kdesc + (uint64_t)(((k >> 2) * kKvAtom + 32 * (k & 3)) >> 4), idesc_qk, k > 0 ? 1u : 0u);
-        tc::mma_commit(smem_u32(&bs.sfull[qn % kSBufs]));
-      }
-    }
-    __syncwarp();
-  } else if (warp == kPvWarp) {
-    // ---------------------------------------------------- P.V MMA issuer
-    if (lane == 0 && ntiles > 0) {
-      const uint32_t kv0 = smem_u32(smem + kOffKv);
-      const uint32_t idesc_pv = m64 ? kIdescPV64 : kIdescPV;
-      int pn = 0;
-      for (; pn < ntiles && !to; ++pn) {
-        if (!mbar_wait(smem_u32(&bs.pfull[pn % kSBufs]), (pn / kSBufs) & 1)) {
-          to = true;
-          break;
-        }
-        tc::fence_after_sync();
-        const uint64_t vdesc = tc::desc_sw128(kv0 + (pn % kKvBufs) * kKvBufBytes + 2 * kKvAtom, kKvAtom, 1024);
-#pragma unroll
-        for (int k = 0; k < kTokN / 16; ++k)
-          tc::mma_ts(tmem + kTmemO, tmem + kTmemS + 64 * (pn % kSBufs) + 8 * k, vdesc + (uint64_t)((2048 * k) >> 4),
-                     idesc_pv, (pn > 0 || k > 0) ? 1u : 0u);
-        tc::mma_commit(smem_u32(&bs.pvdone[pn % kSBufs]));
-      }
-      // no MMA may still be running when the tensor memory is freed
-      if (pn > 0 && !mbar_wait(smem_u32(&bs.pvdone[(pn - 1) % kSBufs]), ((pn - 1) / kSBufs) & 1)) to = true;
-    }
-    __syncwarp();
-  } else if (warp < kSoftWarp0) {
-    // ---------------------------------------------------------- converters
-    const int ct = threadIdx.x - kConvWarp0 * 32;
-    for (int j = 0; j < ntiles && !to; ++j) {
-      const int st = j % kStages, kb = j % kKvBufs;
-      if (!warp_wait(smem_u32(&bs.stage_full[st]), (j / kStages) & 1)) to = true;
-      // the buffer held tile j - kKvBufs: both of its products must be done
-      if (j >= kKvBufs && !to) {
-        const int jp = j - kKvBufs;
-        if (!warp_wait(smem_u32(&bs.pvdone[jp % kSBufs]), (jp / kSBufs) & 1)) to = true;
-      }
-      if (to) break;
-      const int valid = min(kTokN, x.t_hi - (x.t_lo + j * kTokN));
-      const uint8_t* stage = smem + kOffStage + st * kStageBytes;
-      uint8_t* kv = smem + kOffKv + kb * kKvBufBytes;
-      widen_tile64(stage, kv, ct, valid);
-      fence_proxy_async_smem();  // generic writes -> visible to the tensor core
-      __syncwarp();
-      if (lane == 0) {
-        tc::mbar_arrive_local(smem_u32(&bs.stage_empty[st]));
-        tc::mbar_arrive_local(smem_u32(&bs.kvfull[kb]));
-      }
-    }
-  } else {
-    // -------------------------------------------------- softmax + epilogue
-    const int quad = warp & 3;
-    const uint32_t trow = tmem + ((uint32_t)(32 * quad) << 16);
-    // this thread's row: its own lane (full height) or, in half-height mode,
-    // row 16 quad + lane for lanes 0-15 (the lanes such products use)
-    const int r = m64 ? 16 * quad + (lane & 15) : 32 * quad + lane;
-    const bool row_ok = (!m64 || lane < 16) && r < x.rows;
-    const int i = x.i0 + r / a.G, g = r % a.G;
-    const int64_t head_row = ((int64_t)a.q_start[x.b] + i) * a.Hq + (int64_t)x.kvh * a.G + g;  // row of q / out
-    // Q row -> f16 pairs -> the A operand in tensor memory (zeros for padding
-    // rows).  The row is scaled by a power of two qs taking its largest |q|
-    // into (2^14, 2^15], so every finite bf16 row fits f16 and each value at
-    // least 2^-29 of the largest converts exactly; 1 / qs joins the score scale.
-    float qinv = 1.f;
-    {
-      const uint4* qp = reinterpret_cast<const uint4*>(a.q + head_row * kD);
-      float amax = 0.f;
-      if (row_ok) {
-#pragma unroll 4
-        for (int uu = 0; uu < 16; ++uu) {
-          const uint4 w = __ldg(qp + uu);
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(ww[k])), fabsf(bf16_hi(ww[k]))));
-        }
-      }
-      const float qs = pow2_scale(32768.f, amax);
-      qinv = 1.f / qs;  // exact: qs is a power of two
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t f[32];
-#pragma unroll
-        for (int uu = 0; uu < 8; ++uu) {
-          uint4 w = make_uint4(0, 0, 0, 0);
-          if (row_ok) w = __ldg(qp + 8 * half + uu);
-          f[4 * uu] = pack_f16x2(bf16_lo(w.x) * qs, bf16_hi(w.x) * qs);
-          f[4 * uu + 1] = pack_f16x2(bf16_lo(w.y) * qs, bf16_hi(w.y) * qs);
-          f[4 * uu + 2] = pack_f16x2(bf16_lo(w.z) * qs, bf16_hi(w.z) * qs);
-          f[4 * uu + 3] = pack_f16x2(bf16_lo(w.w) * qs, bf16_hi(w.w) * qs);
-        }
-        tc::tmem_st32(trow + kTmemQ + 32 * half, f);
-      }
-      tc::tmem_st_wait();
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.qready));
-    }
-    // keys t < lim are attended by this row
-    const int lim = row_ok ? min(x.L - x.n + i + 1, x.t_end_chunk) : x.t_lo;
-    const float sc = a.score_scale * qinv;
-    float mref = -INFINITY, rthr = -INFINITY, l = 0.f;
-    // a warp whose 32 rows are all padding has nothing to do after writing its
-    // zero Q rows (their scores are 0, which read as f16 pairs are P = 0)
-    const bool warp_live = (m64 ? 16 : 32) * quad < x.rows;
-    for (int j = 0; j < ntiles && !to && warp_live; ++j) {
-      const int kb = j % kSBufs;
-      if (!warp_wait(smem_u32(&bs.sfull[kb]), (j / kSBufs) & 1)) {
-        to = true;
-        break;
-      }
-      tc::fence_after_sync();
-      uint32_t sv[64];
-      {
-        uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
-        uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
-        tc::tmem_ld32(trow + kTmemS + 64 * kb, lo);
-        tc::tmem_ld32(trow + kTmemS + 64 * kb + 32, hi);
-        tc::tmem_ld_wait();
-      }
-      const int tok0 = x.t_lo + j * kTokN;
-      const int nvalid = lim - tok0;  // columns c < nvalid are attended
-      const bool full = nvalid >= kTokN;
-      float mx = -INFINITY;
-      if (!row_ok) {
-        // padding row or unused lane: P stays 0, nothing to track
-      } else {
-        // eight independent chains, then a tree: no 64-long dependency chain
-        float m8[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
-        if (full) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sv[c]));
-        } else {
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (c < nvalid) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sv[c]));
-        }
-        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-      }
-      const bool grow = mx > rthr;
-      if (__any_sync(0xFFFFFFFFu, grow)) {
-        const float mn = grow ? fmaxf(mref, mx * sc) : mref;
-        const float al = grow ? fast_exp2(mref - mn) : 1.f;  // 0 while mref is -inf
-        // the accumulator holds earlier tiles only once P(j - 1) was multiplied in
-        const bool rescale = __any_sync(0xFFFFFFFFu, grow && mref != -INFINITY);
-        if (rescale && j > 0) {
-          if (!warp_wait(smem_u32(&bs.pvdone[(j - 1) % kSBufs]), ((j - 1) / kSBufs) & 1)) {
-            to = true;
-            break;
-          }
-          tc::fence_after_sync();
-#pragma unroll
-          for (int blk = 0; blk < 4; ++blk) {
-            uint32_t ov[32];
-            tc::tmem_ld32(trow + kTmemO + 32 * blk, ov);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * al);
-            tc::tmem_st32(trow + kTmemO + 32 * blk, ov);
-          }
-          tc::tmem_st_wait();
-        }
-        l *= al;
-        mref = mn;
-        rthr = (mn + kRescaleLog2) / sc;
-      }
-      uint32_t pv[32];
-      float ls[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) ls[k] = 0.f;
-      if (!row_ok) {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) pv[c] = 0u;
-      } else if (full) {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * c]), sc, -mref));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * c + 1]), sc, -mref));
-          ls[c & 3] += p0;
-          ls[4 + (c & 3)] += p1;
-          pv[c] = pack_f16x2(p0, p1);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float p0 = 2 * c < nvalid ? fast_exp2(fmaf(__uint_as_float(sv[2 * c]), sc, -mref)) : 0.f;
-          const float p1 = 2 * c + 1 < nvalid ? fast_exp2(fmaf(__uint_as_float(sv[2 * c + 1]), sc, -mref)) : 0.f;
-          ls[c & 3] += p0;
-          ls[4 + (c & 3)] += p1;
-          pv[c] = pack_f16x2(p0, p1);
-        }
-      }
-      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-      tc::tmem_st32(trow + kTmemS + 64 * kb, pv);
-      tc::tmem_st_wait();
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.pfull[kb]));
-    }
-    // ---- epilogue: O (tensor memory) -> output row or partial state
-    if (warp_live) {
-      if (!to && ntiles > 0 &&
-          !warp_wait(smem_u32(&bs.pvdone[(ntiles - 1) % kSBufs]), ((ntiles - 1) / kSBufs) & 1))
-        to = true;
-      tc::fence_after_sync();
-      float* part = direct ? nullptr : a.partials + ((int64_t)u * kRows + r) * kPartStride;
-      const float inv = l > 0.f ? a.out_scale / l : 0.f;
-#pragma unroll
-      for (int blk = 0; blk < 4; ++blk) {
-        uint32_t ov[32];
-        if (ntiles > 0) {
-          tc::tmem_ld32(trow + kTmemO + 32 * blk, ov);
-          tc::tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) ov[c] = 0u;
-        }
-        if (!row_ok || to) continue;
-        if (direct) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int c = 0; c < 16; ++c)
-            pk[c] = pack_bf16x2(__uint_as_float(ov[2 * c]) * inv, __uint_as_float(ov[2 * c + 1]) * inv);
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + head_row * kD + 32 * blk);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-        } else {
-          float4* dst = reinterpret_cast<float4*>(part + 4 + 32 * blk);
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            dst[k] = make_float4(__uint_as_float(ov[4 * k]), __uint_as_float(ov[4 * k + 1]),
-                                 __uint_as_float(ov[4 * k + 2]), __uint_as_float(ov[4 * k + 3]));
-        }
-      }
-      if (row_ok && !to) {
-        if (direct) {
-          if (a.lse) a.lse[head_row] = l > 0.f ? (mref + __log2f(l)) * kLn2 : -INFINITY;
-        } else {
-          part[0] = mref;
-          part[1] = l;
-        }
-      }
-    }
-  }
-
-  if (to) atomicOr(a.status, kErrWaitTimeout);
-  tc::fence_before_sync();
-  __syncthreads();
-  if (warp == kMmaWarp) {
-    tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, kTmemCols);
-  }
-}
-
-// ------------------------------------------------ two row blocks per CTA
-// For several row blocks per (request, KV head) -- a chunked-prefill step --
-// a CTA takes two neighbouring blocks A and B over the same KV chunk: every
-// K/V tile feeds the products of both blocks, and two groups of four softmax
-// warps (each with its own rows, O accumulator and score buffers) run side by
-// side, so the softmax of one block overlaps the other's.  The score products
-// are e4m3 (kind::f8f6f4) on the K rows of the TMA stage, against each Q row
-// split exactly into two e4m3 parts (as in prefillw_kernel below); only V is
-// widened to f16.
-//   tensor memory: block X in columns 256 X .. 256 X + 255: two 64-column
-//   score / P buffers, then O (128 columns); Q's parts of both blocks in
-//   shared memory (the A operands of the score products).
-//   warps: 0 producer, 1 score MMAs, 2-5 widening, 6-9 softmax of block A,
-//   10-13 softmax of block B, 14 P.V MMAs.
-constexpr int k2KvBufs = 3;            // widened V tiles
-constexpr int k2Stages = 6;
-constexpr int k2SBufs = 2;
-constexpr int k2QAtom = kRows * 128;  // [128 rows][128 bytes] swizzled atom: 16 KB
-constexpr int k2OffQ = 0;             // block X: its two e4m3 parts of Q at (2 X + p) k2QAtom
-constexpr int k2VBufBytes = 2 * kKvAtom;  // widened V of a tile (2 atoms): 16 KB
-constexpr int k2OffKv = k2OffQ + 4 * k2QAtom;
-constexpr int k2OffStage = k2OffKv + k2KvBufs * k2VBufBytes;
-constexpr int k2OffBars = k2OffStage + k2Stages * kStageBytes;
-constexpr int k2SmemBytes = k2OffBars + 512 + 1024;
-constexpr int k2ProdWarp = 0, k2MmaWarp = 1, k2ConvWarp0 = 2, k2SoftWarp0 = 6, k2PvWarp = 14;
-constexpr int k2Threads = 15 * 32;
-static_assert(k2SmemBytes <= 232448, "shared memory over the per-CTA limit");
-
-struct Bars2 {
-  uint64_t stage_full[k2Stages], stage_empty[k2Stages];
-  uint64_t kvfull[k2KvBufs], kvfree[k2KvBufs];
-  uint64_t sfull[2][k2SBufs], pfull[2][k2SBufs], pvdone[2][k2SBufs];
-  uint64_t qready;
-  uint32_t tmem_base;
-};
-static_assert(sizeof(Bars2) <= 512, "barrier block");
-
-// Widens the V rows of a 64-token stage (thread ct of the four converter
-// warps takes 16-byte chunks i = ct + 128 m: row i / 8, chunk c = i % 8) into
-// units 2(c % 4), 2(c % 4) + 1 of atom c / 4 at dst; rows at or past `valid`
-// become zeros.  Loads first, then stores (see widen_tile64).
-__device__ __forceinline__ void widen_v64(const uint8_t* vstage, uint8_t* dst, int ct, int valid) {
-  uint4 v[4];
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    const int i = ct + 128 * m;
-    const int row = i >> 3, c = i & 7;
-    v[m] = make_uint4(0, 0, 0, 0);
-    if (row < valid) v[m] = lds128(vstage + (row >> 4) * kBoxBytes + swz(row & 15, c));
-  }
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    const int i = ct + 128 * m;
-    const int row = i >> 3, c = i & 7;
-    uint4 o0, o1;
-    e4m3x4_to_f16x2x2(v[m].x, o0.x, o0.y);
-    e4m3x4_to_f16x2x2(v[m].y, o0.z, o0.w);
-    e4m3x4_to_f16x2x2(v[m].z, o1.x, o1.y);
-    e4m3x4_to_f16x2x2(v[m].w, o1.z, o1.w);
-    const uint32_t d = atom_off(row, 2 * c, kKvAtom);
-    *reinterpret_cast<uint4*>(dst + d) = o0;
-    *reinterpret_cast<uint4*>(dst + (d ^ 16)) = o1;
-  }
-}
-
-__global__ void __launch_bounds__(k2Threads, 1)
-    prefill2_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                    const PrefillArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_addr = smem_u32(smem_raw);
-  uint8_t* const smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-  Bars2& bs = *reinterpret_cast<Bars2*>(smem + k2OffBars);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  // CTA -> (request, KV head, chunk, block pair); the two blocks' units in the
-  // one-block numbering (partial states and the merge use it)
-  const int QB2 = (a.QB + 1) / 2;
-  const int64_t u2 = blockIdx.x;
-  const int qp = (int)(u2 % QB2);
-  const int64_t bkc = u2 / QB2;  // (b * Hkv + kvh) * C + c
-  const int64_t uA = bkc * a.QB + 2 * qp;
-  const bool hasB = 2 * qp + 1 < a.QB;
-  const Unit xa = unit_of(a, uA, threadIdx.x == 0 && (bkc % ((int64_t)a.C * a.Hkv)) == 0 && qp == 0);
-  if (!xa.active) return;  // uniform over the CTA
-  Unit xb = xa;
-  if (hasB) xb = unit_of(a, uA + 1, false);
-  const bool bact = hasB && xb.active;
-  const int ntiles = bact ? max(xa.ntiles, xb.ntiles) : xa.ntiles;
-  const int t_hi = bact ? max(xa.t_hi, xb.t_hi) : xa.t_hi;  // tokens the pair reads
-  const bool direct = a.C == 1;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < k2Stages; ++s) {
-      mbar_init(smem_u32(&bs.stage_full[s]), 1);
-      mbar_init(smem_u32(&bs.stage_empty[s]), 5);  // V widened + both blocks' score products done
-    }
-    for (int k = 0; k < k2KvBufs; ++k) {
-      mbar_init(smem_u32(&bs.kvfull[k]), 4);  // V widened
-      mbar_init(smem_u32(&bs.kvfree[k]), 1);
-    }
-    for (int X = 0; X < 2; ++X) {
-      const int rows = X == 0 ? xa.rows : (bact ? xb.rows : 0);
-      const int live = max(1, min(4, (rows + 31) / 32));
-      for (int k = 0; k < k2SBufs; ++k) {
-        mbar_init(smem_u32(&bs.sfull[X][k]), 1);
-        mbar_init(smem_u32(&bs.pfull[X][k]), live);
-        mbar_init(smem_u32(&bs.pvdone[X][k]), 1);
-      }
-    }
-    mbar_init(smem_u32(&bs.qready), 8);
-    fence_mbar_init();
-    prefetch_tensormap(&tmK);
-    prefetch_tensormap(&tmV);
-  }
-  if (warp == k2MmaWarp) {
-    tc::tmem_alloc(smem_u32(&bs.tmem_base), kTmemCols);
-    tc::tmem_relinquish();
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = bs.tmem_base;
-  bool to = false;  // a bounded wait gave up
-  const int nblk = bact ? 2 : 1;
-
-  if (warp == k2ProdWarp) {
-    // ------------------------------------------------------------ producer
-    const int32_t* bt = a.block_tables + (int64_t)xa.b * a.max_pages;
-    auto load_batch = [&](int j0) {
-      const int j = j0 + lane / kBoxes;
-      const int tb = xa.t_lo + j * kTokN + (lane % kBoxes) * kBoxTok;
-      return (j < ntiles && tb < t_hi) ? __ldg(bt + tb / a.P) : 0;
-    };
-    int cur = load_batch(0), nxt = load_batch(kPageBatch);
-    for (int j = 0; j < ntiles && !to; ++j) {
-      if (j > 0 && j % kPageBatch == 0) {
-        cur = nxt;
-        nxt = load_batch(j + kPageBatch);
-      }
-      const int st = j % k2Stages;
-      if (j >= k2Stages && !warp_wait(smem_u32(&bs.stage_empty[st]), ((j / k2Stages) - 1) & 1)) {
-        to = true;
-        break;
-      }
-      const int tok0 = xa.t_lo + j * kTokN;
-      const int nbox = min(kBoxes, (t_hi - tok0 + kBoxTok - 1) / kBoxTok);
-      const uint32_t bar = smem_u32(&bs.stage_full[st]);
-      if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(2 * nbox * kBoxBytes));
-      __syncwarp();
-      int page = __shfl_sync(0xFFFFFFFFu, cur, (j % kPageBatch) * kBoxes + (lane & 3));
-      if (lane < nbox) {
-        const int tb = tok0 + lane * kBoxTok;
-        if (page < 0 || (int64_t)page >= a.num_pages) {
-          atomicOr(a.status, kErrBadPage);
-          page = -1;  // the box lands outside the tensor and reads zeros
-        }
-        const int row = (page * a.Hkv + xa.kvh) * a.P + tb % a.P;
-        const uint32_t dst = smem_u32(smem + k2OffStage + st * kStageBytes) + lane * kBoxBytes;
-        tma_load_2d(dst, &tmK, 0, row, bar);
-        tma_load_2d(dst + kTokN * kD, &tmV, 0, row, bar);
-      }
-    }
-    for (int j = ntiles > k2Stages ? ntiles - k2Stages : 0; j < ntiles; ++j)
-      if (!mbar_wait(smem_u32(&bs.stage_full[j % k2Stages]), (j / k2Stages) & 1)) to = true;
-  } else if (warp == k2MmaWarp) {
-    // ------------------------------------------------- score MMA issuer
-    // S_X(j) = Q_X . K(j)^T for both blocks, e4m3 products (kind::f8f6f4) on
-    // the K rows of the stage against Q_X's two e4m3 parts, once the stage has
-    // landed and the block's score buffer is free (P.V_X(j - 2) has
-    // completed); a commit after both blocks releases the stage's K.
-    if (lane == 0 && ntiles > 0) {
-      if (!mbar_wait(smem_u32(&bs.qready), 0)) to = true;
-      for (int j = 0; j < ntiles && !to; ++j) {
-        const int st = j % k2Stages;
-        if (!mbar_wait(smem_u32(&bs.stage_full[st]), (j / k2Stages) & 1)) {
-          to = true;
-          break;
-        }
-        const uint64_t kdesc = tc::desc_sw128(smem_u32(smem + k2OffStage + st * kStageBytes), 16, 1024);
-        for (int X = 0; X < nblk && !to; ++X) {
-          if (j >= k2SBufs &&
-              !mbar_wait(smem_u32(&bs.pvdone[X][(j - k2SBufs) % k2SBufs]), ((j - k2SBufs) / k2SBufs) & 1)) {
-            to = true;
-            break;
-          }
-          tc::fence_after_sync();
-          const uint64_t qdesc = tc::desc_sw128(smem_u32(smem + k2OffQ + 2 * X * k2QAtom), 16, 1024);
-#pragma unroll
-          for (int p = 0; p < 2; ++p)
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              tc::mma_ss_e4m3(tmem + 256 * X + 64 * (j % k2SBufs), qdesc + (uint64_t)((p * k2QAtom + 32 * k) >> 4),
-                              kdesc + (uint64_t)((32 * k) >> 4), kIdescQK, (p > 0 || k > 0) ? 1u : 0u);
-          tc::mma_commit(smem_u32(&bs.sfull[X][j % k2SBufs]));
-        }
-        if (!to) tc::mma_commit(smem_u32(&bs.stage_empty[st]));
-      }
-    }
-    __syncwarp();
-  } else if (warp == k2PvWarp) {
-    // ---------------------------------------------------- P.V MMA issuer
-    if (lane == 0 && ntiles > 0) {
-      const uint32_t kv0 = smem_u32(smem + k2OffKv);
-      int j = 0;
-      for (; j < ntiles && !to; ++j) {
-        if (!mbar_wait(smem_u32(&bs.kvfull[j % k2KvBufs]), (j / k2KvBufs) & 1)) {  // V(j) widened
-          to = true;
-          break;
-        }
-        const uint64_t vdesc = tc::desc_sw128(kv0 + (j % k2KvBufs) * k2VBufBytes, kKvAtom, 1024);
-        for (int X = 0; X < nblk && !to; ++X) {
-          if (!mbar_wait(smem_u32(&bs.pfull[X][j % k2SBufs]), (j / k2SBufs) & 1)) {
-            to = true;
-            break;
-          }
-          tc::fence_after_sync();
-#pragma unroll
-          for (int k = 0; k < kTokN / 16; ++k)
-            tc::mma_ts(tmem + 256 * X + 128, tmem + 256 * X + 64 * (j % k2SBufs) + 8 * k,
-                       vdesc + (uint64_t)((2048 * k) >> 4), kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
-          tc::mma_commit(smem_u32(&bs.pvdone[X][j % k2SBufs]));
-        }
-        // both products of the tile issued: the widened V frees once they complete
-        if (!to) tc::mma_commit(smem_u32(&bs.kvfree[j % k2KvBufs]));
-      }
-      // no MMA may still be running when the tensor memory is freed
-      if (j > 0)
-        for (int X = 0; X < nblk; ++X)
-          if (!mbar_wait(smem_u32(&bs.pvdone[X][(j - 1) % k2SBufs]), ((j - 1) / k2SBufs) & 1)) to = true;
-    }
-    __syncwarp();
-  } else if (warp < k2SoftWarp0) {
-    // ---------------------------------------------------------- converters
-    const int ct = threadIdx.x - k2ConvWarp0 * 32;
-    for (int j = 0; j < ntiles && !to; ++j) {
-      const int st = j % k2Stages, kb = j % k2KvBufs;
-      if (!warp_wait(smem_u32(&bs.stage_full[st]), (j / k2Stages) & 1)) to = true;
-      if (j >= k2KvBufs && !to && !warp_wait(smem_u32(&bs.kvfree[kb]), ((j - k2KvBufs) / k2KvBufs) & 1)) to = true;
-      if (to) break;
-      const int valid = min(kTokN, t_hi - (xa.t_lo + j * kTokN));
-      widen_v64(smem + k2OffStage + st * kStageBytes + kTokN * kD, smem + k2OffKv + kb * k2VBufBytes, ct, valid);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tc::mbar_arrive_local(smem_u32(&bs.stage_empty[st]));
-        tc::mbar_arrive_local(smem_u32(&bs.kvfull[kb]));
-      }
-    }
-  } else {
-    // ------------------------------------------- softmax + epilogue (block X)
-    const int X = (warp - k2SoftWarp0) >> 2;
-    const Unit& x = X == 0 ? xa : xb;
-    const int64_t ux = uA + X;
-    const int xrows = X == 0 ? xa.rows : (bact ? xb.rows : 0);
-    const int quad = warp & 3;
-    const int r = 32 * quad + lane;
-    const uint32_t trow = tmem + ((uint32_t)(32 * quad) << 16) + 256 * X;
-    const bool row_ok = r < xrows;
-    const int i = x.i0 + r / a.G, g = r % a.G;
-    const int64_t head_row = ((int64_t)a.q_start[x.b] + i) * a.Hq + (int64_t)x.kvh * a.G + g;
-    // Q row -> two exact e4m3 parts (x = q s, s = 2^floor(log2(448 / max |q|));
-    // part 1 = e4m3(x), part 2 = e4m3(x - part 1)) -> the swizzled K-major A
-    // operands of this block (zeros for padding rows); 1 / s joins the score scale
-    float qinv = 0.f;
-    {
-      const uint4* qp4 = reinterpret_cast<const uint4*>(a.q + head_row * kD);
-      float amax = 0.f;
-      if (row_ok) {
-#pragma unroll 4
-        for (int uu = 0; uu < 16; ++uu) {
-          const uint4 w = __ldg(qp4 + uu);
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(ww[k])), fabsf(bf16_hi(ww[k]))));
-        }
-      }
-      const float qs = pow2_scale(448.f, amax);
-      qinv = row_ok ? 1.f / qs : 0.f;  // exact: qs is a power of two
-#pragma unroll 1
-      for (int c = 0; c < 8; ++c) {  // 16 elements per 16-byte chunk
-        uint32_t p1[4] = {0u, 0u, 0u, 0u}, p2[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint4 w = make_uint4(0, 0, 0, 0);
-          if (row_ok) w = __ldg(qp4 + 2 * c + h);
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float x0 = bf16_lo(ww[k]) * qs, x1 = bf16_hi(ww[k]) * qs;
-            const uint16_t c1 = f32x2_to_e4m3x2(x0, x1);
-            const uint32_t hf = e4m3x2_to_f16x2(c1);
-            const uint16_t c2 = f32x2_to_e4m3x2(x0 - f16_lo(hf), x1 - f16_hi(hf));  // exact difference
-            p1[2 * h + (k >> 1)] |= (uint32_t)c1 << (16 * (k & 1));
-            p2[2 * h + (k >> 1)] |= (uint32_t)c2 << (16 * (k & 1));
-          }
-        }
-        const uint32_t off = r * 128 + 16 * (c ^ (r & 7));  // 128-byte swizzle
-        *reinterpret_cast<uint4*>(smem + k2OffQ + 2 * X * k2QAtom + off) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
-        *reinterpret_cast<uint4*>(smem + k2OffQ + (2 * X + 1) * k2QAtom + off) = make_uint4(p2[0], p2[1], p2[2], p2[3]);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.qready));
-    }
-    const int lim = row_ok ? min(x.L - x.n + i + 1, x.t_end_chunk) : xa.t_lo;
-    const float sc = a.score_scale * qinv;  // the scores carry the row's Q scale
-    float mref = -INFINITY, rthr = -INFINITY, l = 0.f;
-    const bool warp_live = 32 * quad < xrows;
-    for (int j = 0; j < ntiles && !to && warp_live; ++j) {
-      const int kb = j % k2SBufs;
-      if (!warp_wait(smem_u32(&bs.sfull[X][kb]), (j / k2SBufs) & 1)) {
-        to = true;
-        break;
-      }
-      tc::fence_after_sync();
-      const int tok0 = xa.t_lo + j * kTokN;
-      const int nvalid = lim - tok0;
-      const bool full = nvalid >= kTokN;
-      // the scores are read twice, 32 columns at a time (once for the row
-      // maximum, once for P), to keep few registers live
-      float mx = -INFINITY;
-      {
-        float m8[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t sv[32];
-          tc::tmem_ld32(trow + 64 * kb + 32 * h, sv);
-          tc::tmem_ld_wait();
-          if (row_ok) {
-            if (full) {
-#pragma unroll
-              for (int c = 0; c < 32; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sv[c]));
-            } else {
-#pragma unroll
-              for (int c = 0; c < 32; ++c)
-                if (32 * h + c < nvalid) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sv[c]));
-            }
-          }
-        }
-        if (row_ok)
-          mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-      }
-      const bool grow = mx > rthr;
-      if (__any_sync(0xFFFFFFFFu, grow)) {
-        const float mn = grow ? fmaxf(mref, mx * sc) : mref;
-        const float al = grow ? fast_exp2(mref - mn) : 1.f;
-        const bool rescale = __any_sync(0xFFFFFFFFu, grow && mref != -INFINITY);
-        if (rescale && j > 0) {
-          if (!warp_wait(smem_u32(&bs.pvdone[X][(j - 1) % k2SBufs]), ((j - 1) / k2SBufs) & 1)) {
-            to = true;
-            break;
-          }
-          tc::fence_after_sync();
-#pragma unroll
-          for (int blk = 0; blk < 4; ++blk) {
-            uint32_t ov[32];
-            tc::tmem_ld32(trow + 128 + 32 * blk, ov);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * al);
-            tc::tmem_st32(trow + 128 + 32 * blk, ov);
-          }
-          tc::tmem_st_wait();
-        }
-        l *= al;
-        mref = mn;
-        rthr = (mn + kRescaleLog2) / sc;
-      }
-      float ls[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) ls[k] = 0.f;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t sv[32];
-        tc::tmem_ld32(trow + 64 * kb + 32 * h, sv);
-        tc::tmem_ld_wait();
-        uint32_t pv[16];
-        if (!row_ok) {
-#pragma unroll
-          for (int c = 0; c < 16; ++c) pv[c] = 0u;
-        } else if (full) {
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * c]), sc, -mref));
-            const float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * c + 1]), sc, -mref));
-            ls[c & 3] += p0;
-            ls[4 + (c & 3)] += p1;
-            pv[c] = pack_f16x2(p0, p1);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int c0 = 32 * h + 2 * c;
-            const float p0 = c0 < nvalid ? fast_exp2(fmaf(__uint_as_float(sv[2 * c]), sc, -mref)) : 0.f;
-            const float p1 = c0 + 1 < nvalid ? fast_exp2(fmaf(__uint_as_float(sv[2 * c + 1]), sc, -mref)) : 0.f;
-            ls[c & 3] += p0;
-            ls[4 + (c & 3)] += p1;
-            pv[c] = pack_f16x2(p0, p1);
-          }
-        }
-        // P of columns 32 h .. 32 h + 31 overwrites scores 16 h .. 16 h + 15,
-        // which this half has already read (h = 0) or never needs again (h = 1)
-        tc::tmem_st16(trow + 64 * kb + 16 * h, pv);
-      }
-      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-      tc::tmem_st_wait();
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.pfull[X][kb]));
-    }
-    // ---- epilogue: O_X -> output rows or partial state
-    if (warp_live) {
-      if (!to && ntiles > 0 &&
-          !warp_wait(smem_u32(&bs.pvdone[X][(ntiles - 1) % k2SBufs]), ((ntiles - 1) / k2SBufs) & 1))
-        to = true;
-      tc::fence_after_sync();
-      float* part = direct ? nullptr : a.partials + (ux * kRows + r) * kPartStride;
-      const float inv = l > 0.f ? a.out_scale / l : 0.f;
-#pragma unroll
-      for (int blk = 0; blk < 4; ++blk) {
-        uint32_t ov[32];
-        if (ntiles > 0) {
-          tc::tmem_ld32(trow + 128 + 32 * blk, ov);
-          tc::tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) ov[c] = 0u;
-        }
-        if (!row_ok || to) continue;
-        if (direct) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int c = 0; c < 16; ++c)
-            pk[c] = pack_bf16x2(__uint_as_float(ov[2 * c]) * inv, __uint_as_float(ov[2 * c + 1]) * inv);
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + head_row * kD + 32 * blk);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-        } else {
-          float4* dst = reinterpret_cast<float4*>(part + 4 + 32 * blk);
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            dst[k] = make_float4(__uint_as_float(ov[4 * k]), __uint_as_float(ov[4 * k + 1]),
-                                 __uint_as_float(ov[4 * k + 2]), __uint_as_float(ov[4 * k + 3]));
-        }
-      }
-      if (row_ok && !to) {
-        if (direct) {
-          if (a.lse) a.lse[head_row] = l > 0.f ? (mref + __log2f(l)) * kLn2 : -INFINITY;
-        } else {
-          part[0] = mref;
-          part[1] = l;
-        }
-      }
-    }
-  }
-
-  if (to) atomicOr(a.status, kErrWaitTimeout);
-  tc::fence_before_sync();
-  __syncthreads();
-  if (warp == k2MmaWarp) {
-    tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, kTmemCols);
-  }
 }
 
 // ------------------------------------------ wide tiles for a few queries
@@ -1832,8 +925,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32) prefillw_merge_kernel(const 
 // takes one block of 128 rows per CTA over 128-token tiles, with Q's two
 // exact e4m3 parts in tensor memory as the A operand of the score products
 // (kind::f8f6f4, M = 128, N = 128), so those products read only the K rows
-// from shared memory; the shared-memory operand traffic of the two-block
-// kernel, whose score products read Q there, bounded it.  Eight softmax
+// from shared memory (an earlier kernel taking two blocks per CTA, with Q in
+// shared memory because the two blocks' accumulators filled tensor memory,
+// was bound by that operand traffic).  Eight softmax
 // warps, two per lane quadrant, each take 64 of a row's 128 scores: the two
 // halves of a row swap their maxima (and, once per unit, Q's largest
 // magnitude and at the end the row sums) through shared memory, handing over
