@@ -500,24 +500,25 @@ def prefill_timing(pf, peak_gbs, peak_tf, flush, iters):
         "tflops": round(causal_flops(w) / t / 1e12, 2)}
     del s, q, out, st
     torch.cuda.empty_cache()
-    # (b) chunked prefill
-    w = synth.PagedWorkload("chunk", B=4, Hq=64, Hkv=8, D=128, P=16, context_lens=np.full(4, 8192), n_new=1024,
-                            seed=7)
-    s, q, qs = setup(w)
-    out = torch.empty_like(q)
-    st = s.st
-    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
-    fn = lambda: pf.paged_prefill_attn(out, q, st.k_cache, st.v_cache, st.block_tables, st.context_lens, qs,
-                                       w.n_new, 8192, w.k_scale, w.v_scale, w.softmax_scale, workspace=ws)
-    fn()
-    t = time_events(fn, iters, flush)
-    fl = causal_flops(w)
-    res["chunked_prefill_b4_n1024_l8192_h64kv8"] = {
-        "prefill_us": round(t * 1e6, 2), "causal_flop": fl, "tflops": round(fl / t / 1e12, 2),
-        "frac_of_bf16_peak": round(fl / t / 1e12 / peak_tf, 4),
-        "query_tokens_per_s": round(w.B * w.n_new / t, 1)}
-    del s, q, out, st, ws
-    torch.cuda.empty_cache()
+    # (b) chunked prefill, pages of 16 and of 64 tokens
+    for P, key in ((16, "chunked_prefill_b4_n1024_l8192_h64kv8"), (64, "chunked_prefill_b4_n1024_l8192_h64kv8_p64")):
+        w = synth.PagedWorkload("chunk", B=4, Hq=64, Hkv=8, D=128, P=P, context_lens=np.full(4, 8192), n_new=1024,
+                                seed=7)
+        s, q, qs = setup(w)
+        out = torch.empty_like(q)
+        st = s.st
+        ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+        fn = lambda: pf.paged_prefill_attn(out, q, st.k_cache, st.v_cache, st.block_tables, st.context_lens, qs,
+                                           w.n_new, 8192, w.k_scale, w.v_scale, w.softmax_scale, workspace=ws)
+        fn()
+        t = time_events(fn, iters, flush)
+        fl = causal_flops(w)
+        res[key] = {
+            "prefill_us": round(t * 1e6, 2), "page_size": P, "causal_flop": fl, "tflops": round(fl / t / 1e12, 2),
+            "frac_of_bf16_peak": round(fl / t / 1e12 / peak_tf, 4),
+            "query_tokens_per_s": round(w.B * w.n_new / t, 1)}
+        del s, q, out, st, ws
+        torch.cuda.empty_cache()
     return res
 
 
