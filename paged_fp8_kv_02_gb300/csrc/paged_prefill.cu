@@ -189,8 +189,8 @@ constexpr uint32_t kIdescQKW = tc::idesc_f16(64, kWTok, false);  // with kind::f
 constexpr uint32_t kIdescPVW = tc::idesc_f16(64, kD, true);
 constexpr int kWConvWarps = 4;
 constexpr int kWProdWarp = 0, kWMmaWarp = 1, kWConvWarp0 = 2, kWSoftWarp0 = kWConvWarp0 + kWConvWarps,
-              kWPvWarp = kWSoftWarp0 + 4;
-constexpr int kWThreads = (kWPvWarp + 1) * 32;
+              kWPvWarp = kWSoftWarp0 + 4, kWProdWarpV = kWPvWarp + 1;
+constexpr int kWThreads = (kWProdWarpV + 1) * 32;
 constexpr int kWChunks = kWTok * kD / 16 / (32 * kWConvWarps);  // 16-byte chunks of V per converter thread
 
 struct BarsW {
@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kWStages; ++s) {
-      mbar_init(smem_u32(&bs.stage_full[s]), 1);
+      mbar_init(smem_u32(&bs.stage_full[s]), 2);  // the K and the V producer
       mbar_init(smem_u32(&bs.stage_empty[s]), kWConvWarps + 1);  // V read + the score products done
     }
     for (int k = 0; k < kWBufs; ++k) {
@@ -405,8 +405,11 @@ __global__ void __launch_bounds__(kWThreads, 1)
   const int64_t W = a.tile_start[a.B];
   const int64_t f0 = (int64_t)blockIdx.x * W / gridDim.x, f1 = ((int64_t)blockIdx.x + 1) * W / gridDim.x;
 
-  if (warp == kWProdWarp) {
-    // ------------------------------------------------------------ producer
+  if (warp == kWProdWarp || warp == kWProdWarpV) {
+    // ------------------------------------------------------------ producers
+    // warp kWProdWarp copies K, warp kWProdWarpV copies V, each arriving on
+    // the stage with its own byte count (one warp issuing both measured slower)
+    const bool isv = warp == kWProdWarpV;
     // A tile is nb = 128 / box_tok boxes per tensor, each inside one page
     // (tiles start at multiples of 64 tokens): with 64-token pages two 8 KB
     // copies instead of eight 2 KB ones, which measured faster.  A 64-row box
@@ -441,19 +444,19 @@ __global__ void __launch_bounds__(kWThreads, 1)
         const int tok0 = x.t_lo + j * kWTok;
         const int nbox = min(nb, (x.t_hi - tok0 + btok - 1) / btok);
         const uint32_t bar = smem_u32(&bs.stage_full[st]);
-        if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(2 * nbox * btok * kD));
+        if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(nbox * btok * kD));
         __syncwarp();
         int page = __shfl_sync(0xFFFFFFFFu, cur, (j % tpb) * nb + (lane % nb));
         if (lane < nbox) {
           const int tb = tok0 + lane * btok;
           if (page < 0 || (int64_t)page >= a.num_pages) {
-            atomicOr(a.status, kErrBadPage);
+            if (!isv) atomicOr(a.status, kErrBadPage);
             page = -1;  // the box lands outside the tensor and reads zeros
           }
           const int row = (page * a.Hkv + x.kvh) * a.P + tb % a.P;
           const uint32_t dst = smem_u32(smem + kWOffStage + st * kWStageBytes) + lane * btok * kD;
-          tma_load_2d(dst, &tmK, 0, row, bar);
-          tma_load_2d(dst + kWTok * kD, &tmV, 0, row, bar);
+          if (isv) tma_load_2d(dst + kWTok * kD, &tmV, 0, row, bar);
+          else tma_load_2d(dst, &tmK, 0, row, bar);
         }
       }
       g += ntiles;
