@@ -117,12 +117,42 @@ def test_few_rows_across_group_sizes(Hq, Hkv, n_new):
     _check_small(w, split=128)
 
 
-def test_half_height_units_of_the_one_block_kernel():
+def test_partly_padded_128_row_blocks():
     # G 16 x 8 queries = 128 rows per block, but requests 1 and 2 have 48 and
-    # 16 rows: their units take the half-height products of the one-block kernel
+    # 16 rows: their blocks are mostly padding rows
     w = _w("g16_varlen", 16, 1, (100, 50, 300), n_new=1)
     _check_small(w, q_lens=np.array([8, 3, 1]), max_q=8)
     _check_small(w, q_lens=np.array([8, 3, 1]), split=64, max_q=8)
+
+
+@pytest.mark.parametrize("P", [32, 128])
+def test_pages_of_32_and_128_tokens(P):
+    # boxes as tall as the page allows: 32 rows at page 32, two 64-row boxes per
+    # page at page 128; both kernels, contexts ending mid-page and mid-tile
+    w = _w(f"p{P}_wide", 16, 2, (40, 130, 300, 517), n_new=6, P=P)  # 48 rows: the even split
+    _check_small(w)
+    w = _w(f"p{P}_rows", 16, 2, (300, 517, 1000), n_new=40, P=P)  # 320 rows: 128-row blocks
+    _check_small(w)
+    _check_small(w, split=192)
+
+
+def test_128_row_blocks_page64_mha_and_varlen():
+    # G = 1 with 300 new tokens (three blocks, the last one partial) at page 64,
+    # and varlen requests whose blocks are partly padding
+    _check_small(_w("mha_p64", 4, 4, (300, 700, 1301), n_new=300, P=64))
+    w = _w("g8_varlen_p64", 16, 2, (600, 257, 129, 1500), n_new=1, P=64)
+    _check_small(w, q_lens=np.array([100, 17, 0, 64]), max_q=100)
+
+
+def test_128_row_blocks_bad_page_sets_status():
+    p = pf()
+    w = _w("bad_rows", 8, 2, (200, 300), n_new=32).set_scales_host()  # 128 rows per block
+    kc, vc = oracle_fill_paged(w)
+    bt = w.block_tables.copy()
+    bt[1, 3] = w.num_pages + 7
+    out, _, status = _run(p, w, _dev(kc), _dev(vc), bt=bt)
+    assert status & p.DEVERR["BAD_PAGE"]
+    assert np.all(np.isfinite(out))
 
 
 def test_bad_page_and_clamped_context_set_status():
