@@ -314,9 +314,10 @@ PFKV_API int pfkv_paged_decode_attn_scaled(void *out, const void *q, const void 
  *                 Not used when max_q_len * G <= 64 (verification-sized
  *                 calls): the contexts of all (request, KV head) pairs are
  *                 then split evenly over one CTA per SM and the pieces merged
- *                 (workspace: (SMs + batch * num_kv_heads) 64-row partial
- *                 states plus batch + 1 offsets), whatever the value (it is
- *                 still checked)
+ *                 (workspace: (SMs of the current device + batch *
+ *                 num_kv_heads) 64-row partial states plus batch + 1
+ *                 offsets, so query the size on the device that will run the
+ *                 call), whatever the value (it is still checked)
  *   workspace     >= pfkv_paged_prefill_workspace_size(...) bytes, 256-byte
  *                 aligned; lse_out optional fp32 [q_start[batch]][num_q_heads]
  * Other layouts as pfkv_paged_decode_attn.
