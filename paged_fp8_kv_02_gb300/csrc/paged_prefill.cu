@@ -948,8 +948,13 @@ __global__ void __launch_bounds__(kMergeWarps * 32) prefillw_merge_kernel(const 
 //   warp issuing every copy of a tile measured slower, most of all with
 //   16-token pages: 16 copies per tile).
 // Units in order of decreasing row block, so the longest (causal) ones start first.
-constexpr int kMTmemO = 256, kMTmemQ = 384, kMTmemP = 448;
-static_assert(kMTmemP + kWTok / 2 <= kTmemCols, "tensor memory columns");
+// Score and P buffers in tensor memory.  One score buffer and two P buffers
+// (so that P(j + 1) need not wait for P.V(j)) fit as well and give the same
+// output, but measured 0.5-1% slower: S(j + 1) then waits for the softmax
+// to read S(j), a loop of the same length.
+constexpr int kMSBufs = 2, kMPBufs = 1;
+constexpr int kMTmemO = kMSBufs * kWTok, kMTmemQ = kMTmemO + kD, kMTmemP = kMTmemQ + 64;
+static_assert(kMTmemP + kMPBufs * kWTok / 2 <= kTmemCols, "tensor memory columns");
 constexpr int kMStages = 3, kMVBufs = 3;
 constexpr int kMOffV = 0;
 constexpr int kMOffStage = kMOffV + kMVBufs * kWVBytes;
@@ -965,8 +970,8 @@ constexpr int kMThreads = 16 * 32;
 struct BarsM {
   uint64_t stage_full[kMStages], stage_empty[kMStages];
   uint64_t vfull[kMVBufs], vfree[kMVBufs];  // widened V written / read by its P.V
-  uint64_t sfull[kWBufs], sread[kWBufs], pvdone[kWBufs];
-  uint64_t pfull, qready;
+  uint64_t sfull[kMSBufs], sread[kMSBufs], pfull[kMPBufs], pvdone[kMPBufs];
+  uint64_t qready;
   uint64_t xch[4];  // the two softmax warps of a lane quadrant hand over shared values
   uint32_t tmem_base;
 };
@@ -1016,12 +1021,14 @@ __global__ void __launch_bounds__(kMThreads, 1)
       mbar_init(smem_u32(&bs.vfull[k]), kWConvWarps);
       mbar_init(smem_u32(&bs.vfree[k]), 1);
     }
-    for (int k = 0; k < kWBufs; ++k) {
+    for (int k = 0; k < kMSBufs; ++k) {
       mbar_init(smem_u32(&bs.sfull[k]), 1);
       mbar_init(smem_u32(&bs.sread[k]), 8);
+    }
+    for (int k = 0; k < kMPBufs; ++k) {
+      mbar_init(smem_u32(&bs.pfull[k]), 8);
       mbar_init(smem_u32(&bs.pvdone[k]), 1);
     }
-    mbar_init(smem_u32(&bs.pfull), 8);
     mbar_init(smem_u32(&bs.qready), 8);
     for (int q = 0; q < 4; ++q) mbar_init(smem_u32(&bs.xch[q]), 2);
     fence_mbar_init();
@@ -1090,9 +1097,9 @@ __global__ void __launch_bounds__(kMThreads, 1)
     if (lane == 0 && ntiles > 0) {
       if (!mbar_wait(smem_u32(&bs.qready), 0)) to = true;
       for (int j = 0; j < ntiles && !to; ++j) {
-        const int kb = j % kWBufs, st = j % kMStages;
+        const int kb = j % kMSBufs, st = j % kMStages;
         if (!mbar_wait(smem_u32(&bs.stage_full[st]), (j / kMStages) & 1)) to = true;
-        if (j >= kWBufs && !to && !mbar_wait(smem_u32(&bs.sread[kb]), ((j - kWBufs) / kWBufs) & 1)) to = true;
+        if (j >= kMSBufs && !to && !mbar_wait(smem_u32(&bs.sread[kb]), ((j - kMSBufs) / kMSBufs) & 1)) to = true;
         if (to) break;
         tc::fence_after_sync();
         const uint64_t kdesc = tc::desc_sw128(smem_u32(smem + kMOffStage + st * kWStageBytes), 16, 1024);
@@ -1113,8 +1120,9 @@ __global__ void __launch_bounds__(kMThreads, 1)
       const uint32_t v0 = smem_u32(smem + kMOffV);
       int pn = 0;
       for (; pn < ntiles && !to; ++pn) {
-        const int kb = pn % kWBufs, vb = pn % kMVBufs;
-        if (!mbar_wait(smem_u32(&bs.pfull), pn & 1) || !mbar_wait(smem_u32(&bs.vfull[vb]), (pn / kMVBufs) & 1)) {
+        const int kb = pn % kMPBufs, vb = pn % kMVBufs;
+        if (!mbar_wait(smem_u32(&bs.pfull[kb]), (pn / kMPBufs) & 1) ||
+            !mbar_wait(smem_u32(&bs.vfull[vb]), (pn / kMVBufs) & 1)) {
           to = true;
           break;
         }
@@ -1122,12 +1130,12 @@ __global__ void __launch_bounds__(kMThreads, 1)
         const uint64_t vdesc = tc::desc_sw128(v0 + vb * kWVBytes, kWAtom, 1024);
 #pragma unroll
         for (int kk = 0; kk < kWTok / 16; ++kk)
-          tc::mma_ts(tmem + kMTmemO, tmem + kMTmemP + 8 * kk, vdesc + (uint64_t)((2048 * kk) >> 4), kIdescPVM,
+          tc::mma_ts(tmem + kMTmemO, tmem + kMTmemP + 64 * kb + 8 * kk, vdesc + (uint64_t)((2048 * kk) >> 4), kIdescPVM,
                      (pn > 0 || kk > 0) ? 1u : 0u);
         tc::mma_commit(smem_u32(&bs.pvdone[kb]));
         tc::mma_commit(smem_u32(&bs.vfree[vb]));
       }
-      if (pn > 0 && !mbar_wait(smem_u32(&bs.pvdone[(pn - 1) % kWBufs]), ((pn - 1) / kWBufs) & 1)) to = true;
+      if (pn > 0 && !mbar_wait(smem_u32(&bs.pvdone[(pn - 1) % kMPBufs]), ((pn - 1) / kMPBufs) & 1)) to = true;
     }
     __syncwarp();
   } else if (warp < kMSoftWarp0) {
@@ -1226,8 +1234,8 @@ __global__ void __launch_bounds__(kMThreads, 1)
     const float sc = a.score_scale * qinv;  // the scores carry the row's Q scale
     float mref = -INFINITY, rthr = -INFINITY, lpart = 0.f;
     for (int j = 0; j < ntiles && !to; ++j) {
-      const int kb = j % kWBufs;
-      if (!warp_wait(smem_u32(&bs.sfull[kb]), (j / kWBufs) & 1)) {
+      const int kb = j % kMSBufs, pb = j % kMPBufs;
+      if (!warp_wait(smem_u32(&bs.sfull[kb]), (j / kMSBufs) & 1)) {
         to = true;
         break;
       }
@@ -1235,7 +1243,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
       const uint32_t sbase = trow + kWTok * kb + 64 * half;
       const int nv = lim - (x.t_lo + j * kWTok + 64 * half);  // this half's columns c < nv are attended
       const bool full = __all_sync(0xFFFFFFFFu, nv >= 64);
-      // this half's 64 scores in registers at once; the buffer is then free for S(j + 2)
+      // this half's 64 scores in registers at once; the buffer is then free for S(j + kMSBufs)
       uint32_t sv[64];
       {
         uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
@@ -1299,9 +1307,10 @@ __global__ void __launch_bounds__(kMThreads, 1)
         }
       }
       lpart += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      // P and O are free once P.V(j - 1) has completed
-      if (j > 0) {
-        if (!warp_wait(smem_u32(&bs.pvdone[(j - 1) % kWBufs]), ((j - 1) / kWBufs) & 1)) {
+      // P buffer pb is free once P.V(j - kMPBufs) has completed, O once P.V(j - 1) has
+      if (j >= kMPBufs || (rescale && kMPBufs > 1)) {
+        const int jw = rescale ? j - 1 : j - kMPBufs;  // the later of the two when both apply
+        if (!warp_wait(smem_u32(&bs.pvdone[jw % kMPBufs]), (jw / kMPBufs) & 1)) {
           to = true;
           break;
         }
@@ -1318,17 +1327,17 @@ __global__ void __launch_bounds__(kMThreads, 1)
           tc::tmem_st32(trow + kMTmemO + 64 * half + 32 * blk, ov);
         }
       }
-      tc::tmem_st32(trow + kMTmemP + 32 * half, pv);
+      tc::tmem_st32(trow + kMTmemP + 64 * pb + 32 * half, pv);
       tc::tmem_st_wait();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.pfull));
+      if (lane == 0) tc::mbar_arrive_local(smem_u32(&bs.pfull[pb]));
     }
     // ---- epilogue: this half's 64 columns of row r
     if (!to) {
       const float l = lpart + swap(lpart);
       if (!to && ntiles > 0 &&
-          !warp_wait(smem_u32(&bs.pvdone[(ntiles - 1) % kWBufs]), ((ntiles - 1) / kWBufs) & 1))
+          !warp_wait(smem_u32(&bs.pvdone[(ntiles - 1) % kMPBufs]), ((ntiles - 1) / kMPBufs) & 1))
         to = true;
       tc::fence_after_sync();
       float* part = direct ? nullptr : a.partials + (u * kRows + r) * kPartStride;
