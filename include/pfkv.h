@@ -25,6 +25,8 @@
  *    token at logical position t of request b lives in page
  *    block_tables[b][t / P], row t % P ("slot" = page * P + t % P).  The MLA
  *    latent cache is [num_pages][P][Dqk] (the same layout with Hkv = 1).
+ *    A cache holds at least one page: num_pages < 1 is rejected with
+ *    PFKV_ERR_INVALID_ARG, also by a call that would have nothing to do.
  *  - context_lens[b] counts every token attended, including tokens appended
  *    in the same step.
  *  - Return value: PFKV_OK, or a negative pfkv_status for argument, support or

@@ -37,6 +37,8 @@ def _decode_case(case):
             lens[i] = 0
         elif u < 0.35:
             lens[i] = _edge_len(r, P)
+    if lens.max() == 0:  # a cache holds at least one page
+        lens[0] = _edge_len(r, P)
     split = int(r.choice([0, 0, 16, 32, 80, 256]))
     return Hkv, G, P, lens, split
 
@@ -109,3 +111,55 @@ def test_mla_random_configuration(case):
         _mla_check(p, m, st, what=f"mla sweep {case}")
     else:
         _mla_check(p, m, st, topk=topk, what=f"mla sweep {case}")
+
+
+def _scaled_case(case):
+    r = np.random.default_rng(4000 + case)
+    Hkv = int(r.choice([1, 2, 4]))
+    G = int(r.integers(1, 17))
+    P = int(r.choice([16, 32, 48, 64]))
+    B = int(r.integers(1, 8))
+    lens = r.integers(1, 600, size=B)
+    for i in range(B):
+        u = r.random()
+        if u < 0.15:
+            lens[i] = 0
+        elif u < 0.35:
+            lens[i] = _edge_len(r, P)
+    if lens.max() == 0:
+        lens[0] = _edge_len(r, P)
+    split = int(r.choice([0, 0, 16, 48, 128]))
+    spread = int(r.choice([0, 3, 6, 12]))
+    zero_rows = bool(r.random() < 0.4)
+    return Hkv, G, P, lens, split, spread, zero_rows
+
+
+@pytest.mark.parametrize("case", range(24))
+def test_scaled_append_and_decode_random_configuration(case):
+    """The scaled append writes the oracle's codes and scales bit for bit; the
+    decode over those bytes matches the oracle's decode."""
+    import oracle
+    from oracle_helpers import oracle_fill_scaled
+    from test_gpu_scales import GRANS, _decode, _gpu_fill, _scale_rows_used
+    from gpu_helpers import assert_within_tolerance
+    gran = GRANS[case % 3]
+    Hkv, G, P, lens, split, spread, zero_rows = _scaled_case(case)
+    p = pf()
+    w = synth.PagedWorkload(f"ssweep{case}", B=len(lens), Hq=G * Hkv, Hkv=Hkv, D=128, P=P, context_lens=lens,
+                            seed=90 + case)
+    kc, vc, ks, vs = _gpu_fill(p, w, gran, spread, zero_rows)
+    okc, ovc, oks, ovs = oracle_fill_scaled(w, gran, spread, zero_rows)
+    assert np.array_equal(kc.cpu().numpy(), okc)
+    assert np.array_equal(vc.cpu().numpy(), ovc)
+    if gran == oracle.SCALE_TOKEN:
+        for got, ref in ((ks, oks), (vs, ovs)):
+            assert np.array_equal(_scale_rows_used(w, got.cpu().numpy()).view(np.uint32),
+                                  _scale_rows_used(w, ref).view(np.uint32))
+    out, lse, status = _decode(p, w, kc, vc, gran, ks, vs, split)
+    assert status == 0
+    ref, ref_lse = oracle.paged_decode_scaled(w.q_bits(), okc, ovc, gran, oks, ovs, w.block_tables,
+                                              w.context_lens, w.P, w.softmax_scale, w.Hkv)
+    assert_within_tolerance(out, ref, f"scaled sweep {case} gran {gran}")
+    fin = np.isfinite(ref_lse)
+    assert np.all(~np.isfinite(lse[~fin]))
+    np.testing.assert_allclose(lse[fin], ref_lse[fin], rtol=2e-5, atol=2e-4)
