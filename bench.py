@@ -890,6 +890,8 @@ PROFILE_CASES = {
     "gqa_prefix_b64": "GQA 64/8 heads, 64 requests, lognormal contexts, 16 share a 2048-token prefix",
     "long_b2_l262144": "GQA 64/8 heads, 2 requests x 262144 tokens, page 64, 4096-token chunks",
     "mla_b16_topk2048": "MLA 128 heads x 576, 16 requests x 65536 tokens, top-k 2048, page 64",
+    "mla_b64_topk2048_l16384": "MLA 128 heads x 576, 64 requests x 16384 tokens, top-k 2048, page 64 "
+                               "(the full batch, one run per request, on a quarter of the context)",
     "prefill_chunk_b1_n1024_l8192": "multi-query: 1 request, 1024 new tokens on a 7168-token prefix, GQA 64/8",
     "prefill_verify_b2_l262144_q8": "multi-query: 2 requests x 262144 tokens, 8 new tokens each, GQA 64/8, "
                                     "page 64, the tile space split evenly over the SMs",
@@ -948,6 +950,9 @@ def run_profile_case(name):
                                                 context_lens=np.full(2, 262144), n_new=8))
     elif name == "mla_b16_topk2048":
         s = MlaStep(pf, synth.MlaWorkload("mla_b16", B=16, H=128, context_lens=np.full(16, 65536), topk_n=2048,
+                                          P=64))
+    elif name == "mla_b64_topk2048_l16384":
+        s = MlaStep(pf, synth.MlaWorkload("mla_b64_q", B=64, H=128, context_lens=np.full(64, 16384), topk_n=2048,
                                           P=64))
     else:
         raise SystemExit(f"unknown profile case {name}; choose from {sorted(PROFILE_CASES)}")
