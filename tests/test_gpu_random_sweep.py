@@ -55,7 +55,7 @@ def _prefill_case(case):
     r = np.random.default_rng(2000 + case)
     Hkv = int(r.choice([1, 2]))
     G = int(r.choice([1, 2, 4, 8, 16]))
-    P = int(r.choice([16, 32, 48, 64, 128]))
+    P = int(r.choice([16, 32, 48, 64, 96, 128]))
     B = int(r.integers(1, 6))
     lens = r.integers(1, 700, size=B)
     for i in range(B):
@@ -117,7 +117,7 @@ def _scaled_case(case):
     r = np.random.default_rng(4000 + case)
     Hkv = int(r.choice([1, 2, 4]))
     G = int(r.integers(1, 17))
-    P = int(r.choice([16, 32, 48, 64]))
+    P = int(r.choice([16, 32, 48, 64, 96, 128]))
     B = int(r.integers(1, 8))
     lens = r.integers(1, 600, size=B)
     for i in range(B):
