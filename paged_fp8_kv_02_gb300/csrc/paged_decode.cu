@@ -698,22 +698,33 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 2)
     // when vref grows the accumulator is rescaled like the running maximum
     float w0 = 1.f, w8 = 1.f;
     if constexpr (kScl == kSclToken) {
-      // the largest V scale of the tile, read by every thread from the stage
-      const float4* vp = reinterpret_cast<const float4*>(sptr + stage * (kScaleStageBytes / 4) + 16);
-      float4 q4[4] = {vp[0], vp[1], vp[2], vp[3]};
-      if (partial) {
+      // the largest V scale of the tile: with one or two heads per KV head the
+      // tile's work is too short to hide a shuffle chain, so every thread
+      // reads the tile's 16 V scales from the stage; with more heads the
+      // chain is hidden and costs fewer instructions
+      float vm;
+      if (a.G <= 2) {
+        const float4* vp = reinterpret_cast<const float4*>(sptr + stage * (kScaleStageBytes / 4) + 16);
+        float4 q4[4] = {vp[0], vp[1], vp[2], vp[3]};
+        if (partial) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          if (tok0 + 4 * i >= L) q4[i].x = 0.f;
-          if (tok0 + 4 * i + 1 >= L) q4[i].y = 0.f;
-          if (tok0 + 4 * i + 2 >= L) q4[i].z = 0.f;
-          if (tok0 + 4 * i + 3 >= L) q4[i].w = 0.f;
+          for (int i = 0; i < 4; ++i) {
+            if (tok0 + 4 * i >= L) q4[i].x = 0.f;
+            if (tok0 + 4 * i + 1 >= L) q4[i].y = 0.f;
+            if (tok0 + 4 * i + 2 >= L) q4[i].z = 0.f;
+            if (tok0 + 4 * i + 3 >= L) q4[i].w = 0.f;
+          }
         }
-      }
-      float m4[4];
+        float m4[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) m4[i] = fmaxf(fmaxf(q4[i].x, q4[i].y), fmaxf(q4[i].z, q4[i].w));
-      const float vm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        for (int i = 0; i < 4; ++i) m4[i] = fmaxf(fmaxf(q4[i].x, q4[i].y), fmaxf(q4[i].z, q4[i].w));
+        vm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      } else {
+        vm = fmaxf(vs0, vs8);
+        vm = fmaxf(vm, __shfl_xor_sync(0xFFFFFFFFu, vm, 4));
+        vm = fmaxf(vm, __shfl_xor_sync(0xFFFFFFFFu, vm, 8));
+        vm = fmaxf(vm, __shfl_xor_sync(0xFFFFFFFFu, vm, 16));
+      }
       if (vm > vref) {  // warp-uniform
         const float r = vref / vm;
 #pragma unroll
