@@ -946,7 +946,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) prefillw_merge_kernel(const 
 //   warps: 0 K producer, 1 score MMAs, 2-5 widening, 6-13 softmax (warp w:
 //   lane quadrant w % 4, half (w - 6) / 4), 14 P.V MMAs, 15 V producer (one
 //   warp issuing every copy of a tile measured slower, most of all with
-//   16-token pages: 16 copies per tile).
+//   16-token pages: 16 copies per tile; so did one thread issuing both kinds
+//   of MMA, by 25%: the two issuers' MMAs overlap their latencies).
 // Units in order of decreasing row block, so the longest (causal) ones start first.
 // Score and P buffers in tensor memory.  One score buffer and two P buffers
 // (so that P(j + 1) need not wait for P.V(j)) fit as well and give the same
